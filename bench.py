@@ -1,0 +1,328 @@
+"""Attention fwd+bwd throughput on GB300 through the C ABI (libfa.so).
+
+One step = one forward (fa_fwd) and one backward (fa_bwd_preprocess,
+fa_bwd_dkdv, fa_bwd_dq) over one batch of the workload, inputs resident in HBM.
+FLOP convention: forward 4*B*H*Nq*Nk*d, backward 2.5x that, both halved when
+causal.  L2 (129 MB) is flushed by writing a 512 MiB buffer between timed
+steps; each step is timed with CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload per step).  Under torchrun every rank runs
+the same per-GPU workload (independent batch*head units, no collective on the
+data path): weak scaling; rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOP/s and % of GB300 bf16 tensor peak on 1 GPU"
+DEFAULT_WORKLOAD = "bench_b8_n4096_d64_causal"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"bf16_tflops": j["bf16_tflops"], "bf16_tflops_sustained": j.get("bf16_tflops_sustained"),
+                "hbm_gbs": j["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(w, budget_s: float, max_units=None):
+    """Time the oracle on whole batch*head units of the workload until ~budget_s has passed."""
+    import oracle
+    from tiled_attention_04_gb300 import inputs
+    Q, K, V, dO = inputs.make_inputs(w)
+    fwd, bwd = w.flops()
+    per_unit = (fwd + bwd) / w.BH
+    units, t = 0, 0.0
+    limit = max_units or w.BH
+    while units < limit and (t < budget_s or units == 0):
+        b = units % w.BH
+        t0 = time.perf_counter()
+        oracle.attn_bwd_ref(Q.exact[b:b + 1], K.exact[b:b + 1], V.exact[b:b + 1], dO.exact[b:b + 1],
+                            w.scale, w.causal)
+        t += time.perf_counter() - t0
+        units += 1
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": per_unit * units / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{units} of {w.BH} batch*head units of {w.name} (full rows, fwd+bwd), {t:.1f} s"}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    steps = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(w, budget_s=0.0, max_units=1)
+        if i >= args.warmup:
+            steps.append(r)
+    v = statistics.mean(s["value"] for s in steps)
+    per_unit_flop = sum(w.flops()) / w.BH
+    ms = per_unit_flop / (v * 1e12) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w),
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "kind": "oracle", "cores": steps[-1]["cores"],
+                             "sample": f"1 of {w.BH} batch*head units of {w.name} per step (fwd+bwd)"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "seq_len": w.N, "head_dim": w.d, "causal": w.causal,
+            "input_dtype": w.dtype, "l2": "flushed between timed steps (512 MiB write)"}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def kernel_flops(w, path):
+    """Algorithmic FLOP per launch of each kernel (matmul FLOP of the method's steps it performs)."""
+    f = 4.0 * w.BH * w.N * w.N * w.d * (0.5 if w.causal else 1.0)   # two N x N x d matmuls
+    if path == "tc":
+        # dK/dV kernel: S, dP, dV, dK and dQ partials (five matmuls); dQ kernel: fp32 -> dtype convert
+        return {"fwd": f, "bwd_pre": 0.0, "bwd_dkdv": 2.5 * f, "bwd_dq": 0.0}
+    # CUDA-core path: dK/dV kernel recomputes S, dP and forms dV, dK (four); dQ kernel S, dP, dQ (three)
+    return {"fwd": f, "bwd_pre": 0.0, "bwd_dkdv": 2.0 * f, "bwd_dq": 1.5 * f}
+
+
+def run_gpu(args, w, rank, world):
+    import torch
+
+    from tiled_attention_04_gb300 import binding, build, inputs
+    build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.lib()
+    tens = inputs.make_inputs(w)
+    Qd, Kd, Vd, dOd = (inputs.to_torch(t, dev) for t in tens)
+    host = [inputs.to_torch(t).pin_memory() for t in tens]
+    O = torch.empty_like(Qd)
+    L = torch.empty(Qd.shape[:-1], dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(Qd), torch.empty_like(Kd), torch.empty_like(Vd)
+    ws = binding.alloc_workspace(Qd, Kd, w.causal)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    path = binding.path_name(w.N, w.N, w.d, w.causal, binding.dtype_code(Qd))
+    kf = kernel_flops(w, path)
+    fwd_f, bwd_f = w.flops()
+
+    def step(ev):
+        ev[0].record(stream)
+        binding.fa_fwd(Qd, Kd, Vd, is_causal=w.causal, O=O, L=L)
+        ev[1].record(stream)
+        binding.fa_bwd_preprocess(O, dOd, Qd, Kd, w.causal, ws)
+        ev[2].record(stream)
+        binding.fa_bwd_dkdv(Qd, Kd, Vd, dOd, L, dQ, dK, dV, w.causal, ws)
+        ev[3].record(stream)
+        binding.fa_bwd_dq(Qd, Kd, Vd, dOd, L, dQ, w.causal, ws)
+        ev[4].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step(new_events())
+    torch.cuda.synchronize()
+    if binding.fa_get_device_status() != binding.FA_OK:
+        raise RuntimeError("device status not ok after warm-up")
+
+    evs = [new_events() for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for e in evs:
+            flush.fill_(1.0)
+            step(e)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    names = ["fwd", "bwd_pre", "bwd_dkdv", "bwd_dq"]
+    per = {n: [] for n in names}
+    total = []
+    for e in evs:
+        for i, n in enumerate(names):
+            per[n].append(e[i].elapsed_time(e[i + 1]))
+        total.append(e[0].elapsed_time(e[4]))
+    step_ms = sum(total) / len(total)
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    if binding.fa_get_device_status() != binding.FA_OK:
+        raise RuntimeError("device status not ok after timed steps")
+
+    # ---- end to end through the public API with host buffers: H2D inputs, fwd, bwd, D2H outputs
+    hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    hL = torch.empty(L.shape, dtype=L.dtype).pin_memory()
+    hg = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dQ, dK, dV)]
+    h2d = sum(x.numel() * x.element_size() for x in host)
+    d2h = sum(x.numel() * x.element_size() for x in (hO, hL, *hg))
+
+    def e2e_step():
+        for dst, src in zip((Qd, Kd, Vd, dOd), host):
+            dst.copy_(src, non_blocking=True)
+        binding.fa_fwd(Qd, Kd, Vd, is_causal=w.causal, O=O, L=L)
+        binding.fa_bwd(Qd, Kd, Vd, O, dOd, L, is_causal=w.causal, dQ=dQ, dK=dK, dV=dV, workspace=ws)
+        for dst, src in zip((hO, hL, *hg), (O, L, dQ, dK, dV)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    n_e2e = max(3, min(args.steps, 50))
+    for _ in range(n_e2e):
+        flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    e2e_ms = sum(e_ms) / len(e_ms)
+
+    if rank != 0:
+        return
+    pk = peaks()
+    avg = {n: sum(v) / len(v) for n, v in per.items()}
+    dom = max(names, key=lambda n: avg[n])
+    dom_tf = kf[dom] / (avg[dom] * 1e-3) / 1e12
+    value = world * (fwd_f + bwd_f) / (step_ms * 1e-3) / 1e12
+    fwd_tf = fwd_f / (avg["fwd"] * 1e-3) / 1e12
+    bwd_ms = avg["bwd_pre"] + avg["bwd_dkdv"] + avg["bwd_dq"]
+    bwd_tf = bwd_f / (bwd_ms * 1e-3) / 1e12
+    launches_per_step = 4
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": config_of(w),
+        "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
+        "fwd": {"ms": round(avg["fwd"], 5), "tflops": round(fwd_tf, 2), "frac": round(fwd_tf / pk["bf16_tflops"], 4)},
+        "bwd": {"ms": round(bwd_ms, 5), "tflops": round(bwd_tf, 2), "frac": round(bwd_tf / pk["bf16_tflops"], 4),
+                "kernels_ms": {n: round(avg[n], 5) for n in names[1:]}},
+        "path": path,
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(dom_tf, 2), "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(dom_tf / pk["bf16_tflops"], 4), "traffic": None,
+                     "peak_source": f"{pk['source']} bf16 dense burst"},
+        "e2e": {"value": round((fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = oracle_sample(w, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from tiled_attention_04_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_gpu(args, w, rank, world)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

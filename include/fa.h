@@ -1,0 +1,158 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 library, libfa.so.
+ *
+ * What it computes (CS336 A2 field guide "Systems and Parallelism", §1.2-1.3;
+ * FlashAttention-2, Dao 2023):
+ *
+ *   forward  (problem flash_forward (a)-(c)):
+ *     S = scale * Q K^T; causal: keys with index > query index are masked
+ *     (contribute exactly zero, the same as adding -1e6 then exponentiating);
+ *     P = softmax over each row of S; O = P V; L = m + ln(l) per row, the
+ *     natural-log logsumexp of the row that the backward pass reuses.
+ *     S and P are never written to memory: the kernels walk key tiles with an
+ *     online (running max m, running sum l) softmax.
+ *
+ *   backward (problem flash_backward):
+ *     P = exp(S - L) recomputed from Q, K and L; D = rowsum(dO * O);
+ *     dV = P^T dO; dP = dO V^T; dS = P * (dP - D);
+ *     dQ = scale * dS K; dK = scale * dS^T Q.
+ *
+ * Layout.  Q, O, dO, dQ: (B, H, Nq, d) row-major contiguous, i.e. (B*H, Nq, d)
+ * with batch and heads flattened in front (problem flash_forward (b)).
+ * K, V, dK, dV: (B, H, Nk, d).  L: (B*H, Nq) fp32.  All tensors but L and the
+ * workspace share one element type (fa_dtype); O, dQ, dK, dV are written in
+ * that type; accumulation is always fp32.
+ *
+ * Causal alignment: top-left.  Key j is visible to query i iff j <= i
+ * (absolute indices), so every query row sees key 0 and no row is empty.
+ *
+ * Ownership.  The caller owns every buffer (device memory), including the
+ * backward workspace.  The library allocates no device memory per call.
+ * Calls are asynchronous and ordered on the caller's stream; nothing
+ * synchronises inside a call.
+ *
+ * Errors.  Every entry point returns fa_status and never throws.  Arguments
+ * are checked before anything is launched; on a bad argument nothing runs and
+ * no output is touched.  A launch failure maps to FA_ERR_LAUNCH.  The kernels
+ * bound every wait; a wait that runs out sets a device-side status word that
+ * fa_get_device_status() reports as FA_ERR_TIMEOUT.
+ *
+ * Supported: d in {16, 32, 64, 128}; dtype fp32 or bf16; Nq >= 0, Nk >= 1
+ * (Nk >= 0 when Nq == 0); B*H*max(Nq,Nk) < 2^31; every pointer 16-byte
+ * aligned; scale finite.  B*H*Nq == 0 (and B*H*Nk == 0) is a valid empty call.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL_PTR = 1,             /* a required pointer is NULL                      */
+    FA_ERR_BAD_SHAPE = 2,            /* negative / overflowing sizes, Nk == 0 with Nq>0 */
+    FA_ERR_UNSUPPORTED_HEAD_DIM = 3, /* d not in {16,32,64,128}                         */
+    FA_ERR_UNSUPPORTED_DTYPE = 4,    /* dtype not an fa_dtype value                     */
+    FA_ERR_MISALIGNED = 5,           /* a pointer not 16-byte aligned                   */
+    FA_ERR_WORKSPACE = 6,            /* workspace NULL or smaller than required         */
+    FA_ERR_LAUNCH = 7,               /* CUDA launch or descriptor error                 */
+    FA_ERR_TIMEOUT = 8,              /* a device-side bounded wait ran out              */
+    FA_ERR_NO_DEVICE = 9,            /* no usable CUDA device                           */
+    FA_ERR_BAD_ARG = 10              /* other invalid argument (is_causal, scale)       */
+} fa_status;
+
+typedef enum {
+    FA_DTYPE_F32 = 0,
+    FA_DTYPE_BF16 = 1
+} fa_dtype;
+
+/*
+ * Forward pass (flash_forward).  Reads Q, K, V; writes O (input dtype) and
+ * L (fp32, natural-log logsumexp per query row).
+ */
+FA_API fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *L,
+                 int B, int H, int Nq, int Nk, int d, float scale, int is_causal,
+                 fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for this shape (fp32 D, plus an fp32
+ * dQ accumulator on the tensor-core path).  Returns 0 for unsupported
+ * arguments.
+ */
+FA_API size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype);
+
+/*
+ * Backward pass (flash_backward).  Reads Q, K, V, O, dO (input dtype) and L
+ * (fp32, from fa_fwd on the same inputs); writes dQ, dK, dV (input dtype).
+ * Runs fa_bwd_preprocess, then fa_bwd_dkdv and fa_bwd_dq on `stream`.
+ * `workspace` must hold fa_bwd_workspace_size(...) bytes, 16-byte aligned;
+ * its contents need not be initialised and are scratch afterwards.
+ */
+FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                 const float *L, void *dQ, void *dK, void *dV,
+                 int B, int H, int Nq, int Nk, int d, float scale, int is_causal, fa_dtype dtype,
+                 void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * The three phases of fa_bwd, exported so each kernel can be launched and
+ * timed on its own.  They must run in this order on one stream, with the same
+ * arguments and workspace:
+ *   fa_bwd_preprocess: D = rowsum(dO * O) into the workspace (and clears the
+ *                      fp32 dQ accumulator when the tensor-core path uses one);
+ *   fa_bwd_dkdv:       dK, dV (one program per key tile, looping over query tiles);
+ *   fa_bwd_dq:         dQ (one program per query tile, looping over key tiles).
+ */
+FA_API fa_status fa_bwd_preprocess(const void *O, const void *dO,
+                            int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype,
+                            void *workspace, size_t workspace_bytes, fa_stream_t stream);
+FA_API fa_status fa_bwd_dkdv(const void *Q, const void *K, const void *V, const void *dO,
+                      const float *L, void *dQ, void *dK, void *dV,
+                      int B, int H, int Nq, int Nk, int d, float scale, int is_causal, fa_dtype dtype,
+                      void *workspace, size_t workspace_bytes, fa_stream_t stream);
+FA_API fa_status fa_bwd_dq(const void *Q, const void *K, const void *V, const void *dO,
+                    const float *L, void *dQ,
+                    int B, int H, int Nq, int Nk, int d, float scale, int is_causal, fa_dtype dtype,
+                    void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Name of the kernel family fa_fwd / fa_bwd would use for these arguments:
+ * "tc" (tcgen05 tensor-core kernels) or "simt" (fp32 CUDA-core kernels), or
+ * NULL for unsupported arguments.  Host-only; launches nothing.
+ */
+FA_API const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype dtype);
+
+/*
+ * Synchronises `stream`, then returns FA_ERR_TIMEOUT if any kernel since the
+ * last fa_reset_device_status() gave up a bounded wait, else the stream's
+ * CUDA status mapped to FA_OK / FA_ERR_LAUNCH.
+ */
+FA_API fa_status fa_get_device_status(fa_stream_t stream);
+FA_API fa_status fa_reset_device_status(fa_stream_t stream);
+
+/*
+ * Fault injection on the host side: caps every device-side wait loop at
+ * `spins` polls (0 restores the default, about a second of polling).  With a
+ * tiny cap the tensor-core kernels give up early, record FA_ERR_TIMEOUT and
+ * return without hanging; their outputs are then undefined.
+ */
+FA_API void fa_set_wait_limit(uint32_t spins);
+
+FA_API const char *fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_H */

@@ -1,0 +1,197 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerances (elementwise |got - want| <= tol + tol*|want|): 1e-4 for fp32
+inputs, 2e-2 for bf16 inputs, on O, L, dQ, dK and dV.  Small shapes are
+compared in full (several tiles plus ragged tails); the full-size workloads
+are compared at sampled rows against values the oracle wrote ahead of time
+(tests/golden/samples_*.npz, made by tests/golden/make_samples.py), after
+checking that the inputs drawn here hash to the same digests.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from tiled_attention_04_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def run_gpu(tensors, causal, scale=None, canary=True):
+    """fa_fwd then fa_bwd on the device; outputs live inside canary-padded buffers."""
+    torch = _torch()
+    from tiled_attention_04_gb300 import binding
+    dev = torch.device("cuda")
+    Q, K, V, dO = (inputs.to_torch(t, dev) for t in tensors)
+    pad = 128   # elements of sentinel before and after each output
+
+    def padded(shape, dtype):
+        n = math.prod(shape)
+        buf = torch.full((n + 2 * pad,), -7.25, dtype=dtype, device=dev)
+        return buf, buf[pad:pad + n].view(shape)
+
+    bO, O = padded(Q.shape, Q.dtype)
+    bL, L = padded(Q.shape[:-1], torch.float32)
+    bdQ, dQ = padded(Q.shape, Q.dtype)
+    bdK, dK = padded(K.shape, K.dtype)
+    bdV, dV = padded(V.shape, V.dtype)
+    binding.fa_fwd(Q, K, V, is_causal=causal, scale=scale, O=O, L=L)
+    binding.fa_bwd(Q, K, V, O, dO, L, is_causal=causal, scale=scale, dQ=dQ, dK=dK, dV=dV)
+    torch.cuda.synchronize()
+    assert binding.fa_get_device_status() == binding.FA_OK
+    if canary:
+        for name, b in (("O", bO), ("L", bL), ("dQ", bdQ), ("dK", bdK), ("dV", bdV)):
+            for part in (b[:pad], b[-pad:]):
+                assert (part.float() == -7.25).all(), f"write outside {name}"
+    return {k: v.double().cpu().numpy() for k, v in
+            (("O", O), ("L", L), ("dQ", dQ), ("dK", dK), ("dV", dV))}
+
+
+def oracle_all(tensors, causal, scale):
+    Q, K, V, dO = (t.exact for t in tensors)
+    dQ, dK, dV, O, L, D = oracle.attn_bwd_ref(Q, K, V, dO, scale, causal)
+    return {"O": O, "L": L, "dQ": dQ, "dK": dK, "dV": dV}
+
+
+def assert_close(got, want, tol, tag):
+    for k in ("O", "L", "dQ", "dK", "dV"):
+        g, w = got[k], want[k]
+        assert np.isfinite(g).all(), f"{tag}: non-finite {k}"
+        bad = np.abs(g - w) > tol + tol * np.abs(w)
+        if bad.any():
+            err = np.abs(g - w).max()
+            idx = np.argwhere(bad)[0]
+            raise AssertionError(f"{tag}: {k} mismatches at {bad.sum()} of {bad.size} elements "
+                                 f"(first {tuple(idx)}: got {g[tuple(idx)]}, want {w[tuple(idx)]}; max abs {err:.3g})")
+
+
+SWEEP = [(2, 256, 256, d, dt, c) for d in (16, 32, 64, 128) for dt in ("f32", "bf16") for c in (False, True)]
+RAGGED = [
+    (1, 200, 200, 64, "bf16", True), (1, 129, 129, 128, "bf16", False), (3, 1, 1, 32, "f32", True),
+    (1, 17, 17, 16, "f32", False), (2, 100, 100, 128, "f32", True), (1, 64, 192, 64, "bf16", True),
+    (1, 192, 64, 64, "bf16", True), (1, 300, 1000, 128, "bf16", False), (1, 1000, 300, 64, "f32", True),
+    (2, 384, 384, 64, "bf16", True), (1, 640, 640, 128, "bf16", True), (1, 512, 512, 64, "bf16", False),
+    (4, 1152, 1152, 128, "bf16", True), (1, 1088, 1088, 64, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("bh,nq,nk,d,dt,causal", SWEEP + RAGGED)
+def test_parity_small(cuda_lib, bh, nq, nk, d, dt, causal):
+    t = inputs.make_custom(bh, nq, nk, d, dt, seed=1000 + nq + nk + d)
+    sc = 1.0 / math.sqrt(d)
+    got = run_gpu(t, causal)
+    assert_close(got, oracle_all(t, causal, sc), TOL[dt], f"bh={bh} nq={nq} nk={nk} d={d} {dt} causal={causal}")
+
+
+@pytest.mark.parametrize("scale", [0.05, 1.0])
+def test_parity_non_default_scale(cuda_lib, scale):
+    t = inputs.make_custom(2, 256, 256, 64, "bf16", seed=77)
+    got = run_gpu(t, True, scale=scale)
+    assert_close(got, oracle_all(t, True, scale), 2e-2, f"scale={scale}")
+
+
+def test_tiny_f32_workload_full(cuda_lib):
+    """Batch 1, 1 head, N=128, d=16, fp32, causal, seed 0: every output element."""
+    w = inputs.WORKLOADS["tiny_f32_causal"]
+    t = inputs.make_inputs(w)
+    assert_close(run_gpu(t, w.causal), oracle_all(t, w.causal, w.scale), 1e-4, w.name)
+
+
+def test_empty_and_degenerate(cuda_lib):
+    torch = _torch()
+    from tiled_attention_04_gb300 import binding
+    dev = torch.device("cuda")
+    Q = torch.empty(0, 64, 64, device=dev, dtype=torch.bfloat16)
+    O, L = binding.fa_fwd(Q, Q, Q, is_causal=True)
+    assert O.numel() == 0 and L.numel() == 0
+    # no queries: dK and dV are exactly zero
+    Qe = torch.empty(2, 0, 64, device=dev, dtype=torch.bfloat16)
+    K = torch.randn(2, 96, 64, device=dev).to(torch.bfloat16)
+    dK = torch.full_like(K, 3.0)
+    dV = torch.full_like(K, 3.0)
+    Oe = torch.empty_like(Qe)
+    Le = torch.empty(2, 0, device=dev)
+    binding.fa_bwd(Qe, K, K, Oe, Oe, Le, is_causal=False, dQ=torch.empty_like(Qe), dK=dK, dV=dV)
+    torch.cuda.synchronize()
+    assert (dK == 0).all() and (dV == 0).all()
+
+
+def test_single_key_gives_value_row(cuda_lib):
+    t = inputs.make_custom(2, 64, 1, 32, "f32", seed=5)
+    got = run_gpu(t, False)
+    np.testing.assert_allclose(got["O"], np.broadcast_to(t[2].exact, got["O"].shape), rtol=1e-6, atol=1e-6)
+    np.testing.assert_allclose(got["dQ"], 0.0, atol=1e-6)
+    np.testing.assert_allclose(got["dK"], 0.0, atol=1e-6)
+
+
+def test_misaligned_pointer_is_rejected_and_nothing_written(cuda_lib):
+    torch = _torch()
+    from tiled_attention_04_gb300 import binding
+    dev = torch.device("cuda")
+    Q = torch.randn(1, 128, 64, device=dev).to(torch.bfloat16)
+    buf = torch.full((128 * 64 + 8,), 5.0, device=dev, dtype=torch.bfloat16)
+    O = buf[1:1 + 128 * 64].view(1, 128, 64)    # 2-byte offset
+    with pytest.raises(binding.FaError) as e:
+        binding.fa_fwd(Q, Q, Q, is_causal=True, O=O)
+    assert e.value.status == 5
+    torch.cuda.synchronize()
+    assert (buf == 5.0).all()
+
+
+def test_forward_and_dkdv_are_deterministic(cuda_lib):
+    t = inputs.make_custom(2, 1024, 1024, 128, "bf16", seed=9)
+    a = run_gpu(t, True, canary=False)
+    b = run_gpu(t, True, canary=False)
+    for k in ("O", "L", "dK", "dV"):
+        assert np.array_equal(a[k], b[k]), k
+    np.testing.assert_allclose(a["dQ"], b["dQ"], rtol=1e-2, atol=1e-2)
+
+
+def test_autograd_function_saves_only_L_with_query_shape(cuda_lib):
+    torch = _torch()
+    from tiled_attention_04_gb300.autograd import FlashAttention
+    dev = torch.device("cuda")
+    t = inputs.make_custom(4, 128, 128, 64, "bf16", seed=3)
+    Q, K, V, dO = (inputs.to_torch(x, dev).requires_grad_(i < 3) for i, x in enumerate(t))
+    O = FlashAttention.apply(Q, K, V, True)
+    saved = [s for s in O.grad_fn.saved_tensors if tuple(s.shape) == (4, 128)]
+    assert len(saved) == 1
+    O.backward(dO)
+    want = oracle_all(t, True, 1 / 8)
+    got = {"O": O.detach().double().cpu().numpy(), "L": saved[0].double().cpu().numpy(),
+           "dQ": Q.grad.double().cpu().numpy(), "dK": K.grad.double().cpu().numpy(),
+           "dV": V.grad.double().cpu().numpy()}
+    assert_close(got, want, 2e-2, "autograd")
+
+
+FULL = ["bench_b8_n4096_d64_causal", "long_n16384_d128_causal", "vlong_n65536_d64_causal",
+        "layer_xl_b4_h25_n1024_causal", "layer_xl_b4_h25_n1024_full"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(cuda_lib, name):
+    path = os.path.join(GOLDEN, f"samples_{name}.npz")
+    if not os.path.exists(path):
+        pytest.fail(f"missing oracle samples {path} (run tests/golden/make_samples.py)")
+    ref = np.load(path)
+    w = inputs.WORKLOADS[name]
+    t = inputs.make_inputs(w)
+    digests = [inputs.storage_digest(x) for x in t]
+    assert digests == list(ref["digest"]), "inputs drawn here differ from the ones the oracle saw"
+    got = run_gpu(t, w.causal, canary=False)
+    for k in got:
+        assert np.isfinite(got[k]).all(), f"{name}: non-finite {k}"
+    bh, rows, cols = ref["bh"], ref["rows"], ref["cols"]
+    sub = {"O": got["O"][bh][:, rows], "L": got["L"][bh][:, rows], "dQ": got["dQ"][bh][:, rows],
+           "dK": got["dK"][bh][:, cols], "dV": got["dV"][bh][:, cols]}
+    want = {k: ref[k] for k in sub}
+    assert_close(sub, want, TOL[w.dtype], name)

@@ -1,0 +1,45 @@
+// Internal interface between the C-ABI layer (fa_api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa.h"
+
+struct FaProblem {
+    int BH;          // batch * heads
+    int Nq, Nk;      // query / key sequence lengths
+    int d;           // head dimension
+    float scale;     // softmax scale (usually 1/sqrt(d))
+    int causal;      // top-left causal mask
+    fa_dtype dtype;  // element type of Q, K, V, O, dO, dQ, dK, dV
+    uint32_t wait_limit;  // cap on device-side polling loops
+};
+
+// ---- fp32 CUDA-core kernels (fa_simt.cu): every dtype and head dim.
+cudaError_t simt_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
+                     cudaStream_t st);
+cudaError_t simt_bwd_preprocess(const FaProblem &p, const void *O, const void *dO, float *Dvec,
+                                cudaStream_t st);
+cudaError_t simt_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                          const float *L, const float *Dvec, void *dK, void *dV, cudaStream_t st);
+cudaError_t simt_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                        const float *L, const float *Dvec, void *dQ, cudaStream_t st);
+
+// ---- tcgen05 tensor-core kernels (fa_tc_fwd.cu, fa_tc_bwd.cu): bf16, d in {64, 128}.
+bool tc_fwd_supported(const FaProblem &p);
+bool tc_bwd_supported(const FaProblem &p);
+cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
+                   cudaStream_t st);
+cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO, float *Dvec, float *dQacc,
+                              cudaStream_t st);
+cudaError_t tc_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                        const float *L, const float *Dvec, float *dQacc, void *dK, void *dV, cudaStream_t st);
+cudaError_t tc_bwd_dq(const FaProblem &p, const float *dQacc, void *dQ, cudaStream_t st);
+
+// device-side status words of the tensor-core translation units
+cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st);
+cudaError_t tc_bwd_read_status(unsigned *out, cudaStream_t st);
+cudaError_t tc_fwd_reset_status(cudaStream_t st);
+cudaError_t tc_bwd_reset_status(cudaStream_t st);

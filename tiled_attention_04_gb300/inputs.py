@@ -162,11 +162,14 @@ def make_inputs(w: Workload, dtype: str | None = None):
         arrs = [w.amp * normal(w.seed, t, shp) for t in range(4)]
     else:
         dm = w.H * w.d
-        x = normal(w.seed, 0, (w.B, w.N, dm))
+        # x and W sit on fixed-point grids (2^-12 and 2^-20) so every product is a
+        # multiple of 2^-32 and every sum below 2^20: x W^T is then exact in fp64
+        # whatever order a BLAS adds in, and identical on every machine.
+        x = np.round(normal(w.seed, 0, (w.B, w.N, dm)) * 4096.0) / 4096.0
         bound = math.sqrt(6.0 / (dm + dm))
         arrs = []
         for t in (1, 2, 3):
-            W = uniform(w.seed, t, (dm, dm), -bound, bound)
+            W = np.round(uniform(w.seed, t, (dm, dm), -bound, bound) * 1048576.0) / 1048576.0
             y = x.reshape(-1, dm) @ W.T                      # (B*N, dm)
             y = y.reshape(w.B, w.N, w.H, w.d).transpose(0, 2, 1, 3).reshape(shp)
             arrs.append(np.ascontiguousarray(y))
@@ -178,3 +181,19 @@ def make_custom(BH: int, Nq: int, Nk: int, d: int, dtype: str, seed: int, amp: f
     """Q (BH,Nq,d), K, V (BH,Nk,d), dO (BH,Nq,d) for ad-hoc parity shapes."""
     shapes = [(BH, Nq, d), (BH, Nk, d), (BH, Nk, d), (BH, Nq, d)]
     return [quantize(amp * normal(seed, t, s), dtype) for t, s in enumerate(shapes)]
+
+
+def to_torch(t: Tensor, device=None):
+    """The storage bits as a torch tensor (float32 or bfloat16), optionally moved to `device`."""
+    import torch
+    if t.dtype == "bf16":
+        x = torch.from_numpy(np.ascontiguousarray(t.storage).view(np.int16)).view(torch.bfloat16)
+    else:
+        x = torch.from_numpy(np.ascontiguousarray(t.storage))
+    return x if device is None else x.to(device)
+
+
+def storage_digest(t: Tensor) -> str:
+    """SHA-256 of the storage bytes, to confirm two machines drew identical inputs."""
+    import hashlib
+    return hashlib.sha256(np.ascontiguousarray(t.storage).tobytes()).hexdigest()
