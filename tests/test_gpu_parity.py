@@ -92,7 +92,7 @@ def test_parity_small(cuda_lib, bh, nq, nk, d, dt, causal):
     assert_close(got, oracle_all(t, causal, sc), TOL[dt], f"bh={bh} nq={nq} nk={nk} d={d} {dt} causal={causal}")
 
 
-@pytest.mark.parametrize("scale", [0.05, 1.0])
+@pytest.mark.parametrize("scale", [0.05, 0.25])
 def test_parity_non_default_scale(cuda_lib, scale):
     t = inputs.make_custom(2, 256, 256, 64, "bf16", seed=77)
     got = run_gpu(t, True, scale=scale)

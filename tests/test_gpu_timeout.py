@@ -1,0 +1,37 @@
+"""Failure detection without a GPU fault: a host-set cap on device-side polling
+makes the tensor-core kernels give up their waits, report FA_ERR_TIMEOUT
+through fa_get_device_status and return; the context stays usable and the
+next call with the default cap is correct again."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tiled_attention_04_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_forced_wait_timeout_reports_and_recovers(cuda_lib):
+    import torch
+    from tiled_attention_04_gb300 import binding
+    dev = torch.device("cuda")
+    t = inputs.make_custom(2, 512, 512, 128, "bf16", seed=21)
+    Q, K, V, dO = (inputs.to_torch(x, dev) for x in t)
+    assert binding.path_name(512, 512, 128, 1, binding.FA_DTYPE_BF16) == "tc"
+    binding.fa_reset_device_status()
+    try:
+        binding.fa_set_wait_limit(1)
+        binding.fa_fwd(Q, K, V, is_causal=True)
+        assert binding.fa_get_device_status() == 8      # FA_ERR_TIMEOUT
+    finally:
+        binding.fa_set_wait_limit(0)
+    binding.fa_reset_device_status()
+    assert binding.fa_get_device_status() == binding.FA_OK
+    O, L = binding.fa_fwd(Q, K, V, is_causal=True)
+    torch.cuda.synchronize()
+    assert binding.fa_get_device_status() == binding.FA_OK
+    rO, rL = oracle.attn_fwd_ref(t[0].exact, t[1].exact, t[2].exact, 1 / math.sqrt(128), True)
+    np.testing.assert_allclose(O.double().cpu().numpy(), rO, rtol=2e-2, atol=2e-2)
+    np.testing.assert_allclose(L.double().cpu().numpy(), rL, rtol=2e-2, atol=2e-2)

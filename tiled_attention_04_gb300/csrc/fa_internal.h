@@ -27,6 +27,10 @@ cudaError_t simt_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, cons
 cudaError_t simt_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                         const float *L, const float *Dvec, void *dQ, cudaStream_t st);
 
+// (B*H, N, d) bf16 tensor -> 3-D TMA map, boxes of 64 columns x box_rows rows, 128-byte swizzle
+struct CUtensorMap_st;
+bool tc_make_map_3d(CUtensorMap_st *m, const void *ptr, int BH, int N, int d, int box_rows);
+
 // ---- tcgen05 tensor-core kernels (fa_tc_fwd.cu, fa_tc_bwd.cu): bf16, d in {64, 128}.
 bool tc_fwd_supported(const FaProblem &p);
 bool tc_bwd_supported(const FaProblem &p);

@@ -1,17 +1,418 @@
-// tcgen05 forward kernel (placeholder until the tensor-core path lands).
+// FlashAttention-2 forward on sm_103a tensor cores (tcgen05 + TMA + TMEM).
+//
+// Method (CS336 A2 field guide "Systems and Parallelism", §1.2-1.3, problem
+// flash_forward; FlashAttention-2): for one tile of 128 query rows, walk the
+// key tiles with a running row max m and running row sum l, rescale the output
+// accumulator when m moves, divide by l once at the end and write
+// L = m + ln(l).  S and P never leave the SM.  Causal: key tiles wholly above
+// the diagonal are never loaded (§1.3.3's early exit); only tiles that cross
+// the diagonal (or the ragged end of the keys) pay for index compares.
+//
+// GB300 mapping (one CTA = one 128-row query tile of one batch*head):
+//   warp 0      TMA producer: Q once, then K_j and V_j into a ring of smem
+//               stages (128-byte swizzle), each stage guarded by mbarriers.
+//   warp 1      MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into
+//               TMEM (tcgen05.mma, bf16 in, fp32 accumulate), then
+//               O_t += P_j V_j with P read straight from TMEM.
+//   warps 4-7   softmax warpgroup 0: key tiles j = 0, 2, 4, ...
+//   warps 8-11  softmax warpgroup 1: key tiles j = 1, 3, 5, ...
+// Each softmax thread owns one query row (TMEM lane = row), so row max and
+// row sum need no shuffles.  The two warpgroups keep separate (m, l, O) over
+// interleaved halves of the key range -- while one computes exponentials the
+// tensor core works on the other's tile -- and merge the two partial results
+// exactly at the end (O = (a0 O0 + a1 O1) / (a0 l0 + a1 l1), a_t = 2^(m_t - M)).
+// The running max is only moved when it grows by more than 8 (in log2 units),
+// so O is rescaled in TMEM rarely; P stays below 2^8 and the final division
+// by l makes the result exact regardless of the max used.
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256) (P as packed bf16 aliases the
+// first 64 columns of its S), O0 [256, 256+d), O1 [256+d, 256+2d).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <mutex>
+
 #include "fa_internal.h"
+#include "tc_common.cuh"
 
 __device__ unsigned g_fa_fwd_status;
 
-bool tc_fwd_supported(const FaProblem &) { return false; }
-cudaError_t tc_fwd(const FaProblem &, const void *, const void *, const void *, void *, float *, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int BM = 128;          // query rows per tile (MMA M)
+constexpr int BN = 128;          // keys per tile
+constexpr int NTHREADS = 384;    // 12 warps
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int D>
+struct FwdCfg {
+    static constexpr int STAGES = D == 128 ? 2 : 3;
+    static constexpr int CHUNKS = D / 64;                      // 128-byte swizzle chunks per row
+    static constexpr uint32_t CHUNK_BYTES = 128u * 128u;       // 128 rows x 128 bytes
+    static constexpr uint32_t TILE_BYTES = CHUNKS * CHUNK_BYTES;
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t K_OFF = Q_OFF + TILE_BYTES;
+    static constexpr uint32_t V_OFF = K_OFF + STAGES * TILE_BYTES;
+    static constexpr uint32_t BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+    static constexpr int NBAR = 1 + 3 * STAGES + 6 + 1;
+    static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t MISC_OFF = STAT_OFF + 4 * 128 * 4;
+    static constexpr uint32_t USED = MISC_OFF + 16;
+    // at least ~116 KB so that one CTA (which owns all 512 TMEM columns) runs per SM
+    static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u ? USED + 1024 : 120u * 1024u);
+    static constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
+                     float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
+                     uint32_t wait_limit) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // longest work first: high query tiles (more key tiles under causal) start first
+    const int item = blockIdx.x;
+    const int qt = num_q_tiles - 1 - item / BH;
+    const int bh = item % BH;
+    const int q0 = qt * BM;
+    const int kend = CAUSAL ? min(Nk, q0 + BM) : Nk;
+    const int n = (kend + BN - 1) / BN;
+
+    auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
+    const uint32_t q_full = bar(0);
+    auto k_full = [&](int s) { return bar(1 + s); };
+    auto v_full = [&](int s) { return bar(1 + C::STAGES + s); };
+    auto kv_empty = [&](int s) { return bar(1 + 2 * C::STAGES + s); };
+    auto s_full = [&](int t) { return bar(1 + 3 * C::STAGES + t); };
+    auto p_full = [&](int t) { return bar(3 + 3 * C::STAGES + t); };
+    auto o_done = [&](int t) { return bar(5 + 3 * C::STAGES + t); };
+    const uint32_t drain = bar(7 + 3 * C::STAGES);
+    float *m_sm = reinterpret_cast<float *>(sb + C::STAT_OFF);
+    float *l_sm = m_sm + 256;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(q_full, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            tc::mbar_init(k_full(s), 1);
+            tc::mbar_init(v_full(s), 1);
+            tc::mbar_init(kv_empty(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            tc::mbar_init(s_full(t), 1);
+            tc::mbar_init(p_full(t), 128);
+            tc::mbar_init(o_done(t), 1);
+        }
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const tc::Waiter W{abort_flag, &g_fa_fwd_status, wait_limit, 1u};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmQ);
+            tc::tma_prefetch_desc(&tmK);
+            tc::tma_prefetch_desc(&tmV);
+            tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
+            for (int c = 0; c < C::CHUNKS; ++c)
+                tc::tma_load_3d(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh);
+            int issued = 0;
+            for (int j = 0; j < n; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                if (!W.wait(kv_empty(s), ph ^ 1u)) break;
+                tc::mbar_arrive_expect_tx(k_full(s), C::TILE_BYTES);
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tc::tma_load_3d(base + C::K_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK, k_full(s),
+                                    c * 64, j * BN, bh);
+                tc::mbar_arrive_expect_tx(v_full(s), C::TILE_BYTES);
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tc::tma_load_3d(base + C::V_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV, v_full(s),
+                                    c * 64, j * BN, bh);
+                issued = j + 1;
+            }
+            if (*abort_flag) {
+                // let the copies already in flight land before the CTA exits
+                for (int j = issued - 1; j >= 0 && j >= issued - C::STAGES; --j) {
+                    const int s = j % C::STAGES;
+                    const uint32_t ph = (j / C::STAGES) & 1;
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(k_full(s), ph); ++i) {
+                    }
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(v_full(s), ph); ++i) {
+                    }
+                }
+                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN, false, false);
+            constexpr uint32_t idesc_o = tc::idesc_bf16(BM, D, false, true);
+            bool ok = W.wait(q_full, 0);
+            auto pv = [&](int j) -> bool {
+                const int s = j % C::STAGES, t = j & 1, k = j >> 1;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                if (!W.wait(p_full(t), k & 1)) return false;
+                tc::fence_after_sync();
+                if (!W.wait(v_full(s), ph)) return false;
+                const uint32_t vbase = base + C::V_OFF + s * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t bdesc = tc::sdesc_sw128(vbase + kk * 16 * 128, C::CHUNK_BYTES, 1024);
+                    tc::mma_ts(tmem + C::O_COL0 + t * D, tmem + C::S_COL0 + t * 128 + kk * 8, bdesc, idesc_o,
+                               (k > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(o_done(t));
+                tc::mma_commit(kv_empty(s));
+                return true;
+            };
+            for (int j = 0; ok && j < n; ++j) {
+                const int s = j % C::STAGES, t = j & 1;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                if (!(ok = W.wait(k_full(s), ph))) break;
+                const uint32_t kbase = base + C::K_OFF + s * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+                    const uint64_t adesc = tc::sdesc_sw128(base + C::Q_OFF + off, 16, 1024);
+                    const uint64_t bdesc = tc::sdesc_sw128(kbase + off, 16, 1024);
+                    tc::mma_ss(tmem + C::S_COL0 + t * 128, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(s_full(t));
+                if (j >= 1) ok = pv(j - 1);
+            }
+            if (ok) ok = pv(n - 1);
+            if (!ok) {
+                // wait (bounded) for the MMAs already issued before TMEM is released
+                tc::mma_commit(drain);
+                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = (warp - 4) >> 2;
+        const int r = ((warp & 3) << 5) + lane;            // row within the tile = TMEM lane
+        const int row = q0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        const uint32_t tS = tmem + lane_base + C::S_COL0 + t * 128;
+        const uint32_t tO = tmem + lane_base + C::O_COL0 + t * D;
+        const int nt = (n - t + 1) >> 1;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int k = 0; k < nt; ++k) {
+            const int k0 = (2 * k + t) * BN;
+            ok = W.wait(s_full(t), k & 1);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc::fence_after_sync();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_x32(tS + 32 * c, sr[c]);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence_x32(sr[c]);
+            float s[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
+            const bool need_mask = (CAUSAL && k0 + BN - 1 > q0) || (k0 + BN > Nk);
+            if (need_mask) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) {
+                    const int kj = k0 + i;
+                    if (kj >= Nk || (CAUSAL && kj > row)) s[i] = -INFINITY;
+                }
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+            const float m_cand = fmaxf(m, mx * scale_log2);
+            const bool rescale = m_cand > m + kRescaleThreshold;
+            float alpha = 1.f;
+            if (rescale) {
+                alpha = exp2f(m - m_cand);
+                m = m_cand;
+            }
+            l *= alpha;
+            uint32_t p[64];
+            float rs = 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const float e0 = exp2f(fmaf(s[2 * i], scale_log2, -m));
+                const float e1 = exp2f(fmaf(s[2 * i + 1], scale_log2, -m));
+                rs += e0 + e1;
+                p[i] = tc::pack_bf16(e0, e1);
+            }
+            l += rs;
+            tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+            tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+            if (k > 0 && __any_sync(0xffffffffu, rescale)) {
+                // O_t holds the sum up to this warpgroup's previous tile: rescale it in place
+                ok = W.wait(o_done(t), (k - 1) & 1);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + 32 * c, o);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_x32(tO + 32 * c, o);
+                }
+            }
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            tc::mbar_arrive(p_full(t));
+        }
+        // ---- merge the two warpgroups' partial results and write O, L
+        m_sm[t * 128 + r] = m;
+        l_sm[t * 128 + r] = l;
+        tc::named_bar_sync(1, 256);
+        const int n0 = (n + 1) >> 1, n1 = n >> 1;
+        bool fine = !*abort_flag;
+        if (fine) fine = W.wait(o_done(0), (n0 - 1) & 1);
+        if (fine && n1 > 0) fine = W.wait(o_done(1), (n1 - 1) & 1);
+        if (__all_sync(0xffffffffu, fine)) {
+            tc::fence_after_sync();
+            const float m0 = m_sm[r], l0 = l_sm[r];
+            const float m1 = m_sm[128 + r], l1 = l_sm[128 + r];
+            const float M = fmaxf(m0, m1);
+            const float a0 = exp2f(m0 - M);
+            const float a1 = n1 > 0 ? exp2f(m1 - M) : 0.f;
+            const float lsum = l0 * a0 + l1 * a1;
+            const float inv = 1.f / lsum;
+            const uint32_t tO0 = tmem + lane_base + C::O_COL0, tO1 = tO0 + D;
+            __nv_bfloat16 *orow = O + ((size_t)bh * Nq + row) * D;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                const int col = t * (D / 2) + 32 * c;
+                uint32_t o0[32], o1[32] = {};
+                tmem_ld_x32(tO0 + col, o0);
+                if (n1 > 0) tmem_ld_x32(tO1 + col, o1);
+                tc::tmem_ld_wait();
+                reg_fence_x32(o0);
+                reg_fence_x32(o1);
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float v0 = __uint_as_float(o0[2 * i]) * a0, v1 = __uint_as_float(o0[2 * i + 1]) * a0;
+                    if (n1 > 0) {
+                        v0 = fmaf(__uint_as_float(o1[2 * i]), a1, v0);
+                        v1 = fmaf(__uint_as_float(o1[2 * i + 1]), a1, v1);
+                    }
+                    packed[i] = tc::pack_bf16(v0 * inv, v1 * inv);
+                }
+                if (row < Nq) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
+            }
+            if (t == 0 && row < Nq) Lout[(size_t)bh * Nq + row] = M * kLn2 + logf(lsum);
+        }
+    }
+    // ------------------------------------------------------------ teardown
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
 }
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+// (BH, N, d) bf16 tensor -> 3-D map with 64 x rows x 1 boxes, 128-byte swizzle.
+// Rows past N in a batch*head read as zero.
+bool tc_make_map_3d(CUtensorMap_st *m, const void *ptr, int BH, int N, int d, int box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_fwd_supported(const FaProblem &p) {
+    return p.dtype == FA_DTYPE_BF16 && (p.d == 64 || p.d == 128) && p.Nq >= 128 && p.Nk >= 128 && p.BH >= 1;
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                              void *O, float *L, cudaStream_t st) {
+    using C = FwdCfg<D>;
+    auto kern = fa_fwd_tc_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int qtiles = (p.Nq + BM - 1) / BM;
+    const long long grid = (long long)qtiles * p.BH;
+    const float scale_log2 = p.scale * 1.4426950408889634f;
+    kern<<<(unsigned)grid, NTHREADS, C::SMEM_BYTES, st>>>(mq, mk, mv, static_cast<__nv_bfloat16 *>(O), L, p.Nq,
+                                                            p.Nk, p.BH, qtiles, scale_log2, p.wait_limit);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
+                   cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    if (!tc_make_map_3d(&mq, Q, p.BH, p.Nq, p.d, BM) || !tc_make_map_3d(&mk, K, p.BH, p.Nk, p.d, BN) ||
+        !tc_make_map_3d(&mv, V, p.BH, p.Nk, p.d, BN))
+        return cudaErrorInvalidValue;
+    if (p.d == 128) return p.causal ? launch_fwd<128, true>(p, mq, mk, mv, O, L, st)
+                                    : launch_fwd<128, false>(p, mq, mk, mv, O, L, st);
+    return p.causal ? launch_fwd<64, true>(p, mq, mk, mv, O, L, st) : launch_fwd<64, false>(p, mq, mk, mv, O, L, st);
+}
+
 cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fa_fwd_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     return e;
 }
+
 cudaError_t tc_fwd_reset_status(cudaStream_t st) {
     static const unsigned zero = 0;
     return cudaMemcpyToSymbolAsync(g_fa_fwd_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, st);
