@@ -151,12 +151,13 @@ def config_of(w):
 # ---------------------------------------------------------------------------- GPU arm
 
 def kernel_flops(w, path):
-    """Algorithmic FLOP per launch of each kernel (matmul FLOP of the method's steps it performs)."""
+    """Algorithmic FLOP per launch of each kernel (the method's matmuls that kernel performs).
+
+    Both kernel families split the backward into a dK/dV pass (recomputes S and
+    dP, forms dV and dK: four N x N x d matmuls) and a dQ pass (recomputes S
+    and dP, forms dQ: three), as the forward does two.
+    """
     f = 4.0 * w.BH * w.N * w.N * w.d * (0.5 if w.causal else 1.0)   # two N x N x d matmuls
-    if path == "tc":
-        # dK/dV kernel: S, dP, dV, dK and dQ partials (five matmuls); dQ kernel: fp32 -> dtype convert
-        return {"fwd": f, "bwd_pre": 0.0, "bwd_dkdv": 2.5 * f, "bwd_dq": 0.0}
-    # CUDA-core path: dK/dV kernel recomputes S, dP and forms dV, dK (four); dQ kernel S, dP, dQ (three)
     return {"fwd": f, "bwd_pre": 0.0, "bwd_dkdv": 2.0 * f, "bwd_dq": 1.5 * f}
 
 
@@ -186,7 +187,7 @@ def run_gpu(args, w, rank, world):
         ev[0].record(stream)
         binding.fa_fwd(Qd, Kd, Vd, is_causal=w.causal, O=O, L=L)
         ev[1].record(stream)
-        binding.fa_bwd_preprocess(O, dOd, Qd, Kd, w.causal, ws)
+        binding.fa_bwd_preprocess(O, dOd, L, Qd, Kd, w.causal, ws)
         ev[2].record(stream)
         binding.fa_bwd_dkdv(Qd, Kd, Vd, dOd, L, dQ, dK, dV, w.causal, ws)
         ev[3].record(stream)

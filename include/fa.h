@@ -88,9 +88,9 @@ FA_API fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, fl
                  fa_dtype dtype, fa_stream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd needs for this shape (fp32 D, plus an fp32
- * dQ accumulator on the tensor-core path).  Returns 0 for unsupported
- * arguments.
+ * Bytes of device workspace fa_bwd needs for this shape (fp32 D per query row;
+ * on the tensor-core path fp32 D and L per query row, rows padded to a
+ * multiple of 128).  Returns 0 for unsupported arguments.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype);
 
@@ -110,12 +110,12 @@ FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void 
  * The three phases of fa_bwd, exported so each kernel can be launched and
  * timed on its own.  They must run in this order on one stream, with the same
  * arguments and workspace:
- *   fa_bwd_preprocess: D = rowsum(dO * O) into the workspace (and clears the
- *                      fp32 dQ accumulator when the tensor-core path uses one);
+ *   fa_bwd_preprocess: D = rowsum(dO * O) into the workspace (the tensor-core
+ *                      path also stages L there, scaled by log2(e) and padded);
  *   fa_bwd_dkdv:       dK, dV (one program per key tile, looping over query tiles);
  *   fa_bwd_dq:         dQ (one program per query tile, looping over key tiles).
  */
-FA_API fa_status fa_bwd_preprocess(const void *O, const void *dO,
+FA_API fa_status fa_bwd_preprocess(const void *O, const void *dO, const float *L,
                             int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype,
                             void *workspace, size_t workspace_bytes, fa_stream_t stream);
 FA_API fa_status fa_bwd_dkdv(const void *Q, const void *K, const void *V, const void *dO,

@@ -129,8 +129,8 @@ def test_single_key_gives_value_row(cuda_lib):
     t = inputs.make_custom(2, 64, 1, 32, "f32", seed=5)
     got = run_gpu(t, False)
     np.testing.assert_allclose(got["O"], np.broadcast_to(t[2].exact, got["O"].shape), rtol=1e-6, atol=1e-6)
-    np.testing.assert_allclose(got["dQ"], 0.0, atol=1e-6)
-    np.testing.assert_allclose(got["dK"], 0.0, atol=1e-6)
+    np.testing.assert_allclose(got["dQ"], 0.0, atol=1e-5)
+    np.testing.assert_allclose(got["dK"], 0.0, atol=1e-5)
 
 
 def test_misaligned_pointer_is_rejected_and_nothing_written(cuda_lib):

@@ -49,7 +49,7 @@ def lib() -> ctypes.CDLL:
     L.fa_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
     L.fa_bwd_workspace_size.restype = sz
     L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
-    L.fa_bwd_preprocess.argtypes = [vp, vp, i, i, i, i, i, i, i, vp, sz, vp]
+    L.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp]
     L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_path_name.argtypes = [i, i, i, i, i]
@@ -171,9 +171,9 @@ def fa_bwd(Q, K, V, O, dO, L, is_causal=False, scale=None, dQ=None, dK=None, dV=
     return dQ, dK, dV
 
 
-def fa_bwd_preprocess(O, dO, Q, K, is_causal, workspace, stream=None):
+def fa_bwd_preprocess(O, dO, L, Q, K, is_causal, workspace, stream=None):
     B, H = _bh(Q)
-    check(lib().fa_bwd_preprocess(_ptr(O), _ptr(dO), B, H, Q.shape[-2], K.shape[-2], Q.shape[-1],
+    check(lib().fa_bwd_preprocess(_ptr(O), _ptr(dO), _ptr(L), B, H, Q.shape[-2], K.shape[-2], Q.shape[-1],
                                   int(is_causal), dtype_code(Q), _ptr(workspace), workspace.numel(),
                                   _stream(stream)), "fa_bwd_preprocess")
 

@@ -71,17 +71,20 @@ fa_status device_ok() {
 
 size_t elem_bytes(fa_dtype t) { return t == FA_DTYPE_F32 ? 4 : 2; }
 
-// workspace: [D: BH*Nq fp32][dQ accumulator: BH*Nq*d fp32, tensor-core path only]
+// Backward workspace.  CUDA-core path: D (BH*Nq fp32).  Tensor-core path:
+// D then L*log2(e), each BH * padded_rows(Nq) fp32 (see fa_tc_bwd.cu).
 struct Workspace {
-    size_t d_off, d_bytes, acc_off, acc_bytes, total;
+    bool tc;
+    size_t d_off, l_off, total;
 };
 Workspace workspace_layout(const FaProblem &p) {
     Workspace w{};
+    w.tc = tc_bwd_supported(p);
+    const size_t rows = w.tc ? tc_bwd_ld_rows(p) : (size_t)p.BH * p.Nq;
+    const size_t bytes = align_up(rows * sizeof(float), 256);
     w.d_off = 0;
-    w.d_bytes = align_up((size_t)p.BH * p.Nq * sizeof(float), 256);
-    w.acc_off = w.d_bytes;
-    w.acc_bytes = tc_bwd_supported(p) ? align_up((size_t)p.BH * p.Nq * p.d * sizeof(float), 256) : 0;
-    w.total = w.acc_off + w.acc_bytes;
+    w.l_off = bytes;
+    w.total = w.tc ? 2 * bytes : bytes;
     if (w.total == 0) w.total = 256;
     return w;
 }
@@ -150,7 +153,7 @@ size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, int is_causal,
     return workspace_layout(p).total;
 }
 
-fa_status fa_bwd_preprocess(const void *O, const void *dO, int B, int H, int Nq, int Nk, int d,
+fa_status fa_bwd_preprocess(const void *O, const void *dO, const float *L, int B, int H, int Nq, int Nk, int d,
                             int is_causal, fa_dtype dtype, void *workspace, size_t workspace_bytes,
                             fa_stream_t stream) {
     FaProblem p{};
@@ -159,14 +162,13 @@ fa_status fa_bwd_preprocess(const void *O, const void *dO, int B, int H, int Nq,
                            is_causal, dtype, workspace, workspace_bytes, &p, &w, false);
     if (s != FA_OK) return s;
     if ((long long)p.BH * p.Nq == 0) return FA_OK;
-    if ((s = check_ptrs({O, dO})) != FA_OK) return s;
+    if ((s = check_ptrs({O, dO, L})) != FA_OK) return s;
     if ((s = device_ok()) != FA_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
     float *Dv = reinterpret_cast<float *>(ws + w.d_off);
-    cudaError_t e = tc_bwd_supported(p)
-                        ? tc_bwd_preprocess(p, O, dO, Dv, reinterpret_cast<float *>(ws + w.acc_off), st)
-                        : simt_bwd_preprocess(p, O, dO, Dv, st);
+    cudaError_t e = w.tc ? tc_bwd_preprocess(p, O, dO, L, Dv, reinterpret_cast<float *>(ws + w.l_off), st)
+                         : simt_bwd_preprocess(p, O, dO, Dv, st);
     return map_cuda(e);
 }
 
@@ -191,9 +193,8 @@ fa_status fa_bwd_dkdv(const void *Q, const void *K, const void *V, const void *d
     if ((s = check_ptrs({Q, K, V, dO, L, dQ})) != FA_OK) return s;
     char *ws = static_cast<char *>(workspace);
     const float *Dv = reinterpret_cast<const float *>(ws + w.d_off);
-    cudaError_t e = tc_bwd_supported(p)
-                        ? tc_bwd_dkdv(p, Q, K, V, dO, L, Dv, reinterpret_cast<float *>(ws + w.acc_off), dK, dV, st)
-                        : simt_bwd_dkdv(p, Q, K, V, dO, L, Dv, dK, dV, st);
+    cudaError_t e = w.tc ? tc_bwd_dkdv(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off), Dv, dK, dV, st)
+                         : simt_bwd_dkdv(p, Q, K, V, dO, L, Dv, dK, dV, st);
     return map_cuda(e);
 }
 
@@ -211,9 +212,8 @@ fa_status fa_bwd_dq(const void *Q, const void *K, const void *V, const void *dO,
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
     const float *Dv = reinterpret_cast<const float *>(ws + w.d_off);
-    cudaError_t e = tc_bwd_supported(p)
-                        ? tc_bwd_dq(p, reinterpret_cast<const float *>(ws + w.acc_off), dQ, st)
-                        : simt_bwd_dq(p, Q, K, V, dO, L, Dv, dQ, st);
+    cudaError_t e = w.tc ? tc_bwd_dq(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off), Dv, dQ, st)
+                         : simt_bwd_dq(p, Q, K, V, dO, L, Dv, dQ, st);
     return map_cuda(e);
 }
 
@@ -230,7 +230,7 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     if (!any_q && !any_k) return FA_OK;
     if (any_q && (s = check_ptrs({Q, K, V, O, dO, L, dQ})) != FA_OK) return s;
     if (any_k && (s = check_ptrs({dK, dV})) != FA_OK) return s;
-    if ((s = fa_bwd_preprocess(O, dO, B, H, Nq, Nk, d, is_causal, dtype, workspace, workspace_bytes, stream)) !=
+    if ((s = fa_bwd_preprocess(O, dO, L, B, H, Nq, Nk, d, is_causal, dtype, workspace, workspace_bytes, stream)) !=
         FA_OK)
         return s;
     if ((s = fa_bwd_dkdv(Q, K, V, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace,

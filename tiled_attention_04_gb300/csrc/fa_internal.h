@@ -36,11 +36,14 @@ bool tc_fwd_supported(const FaProblem &p);
 bool tc_bwd_supported(const FaProblem &p);
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
                    cudaStream_t st);
-cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO, float *Dvec, float *dQacc,
-                              cudaStream_t st);
+// backward workspace on this path: per batch*head, padded_rows(Nq) fp32 D then the same of L*log2(e)
+size_t tc_bwd_ld_rows(const FaProblem &p);
+cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO, const float *L, float *Dp,
+                              float *Lp, cudaStream_t st);
 cudaError_t tc_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
-                        const float *L, const float *Dvec, float *dQacc, void *dK, void *dV, cudaStream_t st);
-cudaError_t tc_bwd_dq(const FaProblem &p, const float *dQacc, void *dQ, cudaStream_t st);
+                        const float *Lp, const float *Dp, void *dK, void *dV, cudaStream_t st);
+cudaError_t tc_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                      const float *Lp, const float *Dp, void *dQ, cudaStream_t st);
 
 // device-side status words of the tensor-core translation units
 cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st);

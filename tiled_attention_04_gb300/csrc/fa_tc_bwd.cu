@@ -1,22 +1,701 @@
-// tcgen05 backward kernels (placeholder until the tensor-core path lands).
+// FlashAttention-2 backward on sm_103a tensor cores (tcgen05 + TMA + TMEM).
+//
+// Method (CS336 A2 field guide "Systems and Parallelism", problem
+// flash_backward and §1.3.3): P = exp(S - L) is rebuilt from Q, K and the
+// saved logsumexp L; D = rowsum(dO * O) comes from a preprocess pass;
+// dV = P^T dO, dP = dO V^T, dS = P * (dP - D), dQ = scale dS K,
+// dK = scale dS^T Q.  The work is split into two passes so that no program
+// ever adds into another's output (§1.3.3, "split the backward pass into two
+// passes, one for dQ and one for dK and dV"):
+//
+//   preprocess   D and a log2-scaled copy of L, padded per batch*head to a
+//                multiple of 128 rows (padding rows get L = +inf, so their P
+//                is exactly zero), in the caller's workspace;
+//   dK/dV pass   one CTA per 128-key tile; loops over 64-query sub-tiles,
+//                recomputing S^T = K Q^T and dP^T = V dO^T in TMEM,
+//                P^T and dS^T (bf16) written back into TMEM, then
+//                dV += P^T dO and dK += dS^T Q with A read from TMEM;
+//   dQ pass      one CTA per 128-query tile; loops over 64-key sub-tiles,
+//                recomputing S = Q K^T and dP = dO V^T, dS into TMEM,
+//                dQ += dS K.
+//
+// Both passes use the same warp roles as the forward: warp 0 TMA producer,
+// warp 1 MMA issuer / TMEM owner, warps 4-7 and 8-11 two element-wise
+// warpgroups that take alternate sub-tiles, so that one warpgroup's
+// exponentials overlap the tensor core's work on the other's sub-tile.  The
+// accumulators (dK and dV, or dQ) are shared: every MMA is issued by one
+// thread, in order, so the two warpgroups' contributions simply add up.
+// Causal: sub-tiles wholly on the masked side of the diagonal are skipped.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
 #include "fa_internal.h"
+#include "tc_common.cuh"
 
 __device__ unsigned g_fa_bwd_status;
 
-bool tc_bwd_supported(const FaProblem &) { return false; }
-cudaError_t tc_bwd_preprocess(const FaProblem &, const void *, const void *, float *, float *, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int NTHREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// rows of the L/D workspace per batch*head: a multiple of 128
+__host__ __device__ inline int padded_rows(int n) { return (n + 127) / 128 * 128; }
+
+// ------------------------------------------------------------------ preprocess
+// one warp per query row: D = rowsum(dO * O) (fp32), Lp = L * log2(e); padding rows: D = 0, Lp = +inf
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
+                                                         const __nv_bfloat16 *__restrict__ dO,
+                                                         const float *__restrict__ L, float *__restrict__ Dp,
+                                                         float *__restrict__ Lp, int BH, int Nq, int d) {
+    const int nqp = padded_rows(Nq);
+    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= (long long)BH * nqp) return;
+    const int bh = (int)(gw / nqp), q = (int)(gw % nqp);
+    if (q >= Nq) {
+        if (lane == 0) {
+            Dp[gw] = 0.f;
+            Lp[gw] = INFINITY;
+        }
+        return;
+    }
+    const size_t row = ((size_t)bh * Nq + q) * d;
+    float acc = 0.f;
+    for (int c = lane * 8; c < d; c += 256) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(O + row + c);
+        const uint4 b = *reinterpret_cast<const uint4 *>(dO + row + c);
+        const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+        const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
+            acc = fmaf(fa.x, fb.x, acc);
+            acc = fmaf(fa.y, fb.y, acc);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+        Dp[gw] = acc;
+        Lp[gw] = L[(size_t)bh * Nq + q] * kLog2e;
+    }
 }
-cudaError_t tc_bwd_dkdv(const FaProblem &, const void *, const void *, const void *, const void *, const float *,
-                        const float *, float *, void *, void *, cudaStream_t) {
-    return cudaErrorNotSupported;
+
+// ------------------------------------------------------------------ shared layout helpers
+// A "tile" here is R rows x d bf16 held as d/64 chunks of [R rows x 128 B], 128-byte swizzled.
+template <int R, int D>
+struct TileShape {
+    static constexpr uint32_t CHUNK = R * 128u;
+    static constexpr uint32_t BYTES = (D / 64) * CHUNK;
+};
+
+// K-major descriptor for k-step kk (16 elements of d) of a tile with rows `R`
+template <int R>
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+    return tc::sdesc_sw128(tile + (kk >> 2) * (R * 128u) + (kk & 3) * 32u, 16, 1024);
 }
-cudaError_t tc_bwd_dq(const FaProblem &, const float *, void *, cudaStream_t) { return cudaErrorNotSupported; }
+// MN-major descriptor: the tile's rows are the MMA's K dimension; k-step kk covers rows 16kk..16kk+15
+template <int R>
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
+    return tc::sdesc_sw128(tile + kk * 16u * 128u, R * 128u, 1024);
+}
+
+struct Roles {
+    int warp, lane;
+};
+
+// ------------------------------------------------------------------ dK / dV
+template <int D>
+struct DkdvCfg {
+    static constexpr int BK = 128;                 // keys per CTA (MMA M)
+    static constexpr int BQ = 64;                  // queries per sub-tile (MMA N of S^T, K of dV/dK)
+    static constexpr int STAGES = 3;
+    using KT = TileShape<BK, D>;
+    using QT = TileShape<BQ, D>;
+    static constexpr uint32_t K_OFF = 0;
+    static constexpr uint32_t V_OFF = K_OFF + KT::BYTES;
+    static constexpr uint32_t Q_OFF = V_OFF + KT::BYTES;                 // stages of Q sub-tiles
+    static constexpr uint32_t DO_OFF = Q_OFF + STAGES * QT::BYTES;       // stages of dO sub-tiles
+    static constexpr uint32_t LD_OFF = DO_OFF + STAGES * QT::BYTES;      // stages of 64 Lp + 64 D floats
+    static constexpr uint32_t BAR_OFF = LD_OFF + STAGES * 512;
+    // kv_full, q_full[S], q_empty[S], sd_full[2], p_full[2], mma_done[2], drain
+    static constexpr int NBAR = 1 + 2 * STAGES + 6 + 1;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t SMEM_BYTES = (MISC_OFF + 16 + 1024 > 120u * 1024u ? MISC_OFF + 16 + 1024 : 120u * 1024u);
+    // TMEM: S^T_t [128t, 128t+64), dP^T_t [128t+64, 128t+128), dV [256, 256+D), dK [256+D, 256+2D)
+    static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    fa_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                          const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
+                          __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH, int num_k_tiles, float scale,
+                          float scale_log2, uint32_t wait_limit) {
+    using C = DkdvCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // longest first: under causal the first key tiles see the most queries
+    const int item = blockIdx.x;
+    const int kt = CAUSAL ? item / BH : num_k_tiles - 1 - item / BH;
+    const int bh = item % BH;
+    const int k0 = kt * C::BK;
+    const int nqp = padded_rows(Nq);
+    const int i_begin = CAUSAL ? k0 / C::BQ : 0;              // first query sub-tile that sees a key of this tile
+    const int i_end = (Nq + C::BQ - 1) / C::BQ;
+    const int n = i_end > i_begin ? i_end - i_begin : 0;      // sub-tiles to visit
+
+    auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
+    const uint32_t kv_full = bar(0);
+    auto q_full = [&](int s) { return bar(1 + s); };
+    auto q_empty = [&](int s) { return bar(1 + C::STAGES + s); };
+    auto sd_full = [&](int t) { return bar(1 + 2 * C::STAGES + t); };
+    auto p_full = [&](int t) { return bar(3 + 2 * C::STAGES + t); };
+    auto mma_done = [&](int t) { return bar(5 + 2 * C::STAGES + t); };
+    const uint32_t drain = bar(7 + 2 * C::STAGES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(kv_full, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            tc::mbar_init(q_full(s), 1);
+            tc::mbar_init(q_empty(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            tc::mbar_init(sd_full(t), 1);
+            tc::mbar_init(p_full(t), 128);
+            tc::mbar_init(mma_done(t), 1);
+        }
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const tc::Waiter W{abort_flag, &g_fa_bwd_status, wait_limit, 2u};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && n > 0) {
+            tc::tma_prefetch_desc(&tmQ);
+            tc::tma_prefetch_desc(&tmdO);
+            tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
+            for (int c = 0; c < D / 64; ++c) {
+                tc::tma_load_3d(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh);
+                tc::tma_load_3d(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh);
+            }
+            int issued = 0;
+            for (int it = 0; it < n; ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1;
+                if (!W.wait(q_empty(s), ph ^ 1u)) break;
+                const int q0 = (i_begin + it) * C::BQ;
+                tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 512);
+                for (int c = 0; c < D / 64; ++c) {
+                    tc::tma_load_3d(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
+                                    q0, bh);
+                    tc::tma_load_3d(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
+                                    c * 64, q0, bh);
+                }
+                const size_t off = (size_t)bh * nqp + q0;
+                tc::bulk_load(base + C::LD_OFF + s * 512, Lp + off, 256, q_full(s));
+                tc::bulk_load(base + C::LD_OFF + s * 512 + 256, Dp + off, 256, q_full(s));
+                issued = it + 1;
+            }
+            if (*abort_flag) {
+                for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it) {
+                    const int s = it % C::STAGES;
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full(s), (it / C::STAGES) & 1); ++i) {
+                    }
+                }
+                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full, 0); ++i) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BQ, false, false);
+            constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
+            bool ok = W.wait(kv_full, 0);
+            auto grads = [&](int it) -> bool {   // dV += P^T dO, dK += dS^T Q for sub-tile `it`
+                const int s = it % C::STAGES, t = it & 1, k = it >> 1;
+                if (!W.wait(p_full(t), k & 1)) return false;
+                tc::fence_after_sync();
+                const uint32_t qb = base + C::Q_OFF + s * C::QT::BYTES;
+                const uint32_t ob = base + C::DO_OFF + s * C::QT::BYTES;
+#pragma unroll
+                for (int kk = 0; kk < C::BQ / 16; ++kk) {
+                    tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + kk * 8, mnmajor_desc<C::BQ>(ob, kk), idesc_g,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < C::BQ / 16; ++kk) {
+                    tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + kk * 8, mnmajor_desc<C::BQ>(qb, kk),
+                               idesc_g, (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(mma_done(t));
+                tc::mma_commit(q_empty(s));
+                return true;
+            };
+            for (int it = 0; ok && it < n; ++it) {
+                const int s = it % C::STAGES, t = it & 1;
+                if (!(ok = W.wait(q_full(s), (it / C::STAGES) & 1))) break;
+                const uint32_t qb = base + C::Q_OFF + s * C::QT::BYTES;
+                const uint32_t ob = base + C::DO_OFF + s * C::QT::BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)   // S^T = K Q^T
+                    tc::mma_ss(tmem + 128 * t, kmajor_desc<C::BK>(base + C::K_OFF, kk), kmajor_desc<C::BQ>(qb, kk),
+                               idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)   // dP^T = V dO^T
+                    tc::mma_ss(tmem + 128 * t + 64, kmajor_desc<C::BK>(base + C::V_OFF, kk),
+                               kmajor_desc<C::BQ>(ob, kk), idesc_s, kk > 0 ? 1u : 0u);
+                tc::mma_commit(sd_full(t));
+                if (it >= 1) ok = grads(it - 1);
+            }
+            if (ok) ok = grads(n - 1);
+            if (!ok) {
+                tc::mma_commit(drain);
+                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ element-wise warpgroups
+        const int t = (warp - 4) >> 2;
+        const int r = ((warp & 3) << 5) + lane;              // key row within the tile = TMEM lane
+        const int key = k0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        const uint32_t tS = tmem + lane_base + 128 * t;
+        const uint32_t tP = tS + 64;
+        const int nt = (n - t + 1) >> 1;
+        for (int k = 0; k < nt; ++k) {
+            const int it = 2 * k + t;
+            const int s = it % C::STAGES;
+            const int q0 = (i_begin + it) * C::BQ;
+            bool ok = W.wait(sd_full(t), k & 1);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            ok = W.wait(q_full(s), (it / C::STAGES) & 1);      // L and D of this sub-tile are in smem
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            uint32_t sv[2][32], dv[2][32];
+            tmem_ld_x32(tS, sv[0]);
+            tmem_ld_x32(tS + 32, sv[1]);
+            tmem_ld_x32(tP, dv[0]);
+            tmem_ld_x32(tP + 32, dv[1]);
+            tc::tmem_ld_wait();
+            reg_fence_x32(sv[0]);
+            reg_fence_x32(sv[1]);
+            reg_fence_x32(dv[0]);
+            reg_fence_x32(dv[1]);
+            const float *lds = reinterpret_cast<const float *>(sb + C::LD_OFF + s * 512);
+            const bool need_mask = CAUSAL && (k0 + 127 > q0);
+            uint32_t pp[32], dsp[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float p2[2], g2[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = 2 * i + h;
+                    const float sval = __uint_as_float(sv[c >> 5][c & 31]);
+                    float p = exp2f(fmaf(sval, scale_log2, -lds[c]));
+                    if (need_mask && key > q0 + c) p = 0.f;
+                    p2[h] = p;
+                    g2[h] = p * (__uint_as_float(dv[c >> 5][c & 31]) - lds[64 + c]);
+                }
+                pp[i] = tc::pack_bf16(p2[0], p2[1]);
+                dsp[i] = tc::pack_bf16(g2[0], g2[1]);
+            }
+            tmem_st_x32(tS, pp);
+            tmem_st_x32(tP, dsp);
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            tc::mbar_arrive(p_full(t));
+        }
+        // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (rows = keys)
+        tc::named_bar_sync(1, 256);
+        bool fine = !*abort_flag;
+        if (n > 0) {
+            const int n0 = (n + 1) >> 1, n1 = n >> 1;
+            if (fine) fine = W.wait(mma_done(0), (n0 - 1) & 1);
+            if (fine && n1 > 0) fine = W.wait(mma_done(1), (n1 - 1) & 1);
+        }
+        if (__all_sync(0xffffffffu, fine)) {
+            tc::fence_after_sync();
+            __nv_bfloat16 *dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
+            const float mul = t == 0 ? 1.f : scale;
+            const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32];
+                if (n > 0) {
+                    tmem_ld_x32(tA + 32 * c, a);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(a);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) a[i] = 0u;
+                }
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
+                if (key < Nk) {
+                    uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ dQ
+template <int D>
+struct DqCfg {
+    static constexpr int BQ = 128;                 // queries per CTA (MMA M)
+    static constexpr int BK = 64;                  // keys per sub-tile
+    static constexpr int STAGES = 3;
+    using QT = TileShape<BQ, D>;
+    using KT = TileShape<BK, D>;
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t DO_OFF = Q_OFF + QT::BYTES;
+    static constexpr uint32_t K_OFF = DO_OFF + QT::BYTES;                // stages of K sub-tiles
+    static constexpr uint32_t V_OFF = K_OFF + STAGES * KT::BYTES;        // stages of V sub-tiles
+    static constexpr uint32_t BAR_OFF = V_OFF + STAGES * KT::BYTES;
+    // q_full, kv_full[S], kv_empty[S], sd_full[2], p_full[2], mma_done[2], drain
+    static constexpr int NBAR = 1 + 2 * STAGES + 6 + 1;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t SMEM_BYTES = (MISC_OFF + 16 + 1024 > 120u * 1024u ? MISC_OFF + 16 + 1024 : 120u * 1024u);
+    // TMEM: S_t [128t, 128t+64), dP_t [128t+64, 128t+128), dQ [256, 256+D)
+    static constexpr uint32_t DQ_COL = 256;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    fa_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                        const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ,
+                        int Nq, int Nk, int BH, int num_q_tiles, float scale, float scale_log2, uint32_t wait_limit) {
+    using C = DqCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int item = blockIdx.x;
+    const int qt = num_q_tiles - 1 - item / BH;
+    const int bh = item % BH;
+    const int q0 = qt * C::BQ;
+    const int kend = CAUSAL ? min(Nk, q0 + C::BQ) : Nk;
+    const int n = (kend + C::BK - 1) / C::BK;
+    const int nqp = padded_rows(Nq);
+
+    auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
+    const uint32_t q_full = bar(0);
+    auto kv_full = [&](int s) { return bar(1 + s); };
+    auto kv_empty = [&](int s) { return bar(1 + C::STAGES + s); };
+    auto sd_full = [&](int t) { return bar(1 + 2 * C::STAGES + t); };
+    auto p_full = [&](int t) { return bar(3 + 2 * C::STAGES + t); };
+    auto mma_done = [&](int t) { return bar(5 + 2 * C::STAGES + t); };
+    const uint32_t drain = bar(7 + 2 * C::STAGES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(q_full, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            tc::mbar_init(kv_full(s), 1);
+            tc::mbar_init(kv_empty(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            tc::mbar_init(sd_full(t), 1);
+            tc::mbar_init(p_full(t), 128);
+            tc::mbar_init(mma_done(t), 1);
+        }
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const tc::Waiter W{abort_flag, &g_fa_bwd_status, wait_limit, 4u};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmK);
+            tc::tma_prefetch_desc(&tmV);
+            tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
+            for (int c = 0; c < D / 64; ++c) {
+                tc::tma_load_3d(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh);
+                tc::tma_load_3d(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh);
+            }
+            int issued = 0;
+            for (int j = 0; j < n; ++j) {
+                const int s = j % C::STAGES;
+                if (!W.wait(kv_empty(s), ((j / C::STAGES) & 1) ^ 1u)) break;
+                tc::mbar_arrive_expect_tx(kv_full(s), 2 * C::KT::BYTES);
+                for (int c = 0; c < D / 64; ++c) {
+                    tc::tma_load_3d(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
+                                    j * C::BK, bh);
+                    tc::tma_load_3d(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
+                                    j * C::BK, bh);
+                }
+                issued = j + 1;
+            }
+            if (*abort_flag) {
+                for (int j = issued - 1; j >= 0 && j >= issued - C::STAGES; --j) {
+                    const int s = j % C::STAGES;
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full(s), (j / C::STAGES) & 1); ++i) {
+                    }
+                }
+                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BK, false, false);
+            constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
+            bool ok = W.wait(q_full, 0);
+            auto grads = [&](int j) -> bool {   // dQ += dS K_j
+                const int s = j % C::STAGES, t = j & 1, k = j >> 1;
+                if (!W.wait(p_full(t), k & 1)) return false;
+                tc::fence_after_sync();
+                const uint32_t kb = base + C::K_OFF + s * C::KT::BYTES;
+#pragma unroll
+                for (int kk = 0; kk < C::BK / 16; ++kk)
+                    tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 64 + kk * 8, mnmajor_desc<C::BK>(kb, kk), idesc_g,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(mma_done(t));
+                tc::mma_commit(kv_empty(s));
+                return true;
+            };
+            for (int j = 0; ok && j < n; ++j) {
+                const int s = j % C::STAGES, t = j & 1;
+                if (!(ok = W.wait(kv_full(s), (j / C::STAGES) & 1))) break;
+                const uint32_t kb = base + C::K_OFF + s * C::KT::BYTES;
+                const uint32_t vb = base + C::V_OFF + s * C::KT::BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)   // S = Q K^T
+                    tc::mma_ss(tmem + 128 * t, kmajor_desc<C::BQ>(base + C::Q_OFF, kk), kmajor_desc<C::BK>(kb, kk),
+                               idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)   // dP = dO V^T
+                    tc::mma_ss(tmem + 128 * t + 64, kmajor_desc<C::BQ>(base + C::DO_OFF, kk),
+                               kmajor_desc<C::BK>(vb, kk), idesc_s, kk > 0 ? 1u : 0u);
+                tc::mma_commit(sd_full(t));
+                if (j >= 1) ok = grads(j - 1);
+            }
+            if (ok) ok = grads(n - 1);
+            if (!ok) {
+                tc::mma_commit(drain);
+                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        const int t = (warp - 4) >> 2;
+        const int r = ((warp & 3) << 5) + lane;
+        const int row = q0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        const uint32_t tS = tmem + lane_base + 128 * t;
+        const uint32_t tP = tS + 64;
+        const float lrow = Lp[(size_t)bh * nqp + row];      // +inf on padding rows
+        const float drow = Dp[(size_t)bh * nqp + row];
+        const int nt = (n - t + 1) >> 1;
+        for (int k = 0; k < nt; ++k) {
+            const int j = 2 * k + t;
+            const int kb0 = j * C::BK;
+            bool ok = W.wait(sd_full(t), k & 1);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            uint32_t sv[2][32], dv[2][32];
+            tmem_ld_x32(tS, sv[0]);
+            tmem_ld_x32(tS + 32, sv[1]);
+            tmem_ld_x32(tP, dv[0]);
+            tmem_ld_x32(tP + 32, dv[1]);
+            tc::tmem_ld_wait();
+            reg_fence_x32(sv[0]);
+            reg_fence_x32(sv[1]);
+            reg_fence_x32(dv[0]);
+            reg_fence_x32(dv[1]);
+            const bool need_mask = (CAUSAL && kb0 + C::BK - 1 > q0) || (kb0 + C::BK > Nk);
+            uint32_t dsp[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float g2[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = 2 * i + h;
+                    float p = exp2f(fmaf(__uint_as_float(sv[c >> 5][c & 31]), scale_log2, -lrow));
+                    if (need_mask && (kb0 + c >= Nk || (CAUSAL && kb0 + c > row))) p = 0.f;
+                    g2[h] = p * (__uint_as_float(dv[c >> 5][c & 31]) - drow);
+                }
+                dsp[i] = tc::pack_bf16(g2[0], g2[1]);
+            }
+            tmem_st_x32(tP, dsp);
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            tc::mbar_arrive(p_full(t));
+        }
+        tc::named_bar_sync(1, 256);
+        bool fine = !*abort_flag;
+        const int n0 = (n + 1) >> 1, n1 = n >> 1;
+        if (fine) fine = W.wait(mma_done(0), (n0 - 1) & 1);
+        if (fine && n1 > 0) fine = W.wait(mma_done(1), (n1 - 1) & 1);
+        if (__all_sync(0xffffffffu, fine)) {
+            tc::fence_after_sync();
+            __nv_bfloat16 *dst = dQ + ((size_t)bh * Nq + row) * D;
+            const uint32_t tA = tmem + lane_base + C::DQ_COL;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                const int col = t * (D / 2) + 32 * c;
+                uint32_t a[32];
+                tmem_ld_x32(tA + col, a);
+                tc::tmem_ld_wait();
+                reg_fence_x32(a);
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * scale, __uint_as_float(a[2 * i + 1]) * scale);
+                if (row < Nq) {
+                    uint4 *o = reinterpret_cast<uint4 *>(dst + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+template <typename Kern>
+cudaError_t set_smem(Kern k, uint32_t bytes) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+struct Maps {
+    CUtensorMap q, k, v, dO;
+};
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dkdv(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dK, void *dV,
+                        cudaStream_t st) {
+    using C = DkdvCfg<D>;
+    auto kern = fa_bwd_dkdv_tc_kernel<D, CAUSAL>;
+    cudaError_t e = set_smem(kern, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int kt = (p.Nk + C::BK - 1) / C::BK;
+    const long long grid = (long long)kt * p.BH;
+    kern<<<(unsigned)grid, NTHREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, m.dO, Lp, Dp,
+                                                            static_cast<__nv_bfloat16 *>(dK),
+                                                            static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt,
+                                                            p.scale, p.scale * kLog2e, p.wait_limit);
+    return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dq(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dQ,
+                      cudaStream_t st) {
+    using C = DqCfg<D>;
+    auto kern = fa_bwd_dq_tc_kernel<D, CAUSAL>;
+    cudaError_t e = set_smem(kern, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int qt = (p.Nq + C::BQ - 1) / C::BQ;
+    const long long grid = (long long)qt * p.BH;
+    kern<<<(unsigned)grid, NTHREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, m.dO, Lp, Dp,
+                                                            static_cast<__nv_bfloat16 *>(dQ), p.Nq, p.Nk, p.BH, qt,
+                                                            p.scale, p.scale * kLog2e, p.wait_limit);
+    return cudaGetLastError();
+}
+
+bool make_maps(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO, int q_rows,
+               int k_rows, Maps *m) {
+    return tc_make_map_3d(&m->q, Q, p.BH, p.Nq, p.d, q_rows) && tc_make_map_3d(&m->dO, dO, p.BH, p.Nq, p.d, q_rows) &&
+           tc_make_map_3d(&m->k, K, p.BH, p.Nk, p.d, k_rows) && tc_make_map_3d(&m->v, V, p.BH, p.Nk, p.d, k_rows);
+}
+
+}  // namespace
+
+bool tc_bwd_supported(const FaProblem &p) {
+    return p.dtype == FA_DTYPE_BF16 && (p.d == 64 || p.d == 128) && p.Nq >= 128 && p.Nk >= 128 && p.BH >= 1;
+}
+
+size_t tc_bwd_ld_rows(const FaProblem &p) { return (size_t)p.BH * padded_rows(p.Nq); }
+
+cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO, const float *L, float *Dp,
+                              float *Lp, cudaStream_t st) {
+    const long long rows = (long long)p.BH * padded_rows(p.Nq);
+    if (rows == 0) return cudaSuccess;
+    fa_bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(O),
+                                                                   static_cast<const __nv_bfloat16 *>(dO), L, Dp, Lp,
+                                                                   p.BH, p.Nq, p.d);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                        const float *Lp, const float *Dp, void *dK, void *dV, cudaStream_t st) {
+    Maps m;
+    if (!make_maps(p, Q, K, V, dO, 64, 128, &m)) return cudaErrorInvalidValue;
+    if (p.d == 128) return p.causal ? launch_dkdv<128, true>(p, m, Lp, Dp, dK, dV, st)
+                                    : launch_dkdv<128, false>(p, m, Lp, Dp, dK, dV, st);
+    return p.causal ? launch_dkdv<64, true>(p, m, Lp, Dp, dK, dV, st) : launch_dkdv<64, false>(p, m, Lp, Dp, dK, dV, st);
+}
+
+cudaError_t tc_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                      const float *Lp, const float *Dp, void *dQ, cudaStream_t st) {
+    Maps m;
+    if (!make_maps(p, Q, K, V, dO, 128, 64, &m)) return cudaErrorInvalidValue;
+    if (p.d == 128) return p.causal ? launch_dq<128, true>(p, m, Lp, Dp, dQ, st) : launch_dq<128, false>(p, m, Lp, Dp, dQ, st);
+    return p.causal ? launch_dq<64, true>(p, m, Lp, Dp, dQ, st) : launch_dq<64, false>(p, m, Lp, Dp, dQ, st);
+}
+
 cudaError_t tc_bwd_read_status(unsigned *out, cudaStream_t st) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fa_bwd_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     return e;
 }
+
 cudaError_t tc_bwd_reset_status(cudaStream_t st) {
     static const unsigned zero = 0;
     return cudaMemcpyToSymbolAsync(g_fa_bwd_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, st);
