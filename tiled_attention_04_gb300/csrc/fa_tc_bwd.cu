@@ -8,9 +8,9 @@
 // ever adds into another's output (§1.3.3, "split the backward pass into two
 // passes, one for dQ and one for dK and dV"):
 //
-//   preprocess   D and a log2-scaled copy of L, padded per batch*head to a
-//                multiple of 128 rows (padding rows get L = +inf, so their P
-//                is exactly zero), in the caller's workspace;
+//   preprocess   -D and -L*log2(e), padded per batch*head to a multiple of
+//                128 rows (padding rows get -L = -inf, so their P is exactly
+//                zero), in the caller's workspace;
 //   dK/dV pass   one CTA per 128-key tile; loops over 64-query sub-tiles,
 //                recomputing S^T = K Q^T and dP^T = V dO^T in TMEM,
 //                P^T and dS^T (bf16) written back into TMEM, then
@@ -46,28 +46,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 __host__ __device__ inline int padded_rows(int n) { return (n + 127) / 128 * 128; }
 
 // ------------------------------------------------------------------ preprocess
-// one warp per query row: D = rowsum(dO * O) (fp32), Lp = L * log2(e); padding rows: D = 0, Lp = +inf
+// d/8 threads per query row (each reads 16 bytes of O and of dO, so a row is
+// one contiguous, coalesced segment), rows reduced with shuffles.  Writes the
+// negated row constants the passes add: Dn = -rowsum(dO * O), Ln = -L*log2(e);
+// padding rows: Dn = 0, Ln = -inf (so their P = 2^(-inf) = 0).
+template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
                                                          const __nv_bfloat16 *__restrict__ dO,
                                                          const float *__restrict__ L, float *__restrict__ Dp,
-                                                         float *__restrict__ Lp, int BH, int Nq, int d) {
+                                                         float *__restrict__ Lp, int BH, int Nq) {
+    constexpr int TPR = D / 8;                      // threads per row
     const int nqp = padded_rows(Nq);
-    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= (long long)BH * nqp) return;
-    const int bh = (int)(gw / nqp), q = (int)(gw % nqp);
-    if (q >= Nq) {
-        if (lane == 0) {
-            Dp[gw] = 0.f;
-            Lp[gw] = INFINITY;
-        }
-        return;
-    }
-    const size_t row = ((size_t)bh * Nq + q) * d;
+    const long long gr = ((long long)blockIdx.x * 256 + threadIdx.x) / TPR;
+    const int sub = threadIdx.x % TPR;
+    const bool live = gr < (long long)BH * nqp;
+    const int bh = live ? (int)(gr / nqp) : 0, q = live ? (int)(gr % nqp) : 0;
     float acc = 0.f;
-    for (int c = lane * 8; c < d; c += 256) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(O + row + c);
-        const uint4 b = *reinterpret_cast<const uint4 *>(dO + row + c);
+    if (live && q < Nq) {
+        const size_t off = ((size_t)bh * Nq + q) * D + sub * 8;
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(O + off));
+        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + off));
         const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
         const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
 #pragma unroll
@@ -78,10 +76,15 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__
         }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-        Dp[gw] = acc;
-        Lp[gw] = L[(size_t)bh * Nq + q] * kLog2e;
+    for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (live && sub == 0) {
+        if (q < Nq) {
+            Dp[gr] = -acc;
+            Lp[gr] = -L[(size_t)bh * Nq + q] * kLog2e;
+        } else {
+            Dp[gr] = 0.f;
+            Lp[gr] = -INFINITY;
+        }
     }
 }
 
@@ -190,6 +193,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const tc::Waiter W{abort_flag, &g_fa_bwd_status, wait_limit, 2u};
 
+    if (warp < 4) {
+    tc::regs_dec<56>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n > 0) {
@@ -277,7 +282,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        tc::regs_inc<224>();
         // ------------------------------------------------------------ element-wise warpgroups
         const int t = (warp - 4) >> 2;
         const int r = ((warp & 3) << 5) + lane;              // key row within the tile = TMEM lane
@@ -305,23 +312,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             reg_fence_x32(sv[1]);
             reg_fence_x32(dv[0]);
             reg_fence_x32(dv[1]);
-            const float *lds = reinterpret_cast<const float *>(sb + C::LD_OFF + s * 512);
+            const float *lds = reinterpret_cast<const float *>(sb + C::LD_OFF + s * 512);   // -L*log2e, -D
             const bool need_mask = CAUSAL && (k0 + 127 > q0);
+            const int first_visible = key - q0;      // query columns c < key - q0 cannot see this key
             uint32_t pp[32], dsp[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                float p2[2], g2[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = 2 * i + h;
-                    const float sval = __uint_as_float(sv[c >> 5][c & 31]);
-                    float p = exp2f(fmaf(sval, scale_log2, -lds[c]));
-                    if (need_mask && key > q0 + c) p = 0.f;
-                    p2[h] = p;
-                    g2[h] = p * (__uint_as_float(dv[c >> 5][c & 31]) - lds[64 + c]);
+                const float2 nl = *reinterpret_cast<const float2 *>(lds + 2 * i);
+                const float2 nd = *reinterpret_cast<const float2 *>(lds + 64 + 2 * i);
+                const int c = 2 * i;
+                float x0, x1, g0, g1;
+                tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
+                         scale_log2, scale_log2, nl.x, nl.y);
+                float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+                if (need_mask) {
+                    if (c < first_visible) p0 = 0.f;
+                    if (c + 1 < first_visible) p1 = 0.f;
                 }
-                pp[i] = tc::pack_bf16(p2[0], p2[1]);
-                dsp[i] = tc::pack_bf16(g2[0], g2[1]);
+                tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
+                         nd.x, nd.y);
+                tc::mul2(g0, g1, g0, g1, p0, p1);
+                pp[i] = tc::pack_bf16(p0, p1);
+                dsp[i] = tc::pack_bf16(g0, g1);
             }
             tmem_st_x32(tS, pp);
             tmem_st_x32(tP, dsp);
@@ -453,6 +465,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const tc::Waiter W{abort_flag, &g_fa_bwd_status, wait_limit, 4u};
 
+    if (warp < 4) {
+    tc::regs_dec<56>();
     if (warp == 0) {
         if (lane == 0) {
             tc::tma_prefetch_desc(&tmK);
@@ -526,15 +540,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        tc::regs_inc<224>();
         const int t = (warp - 4) >> 2;
         const int r = ((warp & 3) << 5) + lane;
         const int row = q0 + r;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
         const uint32_t tS = tmem + lane_base + 128 * t;
         const uint32_t tP = tS + 64;
-        const float lrow = Lp[(size_t)bh * nqp + row];      // +inf on padding rows
-        const float drow = Dp[(size_t)bh * nqp + row];
+        const float nlrow = Lp[(size_t)bh * nqp + row];     // -L*log2e (-inf on padding rows)
+        const float ndrow = Dp[(size_t)bh * nqp + row];     // -D
         const int nt = (n - t + 1) >> 1;
         for (int k = 0; k < nt; ++k) {
             const int j = 2 * k + t;
@@ -553,18 +569,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             reg_fence_x32(dv[0]);
             reg_fence_x32(dv[1]);
             const bool need_mask = (CAUSAL && kb0 + C::BK - 1 > q0) || (kb0 + C::BK > Nk);
+            const int lim = min(Nk - 1, CAUSAL ? row : Nk - 1) - kb0;   // last visible key column
             uint32_t dsp[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                float g2[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = 2 * i + h;
-                    float p = exp2f(fmaf(__uint_as_float(sv[c >> 5][c & 31]), scale_log2, -lrow));
-                    if (need_mask && (kb0 + c >= Nk || (CAUSAL && kb0 + c > row))) p = 0.f;
-                    g2[h] = p * (__uint_as_float(dv[c >> 5][c & 31]) - drow);
+                const int c = 2 * i;
+                float x0, x1, g0, g1;
+                tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
+                         scale_log2, scale_log2, nlrow, nlrow);
+                float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+                if (need_mask) {
+                    if (c > lim) p0 = 0.f;
+                    if (c + 1 > lim) p1 = 0.f;
                 }
-                dsp[i] = tc::pack_bf16(g2[0], g2[1]);
+                tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
+                         ndrow, ndrow);
+                tc::mul2(g0, g1, g0, g1, p0, p1);
+                dsp[i] = tc::pack_bf16(g0, g1);
             }
             tmem_st_x32(tP, dsp);
             tc::tmem_st_wait();
@@ -667,9 +688,12 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
                               float *Lp, cudaStream_t st) {
     const long long rows = (long long)p.BH * padded_rows(p.Nq);
     if (rows == 0) return cudaSuccess;
-    fa_bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(O),
-                                                                   static_cast<const __nv_bfloat16 *>(dO), L, Dp, Lp,
-                                                                   p.BH, p.Nq, p.d);
+    const auto *o = static_cast<const __nv_bfloat16 *>(O);
+    const auto *g = static_cast<const __nv_bfloat16 *>(dO);
+    if (p.d == 128)
+        fa_bwd_pre_kernel<128><<<(unsigned)((rows * 16 + 255) / 256), 256, 0, st>>>(o, g, L, Dp, Lp, p.BH, p.Nq);
+    else
+        fa_bwd_pre_kernel<64><<<(unsigned)((rows * 8 + 255) / 256), 256, 0, st>>>(o, g, L, Dp, Lp, p.BH, p.Nq);
     return cudaGetLastError();
 }
 

@@ -127,7 +127,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const tc::Waiter W{abort_flag, &g_fa_fwd_status, wait_limit, 1u};
+    // registers: warps 0-3 (producer, MMA issuer, two idle) give theirs to the softmax warpgroups
 
+    // registers: warpgroup 0 (producer, MMA issuer, two idle warps) hands its share
+    // to the two softmax warpgroups; each warpgroup changes its budget in one place
+    if (warp < 4) {
+    tc::regs_dec<56>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -212,7 +217,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        tc::regs_inc<224>();
         // ------------------------------------------------------------ softmax warpgroups
         const int t = (warp - 4) >> 2;
         const int r = ((warp & 3) << 5) + lane;            // row within the tile = TMEM lane
@@ -239,33 +246,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
             const bool need_mask = (CAUSAL && k0 + BN - 1 > q0) || (k0 + BN > Nk);
             if (need_mask) {
+                const int lim = min(Nk - 1, CAUSAL ? row : Nk - 1) - k0;   // last visible column
 #pragma unroll
-                for (int i = 0; i < 128; ++i) {
-                    const int kj = k0 + i;
-                    if (kj >= Nk || (CAUSAL && kj > row)) s[i] = -INFINITY;
-                }
+                for (int i = 0; i < 128; ++i)
+                    if (i > lim) s[i] = -INFINITY;
             }
-            float mx = s[0];
+            float mx = tc::fmax3(s[0], s[1], s[2]);
 #pragma unroll
-            for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+            for (int i = 3; i < 127; i += 2) mx = tc::fmax3(mx, s[i], s[i + 1]);
+            mx = fmaxf(mx, s[127]);
             const float m_cand = fmaxf(m, mx * scale_log2);
             const bool rescale = m_cand > m + kRescaleThreshold;
             float alpha = 1.f;
             if (rescale) {
-                alpha = exp2f(m - m_cand);
+                alpha = tc::ex2(m - m_cand);
                 m = m_cand;
             }
             l *= alpha;
+            const float nm = -m;
             uint32_t p[64];
-            float rs = 0.f;
+            float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-                const float e0 = exp2f(fmaf(s[2 * i], scale_log2, -m));
-                const float e1 = exp2f(fmaf(s[2 * i + 1], scale_log2, -m));
-                rs += e0 + e1;
+                float x0, x1;
+                tc::fma2(x0, x1, s[2 * i], s[2 * i + 1], scale_log2, scale_log2, nm, nm);
+                const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
+                tc::add2(rs0, rs1, rs0, rs1, e0, e1);
                 p[i] = tc::pack_bf16(e0, e1);
             }
-            l += rs;
+            l += rs0 + rs1;
             tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
             tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
             if (k > 0 && __any_sync(0xffffffffu, rescale)) {
