@@ -116,7 +116,9 @@ template <int D>
 struct DkdvCfg {
     static constexpr int BK = 128;                 // keys per CTA (MMA M)
     static constexpr int BQ = 64;                  // queries per sub-tile (MMA N of S^T, K of dV/dK)
-    static constexpr int STAGES = 3;
+    // deep ring: a stage is refilled only after its sub-tile's dV/dK MMAs finish, and
+    // an L2-resident TMA reload takes ~2000 cycles, several sub-tiles' worth of MMA time
+    static constexpr int STAGES = D == 128 ? 4 : 8;
     using KT = TileShape<BK, D>;
     using QT = TileShape<BQ, D>;
     static constexpr uint32_t K_OFF = 0;
@@ -129,6 +131,7 @@ struct DkdvCfg {
     static constexpr int NBAR = 1 + 2 * STAGES + 6 + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = (MISC_OFF + 16 + 1024 > 120u * 1024u ? MISC_OFF + 16 + 1024 : 120u * 1024u);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     // TMEM: S^T_t [128t, 128t+64), dP^T_t [128t+64, 128t+128), dV [256, 256+D), dK [256+D, 256+2D)
     static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
 };
@@ -246,14 +249,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t qb = base + C::Q_OFF + s * C::QT::BYTES;
                 const uint32_t ob = base + C::DO_OFF + s * C::QT::BYTES;
 #pragma unroll
-                for (int kk = 0; kk < C::BQ / 16; ++kk) {
-                    tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + kk * 8, mnmajor_desc<C::BQ>(ob, kk), idesc_g,
-                               (it > 0 || kk > 0) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < C::BQ / 16; ++kk) {
-                    tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + kk * 8, mnmajor_desc<C::BQ>(qb, kk),
-                               idesc_g, (it > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < C::BQ / 16; ++kk) {   // two independent chains, interleaved
+                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + kk * 8, mnmajor_desc<C::BQ>(ob, kk), idesc_g, acc);
+                    tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + kk * 8, mnmajor_desc<C::BQ>(qb, kk), idesc_g,
+                               acc);
                 }
                 tc::mma_commit(mma_done(t));
                 tc::mma_commit(q_empty(s));
@@ -265,13 +265,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t qb = base + C::Q_OFF + s * C::QT::BYTES;
                 const uint32_t ob = base + C::DO_OFF + s * C::QT::BYTES;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)   // S^T = K Q^T
+                for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q^T and dP^T = V dO^T, interleaved
                     tc::mma_ss(tmem + 128 * t, kmajor_desc<C::BK>(base + C::K_OFF, kk), kmajor_desc<C::BQ>(qb, kk),
                                idesc_s, kk > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)   // dP^T = V dO^T
                     tc::mma_ss(tmem + 128 * t + 64, kmajor_desc<C::BK>(base + C::V_OFF, kk),
                                kmajor_desc<C::BQ>(ob, kk), idesc_s, kk > 0 ? 1u : 0u);
+                }
                 tc::mma_commit(sd_full(t));
                 if (it >= 1) ok = grads(it - 1);
             }
@@ -392,7 +391,7 @@ template <int D>
 struct DqCfg {
     static constexpr int BQ = 128;                 // queries per CTA (MMA M)
     static constexpr int BK = 64;                  // keys per sub-tile
-    static constexpr int STAGES = 3;
+    static constexpr int STAGES = D == 128 ? 4 : 8;    // see DkdvCfg
     using QT = TileShape<BQ, D>;
     using KT = TileShape<BK, D>;
     static constexpr uint32_t Q_OFF = 0;
@@ -404,6 +403,7 @@ struct DqCfg {
     static constexpr int NBAR = 1 + 2 * STAGES + 6 + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = (MISC_OFF + 16 + 1024 > 120u * 1024u ? MISC_OFF + 16 + 1024 : 120u * 1024u);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     // TMEM: S_t [128t, 128t+64), dP_t [128t+64, 128t+128), dQ [256, 256+D)
     static constexpr uint32_t DQ_COL = 256;
 };
@@ -523,13 +523,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t kb = base + C::K_OFF + s * C::KT::BYTES;
                 const uint32_t vb = base + C::V_OFF + s * C::KT::BYTES;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)   // S = Q K^T
+                for (int kk = 0; kk < D / 16; ++kk) {   // S = Q K^T and dP = dO V^T, interleaved
                     tc::mma_ss(tmem + 128 * t, kmajor_desc<C::BQ>(base + C::Q_OFF, kk), kmajor_desc<C::BK>(kb, kk),
                                idesc_s, kk > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)   // dP = dO V^T
                     tc::mma_ss(tmem + 128 * t + 64, kmajor_desc<C::BQ>(base + C::DO_OFF, kk),
                                kmajor_desc<C::BK>(vb, kk), idesc_s, kk > 0 ? 1u : 0u);
+                }
                 tc::mma_commit(sd_full(t));
                 if (j >= 1) ok = grads(j - 1);
             }

@@ -50,20 +50,25 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int D>
 struct FwdCfg {
-    static constexpr int STAGES = D == 128 ? 2 : 3;
+    // separate K and V rings: a K slot frees when its S MMAs finish, a V slot
+    // when its PV MMAs finish; K runs one tile ahead of V.  Deep enough to
+    // cover an L2-resident TMA reload (~2000 cycles).
+    static constexpr int KST = D == 128 ? 3 : 6;
+    static constexpr int VST = D == 128 ? 2 : 4;
     static constexpr int CHUNKS = D / 64;                      // 128-byte swizzle chunks per row
     static constexpr uint32_t CHUNK_BYTES = 128u * 128u;       // 128 rows x 128 bytes
     static constexpr uint32_t TILE_BYTES = CHUNKS * CHUNK_BYTES;
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t K_OFF = Q_OFF + TILE_BYTES;
-    static constexpr uint32_t V_OFF = K_OFF + STAGES * TILE_BYTES;
-    static constexpr uint32_t BAR_OFF = V_OFF + STAGES * TILE_BYTES;
-    static constexpr int NBAR = 1 + 3 * STAGES + 6 + 1;
+    static constexpr uint32_t V_OFF = K_OFF + KST * TILE_BYTES;
+    static constexpr uint32_t BAR_OFF = V_OFF + VST * TILE_BYTES;
+    static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 6 + 1;
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t MISC_OFF = STAT_OFF + 4 * 128 * 4;
     static constexpr uint32_t USED = MISC_OFF + 16;
     // at least ~116 KB so that one CTA (which owns all 512 TMEM columns) runs per SM
     static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u ? USED + 1024 : 120u * 1024u);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
 };
 
@@ -90,13 +95,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
     const uint32_t q_full = bar(0);
+    constexpr int RB = 1 + 2 * C::KST + 2 * C::VST;          // first non-ring barrier
     auto k_full = [&](int s) { return bar(1 + s); };
-    auto v_full = [&](int s) { return bar(1 + C::STAGES + s); };
-    auto kv_empty = [&](int s) { return bar(1 + 2 * C::STAGES + s); };
-    auto s_full = [&](int t) { return bar(1 + 3 * C::STAGES + t); };
-    auto p_full = [&](int t) { return bar(3 + 3 * C::STAGES + t); };
-    auto o_done = [&](int t) { return bar(5 + 3 * C::STAGES + t); };
-    const uint32_t drain = bar(7 + 3 * C::STAGES);
+    auto k_empty = [&](int s) { return bar(1 + C::KST + s); };
+    auto v_full = [&](int s) { return bar(1 + 2 * C::KST + s); };
+    auto v_empty = [&](int s) { return bar(1 + 2 * C::KST + C::VST + s); };
+    auto s_full = [&](int t) { return bar(RB + t); };
+    auto p_full = [&](int t) { return bar(RB + 2 + t); };
+    auto o_done = [&](int t) { return bar(RB + 4 + t); };
+    const uint32_t drain = bar(RB + 6);
     float *m_sm = reinterpret_cast<float *>(sb + C::STAT_OFF);
     float *l_sm = m_sm + 256;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
@@ -104,10 +111,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (threadIdx.x == 0) {
         tc::mbar_init(q_full, 1);
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < C::KST; ++s) {
             tc::mbar_init(k_full(s), 1);
+            tc::mbar_init(k_empty(s), 1);
+        }
+        for (int s = 0; s < C::VST; ++s) {
             tc::mbar_init(v_full(s), 1);
-            tc::mbar_init(kv_empty(s), 1);
+            tc::mbar_init(v_empty(s), 1);
         }
         for (int t = 0; t < 2; ++t) {
             tc::mbar_init(s_full(t), 1);
@@ -142,31 +152,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c)
                 tc::tma_load_3d(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh);
-            int issued = 0;
-            for (int j = 0; j < n; ++j) {
-                const int s = j % C::STAGES;
-                const uint32_t ph = (j / C::STAGES) & 1;
-                if (!W.wait(kv_empty(s), ph ^ 1u)) break;
-                tc::mbar_arrive_expect_tx(k_full(s), C::TILE_BYTES);
+            int k_issued = 0, v_issued = 0;
+            auto load = [&](const CUtensorMap *m, uint32_t ring, int st, int j, uint32_t full, uint32_t empty) {
+                if (!W.wait(empty, ((j / st) & 1) ^ 1u)) return false;
+                tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
-                    tc::tma_load_3d(base + C::K_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK, k_full(s),
-                                    c * 64, j * BN, bh);
-                tc::mbar_arrive_expect_tx(v_full(s), C::TILE_BYTES);
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    tc::tma_load_3d(base + C::V_OFF + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV, v_full(s),
-                                    c * 64, j * BN, bh);
-                issued = j + 1;
+                    tc::tma_load_3d(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64, j * BN, bh);
+                return true;
+            };
+            // order K_0, K_1, V_0, K_2, V_1, ...: the MMA warp uses K_{j+1} before V_j
+            for (int j = 0; j <= n; ++j) {
+                if (j < n) {
+                    if (!load(&tmK, base + C::K_OFF, C::KST, j, k_full(j % C::KST), k_empty(j % C::KST))) break;
+                    k_issued = j + 1;
+                }
+                if (j >= 1) {
+                    const int v = j - 1;
+                    if (!load(&tmV, base + C::V_OFF, C::VST, v, v_full(v % C::VST), v_empty(v % C::VST))) break;
+                    v_issued = v + 1;
+                }
             }
             if (*abort_flag) {
                 // let the copies already in flight land before the CTA exits
-                for (int j = issued - 1; j >= 0 && j >= issued - C::STAGES; --j) {
-                    const int s = j % C::STAGES;
-                    const uint32_t ph = (j / C::STAGES) & 1;
-                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(k_full(s), ph); ++i) {
+                for (int j = k_issued - 1; j >= 0 && j >= k_issued - C::KST; --j)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(k_full(j % C::KST), (j / C::KST) & 1); ++i) {
                     }
-                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(v_full(s), ph); ++i) {
+                for (int j = v_issued - 1; j >= 0 && j >= v_issued - C::VST; --j)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(v_full(j % C::VST), (j / C::VST) & 1); ++i) {
                     }
-                }
                 for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
                 }
             }
@@ -178,11 +191,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             constexpr uint32_t idesc_o = tc::idesc_bf16(BM, D, false, true);
             bool ok = W.wait(q_full, 0);
             auto pv = [&](int j) -> bool {
-                const int s = j % C::STAGES, t = j & 1, k = j >> 1;
-                const uint32_t ph = (j / C::STAGES) & 1;
+                const int s = j % C::VST, t = j & 1, k = j >> 1;
                 if (!W.wait(p_full(t), k & 1)) return false;
                 tc::fence_after_sync();
-                if (!W.wait(v_full(s), ph)) return false;
+                if (!W.wait(v_full(s), (j / C::VST) & 1)) return false;
                 const uint32_t vbase = base + C::V_OFF + s * C::TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
@@ -191,13 +203,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                (k > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::mma_commit(o_done(t));
-                tc::mma_commit(kv_empty(s));
+                tc::mma_commit(v_empty(s));
                 return true;
             };
             for (int j = 0; ok && j < n; ++j) {
-                const int s = j % C::STAGES, t = j & 1;
-                const uint32_t ph = (j / C::STAGES) & 1;
-                if (!(ok = W.wait(k_full(s), ph))) break;
+                const int s = j % C::KST, t = j & 1;
+                if (!(ok = W.wait(k_full(s), (j / C::KST) & 1))) break;
                 const uint32_t kbase = base + C::K_OFF + s * C::TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -207,6 +218,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tc::mma_ss(tmem + C::S_COL0 + t * 128, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(s_full(t));
+                tc::mma_commit(k_empty(s));
                 if (j >= 1) ok = pv(j - 1);
             }
             if (ok) ok = pv(n - 1);
