@@ -128,6 +128,38 @@ FA_API fa_status fa_bwd_dq(const void *Q, const void *K, const void *V, const vo
                     void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * fa_bwd without a caller-supplied workspace.  (No counterpart in the method's
+ * description: this exists for callers, not for the algorithm.)
+ *
+ * For callers that cannot allocate device memory -- code that only receives
+ * raw pointers from a host framework and has no allocator of its own, or code
+ * that must not call cudaMalloc/cudaFree because those calls can synchronise
+ * the device and stall unrelated work.  The scratch lives in a fixed array of
+ * FA_NOALLOC_SCRATCH_BYTES of device global memory inside the library, present
+ * on every GPU that loads the library until the process exits.  The caller
+ * still owns and passes every input and output.  Same arguments, layout and
+ * results as fa_bwd.
+ *
+ *  - Shapes needing more than FA_NOALLOC_SCRATCH_BYTES of workspace (see
+ *    fa_bwd_workspace_size) return FA_ERR_WORKSPACE and launch nothing; 8 MiB
+ *    covers about one million query rows (B*H*Nq).
+ *  - Every call shares the one array: calls whose GPU work overlaps (other
+ *    streams, other host threads) race on it.  Serialise them.
+ *  - The array's previous contents never matter: each call writes every
+ *    scratch word before reading it.
+ *  - The first call on each device looks up the array's address with that
+ *    device current; make it before any stream capture starts.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+FA_API fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                                const float *L, void *dQ, void *dK, void *dV,
+                                int B, int H, int Nq, int Nk, int d, float scale, int is_causal, fa_dtype dtype,
+                                fa_stream_t stream);
+/* FA_NOALLOC_SCRATCH_BYTES as compiled into the library. */
+FA_API size_t fa_noalloc_scratch_bytes(void);
+
+/*
  * Name of the kernel family fa_fwd / fa_bwd would use for these arguments:
  * "tc" (tcgen05 tensor-core kernels) or "simt" (fp32 CUDA-core kernels), or
  * NULL for unsupported arguments.  Host-only; launches nothing.

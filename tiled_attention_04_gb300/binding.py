@@ -24,8 +24,8 @@ FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
 
 # every function include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq",
-           "fa_path_name", "fa_get_device_status", "fa_reset_device_status", "fa_set_wait_limit",
-           "fa_status_string")
+           "fa_bwd_noalloc", "fa_noalloc_scratch_bytes", "fa_path_name", "fa_get_device_status",
+           "fa_reset_device_status", "fa_set_wait_limit", "fa_status_string")
 
 _lib = None
 
@@ -52,6 +52,10 @@ def lib() -> ctypes.CDLL:
     L.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp]
     L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
+    L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    L.fa_bwd_noalloc.restype = ctypes.c_int
+    L.fa_noalloc_scratch_bytes.argtypes = []
+    L.fa_noalloc_scratch_bytes.restype = sz
     L.fa_path_name.argtypes = [i, i, i, i, i]
     L.fa_path_name.restype = ctypes.c_char_p
     L.fa_get_device_status.argtypes = [vp]
@@ -168,6 +172,23 @@ def fa_bwd(Q, K, V, O, dO, L, is_causal=False, scale=None, dQ=None, dK=None, dV=
     check(lib().fa_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV),
                        B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _ptr(ws), ws.numel(),
                        _stream(stream)), "fa_bwd")
+    return dQ, dK, dV
+
+
+def fa_bwd_noalloc(Q, K, V, O, dO, L, is_causal=False, scale=None, dQ=None, dK=None, dV=None, stream=None):
+    """fa_bwd with the library's own fixed scratch array instead of a workspace (see include/fa.h)."""
+    torch = _torch()
+    _check_inputs(Q, K, V, O, dO)
+    B, H = _bh(Q)
+    Nq, d = Q.shape[-2], Q.shape[-1]
+    Nk = K.shape[-2]
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    check(lib().fa_bwd_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK),
+                               _ptr(dV), B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _stream(stream)),
+          "fa_bwd_noalloc")
     return dQ, dK, dV
 
 

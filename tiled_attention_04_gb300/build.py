@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libfa.so")
 
-SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu"]
+SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu", "fa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,81 @@
+// fa_bwd_noalloc: the backward pass with its scratch memory inside the library.
+//
+// fa_bwd needs a caller-owned device workspace (per query row: D = rowsum(dO*O)
+// and, on the tensor-core path, a copy of L).  Some callers cannot provide
+// one: code that only receives raw pointers from a host framework and has no
+// allocator of its own, or code that must not call cudaMalloc/cudaFree because
+// those calls can synchronise the whole device and stall unrelated streams.
+// For them this entry point uses a fixed-size array in device global memory
+// that lives in this translation unit.  The array exists on every GPU that
+// loads the library and stays allocated until the process exits.
+//
+// Rules for callers:
+//  * the scratch is shared by every call: calls whose GPU work overlaps (two
+//    streams, or two host threads) race on it and give wrong results; order
+//    them on one stream or serialise them;
+//  * nothing in the scratch needs to start at zero: each call writes every
+//    scratch word it later reads, so the previous call's leftovers are harmless;
+//  * the first call on a device looks up the array's device address (with that
+//    device current) and caches it; make that first call before any stream
+//    capture begins;
+//  * shapes whose workspace would exceed FA_NOALLOC_SCRATCH_BYTES are refused
+//    with FA_ERR_WORKSPACE before anything is launched.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// device address of the scratch array on the current device (looked up once per device)
+fa_status scratch_for_current_device(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return FA_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return FA_ERR_LAUNCH;
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_noalloc_scratch_bytes(void) { return FA_NOALLOC_SCRATCH_BYTES; }
+
+fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *L,
+                         void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nk, int d, float scale,
+                         int is_causal, fa_dtype dtype, fa_stream_t stream) {
+    const size_t need = fa_bwd_workspace_size(B, H, Nq, Nk, d, is_causal, dtype);
+    if (need == 0) {
+        // unsupported arguments: let fa_bwd name the problem (it launches nothing)
+        return fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, nullptr, 0, stream);
+    }
+    if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    const fa_status s = scratch_for_current_device(&scratch);
+    if (s != FA_OK) return s;
+    return fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, scratch,
+                  FA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+}  // extern "C"
