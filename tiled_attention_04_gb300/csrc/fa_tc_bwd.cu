@@ -238,48 +238,60 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n > 0) {
+        // whole warp in the loop (uniform descriptors), one elected lane issues
+        const bool leader = tc::elect_one();
+        if (n > 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BQ, false, false);
             constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
-            bool ok = W.wait(kv_full, 0);
+            const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);     // A of S^T, K-major
+            const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, 16, 1024);     // A of dP^T
+            const uint64_t qk = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);     // B of S^T, K-major, stage 0
+            const uint64_t ok_ = tc::sdesc_sw128(base + C::DO_OFF, 16, 1024);   // B of dP^T
+            const uint64_t qm = tc::sdesc_sw128(base + C::Q_OFF, C::QT::CHUNK, 1024);    // B of dK, MN-major
+            const uint64_t om = tc::sdesc_sw128(base + C::DO_OFF, C::QT::CHUNK, 1024);   // B of dV, MN-major
+            bool ok = __all_sync(0xffffffffu, W.wait(kv_full, 0));
             auto grads = [&](int it) -> bool {   // dV += P^T dO, dK += dS^T Q for sub-tile `it`
                 const int s = it % C::STAGES, t = it & 1, k = it >> 1;
-                if (!W.wait(p_full(t), k & 1)) return false;
+                if (!__all_sync(0xffffffffu, W.wait(p_full(t), k & 1))) return false;
                 tc::fence_after_sync();
-                const uint32_t qb = base + C::Q_OFF + s * C::QT::BYTES;
-                const uint32_t ob = base + C::DO_OFF + s * C::QT::BYTES;
+                if (leader) {
+                    const uint32_t st = (s * C::QT::BYTES) >> 4;
 #pragma unroll
-                for (int kk = 0; kk < C::BQ / 16; ++kk) {   // two independent chains, interleaved
-                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + kk * 8, mnmajor_desc<C::BQ>(ob, kk), idesc_g, acc);
-                    tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + kk * 8, mnmajor_desc<C::BQ>(qb, kk), idesc_g,
-                               acc);
+                    for (int kk = 0; kk < C::BQ / 16; ++kk) {   // two independent chains, interleaved
+                        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                        tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + kk * 8, om + st + kk * 128, idesc_g, acc);
+                        tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + kk * 8, qm + st + kk * 128, idesc_g, acc);
+                    }
+                    tc::mma_commit(mma_done(t));
+                    tc::mma_commit(q_empty(s));
                 }
-                tc::mma_commit(mma_done(t));
-                tc::mma_commit(q_empty(s));
+                __syncwarp();
                 return true;
             };
             for (int it = 0; ok && it < n; ++it) {
                 const int s = it % C::STAGES, t = it & 1;
-                if (!(ok = W.wait(q_full(s), (it / C::STAGES) & 1))) break;
-                const uint32_t qb = base + C::Q_OFF + s * C::QT::BYTES;
-                const uint32_t ob = base + C::DO_OFF + s * C::QT::BYTES;
+                if (!(ok = __all_sync(0xffffffffu, W.wait(q_full(s), (it / C::STAGES) & 1)))) break;
+                if (leader) {
+                    const uint32_t st = (s * C::QT::BYTES) >> 4;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q^T and dP^T = V dO^T, interleaved
-                    tc::mma_ss(tmem + 128 * t, kmajor_desc<C::BK>(base + C::K_OFF, kk), kmajor_desc<C::BQ>(qb, kk),
-                               idesc_s, kk > 0 ? 1u : 0u);
-                    tc::mma_ss(tmem + 128 * t + 64, kmajor_desc<C::BK>(base + C::V_OFF, kk),
-                               kmajor_desc<C::BQ>(ob, kk), idesc_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q^T and dP^T = V dO^T, interleaved
+                        const uint32_t oa = ((kk >> 2) * C::KT::CHUNK + (kk & 3) * 32) >> 4;
+                        const uint32_t ob = ((kk >> 2) * C::QT::CHUNK + (kk & 3) * 32) >> 4;
+                        tc::mma_ss(tmem + 128 * t, kd + oa, qk + st + ob, idesc_s, kk > 0 ? 1u : 0u);
+                        tc::mma_ss(tmem + 128 * t + 64, vd + oa, ok_ + st + ob, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(sd_full(t));
                 }
-                tc::mma_commit(sd_full(t));
+                __syncwarp();
                 if (it >= 1) ok = grads(it - 1);
             }
             if (ok) ok = grads(n - 1);
-            if (!ok) {
+            if (!ok && leader) {
                 tc::mma_commit(drain);
                 for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
                 }
             }
+            __syncwarp();
         }
     }
     } else {
@@ -500,45 +512,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BK, false, false);
-            constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
-            bool ok = W.wait(q_full, 0);
-            auto grads = [&](int j) -> bool {   // dQ += dS K_j
-                const int s = j % C::STAGES, t = j & 1, k = j >> 1;
-                if (!W.wait(p_full(t), k & 1)) return false;
-                tc::fence_after_sync();
-                const uint32_t kb = base + C::K_OFF + s * C::KT::BYTES;
+        // whole warp in the loop (uniform descriptors), one elected lane issues
+        const bool leader = tc::elect_one();
+        constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BK, false, false);
+        constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
+        const uint64_t qd = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);      // A of S, K-major
+        const uint64_t od = tc::sdesc_sw128(base + C::DO_OFF, 16, 1024);     // A of dP
+        const uint64_t kk_ = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);    // B of S, K-major, stage 0
+        const uint64_t vk = tc::sdesc_sw128(base + C::V_OFF, 16, 1024);     // B of dP
+        const uint64_t km = tc::sdesc_sw128(base + C::K_OFF, C::KT::CHUNK, 1024);   // B of dQ, MN-major
+        bool ok = __all_sync(0xffffffffu, W.wait(q_full, 0));
+        auto grads = [&](int j) -> bool {   // dQ += dS K_j
+            const int s = j % C::STAGES, t = j & 1, k = j >> 1;
+            if (!__all_sync(0xffffffffu, W.wait(p_full(t), k & 1))) return false;
+            tc::fence_after_sync();
+            if (leader) {
+                const uint32_t st = (s * C::KT::BYTES) >> 4;
 #pragma unroll
                 for (int kk = 0; kk < C::BK / 16; ++kk)
-                    tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 64 + kk * 8, mnmajor_desc<C::BK>(kb, kk), idesc_g,
+                    tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 64 + kk * 8, km + st + kk * 128, idesc_g,
                                (j > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(mma_done(t));
                 tc::mma_commit(kv_empty(s));
-                return true;
-            };
-            for (int j = 0; ok && j < n; ++j) {
-                const int s = j % C::STAGES, t = j & 1;
-                if (!(ok = W.wait(kv_full(s), (j / C::STAGES) & 1))) break;
-                const uint32_t kb = base + C::K_OFF + s * C::KT::BYTES;
-                const uint32_t vb = base + C::V_OFF + s * C::KT::BYTES;
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int j = 0; ok && j < n; ++j) {
+            const int s = j % C::STAGES, t = j & 1;
+            if (!(ok = __all_sync(0xffffffffu, W.wait(kv_full(s), (j / C::STAGES) & 1)))) break;
+            if (leader) {
+                const uint32_t st = (s * C::KT::BYTES) >> 4;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {   // S = Q K^T and dP = dO V^T, interleaved
-                    tc::mma_ss(tmem + 128 * t, kmajor_desc<C::BQ>(base + C::Q_OFF, kk), kmajor_desc<C::BK>(kb, kk),
-                               idesc_s, kk > 0 ? 1u : 0u);
-                    tc::mma_ss(tmem + 128 * t + 64, kmajor_desc<C::BQ>(base + C::DO_OFF, kk),
-                               kmajor_desc<C::BK>(vb, kk), idesc_s, kk > 0 ? 1u : 0u);
+                    const uint32_t oa = ((kk >> 2) * C::QT::CHUNK + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = ((kk >> 2) * C::KT::CHUNK + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 128 * t, qd + oa, kk_ + st + ob, idesc_s, kk > 0 ? 1u : 0u);
+                    tc::mma_ss(tmem + 128 * t + 64, od + oa, vk + st + ob, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(sd_full(t));
-                if (j >= 1) ok = grads(j - 1);
             }
-            if (ok) ok = grads(n - 1);
-            if (!ok) {
-                tc::mma_commit(drain);
-                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
-                }
+            __syncwarp();
+            if (j >= 1) ok = grads(j - 1);
+        }
+        if (ok) ok = grads(n - 1);
+        if (!ok && leader) {
+            tc::mma_commit(drain);
+            for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
             }
         }
+        __syncwarp();
     }
     } else {
         tc::regs_inc<224>();

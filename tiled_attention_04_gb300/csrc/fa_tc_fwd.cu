@@ -186,49 +186,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN, false, false);
-            constexpr uint32_t idesc_o = tc::idesc_bf16(BM, D, false, true);
-            bool ok = W.wait(q_full, 0);
-            auto pv = [&](int j) -> bool {
-                const int s = j % C::VST, t = j & 1, k = j >> 1;
-                if (!W.wait(p_full(t), k & 1)) return false;
-                tc::fence_after_sync();
-                if (!W.wait(v_full(s), (j / C::VST) & 1)) return false;
-                const uint32_t vbase = base + C::V_OFF + s * C::TILE_BYTES;
+        // The whole warp runs the loop so that descriptors stay warp-uniform and
+        // cheap to form; one elected lane issues the tcgen05 instructions.
+        const bool leader = tc::elect_one();
+        constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN, false, false);
+        constexpr uint32_t idesc_o = tc::idesc_bf16(BM, D, false, true);
+        const uint64_t qd = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);
+        const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);
+        const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, C::CHUNK_BYTES, 1024);
+        bool ok = __all_sync(0xffffffffu, W.wait(q_full, 0));
+        auto pv = [&](int j) -> bool {
+            const int s = j % C::VST, t = j & 1, k = j >> 1;
+            if (!__all_sync(0xffffffffu, W.wait(p_full(t), k & 1))) return false;
+            if (!__all_sync(0xffffffffu, W.wait(v_full(s), (j / C::VST) & 1))) return false;
+            tc::fence_after_sync();
+            if (leader) {
+                const uint64_t vs = vd + ((s * C::TILE_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bdesc = tc::sdesc_sw128(vbase + kk * 16 * 128, C::CHUNK_BYTES, 1024);
-                    tc::mma_ts(tmem + C::O_COL0 + t * D, tmem + C::S_COL0 + t * 128 + kk * 8, bdesc, idesc_o,
-                               (k > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 16 rows of V = 2048 bytes per k-step
+                    tc::mma_ts(tmem + C::O_COL0 + t * D, tmem + C::S_COL0 + t * 128 + kk * 8, vs + kk * 128,
+                               idesc_o, (k > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(o_done(t));
                 tc::mma_commit(v_empty(s));
-                return true;
-            };
-            for (int j = 0; ok && j < n; ++j) {
-                const int s = j % C::KST, t = j & 1;
-                if (!(ok = W.wait(k_full(s), (j / C::KST) & 1))) break;
-                const uint32_t kbase = base + C::K_OFF + s * C::TILE_BYTES;
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int j = 0; ok && j < n; ++j) {
+            const int s = j % C::KST, t = j & 1;
+            if (!(ok = __all_sync(0xffffffffu, W.wait(k_full(s), (j / C::KST) & 1)))) break;
+            if (leader) {
+                const uint64_t ks = kd + ((s * C::TILE_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-                    const uint64_t adesc = tc::sdesc_sw128(base + C::Q_OFF + off, 16, 1024);
-                    const uint64_t bdesc = tc::sdesc_sw128(kbase + off, 16, 1024);
-                    tc::mma_ss(tmem + C::S_COL0 + t * 128, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + C::S_COL0 + t * 128, qd + off, ks + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(s_full(t));
                 tc::mma_commit(k_empty(s));
-                if (j >= 1) ok = pv(j - 1);
             }
-            if (ok) ok = pv(n - 1);
-            if (!ok) {
-                // wait (bounded) for the MMAs already issued before TMEM is released
-                tc::mma_commit(drain);
-                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
-                }
+            __syncwarp();
+            if (j >= 1) ok = pv(j - 1);
+        }
+        if (ok) ok = pv(n - 1);
+        if (!ok && leader) {
+            // wait (bounded) for the MMAs already issued before TMEM is released
+            tc::mma_commit(drain);
+            for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
             }
         }
+        __syncwarp();
     }
     } else {
         tc::regs_inc<224>();

@@ -161,6 +161,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// one lane of a converged warp (the same lane every call)
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ------------------------------------------------------------------ element-wise helpers
 // 2^x on the MUFU unit (flush-to-zero; -inf gives 0)
 __device__ __forceinline__ float ex2(float x) {
