@@ -182,6 +182,16 @@ FA_API fa_status fa_reset_device_status(fa_stream_t stream);
  */
 FA_API void fa_set_wait_limit(uint32_t spins);
 
+/*
+ * Fault injection on the host side: while `on` is nonzero, the tensor-core
+ * forward kernel's MMA issuer first waits on a barrier that nothing ever
+ * arrives on.  The bounded wait gives up (after the fa_set_wait_limit cap,
+ * else about two seconds), the kernel records FA_ERR_TIMEOUT for
+ * fa_get_device_status, releases its resources and returns; O and L are then
+ * undefined.  For testing the failure path without faulting the GPU.
+ */
+FA_API void fa_debug_force_stall(int on);
+
 FA_API const char *fa_status_string(fa_status s);
 
 #ifdef __cplusplus

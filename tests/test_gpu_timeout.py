@@ -1,7 +1,8 @@
-"""Failure detection without a GPU fault: a host-set cap on device-side polling
-makes the tensor-core kernels give up their waits, report FA_ERR_TIMEOUT
-through fa_get_device_status and return; the context stays usable and the
-next call with the default cap is correct again."""
+"""Failure detection without a GPU fault: a host switch makes the forward's
+MMA issuer wait on a barrier that nothing arrives on; with a small poll cap the
+bounded wait gives up, the kernel reports FA_ERR_TIMEOUT through
+fa_get_device_status and returns.  The context stays usable and the next call
+(switch off, default cap) is correct again."""
 import math
 
 import numpy as np
@@ -22,10 +23,12 @@ def test_forced_wait_timeout_reports_and_recovers(cuda_lib):
     assert binding.path_name(512, 512, 128, 1, binding.FA_DTYPE_BF16) == "tc"
     binding.fa_reset_device_status()
     try:
-        binding.fa_set_wait_limit(1)
+        binding.fa_set_wait_limit(1000)
+        binding.fa_debug_force_stall(True)
         binding.fa_fwd(Q, K, V, is_causal=True)
         assert binding.fa_get_device_status() == 8      # FA_ERR_TIMEOUT
     finally:
+        binding.fa_debug_force_stall(False)
         binding.fa_set_wait_limit(0)
     binding.fa_reset_device_status()
     assert binding.fa_get_device_status() == binding.FA_OK

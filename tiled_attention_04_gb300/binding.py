@@ -25,7 +25,7 @@ FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
 # every function include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq",
            "fa_bwd_noalloc", "fa_noalloc_scratch_bytes", "fa_path_name", "fa_get_device_status",
-           "fa_reset_device_status", "fa_set_wait_limit", "fa_status_string")
+           "fa_reset_device_status", "fa_set_wait_limit", "fa_debug_force_stall", "fa_status_string")
 
 _lib = None
 
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
     L.fa_reset_device_status.argtypes = [vp]
     L.fa_set_wait_limit.argtypes = [ctypes.c_uint32]
     L.fa_set_wait_limit.restype = None
+    L.fa_debug_force_stall.argtypes = [ctypes.c_int]
+    L.fa_debug_force_stall.restype = None
     L.fa_status_string.argtypes = [i]
     L.fa_status_string.restype = ctypes.c_char_p
     for name in ("fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_get_device_status",
@@ -227,3 +229,7 @@ def fa_reset_device_status(stream=None):
 
 def fa_set_wait_limit(spins: int):
     lib().fa_set_wait_limit(int(spins))
+
+
+def fa_debug_force_stall(on: bool):
+    lib().fa_debug_force_stall(1 if on else 0)

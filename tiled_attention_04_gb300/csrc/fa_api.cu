@@ -16,6 +16,7 @@
 namespace {
 
 std::atomic<uint32_t> g_wait_limit{0};
+std::atomic<uint32_t> g_force_stall{0};
 constexpr uint32_t kDefaultWaitLimit = 1u << 26;   // polls; far above any legitimate wait
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -42,6 +43,7 @@ fa_status check_common(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dt
     out->dtype = dtype;
     const uint32_t w = g_wait_limit.load(std::memory_order_relaxed);
     out->wait_limit = w ? w : kDefaultWaitLimit;
+    out->force_stall = g_force_stall.load(std::memory_order_relaxed);
     return FA_OK;
 }
 
@@ -127,6 +129,8 @@ const char *fa_status_string(fa_status s) {
 }
 
 void fa_set_wait_limit(uint32_t spins) { g_wait_limit.store(spins, std::memory_order_relaxed); }
+
+void fa_debug_force_stall(int on) { g_force_stall.store(on ? 1u : 0u, std::memory_order_relaxed); }
 
 const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype dtype) {
     FaProblem p{};

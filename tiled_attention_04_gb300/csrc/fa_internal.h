@@ -15,6 +15,7 @@ struct FaProblem {
     int causal;      // top-left causal mask
     fa_dtype dtype;  // element type of Q, K, V, O, dO, dQ, dK, dV
     uint32_t wait_limit;  // cap on device-side polling loops
+    uint32_t force_stall; // fault injection: the forward's MMA issuer waits on a barrier nobody arrives on
 };
 
 // ---- fp32 CUDA-core kernels (fa_simt.cu): every dtype and head dim.

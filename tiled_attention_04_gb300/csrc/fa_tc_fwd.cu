@@ -27,11 +27,20 @@
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256) (P as packed bf16 aliases the
 // first 64 columns of its S), O0 [256, 256+d), O1 [256+d, 256+2d).
+//
+// Split work items (SPLIT = 2): when there are too few query tiles to fill the
+// GPU, or the longest causal row would dominate the run, a cluster of two CTAs
+// shares one query tile: rank 0 takes the first half of the key tiles, rank 1
+// the rest.  Rank 1 leaves its merged, unnormalised partial (O, m, l) in its
+// shared memory; rank 0 reads it through distributed shared memory, merges it
+// exactly like the two warpgroups' halves, and writes O and L.  The hand-over
+// uses mbarriers arrived on from the other CTA and waited on with a bound.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "fa_internal.h"
@@ -62,22 +71,28 @@ struct FwdCfg {
     static constexpr uint32_t K_OFF = Q_OFF + TILE_BYTES;
     static constexpr uint32_t V_OFF = K_OFF + KST * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = V_OFF + VST * TILE_BYTES;
-    static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 6 + 1;
+    static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 6 + 2;
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t MISC_OFF = STAT_OFF + 4 * 128 * 4;
-    static constexpr uint32_t USED = MISC_OFF + 16;
+    static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;                  // peer_ready, peer_done
+    static constexpr uint32_t USED = PEER_BAR_OFF + 16;
+    // split items: rank 1's partial O (fp32, rows padded by 4 floats) and its m, l, in the K ring
+    static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
+    static constexpr uint32_t PART_OFF = K_OFF;
+    static constexpr uint32_t PART_ML_OFF = PART_OFF + 128 * PART_STRIDE;
+    static_assert(PART_ML_OFF + 2 * 128 * 4 <= K_OFF + KST * TILE_BYTES, "partial fits the K ring");
     // at least ~116 KB so that one CTA (which owns all 512 TMEM columns) runs per SM
     static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u ? USED + 1024 : 120u * 1024u);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
-                     uint32_t wait_limit) {
+                     uint32_t wait_limit, uint32_t force_stall) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -86,12 +101,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // longest work first: high query tiles (more key tiles under causal) start first
-    const int item = blockIdx.x;
+    const int item = blockIdx.x / SPLIT;
+    const uint32_t rank = SPLIT > 1 ? tc::cluster_rank() : 0u;
     const int qt = num_q_tiles - 1 - item / BH;
     const int bh = item % BH;
     const int q0 = qt * BM;
     const int kend = CAUSAL ? min(Nk, q0 + BM) : Nk;
-    const int n = (kend + BN - 1) / BN;
+    const int n_all = (kend + BN - 1) / BN;
+    // this CTA's key tiles [jb, jb + n): all of them, or one half of a split item
+    const int n_first = SPLIT > 1 ? (n_all + 1) / 2 : n_all;
+    const int jb = rank == 0 ? 0 : n_first;
+    const int n = rank == 0 ? n_first : n_all - n_first;
 
     auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
     const uint32_t q_full = bar(0);
@@ -104,6 +124,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto p_full = [&](int t) { return bar(RB + 2 + t); };
     auto o_done = [&](int t) { return bar(RB + 4 + t); };
     const uint32_t drain = bar(RB + 6);
+    const uint32_t never = bar(RB + 7);   // fault injection: nothing ever arrives here
     float *m_sm = reinterpret_cast<float *>(sb + C::STAT_OFF);
     float *l_sm = m_sm + 256;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
@@ -125,6 +146,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(o_done(t), 1);
         }
         tc::mbar_init(drain, 1);
+        tc::mbar_init(never, 1);
+        if (SPLIT > 1) {
+            tc::mbar_init(base + C::PEER_BAR_OFF, 256);       // peer_ready: rank 1's 256 softmax threads
+            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 256);   // peer_done: rank 0's 256 softmax threads
+        }
         *abort_flag = 0u;
         tc::fence_mbar_init();
     }
@@ -134,6 +160,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
+    if (SPLIT > 1) tc::cluster_sync_all();   // the peer's barriers are initialised before anyone arrives
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const tc::Waiter W{abort_flag, &g_fa_fwd_status, wait_limit, 1u};
@@ -157,7 +184,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!W.wait(empty, ((j / st) & 1) ^ 1u)) return false;
                 tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
-                    tc::tma_load_3d(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64, j * BN, bh);
+                    tc::tma_load_3d(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64,
+                                    (jb + j) * BN, bh);
                 return true;
             };
             // order K_0, K_1, V_0, K_2, V_1, ...: the MMA warp uses K_{j+1} before V_j
@@ -195,6 +223,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);
         const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, C::CHUNK_BYTES, 1024);
         bool ok = __all_sync(0xffffffffu, W.wait(q_full, 0));
+        if (force_stall) ok = __all_sync(0xffffffffu, W.wait(never, 0));
         auto pv = [&](int j) -> bool {
             const int s = j % C::VST, t = j & 1, k = j >> 1;
             if (!__all_sync(0xffffffffu, W.wait(p_full(t), k & 1))) return false;
@@ -228,7 +257,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (j >= 1) ok = pv(j - 1);
         }
-        if (ok) ok = pv(n - 1);
+        if (ok && n > 0) ok = pv(n - 1);
         if (!ok && leader) {
             // wait (bounded) for the MMAs already issued before TMEM is released
             tc::mma_commit(drain);
@@ -250,7 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int k = 0; k < nt; ++k) {
-            const int k0 = (2 * k + t) * BN;
+            const int k0 = (jb + 2 * k + t) * BN;
             ok = W.wait(s_full(t), k & 1);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc::fence_after_sync();
@@ -316,25 +345,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_before_sync();
             tc::mbar_arrive(p_full(t));
         }
-        // ---- merge the two warpgroups' partial results and write O, L
+        // ---- merge the two warpgroups' partial results (and, for split items, the peer CTA's)
         m_sm[t * 128 + r] = m;
         l_sm[t * 128 + r] = l;
         tc::named_bar_sync(1, 256);
         const int n0 = (n + 1) >> 1, n1 = n >> 1;
         bool fine = !*abort_flag;
-        if (fine) fine = W.wait(o_done(0), (n0 - 1) & 1);
+        if (fine && n0 > 0) fine = W.wait(o_done(0), (n0 - 1) & 1);
         if (fine && n1 > 0) fine = W.wait(o_done(1), (n1 - 1) & 1);
-        if (__all_sync(0xffffffffu, fine)) {
+        fine = __all_sync(0xffffffffu, fine);
+        // this CTA's partial for row r, columns [t*D/2, (t+1)*D/2), relative to max Mc (unnormalised)
+        float v[D / 2];
+        float Mc = -INFINITY, lc = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) v[i] = 0.f;
+        if (fine && n0 > 0) {
             tc::fence_after_sync();
             const float m0 = m_sm[r], l0 = l_sm[r];
             const float m1 = m_sm[128 + r], l1 = l_sm[128 + r];
-            const float M = fmaxf(m0, m1);
-            const float a0 = exp2f(m0 - M);
-            const float a1 = n1 > 0 ? exp2f(m1 - M) : 0.f;
-            const float lsum = l0 * a0 + l1 * a1;
-            const float inv = 1.f / lsum;
+            Mc = fmaxf(m0, m1);
+            const float a0 = exp2f(m0 - Mc);
+            const float a1 = n1 > 0 ? exp2f(m1 - Mc) : 0.f;
+            lc = l0 * a0 + l1 * a1;
             const uint32_t tO0 = tmem + lane_base + C::O_COL0, tO1 = tO0 + D;
-            __nv_bfloat16 *orow = O + ((size_t)bh * Nq + row) * D;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 const int col = t * (D / 2) + 32 * c;
@@ -344,24 +377,83 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc::tmem_ld_wait();
                 reg_fence_x32(o0);
                 reg_fence_x32(o1);
-                uint32_t packed[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float v0 = __uint_as_float(o0[2 * i]) * a0, v1 = __uint_as_float(o0[2 * i + 1]) * a0;
-                    if (n1 > 0) {
-                        v0 = fmaf(__uint_as_float(o1[2 * i]), a1, v0);
-                        v1 = fmaf(__uint_as_float(o1[2 * i + 1]), a1, v1);
-                    }
-                    packed[i] = tc::pack_bf16(v0 * inv, v1 * inv);
-                }
-                if (row < Nq) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + col);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                for (int i = 0; i < 32; ++i) {
+                    float x = __uint_as_float(o0[i]) * a0;
+                    if (n1 > 0) x = fmaf(__uint_as_float(o1[i]), a1, x);
+                    v[32 * c + i] = x;
                 }
             }
-            if (t == 0 && row < Nq) Lout[(size_t)bh * Nq + row] = M * kLn2 + logf(lsum);
+        }
+        auto store_row = [&](const float *vals, float Mrow, float lrow) {
+            const float inv = 1.f / lrow;
+            __nv_bfloat16 *orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
+            if (row < Nq) {
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                    uint4 q;
+                    q.x = tc::pack_bf16(vals[8 * c + 0] * inv, vals[8 * c + 1] * inv);
+                    q.y = tc::pack_bf16(vals[8 * c + 2] * inv, vals[8 * c + 3] * inv);
+                    q.z = tc::pack_bf16(vals[8 * c + 4] * inv, vals[8 * c + 5] * inv);
+                    q.w = tc::pack_bf16(vals[8 * c + 6] * inv, vals[8 * c + 7] * inv);
+                    reinterpret_cast<uint4 *>(orow)[c] = q;
+                }
+                if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
+            }
+        };
+        // hand-over waits: bounded, but not cut short by this CTA's own abort flag, so
+        // that neither CTA exits while the other may still touch its shared memory
+        auto wait_peer = [&](uint32_t b) -> bool {
+            uint64_t deadline = 0;
+            for (uint32_t i = 0;; ++i) {
+                if (tc::mbar_try_wait_cluster(b, 0)) return true;
+                if ((i & 255u) == 0) {
+                    const uint64_t now = tc::globaltimer();
+                    if (deadline == 0) deadline = now + 2000000000ull;
+                    else if (now > deadline) break;
+                }
+            }
+            atomicOr(&g_fa_fwd_status, 1u);
+            return false;
+        };
+        if constexpr (SPLIT == 1) {
+            if (fine) store_row(v, Mc, lc);
+        } else {
+            const uint32_t peer_ready = base + C::PEER_BAR_OFF, peer_done = peer_ready + 8;
+            if (rank == 1) {
+                // leave the partial in this CTA's shared memory for rank 0, then wait until it has been read
+                float *part = reinterpret_cast<float *>(sb + C::PART_OFF + r * C::PART_STRIDE) + t * (D / 2);
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c)
+                    reinterpret_cast<float4 *>(part)[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                if (t == 0) {
+                    float *ml = reinterpret_cast<float *>(sb + C::PART_ML_OFF);
+                    ml[r] = Mc;
+                    ml[128 + r] = lc;
+                }
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, 0));
+                wait_peer(peer_done);   // rank 0 reads this CTA's shared memory until then
+            } else {
+                const bool got = wait_peer(peer_ready);
+                if (__all_sync(0xffffffffu, fine && got)) {
+                    const uint32_t prow = tc::map_to_rank(base + C::PART_OFF + r * C::PART_STRIDE, 1) + t * (D / 2) * 4;
+                    const uint32_t pml = tc::map_to_rank(base + C::PART_ML_OFF, 1);
+                    const float M1 = tc::ld_cluster_f32(pml + r * 4), l1 = tc::ld_cluster_f32(pml + (128 + r) * 4);
+                    const float M = fmaxf(Mc, M1);
+                    const float b0 = exp2f(Mc - M);
+                    const float b1 = l1 > 0.f ? exp2f(M1 - M) : 0.f;
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) {
+                        const float4 pv = tc::ld_cluster_v4(prow + 16 * c);
+                        v[4 * c + 0] = fmaf(pv.x, b1, v[4 * c + 0] * b0);
+                        v[4 * c + 1] = fmaf(pv.y, b1, v[4 * c + 1] * b0);
+                        v[4 * c + 2] = fmaf(pv.z, b1, v[4 * c + 2] * b0);
+                        v[4 * c + 3] = fmaf(pv.w, b1, v[4 * c + 3] * b0);
+                    }
+                    store_row(v, M, lc * b0 + l1 * b1);
+                }
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_done, 1));
+            }
         }
     }
     // ------------------------------------------------------------ teardown
@@ -409,19 +501,58 @@ bool tc_fwd_supported(const FaProblem &p) {
     return p.dtype == FA_DTYPE_BF16 && (p.d == 64 || p.d == 128) && p.Nq >= 128 && p.Nk >= 128 && p.BH >= 1;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int SPLIT>
 static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                               void *O, float *L, cudaStream_t st) {
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_tc_kernel<D, CAUSAL>;
+    auto kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int qtiles = (p.Nq + BM - 1) / BM;
-    const long long grid = (long long)qtiles * p.BH;
+    const long long grid = (long long)qtiles * p.BH * SPLIT;
     const float scale_log2 = p.scale * 1.4426950408889634f;
-    kern<<<(unsigned)grid, NTHREADS, C::SMEM_BYTES, st>>>(mq, mk, mv, static_cast<__nv_bfloat16 *>(O), L, p.Nq,
-                                                            p.Nk, p.BH, qtiles, scale_log2, p.wait_limit);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = SPLIT;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = SPLIT > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, static_cast<__nv_bfloat16 *>(O), L, p.Nq, p.Nk, p.BH, qtiles,
+                           scale_log2, p.wait_limit, p.force_stall);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// Work items are split over a cluster of two CTAs when the longest item (a
+// whole row of key tiles) is more than 1.5x the average number of key tiles per
+// SM: then it, not the total work, would set the run time.
+static bool fwd_split(const FaProblem &p) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long qtiles = (p.Nq + BM - 1) / BM, ktiles = (p.Nk + BN - 1) / BN;
+    long long total = 0, n_max = 0;
+    for (long long qt = 0; qt < qtiles; ++qt) {
+        const long long kend = p.causal ? std::min<long long>(p.Nk, (qt + 1) * BM) : p.Nk;
+        const long long n = (kend + BN - 1) / BN;
+        total += n;
+        n_max = std::max(n_max, n);
+    }
+    total *= p.BH;
+    (void)ktiles;
+    return n_max >= 4 && 2 * n_max * sms > 3 * total;
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_fwd_any(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                                  const CUtensorMap &mv, void *O, float *L, cudaStream_t st) {
+    return fwd_split(p) ? launch_fwd<D, CAUSAL, 2>(p, mq, mk, mv, O, L, st)
+                        : launch_fwd<D, CAUSAL, 1>(p, mq, mk, mv, O, L, st);
 }
 
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
@@ -430,9 +561,10 @@ cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void 
     if (!tc_make_map_3d(&mq, Q, p.BH, p.Nq, p.d, BM) || !tc_make_map_3d(&mk, K, p.BH, p.Nk, p.d, BN) ||
         !tc_make_map_3d(&mv, V, p.BH, p.Nk, p.d, BN))
         return cudaErrorInvalidValue;
-    if (p.d == 128) return p.causal ? launch_fwd<128, true>(p, mq, mk, mv, O, L, st)
-                                    : launch_fwd<128, false>(p, mq, mk, mv, O, L, st);
-    return p.causal ? launch_fwd<64, true>(p, mq, mk, mv, O, L, st) : launch_fwd<64, false>(p, mq, mk, mv, O, L, st);
+    if (p.d == 128) return p.causal ? launch_fwd_any<128, true>(p, mq, mk, mv, O, L, st)
+                                    : launch_fwd_any<128, false>(p, mq, mk, mv, O, L, st);
+    return p.causal ? launch_fwd_any<64, true>(p, mq, mk, mv, O, L, st)
+                    : launch_fwd_any<64, false>(p, mq, mk, mv, O, L, st);
 }
 
 cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st) {
