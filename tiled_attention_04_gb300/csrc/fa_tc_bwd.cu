@@ -31,6 +31,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "fa_internal.h"
 #include "tc_common.cuh"
 
@@ -130,13 +132,18 @@ struct DkdvCfg {
     // kv_full, q_full[S], q_empty[S], sd_full[2], p_full[2], mma_done[2], drain
     static constexpr int NBAR = 1 + 2 * STAGES + 6 + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = (MISC_OFF + 16 + 1024 > 120u * 1024u ? MISC_OFF + 16 + 1024 : 120u * 1024u);
+    static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;
+    static constexpr uint32_t SMEM_BYTES = (PEER_BAR_OFF + 16 + 1024 > 120u * 1024u ? PEER_BAR_OFF + 16 + 1024 : 120u * 1024u);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    // split items: rank 1's partial dV (rows 0..127) and dK (rows 128..255), fp32, over the tile rings
+    static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
+    static constexpr uint32_t PART_OFF = 0;
+    static_assert(PART_OFF + 256 * PART_STRIDE <= BAR_OFF, "partial fits the rings");
     // TMEM: S^T_t [128t, 128t+64), dP^T_t [128t+64, 128t+128), dV [256, 256+D), dK [256+D, 256+2D)
     static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -151,14 +158,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // longest first: under causal the first key tiles see the most queries
-    const int item = blockIdx.x;
+    const int item = blockIdx.x / SPLIT;
+    const uint32_t rank = SPLIT > 1 ? tc::cluster_rank() : 0u;
     const int kt = CAUSAL ? item / BH : num_k_tiles - 1 - item / BH;
     const int bh = item % BH;
     const int k0 = kt * C::BK;
     const int nqp = padded_rows(Nq);
-    const int i_begin = CAUSAL ? k0 / C::BQ : 0;              // first query sub-tile that sees a key of this tile
     const int i_end = (Nq + C::BQ - 1) / C::BQ;
-    const int n = i_end > i_begin ? i_end - i_begin : 0;      // sub-tiles to visit
+    const int i_first = CAUSAL ? k0 / C::BQ : 0;              // first query sub-tile that sees a key of this tile
+    const int n_all = i_end > i_first ? i_end - i_first : 0;
+    // this CTA's query sub-tiles: all of them, or one half of a split item
+    const int n_half = SPLIT > 1 ? (n_all + 1) / 2 : n_all;
+    const int i_begin = i_first + (rank == 0 ? 0 : n_half);
+    const int n = rank == 0 ? n_half : n_all - n_half;        // sub-tiles to visit
 
     auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
     const uint32_t kv_full = bar(0);
@@ -183,6 +195,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(mma_done(t), 1);
         }
         tc::mbar_init(drain, 1);
+        if (SPLIT > 1) {
+            tc::mbar_init(base + C::PEER_BAR_OFF, 256);
+            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 256);
+        }
         *abort_flag = 0u;
         tc::fence_mbar_init();
     }
@@ -192,6 +208,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
+    if (SPLIT > 1) tc::cluster_sync_all();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const tc::Waiter W{abort_flag, &g_fa_bwd_status, wait_limit, 2u};
@@ -352,7 +369,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_before_sync();
             tc::mbar_arrive(p_full(t));
         }
-        // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (rows = keys)
+        // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (rows = keys);
+        // a split item's rank 1 leaves its partial sums for rank 0 to add
         tc::named_bar_sync(1, 256);
         bool fine = !*abort_flag;
         if (n > 0) {
@@ -360,32 +378,64 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (fine) fine = W.wait(mma_done(0), (n0 - 1) & 1);
             if (fine && n1 > 0) fine = W.wait(mma_done(1), (n1 - 1) & 1);
         }
-        if (__all_sync(0xffffffffu, fine)) {
-            tc::fence_after_sync();
-            __nv_bfloat16 *dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
-            const float mul = t == 0 ? 1.f : scale;
-            const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
+        fine = __all_sync(0xffffffffu, fine);
+        if (fine && n > 0) tc::fence_after_sync();
+        __nv_bfloat16 *dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
+        const float mul = t == 0 ? 1.f : scale;
+        const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
+        const uint32_t part = base + C::PART_OFF + (t * 128 + r) * C::PART_STRIDE;   // this thread's partial row
+        const uint32_t peer_ready = base + C::PEER_BAR_OFF, peer_done = peer_ready + 8;
+        bool merge = false;
+        if constexpr (SPLIT > 1) {
+            if (rank == 0) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 2u);
+        }
+        const uint32_t rpart = SPLIT > 1 ? tc::map_to_rank(part, 1) : 0u;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[32];
-                if (n > 0) {
-                    tmem_ld_x32(tA + 32 * c, a);
-                    tc::tmem_ld_wait();
-                    reg_fence_x32(a);
-                } else {
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t a[32];
+            if (fine && n > 0) {
+                tmem_ld_x32(tA + 32 * c, a);
+                tc::tmem_ld_wait();
+                reg_fence_x32(a);
+            } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) a[i] = 0u;
+                for (int i = 0; i < 32; ++i) a[i] = 0u;
+            }
+            if (SPLIT > 1 && rank == 1) {
+                float4 *pr = reinterpret_cast<float4 *>(sb + (part - base)) + 8 * c;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    pr[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                        __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+                continue;
+            }
+            if (merge) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 q = tc::ld_cluster_v4(rpart + 128 * c + 16 * i);
+                    a[4 * i + 0] = __float_as_uint(__uint_as_float(a[4 * i + 0]) + q.x);
+                    a[4 * i + 1] = __float_as_uint(__uint_as_float(a[4 * i + 1]) + q.y);
+                    a[4 * i + 2] = __float_as_uint(__uint_as_float(a[4 * i + 2]) + q.z);
+                    a[4 * i + 3] = __float_as_uint(__uint_as_float(a[4 * i + 3]) + q.w);
                 }
-                uint32_t packed[16];
+            }
+            uint32_t packed[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
-                if (key < Nk) {
-                    uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
+            for (int i = 0; i < 16; ++i)
+                packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
+            if (fine && key < Nk) {
+                uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-                }
+                for (int i = 0; i < 4; ++i)
+                    o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            }
+        }
+        if constexpr (SPLIT > 1) {
+            if (rank == 1) {
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, 0));
+                tc::wait_peer(peer_done, &g_fa_bwd_status, 2u);   // rank 0 reads this partial until then
+            } else {
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_done, 1));
             }
         }
     }
@@ -414,13 +464,18 @@ struct DqCfg {
     // q_full, kv_full[S], kv_empty[S], sd_full[2], p_full[2], mma_done[2], drain
     static constexpr int NBAR = 1 + 2 * STAGES + 6 + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = (MISC_OFF + 16 + 1024 > 120u * 1024u ? MISC_OFF + 16 + 1024 : 120u * 1024u);
+    static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;
+    static constexpr uint32_t SMEM_BYTES = (PEER_BAR_OFF + 16 + 1024 > 120u * 1024u ? PEER_BAR_OFF + 16 + 1024 : 120u * 1024u);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    // split items: rank 1's partial dQ (fp32) over the K/V rings
+    static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
+    static constexpr uint32_t PART_OFF = K_OFF;
+    static_assert(PART_OFF + 128 * PART_STRIDE <= BAR_OFF, "partial fits the rings");
     // TMEM: S_t [128t, 128t+64), dP_t [128t+64, 128t+128), dQ [256, 256+D)
     static constexpr uint32_t DQ_COL = 256;
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -433,12 +488,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t *sb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int item = blockIdx.x;
+    const int item = blockIdx.x / SPLIT;
+    const uint32_t rank = SPLIT > 1 ? tc::cluster_rank() : 0u;
     const int qt = num_q_tiles - 1 - item / BH;
     const int bh = item % BH;
     const int q0 = qt * C::BQ;
     const int kend = CAUSAL ? min(Nk, q0 + C::BQ) : Nk;
-    const int n = (kend + C::BK - 1) / C::BK;
+    const int n_all = (kend + C::BK - 1) / C::BK;
+    // this CTA's key sub-tiles [jb, jb + n): all of them, or one half of a split item
+    const int n_half = SPLIT > 1 ? (n_all + 1) / 2 : n_all;
+    const int jb = rank == 0 ? 0 : n_half;
+    const int n = rank == 0 ? n_half : n_all - n_half;
     const int nqp = padded_rows(Nq);
 
     auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
@@ -464,6 +524,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(mma_done(t), 1);
         }
         tc::mbar_init(drain, 1);
+        if (SPLIT > 1) {
+            tc::mbar_init(base + C::PEER_BAR_OFF, 256);
+            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 256);
+        }
         *abort_flag = 0u;
         tc::fence_mbar_init();
     }
@@ -473,6 +537,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
+    if (SPLIT > 1) tc::cluster_sync_all();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const tc::Waiter W{abort_flag, &g_fa_bwd_status, wait_limit, 4u};
@@ -495,9 +560,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc::mbar_arrive_expect_tx(kv_full(s), 2 * C::KT::BYTES);
                 for (int c = 0; c < D / 64; ++c) {
                     tc::tma_load_3d(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
-                                    j * C::BK, bh);
+                                    (jb + j) * C::BK, bh);
                     tc::tma_load_3d(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
-                                    j * C::BK, bh);
+                                    (jb + j) * C::BK, bh);
                 }
                 issued = j + 1;
             }
@@ -555,7 +620,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (j >= 1) ok = grads(j - 1);
         }
-        if (ok) ok = grads(n - 1);
+        if (ok && n > 0) ok = grads(n - 1);
         if (!ok && leader) {
             tc::mma_commit(drain);
             for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
@@ -576,7 +641,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int nt = (n - t + 1) >> 1;
         for (int k = 0; k < nt; ++k) {
             const int j = 2 * k + t;
-            const int kb0 = j * C::BK;
+            const int kb0 = (jb + j) * C::BK;
             bool ok = W.wait(sd_full(t), k & 1);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
@@ -617,29 +682,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::named_bar_sync(1, 256);
         bool fine = !*abort_flag;
         const int n0 = (n + 1) >> 1, n1 = n >> 1;
-        if (fine) fine = W.wait(mma_done(0), (n0 - 1) & 1);
+        if (fine && n0 > 0) fine = W.wait(mma_done(0), (n0 - 1) & 1);
         if (fine && n1 > 0) fine = W.wait(mma_done(1), (n1 - 1) & 1);
-        if (__all_sync(0xffffffffu, fine)) {
-            tc::fence_after_sync();
-            __nv_bfloat16 *dst = dQ + ((size_t)bh * Nq + row) * D;
-            const uint32_t tA = tmem + lane_base + C::DQ_COL;
+        fine = __all_sync(0xffffffffu, fine);
+        if (fine && n > 0) tc::fence_after_sync();
+        __nv_bfloat16 *dst = dQ + ((size_t)bh * Nq + row) * D;
+        const uint32_t tA = tmem + lane_base + C::DQ_COL;
+        const uint32_t part = base + C::PART_OFF + r * C::PART_STRIDE;
+        const uint32_t peer_ready = base + C::PEER_BAR_OFF, peer_done = peer_ready + 8;
+        bool merge = false;
+        if constexpr (SPLIT > 1) {
+            if (rank == 0) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 4u);
+        }
+        const uint32_t rpart = SPLIT > 1 ? tc::map_to_rank(part, 1) : 0u;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                const int col = t * (D / 2) + 32 * c;
-                uint32_t a[32];
+        for (int c = 0; c < D / 64; ++c) {
+            const int col = t * (D / 2) + 32 * c;
+            uint32_t a[32];
+            if (fine && n > 0) {
                 tmem_ld_x32(tA + col, a);
                 tc::tmem_ld_wait();
                 reg_fence_x32(a);
-                uint32_t packed[16];
+            } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * scale, __uint_as_float(a[2 * i + 1]) * scale);
-                if (row < Nq) {
-                    uint4 *o = reinterpret_cast<uint4 *>(dst + col);
+                for (int i = 0; i < 32; ++i) a[i] = 0u;
+            }
+            if (SPLIT > 1 && rank == 1) {
+                float4 *pr = reinterpret_cast<float4 *>(sb + (part - base) + col * 4);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                for (int i = 0; i < 8; ++i)
+                    pr[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                        __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+                continue;
+            }
+            if (merge) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 q = tc::ld_cluster_v4(rpart + col * 4 + 16 * i);
+                    a[4 * i + 0] = __float_as_uint(__uint_as_float(a[4 * i + 0]) + q.x);
+                    a[4 * i + 1] = __float_as_uint(__uint_as_float(a[4 * i + 1]) + q.y);
+                    a[4 * i + 2] = __float_as_uint(__uint_as_float(a[4 * i + 2]) + q.z);
+                    a[4 * i + 3] = __float_as_uint(__uint_as_float(a[4 * i + 3]) + q.w);
                 }
+            }
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * scale, __uint_as_float(a[2 * i + 1]) * scale);
+            if (fine && row < Nq) {
+                uint4 *o = reinterpret_cast<uint4 *>(dst + col);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            }
+        }
+        if constexpr (SPLIT > 1) {
+            if (rank == 1) {
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, 0));
+                tc::wait_peer(peer_done, &g_fa_bwd_status, 4u);
+            } else {
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_done, 1));
             }
         }
     }
@@ -661,35 +763,93 @@ struct Maps {
     CUtensorMap q, k, v, dO;
 };
 
-template <int D, bool CAUSAL>
-cudaError_t launch_dkdv(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dK, void *dV,
-                        cudaStream_t st) {
-    using C = DkdvCfg<D>;
-    auto kern = fa_bwd_dkdv_tc_kernel<D, CAUSAL>;
-    cudaError_t e = set_smem(kern, C::SMEM_BYTES);
+template <typename Kern, typename... Args>
+cudaError_t launch_cluster(Kern kern, uint32_t smem, long long grid, int split, cudaStream_t st, Args... args) {
+    cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    const int kt = (p.Nk + C::BK - 1) / C::BK;
-    const long long grid = (long long)kt * p.BH;
-    kern<<<(unsigned)grid, NTHREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, m.dO, Lp, Dp,
-                                                            static_cast<__nv_bfloat16 *>(dK),
-                                                            static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt,
-                                                            p.scale, p.scale * kLog2e, p.wait_limit);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = split > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+int sm_count() {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+// Split an item over a two-CTA cluster when the longest item's loop is more than
+// 1.5x the average loop length per SM (it, not the total work, would set the time).
+bool worth_splitting(long long n_max, long long total) { return n_max >= 4 && 2 * n_max * sm_count() > 3 * total; }
+
+bool dkdv_split(const FaProblem &p) {
+    const long long ktiles = (p.Nk + 127) / 128, i_end = (p.Nq + 63) / 64;
+    long long total = 0, n_max = 0;
+    for (long long kt = 0; kt < ktiles; ++kt) {
+        const long long first = p.causal ? kt * 2 : 0;
+        const long long n = i_end > first ? i_end - first : 0;
+        total += n;
+        n_max = std::max(n_max, n);
+    }
+    return worth_splitting(n_max, total * p.BH);
+}
+
+bool dq_split(const FaProblem &p) {
+    const long long qtiles = (p.Nq + 127) / 128;
+    long long total = 0, n_max = 0;
+    for (long long qt = 0; qt < qtiles; ++qt) {
+        const long long kend = p.causal ? std::min<long long>(p.Nk, (qt + 1) * 128) : p.Nk;
+        const long long n = (kend + 63) / 64;
+        total += n;
+        n_max = std::max(n_max, n);
+    }
+    return worth_splitting(n_max, total * p.BH);
+}
+
+template <int D, bool CAUSAL, int SPLIT>
+cudaError_t launch_dkdv(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dK, void *dV,
+                        cudaStream_t st) {
+    using C = DkdvCfg<D>;
+    const int kt = (p.Nk + C::BK - 1) / C::BK;
+    return launch_cluster(fa_bwd_dkdv_tc_kernel<D, CAUSAL, SPLIT>, C::SMEM_BYTES, (long long)kt * p.BH * SPLIT, SPLIT,
+                          st, m.q, m.k, m.v, m.dO, Lp, Dp, static_cast<__nv_bfloat16 *>(dK),
+                          static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt, p.scale, p.scale * kLog2e,
+                          p.wait_limit);
+}
+
+template <int D, bool CAUSAL, int SPLIT>
 cudaError_t launch_dq(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dQ,
                       cudaStream_t st) {
     using C = DqCfg<D>;
-    auto kern = fa_bwd_dq_tc_kernel<D, CAUSAL>;
-    cudaError_t e = set_smem(kern, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
     const int qt = (p.Nq + C::BQ - 1) / C::BQ;
-    const long long grid = (long long)qt * p.BH;
-    kern<<<(unsigned)grid, NTHREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, m.dO, Lp, Dp,
-                                                            static_cast<__nv_bfloat16 *>(dQ), p.Nq, p.Nk, p.BH, qt,
-                                                            p.scale, p.scale * kLog2e, p.wait_limit);
-    return cudaGetLastError();
+    return launch_cluster(fa_bwd_dq_tc_kernel<D, CAUSAL, SPLIT>, C::SMEM_BYTES, (long long)qt * p.BH * SPLIT, SPLIT,
+                          st, m.q, m.k, m.v, m.dO, Lp, Dp, static_cast<__nv_bfloat16 *>(dQ), p.Nq, p.Nk, p.BH, qt,
+                          p.scale, p.scale * kLog2e, p.wait_limit);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dkdv_any(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dK, void *dV,
+                            cudaStream_t st) {
+    return dkdv_split(p) ? launch_dkdv<D, CAUSAL, 2>(p, m, Lp, Dp, dK, dV, st)
+                         : launch_dkdv<D, CAUSAL, 1>(p, m, Lp, Dp, dK, dV, st);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dq_any(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dQ,
+                          cudaStream_t st) {
+    return dq_split(p) ? launch_dq<D, CAUSAL, 2>(p, m, Lp, Dp, dQ, st) : launch_dq<D, CAUSAL, 1>(p, m, Lp, Dp, dQ, st);
 }
 
 bool make_maps(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO, int q_rows,
@@ -723,17 +883,19 @@ cudaError_t tc_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const 
                         const float *Lp, const float *Dp, void *dK, void *dV, cudaStream_t st) {
     Maps m;
     if (!make_maps(p, Q, K, V, dO, 64, 128, &m)) return cudaErrorInvalidValue;
-    if (p.d == 128) return p.causal ? launch_dkdv<128, true>(p, m, Lp, Dp, dK, dV, st)
-                                    : launch_dkdv<128, false>(p, m, Lp, Dp, dK, dV, st);
-    return p.causal ? launch_dkdv<64, true>(p, m, Lp, Dp, dK, dV, st) : launch_dkdv<64, false>(p, m, Lp, Dp, dK, dV, st);
+    if (p.d == 128) return p.causal ? launch_dkdv_any<128, true>(p, m, Lp, Dp, dK, dV, st)
+                                    : launch_dkdv_any<128, false>(p, m, Lp, Dp, dK, dV, st);
+    return p.causal ? launch_dkdv_any<64, true>(p, m, Lp, Dp, dK, dV, st)
+                    : launch_dkdv_any<64, false>(p, m, Lp, Dp, dK, dV, st);
 }
 
 cudaError_t tc_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                       const float *Lp, const float *Dp, void *dQ, cudaStream_t st) {
     Maps m;
     if (!make_maps(p, Q, K, V, dO, 128, 64, &m)) return cudaErrorInvalidValue;
-    if (p.d == 128) return p.causal ? launch_dq<128, true>(p, m, Lp, Dp, dQ, st) : launch_dq<128, false>(p, m, Lp, Dp, dQ, st);
-    return p.causal ? launch_dq<64, true>(p, m, Lp, Dp, dQ, st) : launch_dq<64, false>(p, m, Lp, Dp, dQ, st);
+    if (p.d == 128) return p.causal ? launch_dq_any<128, true>(p, m, Lp, Dp, dQ, st)
+                                    : launch_dq_any<128, false>(p, m, Lp, Dp, dQ, st);
+    return p.causal ? launch_dq_any<64, true>(p, m, Lp, Dp, dQ, st) : launch_dq_any<64, false>(p, m, Lp, Dp, dQ, st);
 }
 
 cudaError_t tc_bwd_read_status(unsigned *out, cudaStream_t st) {

@@ -120,6 +120,23 @@ struct Waiter {
     }
 };
 
+// Hand-over wait between the two CTAs of a split work item: bounded (two
+// seconds of global time), but not cut short by this CTA's own abort flag, so
+// that neither CTA exits while the other may still touch its shared memory.
+__device__ __forceinline__ bool wait_peer(uint32_t bar, unsigned *status, uint32_t code) {
+    uint64_t deadline = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait_cluster(bar, 0)) return true;
+        if ((i & 255u) == 0) {
+            const uint64_t now = globaltimer();
+            if (deadline == 0) deadline = now + 2000000000ull;
+            else if (now > deadline) break;
+        }
+    }
+    atomicOr(status, code);
+    return false;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
