@@ -25,8 +25,11 @@
 // so O is rescaled in TMEM rarely; P stays below 2^8 and the final division
 // by l makes the result exact regardless of the max used.
 //
-// TMEM (512 columns): S0 [0,128), S1 [128,256) (P as packed bf16 aliases the
-// first 64 columns of its S), O0 [256, 256+d), O1 [256+d, 256+2d).
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256, 256+d), O1 [256+d,
+// 256+2d).  P (packed bf16, 64 columns) aliases the first half of its S for
+// d = 128; for d = 64 it has its own columns [384 + 64t, 448 + 64t), and the
+// MMA warp issues S_{j+2} as soon as the softmax has read S_j (one barrier
+// per tile), so the tensor core computes the next scores under the softmax.
 //
 // Split work items (SPLIT = 2): when there are too few query tiles to fill the
 // GPU, or the longest causal row would dominate the run, a cluster of two CTAs
@@ -71,7 +74,7 @@ struct FwdCfg {
     static constexpr uint32_t K_OFF = Q_OFF + TILE_BYTES;
     static constexpr uint32_t V_OFF = K_OFF + KST * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = V_OFF + VST * TILE_BYTES;
-    static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 6 + 2;
+    static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 6 + 2 + 2;
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t MISC_OFF = STAT_OFF + 4 * 128 * 4;
     static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;                  // peer_ready, peer_done
@@ -85,6 +88,11 @@ struct FwdCfg {
     static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u ? USED + 1024 : 120u * 1024u);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
+    // d = 64 leaves 128 TMEM columns free: P gets its own columns there, so the
+    // next S of a warpgroup can be issued as soon as the current S has been read
+    static constexpr bool SEP_P = D == 64;
+    static constexpr uint32_t P_COL0 = SEP_P ? 384 : 0;   // P_t at P_COL0 + (SEP_P ? 64 : 128) * t
+    static constexpr uint32_t P_STRIDE = SEP_P ? 64 : 128;
 };
 
 template <int D, bool CAUSAL, int SPLIT>
@@ -125,6 +133,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto o_done = [&](int t) { return bar(RB + 4 + t); };
     const uint32_t drain = bar(RB + 6);
     const uint32_t never = bar(RB + 7);   // fault injection: nothing ever arrives here
+    auto s_free = [&](int t) { return bar(RB + 8 + t); };   // softmax has read S_t (separate-P layout)
     float *m_sm = reinterpret_cast<float *>(sb + C::STAT_OFF);
     float *l_sm = m_sm + 256;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
@@ -144,6 +153,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(s_full(t), 1);
             tc::mbar_init(p_full(t), 128);
             tc::mbar_init(o_done(t), 1);
+            tc::mbar_init(s_free(t), 128);
         }
         tc::mbar_init(drain, 1);
         tc::mbar_init(never, 1);
@@ -233,7 +243,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint64_t vs = vd + ((s * C::TILE_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 16 rows of V = 2048 bytes per k-step
-                    tc::mma_ts(tmem + C::O_COL0 + t * D, tmem + C::S_COL0 + t * 128 + kk * 8, vs + kk * 128,
+                    tc::mma_ts(tmem + C::O_COL0 + t * D, tmem + C::P_COL0 + t * C::P_STRIDE + kk * 8, vs + kk * 128,
                                idesc_o, (k > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(o_done(t));
                 tc::mma_commit(v_empty(s));
@@ -241,9 +251,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             return true;
         };
-        for (int j = 0; ok && j < n; ++j) {
+        auto issue_s = [&](int j) -> bool {   // S_j = Q K_j^T into S_{j&1}
             const int s = j % C::KST, t = j & 1;
-            if (!(ok = __all_sync(0xffffffffu, W.wait(k_full(s), (j / C::KST) & 1)))) break;
+            if (!__all_sync(0xffffffffu, W.wait(k_full(s), (j / C::KST) & 1))) return false;
             if (leader) {
                 const uint64_t ks = kd + ((s * C::TILE_BYTES) >> 4);
 #pragma unroll
@@ -255,9 +265,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc::mma_commit(k_empty(s));
             }
             __syncwarp();
-            if (j >= 1) ok = pv(j - 1);
+            return true;
+        };
+        if constexpr (C::SEP_P) {
+            // S_0, S_1, then per tile: S_{j+2} once S_j has been read, then PV_j once P_j is ready
+            for (int j = 0; ok && j < n && j < 2; ++j) ok = issue_s(j);
+            for (int j = 0; ok && j < n; ++j) {
+                if (j + 2 < n) {
+                    if (!(ok = __all_sync(0xffffffffu, W.wait(s_free(j & 1), (j >> 1) & 1)))) break;
+                    if (!(ok = issue_s(j + 2))) break;
+                }
+                ok = pv(j);
+            }
+        } else {
+            // P aliases S: S_{j+2} can only follow PV_j
+            for (int j = 0; ok && j < n; ++j) {
+                if (!(ok = issue_s(j))) break;
+                if (j >= 1) ok = pv(j - 1);
+            }
+            if (ok && n > 0) ok = pv(n - 1);
         }
-        if (ok && n > 0) ok = pv(n - 1);
         if (!ok && leader) {
             // wait (bounded) for the MMAs already issued before TMEM is released
             tc::mma_commit(drain);
@@ -274,6 +301,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int row = q0 + r;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
         const uint32_t tS = tmem + lane_base + C::S_COL0 + t * 128;
+        const uint32_t tP = tmem + lane_base + C::P_COL0 + t * C::P_STRIDE;
         const uint32_t tO = tmem + lane_base + C::O_COL0 + t * D;
         const int nt = (n - t + 1) >> 1;
         float m = -INFINITY, l = 0.f;
@@ -289,6 +317,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 4; ++c) reg_fence_x32(sr[c]);
+            if constexpr (C::SEP_P) {
+                tc::fence_before_sync();
+                tc::mbar_arrive(s_free(t));   // S_t may now be overwritten by S_{j+2}
+            }
             float s[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
@@ -299,10 +331,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int i = 0; i < 128; ++i)
                     if (i > lim) s[i] = -INFINITY;
             }
-            float mx = tc::fmax3(s[0], s[1], s[2]);
+            // row max as four independent chains (short dependency paths)
+            float mq[4];
 #pragma unroll
-            for (int i = 3; i < 127; i += 2) mx = tc::fmax3(mx, s[i], s[i + 1]);
-            mx = fmaxf(mx, s[127]);
+            for (int q = 0; q < 4; ++q) mq[q] = tc::fmax3(s[q], s[4 + q], s[8 + q]);
+#pragma unroll
+            for (int i = 12; i < 124; i += 8)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mq[q] = tc::fmax3(mq[q], s[i + q], s[i + 4 + q]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mq[q] = fmaxf(mq[q], s[124 + q]);
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             const float m_cand = fmaxf(m, mx * scale_log2);
             const bool rescale = m_cand > m + kRescaleThreshold;
             float alpha = 1.f;
@@ -313,18 +352,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             l *= alpha;
             const float nm = -m;
             uint32_t p[64];
-            float rs0 = 0.f, rs1 = 0.f;
+            float rs[4][2] = {};
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
                 float x0, x1;
                 tc::fma2(x0, x1, s[2 * i], s[2 * i + 1], scale_log2, scale_log2, nm, nm);
                 const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
-                tc::add2(rs0, rs1, rs0, rs1, e0, e1);
+                tc::add2(rs[i & 3][0], rs[i & 3][1], rs[i & 3][0], rs[i & 3][1], e0, e1);
                 p[i] = tc::pack_bf16(e0, e1);
             }
-            l += rs0 + rs1;
-            tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-            tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+            l += ((rs[0][0] + rs[0][1]) + (rs[1][0] + rs[1][1])) + ((rs[2][0] + rs[2][1]) + (rs[3][0] + rs[3][1]));
+            if (C::SEP_P && k > 0) {
+                // P_t is still read by PV of this warpgroup's previous tile until that completes
+                ok = W.wait(o_done(t), (k - 1) & 1);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc::fence_after_sync();
+            }
+            tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+            tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
             if (k > 0 && __any_sync(0xffffffffu, rescale)) {
                 // O_t holds the sum up to this warpgroup's previous tile: rescale it in place
                 ok = W.wait(o_done(t), (k - 1) & 1);
