@@ -279,8 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + kk * 8, om + st + kk * 128, idesc_g, acc);
                         tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + kk * 8, qm + st + kk * 128, idesc_g, acc);
                     }
-                    tc::mma_commit(mma_done(t));
-                    tc::mma_commit(q_empty(s));
+                    tc::mma_commit(q_empty(s));   // sub-tile `it` done: its stage is free
                 }
                 __syncwarp();
                 return true;
@@ -373,11 +372,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // a split item's rank 1 leaves its partial sums for rank 0 to add
         tc::named_bar_sync(1, 256);
         bool fine = !*abort_flag;
-        if (n > 0) {
-            const int n0 = (n + 1) >> 1, n1 = n >> 1;
-            if (fine) fine = W.wait(mma_done(0), (n0 - 1) & 1);
-            if (fine && n1 > 0) fine = W.wait(mma_done(1), (n1 - 1) & 1);
-        }
+        // the last sub-tile's stage release means every MMA has completed (they run in order)
+        if (fine && n > 0) fine = W.wait(q_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
         __nv_bfloat16 *dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
@@ -597,8 +593,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int kk = 0; kk < C::BK / 16; ++kk)
                     tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 64 + kk * 8, km + st + kk * 128, idesc_g,
                                (j > 0 || kk > 0) ? 1u : 0u);
-                tc::mma_commit(mma_done(t));
-                tc::mma_commit(kv_empty(s));
+                tc::mma_commit(kv_empty(s));   // sub-tile j done: its stage is free
             }
             __syncwarp();
             return true;
@@ -681,9 +676,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tc::named_bar_sync(1, 256);
         bool fine = !*abort_flag;
-        const int n0 = (n + 1) >> 1, n1 = n >> 1;
-        if (fine && n0 > 0) fine = W.wait(mma_done(0), (n0 - 1) & 1);
-        if (fine && n1 > 0) fine = W.wait(mma_done(1), (n1 - 1) & 1);
+        // the last sub-tile's stage release means every MMA has completed (they run in order)
+        if (fine && n > 0) fine = W.wait(kv_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
         __nv_bfloat16 *dst = dQ + ((size_t)bh * Nq + row) * D;

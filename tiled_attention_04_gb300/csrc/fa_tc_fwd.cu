@@ -67,6 +67,10 @@ struct FwdCfg {
     // cover an L2-resident TMA reload (~2000 cycles).
     static constexpr int KST = D == 128 ? 3 : 6;
     static constexpr int VST = D == 128 ? 2 : 4;
+    // one "PV_j complete" barrier per tile in a ring of R > KST, VST: it frees K_j's
+    // and V_j's slots (in-order completion covers S_j) and tells the softmax that
+    // P_j / O may be touched again -- one commit instead of three
+    static constexpr int R = D == 128 ? 4 : 8;
     static constexpr int CHUNKS = D / 64;                      // 128-byte swizzle chunks per row
     static constexpr uint32_t CHUNK_BYTES = 128u * 128u;       // 128 rows x 128 bytes
     static constexpr uint32_t TILE_BYTES = CHUNKS * CHUNK_BYTES;
@@ -74,7 +78,7 @@ struct FwdCfg {
     static constexpr uint32_t K_OFF = Q_OFF + TILE_BYTES;
     static constexpr uint32_t V_OFF = K_OFF + KST * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = V_OFF + VST * TILE_BYTES;
-    static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 6 + 2 + 2;
+    static constexpr int NBAR = 1 + KST + VST + R + 4 + 2 + 2;
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t MISC_OFF = STAT_OFF + 4 * 128 * 4;
     static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;                  // peer_ready, peer_done
@@ -123,17 +127,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
     const uint32_t q_full = bar(0);
-    constexpr int RB = 1 + 2 * C::KST + 2 * C::VST;          // first non-ring barrier
+    constexpr int RB = 1 + C::KST + C::VST + C::R;          // first non-ring barrier
     auto k_full = [&](int s) { return bar(1 + s); };
-    auto k_empty = [&](int s) { return bar(1 + C::KST + s); };
-    auto v_full = [&](int s) { return bar(1 + 2 * C::KST + s); };
-    auto v_empty = [&](int s) { return bar(1 + 2 * C::KST + C::VST + s); };
+    auto v_full = [&](int s) { return bar(1 + C::KST + s); };
+    auto pv_done_bar = [&](int j) { return bar(1 + C::KST + C::VST + j % C::R); };
     auto s_full = [&](int t) { return bar(RB + t); };
     auto p_full = [&](int t) { return bar(RB + 2 + t); };
-    auto o_done = [&](int t) { return bar(RB + 4 + t); };
-    const uint32_t drain = bar(RB + 6);
-    const uint32_t never = bar(RB + 7);   // fault injection: nothing ever arrives here
-    auto s_free = [&](int t) { return bar(RB + 8 + t); };   // softmax has read S_t (separate-P layout)
+    const uint32_t drain = bar(RB + 4);
+    const uint32_t never = bar(RB + 5);   // fault injection: nothing ever arrives here
+    auto s_free = [&](int t) { return bar(RB + 6 + t); };   // softmax has read S_t (separate-P layout)
     float *m_sm = reinterpret_cast<float *>(sb + C::STAT_OFF);
     float *l_sm = m_sm + 256;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
@@ -141,18 +143,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (threadIdx.x == 0) {
         tc::mbar_init(q_full, 1);
-        for (int s = 0; s < C::KST; ++s) {
-            tc::mbar_init(k_full(s), 1);
-            tc::mbar_init(k_empty(s), 1);
-        }
-        for (int s = 0; s < C::VST; ++s) {
-            tc::mbar_init(v_full(s), 1);
-            tc::mbar_init(v_empty(s), 1);
-        }
+        for (int s = 0; s < C::KST; ++s) tc::mbar_init(k_full(s), 1);
+        for (int s = 0; s < C::VST; ++s) tc::mbar_init(v_full(s), 1);
+        for (int s = 0; s < C::R; ++s) tc::mbar_init(pv_done_bar(s), 1);
         for (int t = 0; t < 2; ++t) {
             tc::mbar_init(s_full(t), 1);
             tc::mbar_init(p_full(t), 128);
-            tc::mbar_init(o_done(t), 1);
             tc::mbar_init(s_free(t), 128);
         }
         tc::mbar_init(drain, 1);
@@ -190,8 +186,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int c = 0; c < C::CHUNKS; ++c)
                 tc::tma_load_3d(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh);
             int k_issued = 0, v_issued = 0;
-            auto load = [&](const CUtensorMap *m, uint32_t ring, int st, int j, uint32_t full, uint32_t empty) {
-                if (!W.wait(empty, ((j / st) & 1) ^ 1u)) return false;
+            auto load = [&](const CUtensorMap *m, uint32_t ring, int st, int j, uint32_t full) {
+                // the slot last held tile j - st: wait until PV of that tile has completed
+                if (j >= st && !W.wait(pv_done_bar(j - st), ((j - st) / C::R) & 1)) return false;
                 tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
                     tc::tma_load_3d(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64,
@@ -201,12 +198,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // order K_0, K_1, V_0, K_2, V_1, ...: the MMA warp uses K_{j+1} before V_j
             for (int j = 0; j <= n; ++j) {
                 if (j < n) {
-                    if (!load(&tmK, base + C::K_OFF, C::KST, j, k_full(j % C::KST), k_empty(j % C::KST))) break;
+                    if (!load(&tmK, base + C::K_OFF, C::KST, j, k_full(j % C::KST))) break;
                     k_issued = j + 1;
                 }
                 if (j >= 1) {
                     const int v = j - 1;
-                    if (!load(&tmV, base + C::V_OFF, C::VST, v, v_full(v % C::VST), v_empty(v % C::VST))) break;
+                    if (!load(&tmV, base + C::V_OFF, C::VST, v, v_full(v % C::VST))) break;
                     v_issued = v + 1;
                 }
             }
@@ -245,8 +242,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 16 rows of V = 2048 bytes per k-step
                     tc::mma_ts(tmem + C::O_COL0 + t * D, tmem + C::P_COL0 + t * C::P_STRIDE + kk * 8, vs + kk * 128,
                                idesc_o, (k > 0 || kk > 0) ? 1u : 0u);
-                tc::mma_commit(o_done(t));
-                tc::mma_commit(v_empty(s));
+                tc::mma_commit(pv_done_bar(j));
             }
             __syncwarp();
             return true;
@@ -262,7 +258,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tc::mma_ss(tmem + C::S_COL0 + t * 128, qd + off, ks + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(s_full(t));
-                tc::mma_commit(k_empty(s));
             }
             __syncwarp();
             return true;
@@ -364,7 +359,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             l += ((rs[0][0] + rs[0][1]) + (rs[1][0] + rs[1][1])) + ((rs[2][0] + rs[2][1]) + (rs[3][0] + rs[3][1]));
             if (C::SEP_P && k > 0) {
                 // P_t is still read by PV of this warpgroup's previous tile until that completes
-                ok = W.wait(o_done(t), (k - 1) & 1);
+                ok = W.wait(pv_done_bar(2 * k + t - 2), ((2 * k + t - 2) / C::R) & 1);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::fence_after_sync();
             }
@@ -372,7 +367,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
             if (k > 0 && __any_sync(0xffffffffu, rescale)) {
                 // O_t holds the sum up to this warpgroup's previous tile: rescale it in place
-                ok = W.wait(o_done(t), (k - 1) & 1);
+                ok = W.wait(pv_done_bar(2 * k + t - 2), ((2 * k + t - 2) / C::R) & 1);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::fence_after_sync();
 #pragma unroll
@@ -396,8 +391,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::named_bar_sync(1, 256);
         const int n0 = (n + 1) >> 1, n1 = n >> 1;
         bool fine = !*abort_flag;
-        if (fine && n0 > 0) fine = W.wait(o_done(0), (n0 - 1) & 1);
-        if (fine && n1 > 0) fine = W.wait(o_done(1), (n1 - 1) & 1);
+        if (fine && n0 > 0) fine = W.wait(pv_done_bar(2 * n0 - 2), ((2 * n0 - 2) / C::R) & 1);
+        if (fine && n1 > 0) fine = W.wait(pv_done_bar(2 * n1 - 1), ((2 * n1 - 1) / C::R) & 1);
         fine = __all_sync(0xffffffffu, fine);
         // this CTA's partial for row r, columns [t*D/2, (t+1)*D/2), relative to max Mc (unnormalised)
         float v[D / 2];
