@@ -210,6 +210,18 @@ def kernel_flops(w, path):
     return {"fwd": f, "bwd_pre": 0.0, "bwd_dkdv": 2.0 * f, "bwd_dq": 1.5 * f}
 
 
+# DRAM bytes (read + write) per launch of the dominant kernel, from one
+# `ncu --set full` capture of the current kernels (profiles/fa_tc_kernels_*.md);
+# None where no capture of the current build exists for that workload.
+NCU_TRAFFIC = {
+    ("bench_b8_n4096_d64_causal", "bwd_dkdv"): 17069312,
+    ("bench_b8_n4096_d64_causal", "bwd_dq"): 17065216,
+    ("bench_b8_n4096_d64_causal", "fwd"): 12625664,
+    ("long_n16384_d128_causal", "bwd_dkdv"): 16947200,
+    ("long_n16384_d128_causal", "fwd"): 12634624,
+}
+
+
 def run_gpu(args, w, rank, world):
     import torch
 
@@ -331,7 +343,8 @@ def run_gpu(args, w, rank, world):
                 "kernels_ms": {n: round(avg[n], 5) for n in names[1:]}},
         "path": path,
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(dom_tf, 2), "peak": pk["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": round(dom_tf / pk["bf16_tflops"], 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(dom_tf / pk["bf16_tflops"], 4),
+                     "traffic": NCU_TRAFFIC.get((w.name, dom)),
                      "peak_source": f"{pk['source']} bf16 dense burst"},
         "e2e": {"value": round((fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
