@@ -1,7 +1,8 @@
 """Attention fwd+bwd throughput on GB300 through the C ABI (libfa.so).
 
-One step = one forward (fa_fwd) and one backward (fa_bwd_preprocess,
-fa_bwd_dkdv, fa_bwd_dq) over one batch of the workload, inputs resident in HBM.
+One step = one forward (fa_fwd) and one backward (fa_bwd_preprocess, then
+fa_bwd_grads for dK, dV and dQ) over one batch of the workload, inputs
+resident in HBM.
 FLOP convention: forward 4*B*H*Nq*Nk*d, backward 2.5x that, both halved when
 causal.  L2 (129 MB) is flushed by writing a 512 MiB buffer between timed
 steps; each step is timed with CUDA events on the launching stream.
@@ -207,17 +208,15 @@ def kernel_flops(w, path):
     and dP, forms dQ: three), as the forward does two.
     """
     f = 4.0 * w.BH * w.N * w.N * w.d * (0.5 if w.causal else 1.0)   # two N x N x d matmuls
-    return {"fwd": f, "bwd_pre": 0.0, "bwd_dkdv": 2.0 * f, "bwd_dq": 1.5 * f}
+    # fa_bwd_grads runs both passes (one launch on the tensor-core path): 4 + 3 matmuls
+    return {"fwd": f, "bwd_pre": 0.0, "bwd_grads": 3.5 * f}
 
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one
 # `ncu --set full` capture of the current kernels (profiles/fa_tc_kernels_*.md);
 # None where no capture of the current build exists for that workload.
 NCU_TRAFFIC = {
-    ("bench_b8_n4096_d64_causal", "bwd_dkdv"): 17069312,
-    ("bench_b8_n4096_d64_causal", "bwd_dq"): 17065216,
     ("bench_b8_n4096_d64_causal", "fwd"): 12625664,
-    ("long_n16384_d128_causal", "bwd_dkdv"): 16947200,
     ("long_n16384_d128_causal", "fwd"): 12634624,
 }
 
@@ -250,13 +249,11 @@ def run_gpu(args, w, rank, world):
         ev[1].record(stream)
         binding.fa_bwd_preprocess(O, dOd, L, Qd, Kd, w.causal, ws)
         ev[2].record(stream)
-        binding.fa_bwd_dkdv(Qd, Kd, Vd, dOd, L, dQ, dK, dV, w.causal, ws)
+        binding.fa_bwd_grads(Qd, Kd, Vd, dOd, L, dQ, dK, dV, w.causal, ws)
         ev[3].record(stream)
-        binding.fa_bwd_dq(Qd, Kd, Vd, dOd, L, dQ, w.causal, ws)
-        ev[4].record(stream)
 
     def new_events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -276,13 +273,13 @@ def run_gpu(args, w, rank, world):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    names = ["fwd", "bwd_pre", "bwd_dkdv", "bwd_dq"]
+    names = ["fwd", "bwd_pre", "bwd_grads"]
     per = {n: [] for n in names}
     total = []
     for e in evs:
         for i, n in enumerate(names):
             per[n].append(e[i].elapsed_time(e[i + 1]))
-        total.append(e[0].elapsed_time(e[4]))
+        total.append(e[0].elapsed_time(e[3]))
     step_ms = sum(total) / len(total)
     if world > 1:
         t = torch.tensor([step_ms], device=dev)
@@ -329,9 +326,9 @@ def run_gpu(args, w, rank, world):
     dom_tf = kf[dom] / (avg[dom] * 1e-3) / 1e12
     value = world * (fwd_f + bwd_f) / (step_ms * 1e-3) / 1e12
     fwd_tf = fwd_f / (avg["fwd"] * 1e-3) / 1e12
-    bwd_ms = avg["bwd_pre"] + avg["bwd_dkdv"] + avg["bwd_dq"]
+    bwd_ms = avg["bwd_pre"] + avg["bwd_grads"]
     bwd_tf = bwd_f / (bwd_ms * 1e-3) / 1e12
-    launches_per_step = 4
+    launches_per_step = 3 if path == "tc" else 4
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",

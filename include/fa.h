@@ -97,7 +97,7 @@ FA_API size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, int is_
 /*
  * Backward pass (flash_backward).  Reads Q, K, V, O, dO (input dtype) and L
  * (fp32, from fa_fwd on the same inputs); writes dQ, dK, dV (input dtype).
- * Runs fa_bwd_preprocess, then fa_bwd_dkdv and fa_bwd_dq on `stream`.
+ * Runs fa_bwd_preprocess, then fa_bwd_grads, on `stream`.
  * `workspace` must hold fa_bwd_workspace_size(...) bytes, 16-byte aligned;
  * its contents need not be initialised and are scratch afterwards.
  */
@@ -107,13 +107,16 @@ FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void 
                  void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
- * The three phases of fa_bwd, exported so each kernel can be launched and
- * timed on its own.  They must run in this order on one stream, with the same
- * arguments and workspace:
+ * The phases of fa_bwd, exported so each kernel can be launched and timed on
+ * its own.  On one stream, with the same arguments and workspace, run
+ * fa_bwd_preprocess first, then either fa_bwd_grads or both fa_bwd_dkdv and
+ * fa_bwd_dq (any order):
  *   fa_bwd_preprocess: D = rowsum(dO * O) into the workspace (the tensor-core
  *                      path also stages L there, scaled by log2(e) and padded);
  *   fa_bwd_dkdv:       dK, dV (one program per key tile, looping over query tiles);
- *   fa_bwd_dq:         dQ (one program per query tile, looping over key tiles).
+ *   fa_bwd_dq:         dQ (one program per query tile, looping over key tiles);
+ *   fa_bwd_grads:      dK, dV and dQ; on the tensor-core path one launch whose
+ *                      programs take either kind of work, longest first.
  */
 FA_API fa_status fa_bwd_preprocess(const void *O, const void *dO, const float *L,
                             int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype,
@@ -126,6 +129,10 @@ FA_API fa_status fa_bwd_dq(const void *Q, const void *K, const void *V, const vo
                     const float *L, void *dQ,
                     int B, int H, int Nq, int Nk, int d, float scale, int is_causal, fa_dtype dtype,
                     void *workspace, size_t workspace_bytes, fa_stream_t stream);
+FA_API fa_status fa_bwd_grads(const void *Q, const void *K, const void *V, const void *dO,
+                       const float *L, void *dQ, void *dK, void *dV,
+                       int B, int H, int Nq, int Nk, int d, float scale, int is_causal, fa_dtype dtype,
+                       void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
  * fa_bwd without a caller-supplied workspace.  (No counterpart in the method's

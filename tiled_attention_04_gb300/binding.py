@@ -24,6 +24,7 @@ FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
 
 # every function include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq",
+           "fa_bwd_grads",
            "fa_bwd_noalloc", "fa_noalloc_scratch_bytes", "fa_path_name", "fa_get_device_status",
            "fa_reset_device_status", "fa_set_wait_limit", "fa_debug_force_stall", "fa_status_string")
 
@@ -52,6 +53,7 @@ def lib() -> ctypes.CDLL:
     L.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp]
     L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
+    L.fa_bwd_grads.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     L.fa_bwd_noalloc.restype = ctypes.c_int
     L.fa_noalloc_scratch_bytes.argtypes = []
@@ -66,7 +68,8 @@ def lib() -> ctypes.CDLL:
     L.fa_debug_force_stall.restype = None
     L.fa_status_string.argtypes = [i]
     L.fa_status_string.restype = ctypes.c_char_p
-    for name in ("fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_get_device_status",
+    for name in ("fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_grads",
+                 "fa_get_device_status",
                  "fa_reset_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -217,6 +220,15 @@ def fa_bwd_dq(Q, K, V, dO, L, dQ, is_causal, workspace, scale=None, stream=None)
     check(lib().fa_bwd_dq(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(dQ), B, H, Q.shape[-2],
                           K.shape[-2], d, sc, int(is_causal), dtype_code(Q), _ptr(workspace), workspace.numel(),
                           _stream(stream)), "fa_bwd_dq")
+
+
+def fa_bwd_grads(Q, K, V, dO, L, dQ, dK, dV, is_causal, workspace, scale=None, stream=None):
+    B, H = _bh(Q)
+    d = Q.shape[-1]
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    check(lib().fa_bwd_grads(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV), B, H,
+                             Q.shape[-2], K.shape[-2], d, sc, int(is_causal), dtype_code(Q), _ptr(workspace),
+                             workspace.numel(), _stream(stream)), "fa_bwd_grads")
 
 
 def fa_get_device_status(stream=None) -> int:

@@ -221,6 +221,32 @@ fa_status fa_bwd_dq(const void *Q, const void *K, const void *V, const void *dO,
     return map_cuda(e);
 }
 
+fa_status fa_bwd_grads(const void *Q, const void *K, const void *V, const void *dO, const float *L, void *dQ,
+                       void *dK, void *dV, int B, int H, int Nq, int Nk, int d, float scale, int is_causal,
+                       fa_dtype dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    FaProblem p{};
+    Workspace w{};
+    fa_status s = bwd_args(Q, K, V, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace,
+                           workspace_bytes, &p, &w, false);
+    if (s != FA_OK) return s;
+    const bool any_q = (long long)p.BH * p.Nq > 0, any_k = (long long)p.BH * p.Nk > 0;
+    if (!any_q && !any_k) return FA_OK;
+    if (any_q && (s = check_ptrs({Q, K, V, dO, L, dQ})) != FA_OK) return s;
+    if (any_k && (s = check_ptrs({dK, dV})) != FA_OK) return s;
+    if (!w.tc || !any_q) {   // CUDA-core kernels, or no queries (then dK = dV = 0)
+        if ((s = fa_bwd_dkdv(Q, K, V, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace,
+                             workspace_bytes, stream)) != FA_OK)
+            return s;
+        return fa_bwd_dq(Q, K, V, dO, L, dQ, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace, workspace_bytes,
+                         stream);
+    }
+    if ((s = device_ok()) != FA_OK) return s;
+    char *ws = static_cast<char *>(workspace);
+    return map_cuda(tc_bwd_grads(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off),
+                                 reinterpret_cast<const float *>(ws + w.d_off), dQ, dK, dV, true, true,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *L,
                  void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nk, int d, float scale, int is_causal,
                  fa_dtype dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
@@ -237,11 +263,8 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     if ((s = fa_bwd_preprocess(O, dO, L, B, H, Nq, Nk, d, is_causal, dtype, workspace, workspace_bytes, stream)) !=
         FA_OK)
         return s;
-    if ((s = fa_bwd_dkdv(Q, K, V, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace,
-                         workspace_bytes, stream)) != FA_OK)
-        return s;
-    return fa_bwd_dq(Q, K, V, dO, L, dQ, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace, workspace_bytes,
-                     stream);
+    return fa_bwd_grads(Q, K, V, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace,
+                        workspace_bytes, stream);
 }
 
 fa_status fa_get_device_status(fa_stream_t stream) {

@@ -45,6 +45,10 @@ cudaError_t tc_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const 
                         const float *Lp, const float *Dp, void *dK, void *dV, cudaStream_t st);
 cudaError_t tc_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                       const float *Lp, const float *Dp, void *dQ, cudaStream_t st);
+// dK, dV and dQ in one launch (either pass may be switched off)
+cudaError_t tc_bwd_grads(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                         const float *Lp, const float *Dp, void *dQ, void *dK, void *dV, bool do_kv, bool do_q,
+                         cudaStream_t st);
 
 // device-side status words of the tensor-core translation units
 cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st);

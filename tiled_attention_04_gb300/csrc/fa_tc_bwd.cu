@@ -143,13 +143,13 @@ struct DkdvCfg {
     static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
 };
 
+// one dK/dV work item: key tile kt of batch*head bh (a half of it when SPLIT = 2)
 template <int D, bool CAUSAL, int SPLIT>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    fa_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                          const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
-                          __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH, int num_k_tiles, float scale,
-                          float scale_log2, uint32_t wait_limit) {
+__device__ __forceinline__ void dkdv_item(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                          const CUtensorMap &tmdO, const float *__restrict__ Lp,
+                                          const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
+                                          __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, float scale,
+                                          float scale_log2, uint32_t wait_limit) {
     using C = DkdvCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -157,11 +157,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t *sb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // longest first: under causal the first key tiles see the most queries
-    const int item = blockIdx.x / SPLIT;
     const uint32_t rank = SPLIT > 1 ? tc::cluster_rank() : 0u;
-    const int kt = CAUSAL ? item / BH : num_k_tiles - 1 - item / BH;
-    const int bh = item % BH;
     const int k0 = kt * C::BK;
     const int nqp = padded_rows(Nq);
     const int i_end = (Nq + C::BQ - 1) / C::BQ;
@@ -471,12 +467,12 @@ struct DqCfg {
     static constexpr uint32_t DQ_COL = 256;
 };
 
+// one dQ work item: query tile qt of batch*head bh (a half of its keys when SPLIT = 2)
 template <int D, bool CAUSAL, int SPLIT>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    fa_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                        const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ,
-                        int Nq, int Nk, int BH, int num_q_tiles, float scale, float scale_log2, uint32_t wait_limit) {
+__device__ __forceinline__ void dq_item(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                        const CUtensorMap &tmdO, const float *__restrict__ Lp,
+                                        const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ, int Nq, int Nk,
+                                        int qt, int bh, float scale, float scale_log2, uint32_t wait_limit) {
     using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -484,10 +480,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t *sb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int item = blockIdx.x / SPLIT;
     const uint32_t rank = SPLIT > 1 ? tc::cluster_rank() : 0u;
-    const int qt = num_q_tiles - 1 - item / BH;
-    const int bh = item % BH;
     const int q0 = qt * C::BQ;
     const int kend = CAUSAL ? min(Nk, q0 + C::BQ) : Nk;
     const int n_all = (kend + C::BK - 1) / C::BK;
@@ -748,6 +741,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// Both gradient passes in one launch.  The two lists of work items (dK/dV per
+// key tile, dQ per query tile; each longest first) are interleaved so that the
+// long items of both start first and the short ones of both fill the end --
+// one kernel tail instead of two, and the passes balance each other's load.
+template <int D, bool CAUSAL, int SPLIT>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap qA, const __grid_constant__ CUtensorMap kA,
+                     const __grid_constant__ CUtensorMap vA, const __grid_constant__ CUtensorMap dOA,
+                     const __grid_constant__ CUtensorMap qB, const __grid_constant__ CUtensorMap kB,
+                     const __grid_constant__ CUtensorMap vB, const __grid_constant__ CUtensorMap dOB,
+                     const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ,
+                     __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH,
+                     int k_tiles, int q_tiles, int n_kv_items, int n_q_items, float scale, float scale_log2,
+                     uint32_t wait_limit) {
+    const int item = blockIdx.x / SPLIT;
+    const int both = min(n_kv_items, n_q_items);
+    int role, idx;
+    if (item < 2 * both) {
+        role = item & 1;
+        idx = item >> 1;
+    } else {
+        role = n_kv_items > n_q_items ? 0 : 1;
+        idx = item - both;
+    }
+    const int bh = idx % BH;
+    if (role == 0) {
+        const int r = idx / BH;
+        const int kt = CAUSAL ? r : k_tiles - 1 - r;    // causal: the first key tiles see the most queries
+        dkdv_item<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, scale, scale_log2, wait_limit);
+    } else {
+        const int qt = q_tiles - 1 - idx / BH;           // causal: the last query tiles see the most keys
+        dq_item<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, scale, scale_log2, wait_limit);
+    }
+}
+
 template <typename Kern>
 cudaError_t set_smem(Kern k, uint32_t bytes) {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -812,38 +840,29 @@ bool dq_split(const FaProblem &p) {
     return worth_splitting(n_max, total * p.BH);
 }
 
-template <int D, bool CAUSAL, int SPLIT>
-cudaError_t launch_dkdv(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dK, void *dV,
-                        cudaStream_t st) {
-    using C = DkdvCfg<D>;
-    const int kt = (p.Nk + C::BK - 1) / C::BK;
-    return launch_cluster(fa_bwd_dkdv_tc_kernel<D, CAUSAL, SPLIT>, C::SMEM_BYTES, (long long)kt * p.BH * SPLIT, SPLIT,
-                          st, m.q, m.k, m.v, m.dO, Lp, Dp, static_cast<__nv_bfloat16 *>(dK),
-                          static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt, p.scale, p.scale * kLog2e,
-                          p.wait_limit);
-}
+struct Maps2 {
+    Maps a, b;   // a: dK/dV pass boxes (Q, dO 64 rows; K, V 128); b: dQ pass boxes (Q, dO 128; K, V 64)
+};
 
 template <int D, bool CAUSAL, int SPLIT>
-cudaError_t launch_dq(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dQ,
-                      cudaStream_t st) {
-    using C = DqCfg<D>;
-    const int qt = (p.Nq + C::BQ - 1) / C::BQ;
-    return launch_cluster(fa_bwd_dq_tc_kernel<D, CAUSAL, SPLIT>, C::SMEM_BYTES, (long long)qt * p.BH * SPLIT, SPLIT,
-                          st, m.q, m.k, m.v, m.dO, Lp, Dp, static_cast<__nv_bfloat16 *>(dQ), p.Nq, p.Nk, p.BH, qt,
-                          p.scale, p.scale * kLog2e, p.wait_limit);
+cudaError_t launch_bwd(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dQ, void *dK,
+                       void *dV, bool do_kv, bool do_q, cudaStream_t st) {
+    constexpr uint32_t smem = DkdvCfg<D>::SMEM_BYTES > DqCfg<D>::SMEM_BYTES ? DkdvCfg<D>::SMEM_BYTES
+                                                                           : DqCfg<D>::SMEM_BYTES;
+    const int kt = (p.Nk + 127) / 128, qt = (p.Nq + 127) / 128;
+    const long long na = do_kv ? (long long)kt * p.BH : 0, nb = do_q ? (long long)qt * p.BH : 0;
+    return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q, m.a.k, m.a.v,
+                          m.a.dO, m.b.q, m.b.k, m.b.v, m.b.dO, Lp, Dp, static_cast<__nv_bfloat16 *>(dQ),
+                          static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt, qt,
+                          (int)na, (int)nb, p.scale, p.scale * kLog2e, p.wait_limit);
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch_dkdv_any(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dK, void *dV,
-                            cudaStream_t st) {
-    return dkdv_split(p) ? launch_dkdv<D, CAUSAL, 2>(p, m, Lp, Dp, dK, dV, st)
-                         : launch_dkdv<D, CAUSAL, 1>(p, m, Lp, Dp, dK, dV, st);
-}
-
-template <int D, bool CAUSAL>
-cudaError_t launch_dq_any(const FaProblem &p, const Maps &m, const float *Lp, const float *Dp, void *dQ,
-                          cudaStream_t st) {
-    return dq_split(p) ? launch_dq<D, CAUSAL, 2>(p, m, Lp, Dp, dQ, st) : launch_dq<D, CAUSAL, 1>(p, m, Lp, Dp, dQ, st);
+cudaError_t launch_bwd_any(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dQ, void *dK,
+                           void *dV, bool do_kv, bool do_q, cudaStream_t st) {
+    const bool split = (do_kv && dkdv_split(p)) || (do_q && dq_split(p));
+    return split ? launch_bwd<D, CAUSAL, 2>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                 : launch_bwd<D, CAUSAL, 1>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
 }
 
 bool make_maps(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO, int q_rows,
@@ -873,23 +892,26 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
     return cudaGetLastError();
 }
 
+cudaError_t tc_bwd_grads(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                         const float *Lp, const float *Dp, void *dQ, void *dK, void *dV, bool do_kv, bool do_q,
+                         cudaStream_t st) {
+    Maps2 m;
+    if (!make_maps(p, Q, K, V, dO, 64, 128, &m.a) || !make_maps(p, Q, K, V, dO, 128, 64, &m.b))
+        return cudaErrorInvalidValue;
+    if (p.d == 128) return p.causal ? launch_bwd_any<128, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                                    : launch_bwd_any<128, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+    return p.causal ? launch_bwd_any<64, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                    : launch_bwd_any<64, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+}
+
 cudaError_t tc_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                         const float *Lp, const float *Dp, void *dK, void *dV, cudaStream_t st) {
-    Maps m;
-    if (!make_maps(p, Q, K, V, dO, 64, 128, &m)) return cudaErrorInvalidValue;
-    if (p.d == 128) return p.causal ? launch_dkdv_any<128, true>(p, m, Lp, Dp, dK, dV, st)
-                                    : launch_dkdv_any<128, false>(p, m, Lp, Dp, dK, dV, st);
-    return p.causal ? launch_dkdv_any<64, true>(p, m, Lp, Dp, dK, dV, st)
-                    : launch_dkdv_any<64, false>(p, m, Lp, Dp, dK, dV, st);
+    return tc_bwd_grads(p, Q, K, V, dO, Lp, Dp, nullptr, dK, dV, true, false, st);
 }
 
 cudaError_t tc_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                       const float *Lp, const float *Dp, void *dQ, cudaStream_t st) {
-    Maps m;
-    if (!make_maps(p, Q, K, V, dO, 128, 64, &m)) return cudaErrorInvalidValue;
-    if (p.d == 128) return p.causal ? launch_dq_any<128, true>(p, m, Lp, Dp, dQ, st)
-                                    : launch_dq_any<128, false>(p, m, Lp, Dp, dQ, st);
-    return p.causal ? launch_dq_any<64, true>(p, m, Lp, Dp, dQ, st) : launch_dq_any<64, false>(p, m, Lp, Dp, dQ, st);
+    return tc_bwd_grads(p, Q, K, V, dO, Lp, Dp, dQ, nullptr, nullptr, false, true, st);
 }
 
 cudaError_t tc_bwd_read_status(unsigned *out, cudaStream_t st) {
