@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "tc_common.cuh"
@@ -109,13 +110,692 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
     return tc::sdesc_sw128(tile + kk * 16u * 128u, R * 128u, 1024);
 }
 
-struct Roles {
-    int warp, lane;
+// ================================================================== wide sub-tiles (d = 64)
+// ------------------------------------------------------------------ dK / dV (wide)
+// One CTA per 128-key tile (MMA M = 128 keys), looping over 128-query
+// sub-tiles (MMA N = 128 for S^T and dP^T, which run at full rate; K = 128 for
+// dV and dK).  Both element-wise warpgroups work on every sub-tile, warpgroup t
+// on query columns [64t, 64t + 64).
+template <int D>
+struct DkdvWideCfg {
+    static constexpr int BK = 128;                 // keys per CTA (MMA M)
+    static constexpr int BQ = 128;                 // queries per sub-tile
+    // d = 64 leaves TMEM for P^T and dS^T of their own, so S^T and dP^T of the
+    // next sub-tile are computed while the element-wise warps work on this one;
+    // d = 128 writes P^T and dS^T over S^T and dP^T.
+    static constexpr bool SEP = D == 64;
+    static constexpr int STAGES = D == 128 ? 2 : 3;
+    using KT = TileShape<BK, D>;
+    using QT = TileShape<BQ, D>;
+    static constexpr uint32_t K_OFF = 0;
+    static constexpr uint32_t V_OFF = K_OFF + KT::BYTES;
+    static constexpr uint32_t Q_OFF = V_OFF + KT::BYTES;                 // stages of Q sub-tiles
+    static constexpr uint32_t DO_OFF = Q_OFF + STAGES * QT::BYTES;       // stages of dO sub-tiles
+    static constexpr uint32_t LD_OFF = DO_OFF + STAGES * QT::BYTES;      // stages of 128 -L*log2e + 128 -D floats
+    static constexpr uint32_t BAR_OFF = LD_OFF + STAGES * 1024;
+    // kv_full, q_full[S], q_empty[S], sd_full, sd_free, p_full, drain
+    static constexpr int NBAR = 1 + 2 * STAGES + 4;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;
+    static constexpr uint32_t SMEM_BYTES = (PEER_BAR_OFF + 16 + 1024 > 120u * 1024u ? PEER_BAR_OFF + 16 + 1024 : 120u * 1024u);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    // split items: rank 1's partial dV (rows 0..127) and dK (rows 128..255), fp32, over the tile rings
+    static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
+    static constexpr uint32_t PART_OFF = 0;
+    static_assert(PART_OFF + 256 * PART_STRIDE <= BAR_OFF, "partial fits the rings");
+    // TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D);
+    // P^T and dS^T (bf16, 64 columns each) at [384,448) and [448,512), or over S^T / dP^T
+    static constexpr uint32_t ST_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
+    static constexpr uint32_t PT_COL = SEP ? 384 : 0, DS_COL = SEP ? 448 : 128;
 };
 
-// ------------------------------------------------------------------ dK / dV
+// one dK/dV work item: key tile kt of batch*head bh (a half of its queries when SPLIT = 2)
+template <int D, bool CAUSAL, int SPLIT>
+__device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                          const CUtensorMap &tmdO, const float *__restrict__ Lp,
+                                          const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
+                                          __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, float scale,
+                                          float scale_log2, uint32_t wait_limit) {
+    using C = DkdvWideCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const uint32_t rank = SPLIT > 1 ? tc::cluster_rank() : 0u;
+    const int k0 = kt * C::BK;
+    const int nqp = padded_rows(Nq);
+    const int i_end = (Nq + C::BQ - 1) / C::BQ;
+    const int i_first = CAUSAL ? kt : 0;                      // first query sub-tile that sees a key of this tile
+    const int n_all = i_end > i_first ? i_end - i_first : 0;
+    // this CTA's query sub-tiles: all of them, or one half of a split item
+    const int n_half = SPLIT > 1 ? (n_all + 1) / 2 : n_all;
+    const int i_begin = i_first + (rank == 0 ? 0 : n_half);
+    const int n = rank == 0 ? n_half : n_all - n_half;        // sub-tiles to visit
+
+    auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
+    const uint32_t kv_full = bar(0);
+    auto q_full = [&](int s) { return bar(1 + s); };
+    auto q_empty = [&](int s) { return bar(1 + C::STAGES + s); };   // sub-tile's dV/dK MMAs done
+    const uint32_t sd_full = bar(1 + 2 * C::STAGES);
+    const uint32_t sd_free = bar(2 + 2 * C::STAGES);
+    const uint32_t p_full = bar(3 + 2 * C::STAGES);
+    const uint32_t drain = bar(4 + 2 * C::STAGES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(kv_full, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            tc::mbar_init(q_full(s), 1);
+            tc::mbar_init(q_empty(s), 1);
+        }
+        tc::mbar_init(sd_full, 1);
+        tc::mbar_init(sd_free, 256);
+        tc::mbar_init(p_full, 256);
+        tc::mbar_init(drain, 1);
+        if (SPLIT > 1) {
+            tc::mbar_init(base + C::PEER_BAR_OFF, 256);
+            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 256);
+        }
+        *abort_flag = 0u;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (SPLIT > 1) tc::cluster_sync_all();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const tc::Waiter W{abort_flag, &g_fa_bwd_status, wait_limit, 2u};
+
+    if (warp < 4) {
+    tc::regs_dec<56>();
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && n > 0) {
+            tc::tma_prefetch_desc(&tmQ);
+            tc::tma_prefetch_desc(&tmdO);
+            tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
+            for (int c = 0; c < D / 64; ++c) {
+                tc::tma_load_3d(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh);
+                tc::tma_load_3d(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh);
+            }
+            int issued = 0;
+            for (int it = 0; it < n; ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1;
+                if (!W.wait(q_empty(s), ph ^ 1u)) break;
+                const int q0 = (i_begin + it) * C::BQ;
+                tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 1024);
+                for (int c = 0; c < D / 64; ++c) {
+                    tc::tma_load_3d(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
+                                    q0, bh);
+                    tc::tma_load_3d(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
+                                    c * 64, q0, bh);
+                }
+                const size_t off = (size_t)bh * nqp + q0;
+                tc::bulk_load(base + C::LD_OFF + s * 1024, Lp + off, 512, q_full(s));
+                tc::bulk_load(base + C::LD_OFF + s * 1024 + 512, Dp + off, 512, q_full(s));
+                issued = it + 1;
+            }
+            if (*abort_flag) {
+                for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it) {
+                    const int s = it % C::STAGES;
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full(s), (it / C::STAGES) & 1); ++i) {
+                    }
+                }
+                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full, 0); ++i) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // whole warp in the loop (uniform descriptors), one elected lane issues
+        const bool leader = tc::elect_one();
+        if (n > 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BQ, false, false);
+            constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
+            const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);     // A of S^T, K-major
+            const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, 16, 1024);     // A of dP^T
+            const uint64_t qk = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);     // B of S^T, K-major, stage 0
+            const uint64_t gk = tc::sdesc_sw128(base + C::DO_OFF, 16, 1024);    // B of dP^T
+            const uint64_t qm = tc::sdesc_sw128(base + C::Q_OFF, C::QT::CHUNK, 1024);    // B of dK, MN-major
+            const uint64_t gm = tc::sdesc_sw128(base + C::DO_OFF, C::QT::CHUNK, 1024);   // B of dV, MN-major
+            bool ok = __all_sync(0xffffffffu, W.wait(kv_full, 0));
+            auto sdp = [&](int it) -> bool {   // S^T = K Q^T and dP^T = V dO^T for sub-tile `it`
+                const int s = it % C::STAGES;
+                if (!__all_sync(0xffffffffu, W.wait(q_full(s), (it / C::STAGES) & 1))) return false;
+                if (leader) {
+                    const uint32_t st = (s * C::QT::BYTES) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {   // two independent chains, interleaved
+                        const uint32_t oa = ((kk >> 2) * C::KT::CHUNK + (kk & 3) * 32) >> 4;
+                        const uint32_t ob = ((kk >> 2) * C::QT::CHUNK + (kk & 3) * 32) >> 4;
+                        tc::mma_ss(tmem + C::ST_COL, kd + oa, qk + st + ob, idesc_s, kk > 0 ? 1u : 0u);
+                        tc::mma_ss(tmem + C::DP_COL, vd + oa, gk + st + ob, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(sd_full);
+                }
+                __syncwarp();
+                return true;
+            };
+            auto grads = [&](int it) -> bool {   // dV += P^T dO, dK += dS^T Q for sub-tile `it`
+                const int s = it % C::STAGES;
+                if (!__all_sync(0xffffffffu, W.wait(p_full, it & 1))) return false;
+                tc::fence_after_sync();
+                if (leader) {
+                    const uint32_t st = (s * C::QT::BYTES) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < C::BQ / 16; ++kk) {
+                        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                        tc::mma_ts(tmem + C::DV_COL, tmem + C::PT_COL + kk * 8, gm + st + kk * 128, idesc_g, acc);
+                        tc::mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8, qm + st + kk * 128, idesc_g, acc);
+                    }
+                    tc::mma_commit(q_empty(s));   // sub-tile done: its stage is free
+                }
+                __syncwarp();
+                return true;
+            };
+            if (ok) ok = sdp(0);
+            for (int it = 0; ok && it < n; ++it) {
+                if constexpr (C::SEP) {
+                    // the next scores once this sub-tile's have been read, then this sub-tile's gradients
+                    if (it + 1 < n) {
+                        if (!(ok = __all_sync(0xffffffffu, W.wait(sd_free, it & 1)))) break;
+                        if (!(ok = sdp(it + 1))) break;
+                    }
+                    ok = grads(it);
+                } else {
+                    // P^T and dS^T live over S^T and dP^T: the next scores follow the gradients
+                    if (!(ok = grads(it))) break;
+                    if (it + 1 < n) ok = sdp(it + 1);
+                }
+            }
+            if (!ok && leader) {
+                tc::mma_commit(drain);
+                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
+                }
+            }
+            __syncwarp();
+        }
+    }
+    } else {
+        tc::regs_inc<224>();
+        // ------------------------------------------------------------ element-wise warpgroups
+        const int t = (warp - 4) >> 2;                       // query columns [64t, 64t + 64)
+        const int r = ((warp & 3) << 5) + lane;              // key row within the tile = TMEM lane
+        const int key = k0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        const uint32_t tS = tmem + lane_base + C::ST_COL + 64 * t;
+        const uint32_t tD = tmem + lane_base + C::DP_COL + 64 * t;
+        const uint32_t tPT = tmem + lane_base + C::PT_COL + 32 * t;
+        const uint32_t tDS = tmem + lane_base + C::DS_COL + 32 * t;
+        for (int it = 0; it < n; ++it) {
+            const int s = it % C::STAGES;
+            const int qc = (i_begin + it) * C::BQ + 64 * t;      // this warpgroup's first query column
+            bool ok = W.wait(sd_full, it & 1);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            ok = W.wait(q_full(s), (it / C::STAGES) & 1);      // L and D of this sub-tile are in smem
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            uint32_t sv[2][32], dv[2][32];
+            tmem_ld_x32(tS, sv[0]);
+            tmem_ld_x32(tS + 32, sv[1]);
+            tmem_ld_x32(tD, dv[0]);
+            tmem_ld_x32(tD + 32, dv[1]);
+            tc::tmem_ld_wait();
+            reg_fence_x32(sv[0]);
+            reg_fence_x32(sv[1]);
+            reg_fence_x32(dv[0]);
+            reg_fence_x32(dv[1]);
+            tc::fence_before_sync();
+            tc::mbar_arrive(sd_free);                                   // this half of S^T, dP^T has been read
+            if constexpr (!C::SEP) {
+                // P^T / dS^T land over S^T / dP^T: wait until the other warpgroup has read its half too
+                ok = W.wait(sd_free, it & 1);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            const float *lds = reinterpret_cast<const float *>(sb + C::LD_OFF + s * 1024) + 64 * t;   // -L*log2e
+            const bool need_mask = CAUSAL && (key > qc);
+            const int first_visible = key - qc;      // query columns c < key - qc cannot see this key
+            uint32_t pp[32], dsp[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float2 nl = *reinterpret_cast<const float2 *>(lds + 2 * i);
+                const float2 nd = *reinterpret_cast<const float2 *>(lds + 128 + 2 * i);   // -D
+                const int c = 2 * i;
+                float x0, x1, g0, g1;
+                tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
+                         scale_log2, scale_log2, nl.x, nl.y);
+                float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+                if (need_mask) {
+                    if (c < first_visible) p0 = 0.f;
+                    if (c + 1 < first_visible) p1 = 0.f;
+                }
+                tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
+                         nd.x, nd.y);
+                tc::mul2(g0, g1, g0, g1, p0, p1);
+                pp[i] = tc::pack_bf16(p0, p1);
+                dsp[i] = tc::pack_bf16(g0, g1);
+            }
+            if (C::SEP && it > 0) {
+                // P^T and dS^T are still read by the previous sub-tile's gradient MMAs until they complete
+                ok = W.wait(q_empty((it - 1) % C::STAGES), ((it - 1) / C::STAGES) & 1);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                tc::fence_after_sync();
+            }
+            tmem_st_x32(tPT, pp);
+            tmem_st_x32(tDS, dsp);
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            tc::mbar_arrive(p_full);
+        }
+        // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (rows = keys);
+        // a split item's rank 1 leaves its partial sums for rank 0 to add
+        tc::named_bar_sync(1, 256);
+        bool fine = !*abort_flag;
+        // the last sub-tile's stage release means every MMA has completed (they run in order)
+        if (fine && n > 0) fine = W.wait(q_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
+        fine = __all_sync(0xffffffffu, fine);
+        if (fine && n > 0) tc::fence_after_sync();
+        __nv_bfloat16 *dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
+        const float mul = t == 0 ? 1.f : scale;
+        const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
+        const uint32_t part = base + C::PART_OFF + (t * 128 + r) * C::PART_STRIDE;   // this thread's partial row
+        const uint32_t peer_ready = base + C::PEER_BAR_OFF, peer_done = peer_ready + 8;
+        bool merge = false;
+        if constexpr (SPLIT > 1) {
+            if (rank == 0) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 2u);
+        }
+        const uint32_t rpart = SPLIT > 1 ? tc::map_to_rank(part, 1) : 0u;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t a[32];
+            if (fine && n > 0) {
+                tmem_ld_x32(tA + 32 * c, a);
+                tc::tmem_ld_wait();
+                reg_fence_x32(a);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a[i] = 0u;
+            }
+            if (SPLIT > 1 && rank == 1) {
+                float4 *pr = reinterpret_cast<float4 *>(sb + (part - base)) + 8 * c;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    pr[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                        __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+                continue;
+            }
+            if (merge) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 q = tc::ld_cluster_v4(rpart + 128 * c + 16 * i);
+                    a[4 * i + 0] = __float_as_uint(__uint_as_float(a[4 * i + 0]) + q.x);
+                    a[4 * i + 1] = __float_as_uint(__uint_as_float(a[4 * i + 1]) + q.y);
+                    a[4 * i + 2] = __float_as_uint(__uint_as_float(a[4 * i + 2]) + q.z);
+                    a[4 * i + 3] = __float_as_uint(__uint_as_float(a[4 * i + 3]) + q.w);
+                }
+            }
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
+            if (fine && key < Nk) {
+                uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            }
+        }
+        if constexpr (SPLIT > 1) {
+            if (rank == 1) {
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, 0));
+                tc::wait_peer(peer_done, &g_fa_bwd_status, 2u);   // rank 0 reads this partial until then
+            } else {
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_done, 1));
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ dQ (wide)
+// One CTA per 128-query tile (MMA M = 128 queries), looping over 128-key
+// sub-tiles (MMA N = 128 for S and dP; K = 128 for dQ += dS K).  Warpgroup t
+// handles key columns [64t, 64t + 64).  dS has TMEM columns of its own, so the
+// next sub-tile's S and dP are computed while the element-wise warps work.
 template <int D>
-struct DkdvCfg {
+struct DqWideCfg {
+    static constexpr int BQ = 128;                 // queries per CTA (MMA M)
+    static constexpr int BK = 128;                 // keys per sub-tile
+    static constexpr int STAGES = D == 128 ? 2 : 3;
+    using QT = TileShape<BQ, D>;
+    using KT = TileShape<BK, D>;
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t DO_OFF = Q_OFF + QT::BYTES;
+    static constexpr uint32_t K_OFF = DO_OFF + QT::BYTES;                // stages of K sub-tiles
+    static constexpr uint32_t V_OFF = K_OFF + STAGES * KT::BYTES;        // stages of V sub-tiles
+    static constexpr uint32_t BAR_OFF = V_OFF + STAGES * KT::BYTES;
+    // q_full, kv_full[S], kv_empty[S], sd_full, sd_free, p_full, drain
+    static constexpr int NBAR = 1 + 2 * STAGES + 4;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;
+    static constexpr uint32_t SMEM_BYTES = (PEER_BAR_OFF + 16 + 1024 > 120u * 1024u ? PEER_BAR_OFF + 16 + 1024 : 120u * 1024u);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    // split items: rank 1's partial dQ (fp32) over the K/V rings
+    static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
+    static constexpr uint32_t PART_OFF = K_OFF;
+    static_assert(PART_OFF + 128 * PART_STRIDE <= BAR_OFF, "partial fits the rings");
+    // TMEM: S [0,128), dP [128,256), dQ [256, 256+D), dS (bf16, 64 columns) [384, 448)
+    static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256, DS_COL = 384;
+};
+
+// one dQ work item: query tile qt of batch*head bh (a half of its keys when SPLIT = 2)
+template <int D, bool CAUSAL, int SPLIT>
+__device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                        const CUtensorMap &tmdO, const float *__restrict__ Lp,
+                                        const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ, int Nq, int Nk,
+                                        int qt, int bh, float scale, float scale_log2, uint32_t wait_limit) {
+    using C = DqWideCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const uint32_t rank = SPLIT > 1 ? tc::cluster_rank() : 0u;
+    const int q0 = qt * C::BQ;
+    const int kend = CAUSAL ? min(Nk, q0 + C::BQ) : Nk;
+    const int n_all = (kend + C::BK - 1) / C::BK;
+    // this CTA's key sub-tiles [jb, jb + n): all of them, or one half of a split item
+    const int n_half = SPLIT > 1 ? (n_all + 1) / 2 : n_all;
+    const int jb = rank == 0 ? 0 : n_half;
+    const int n = rank == 0 ? n_half : n_all - n_half;
+    const int nqp = padded_rows(Nq);
+
+    auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
+    const uint32_t q_full = bar(0);
+    auto kv_full = [&](int s) { return bar(1 + s); };
+    auto kv_empty = [&](int s) { return bar(1 + C::STAGES + s); };   // sub-tile's dQ MMAs done
+    const uint32_t sd_full = bar(1 + 2 * C::STAGES);
+    const uint32_t sd_free = bar(2 + 2 * C::STAGES);
+    const uint32_t p_full = bar(3 + 2 * C::STAGES);
+    const uint32_t drain = bar(4 + 2 * C::STAGES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(q_full, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            tc::mbar_init(kv_full(s), 1);
+            tc::mbar_init(kv_empty(s), 1);
+        }
+        tc::mbar_init(sd_full, 1);
+        tc::mbar_init(sd_free, 256);
+        tc::mbar_init(p_full, 256);
+        tc::mbar_init(drain, 1);
+        if (SPLIT > 1) {
+            tc::mbar_init(base + C::PEER_BAR_OFF, 256);
+            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 256);
+        }
+        *abort_flag = 0u;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (SPLIT > 1) tc::cluster_sync_all();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const tc::Waiter W{abort_flag, &g_fa_bwd_status, wait_limit, 4u};
+
+    if (warp < 4) {
+    tc::regs_dec<56>();
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmK);
+            tc::tma_prefetch_desc(&tmV);
+            tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
+            for (int c = 0; c < D / 64; ++c) {
+                tc::tma_load_3d(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh);
+                tc::tma_load_3d(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh);
+            }
+            int issued = 0;
+            for (int j = 0; j < n; ++j) {
+                const int s = j % C::STAGES;
+                if (!W.wait(kv_empty(s), ((j / C::STAGES) & 1) ^ 1u)) break;
+                tc::mbar_arrive_expect_tx(kv_full(s), 2 * C::KT::BYTES);
+                for (int c = 0; c < D / 64; ++c) {
+                    tc::tma_load_3d(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
+                                    (jb + j) * C::BK, bh);
+                    tc::tma_load_3d(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
+                                    (jb + j) * C::BK, bh);
+                }
+                issued = j + 1;
+            }
+            if (*abort_flag) {
+                for (int j = issued - 1; j >= 0 && j >= issued - C::STAGES; --j) {
+                    const int s = j % C::STAGES;
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full(s), (j / C::STAGES) & 1); ++i) {
+                    }
+                }
+                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // whole warp in the loop (uniform descriptors), one elected lane issues
+        const bool leader = tc::elect_one();
+        constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BK, false, false);
+        constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
+        const uint64_t qd = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);      // A of S, K-major
+        const uint64_t gd = tc::sdesc_sw128(base + C::DO_OFF, 16, 1024);     // A of dP
+        const uint64_t kk_ = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);    // B of S, K-major, stage 0
+        const uint64_t vk = tc::sdesc_sw128(base + C::V_OFF, 16, 1024);     // B of dP
+        const uint64_t km = tc::sdesc_sw128(base + C::K_OFF, C::KT::CHUNK, 1024);   // B of dQ, MN-major
+        bool ok = __all_sync(0xffffffffu, W.wait(q_full, 0));
+        auto sdp = [&](int j) -> bool {   // S = Q K_j^T and dP = dO V_j^T
+            const int s = j % C::STAGES;
+            if (!__all_sync(0xffffffffu, W.wait(kv_full(s), (j / C::STAGES) & 1))) return false;
+            if (leader) {
+                const uint32_t st = (s * C::KT::BYTES) >> 4;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {   // two independent chains, interleaved
+                    const uint32_t oa = ((kk >> 2) * C::QT::CHUNK + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = ((kk >> 2) * C::KT::CHUNK + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + C::S_COL, qd + oa, kk_ + st + ob, idesc_s, kk > 0 ? 1u : 0u);
+                    tc::mma_ss(tmem + C::DP_COL, gd + oa, vk + st + ob, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(sd_full);
+            }
+            __syncwarp();
+            return true;
+        };
+        auto grads = [&](int j) -> bool {   // dQ += dS K_j
+            const int s = j % C::STAGES;
+            if (!__all_sync(0xffffffffu, W.wait(p_full, j & 1))) return false;
+            tc::fence_after_sync();
+            if (leader) {
+                const uint32_t st = (s * C::KT::BYTES) >> 4;
+#pragma unroll
+                for (int kk = 0; kk < C::BK / 16; ++kk)
+                    tc::mma_ts(tmem + C::DQ_COL, tmem + C::DS_COL + kk * 8, km + st + kk * 128, idesc_g,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(kv_empty(s));   // sub-tile done: its stage is free
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok && n > 0) ok = sdp(0);
+        for (int j = 0; ok && j < n; ++j) {
+            if (j + 1 < n) {
+                if (!(ok = __all_sync(0xffffffffu, W.wait(sd_free, j & 1)))) break;
+                if (!(ok = sdp(j + 1))) break;
+            }
+            ok = grads(j);
+        }
+        if (!ok && leader) {
+            tc::mma_commit(drain);
+            for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
+            }
+        }
+        __syncwarp();
+    }
+    } else {
+        tc::regs_inc<224>();
+        const int t = (warp - 4) >> 2;                       // key columns [64t, 64t + 64)
+        const int r = ((warp & 3) << 5) + lane;
+        const int row = q0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        const uint32_t tS = tmem + lane_base + C::S_COL + 64 * t;
+        const uint32_t tD = tmem + lane_base + C::DP_COL + 64 * t;
+        const uint32_t tDS = tmem + lane_base + C::DS_COL + 32 * t;
+        const float nlrow = Lp[(size_t)bh * nqp + row];     // -L*log2e (-inf on padding rows)
+        const float ndrow = Dp[(size_t)bh * nqp + row];     // -D
+        for (int j = 0; j < n; ++j) {
+            const int kc = (jb + j) * C::BK + 64 * t;        // this warpgroup's first key column
+            bool ok = W.wait(sd_full, j & 1);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            uint32_t sv[2][32], dv[2][32];
+            tmem_ld_x32(tS, sv[0]);
+            tmem_ld_x32(tS + 32, sv[1]);
+            tmem_ld_x32(tD, dv[0]);
+            tmem_ld_x32(tD + 32, dv[1]);
+            tc::tmem_ld_wait();
+            reg_fence_x32(sv[0]);
+            reg_fence_x32(sv[1]);
+            reg_fence_x32(dv[0]);
+            reg_fence_x32(dv[1]);
+            tc::fence_before_sync();
+            tc::mbar_arrive(sd_free);                         // S and dP may be overwritten
+            const bool need_mask = (CAUSAL && kc + 63 > row) || (kc + 64 > Nk);
+            const int lim = min(Nk - 1, CAUSAL ? row : Nk - 1) - kc;   // last visible key column
+            uint32_t dsp[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = 2 * i;
+                float x0, x1, g0, g1;
+                tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
+                         scale_log2, scale_log2, nlrow, nlrow);
+                float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+                if (need_mask) {
+                    if (c > lim) p0 = 0.f;
+                    if (c + 1 > lim) p1 = 0.f;
+                }
+                tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
+                         ndrow, ndrow);
+                tc::mul2(g0, g1, g0, g1, p0, p1);
+                dsp[i] = tc::pack_bf16(g0, g1);
+            }
+            if (j > 0) {
+                // dS is still read by the previous sub-tile's dQ MMAs until they complete
+                ok = W.wait(kv_empty((j - 1) % C::STAGES), ((j - 1) / C::STAGES) & 1);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                tc::fence_after_sync();
+            }
+            tmem_st_x32(tDS, dsp);
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            tc::mbar_arrive(p_full);
+        }
+        tc::named_bar_sync(1, 256);
+        bool fine = !*abort_flag;
+        // the last sub-tile's stage release means every MMA has completed (they run in order)
+        if (fine && n > 0) fine = W.wait(kv_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
+        fine = __all_sync(0xffffffffu, fine);
+        if (fine && n > 0) tc::fence_after_sync();
+        __nv_bfloat16 *dst = dQ + ((size_t)bh * Nq + row) * D;
+        const uint32_t tA = tmem + lane_base + C::DQ_COL;
+        const uint32_t part = base + C::PART_OFF + r * C::PART_STRIDE;
+        const uint32_t peer_ready = base + C::PEER_BAR_OFF, peer_done = peer_ready + 8;
+        bool merge = false;
+        if constexpr (SPLIT > 1) {
+            if (rank == 0) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 4u);
+        }
+        const uint32_t rpart = SPLIT > 1 ? tc::map_to_rank(part, 1) : 0u;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            const int col = t * (D / 2) + 32 * c;
+            uint32_t a[32];
+            if (fine && n > 0) {
+                tmem_ld_x32(tA + col, a);
+                tc::tmem_ld_wait();
+                reg_fence_x32(a);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a[i] = 0u;
+            }
+            if (SPLIT > 1 && rank == 1) {
+                float4 *pr = reinterpret_cast<float4 *>(sb + (part - base) + col * 4);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    pr[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                        __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+                continue;
+            }
+            if (merge) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 q = tc::ld_cluster_v4(rpart + col * 4 + 16 * i);
+                    a[4 * i + 0] = __float_as_uint(__uint_as_float(a[4 * i + 0]) + q.x);
+                    a[4 * i + 1] = __float_as_uint(__uint_as_float(a[4 * i + 1]) + q.y);
+                    a[4 * i + 2] = __float_as_uint(__uint_as_float(a[4 * i + 2]) + q.z);
+                    a[4 * i + 3] = __float_as_uint(__uint_as_float(a[4 * i + 3]) + q.w);
+                }
+            }
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * scale, __uint_as_float(a[2 * i + 1]) * scale);
+            if (fine && row < Nq) {
+                uint4 *o = reinterpret_cast<uint4 *>(dst + col);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            }
+        }
+        if constexpr (SPLIT > 1) {
+            if (rank == 1) {
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, 0));
+                tc::wait_peer(peer_done, &g_fa_bwd_status, 4u);
+            } else {
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_done, 1));
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ================================================================== narrow sub-tiles (d = 128)
+// dK / dV and dQ with 64-wide sub-tiles, each warpgroup taking whole
+// alternate sub-tiles with its own S/dP TMEM buffers (double-buffered), which
+// measures faster than the 128-wide form at d = 128, where TMEM has no room to
+// keep P^T / dS^T apart from S^T / dP^T.
+// ------------------------------------------------------------------ dK / dV (narrow)
+template <int D>
+struct DkdvNarrowCfg {
     static constexpr int BK = 128;                 // keys per CTA (MMA M)
     static constexpr int BQ = 64;                  // queries per sub-tile (MMA N of S^T, K of dV/dK)
     // deep ring: a stage is refilled only after its sub-tile's dV/dK MMAs finish, and
@@ -145,12 +825,12 @@ struct DkdvCfg {
 
 // one dK/dV work item: key tile kt of batch*head bh (a half of it when SPLIT = 2)
 template <int D, bool CAUSAL, int SPLIT>
-__device__ __forceinline__ void dkdv_item(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+__device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                           const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                           const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
                                           __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, float scale,
                                           float scale_log2, uint32_t wait_limit) {
-    using C = DkdvCfg<D>;
+    using C = DkdvNarrowCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -440,12 +1120,12 @@ __device__ __forceinline__ void dkdv_item(const CUtensorMap &tmQ, const CUtensor
     }
 }
 
-// ------------------------------------------------------------------ dQ
+// ------------------------------------------------------------------ dQ (narrow)
 template <int D>
-struct DqCfg {
+struct DqNarrowCfg {
     static constexpr int BQ = 128;                 // queries per CTA (MMA M)
     static constexpr int BK = 64;                  // keys per sub-tile
-    static constexpr int STAGES = D == 128 ? 4 : 8;    // see DkdvCfg
+    static constexpr int STAGES = D == 128 ? 4 : 8;    // see DkdvNarrowCfg
     using QT = TileShape<BQ, D>;
     using KT = TileShape<BK, D>;
     static constexpr uint32_t Q_OFF = 0;
@@ -469,11 +1149,11 @@ struct DqCfg {
 
 // one dQ work item: query tile qt of batch*head bh (a half of its keys when SPLIT = 2)
 template <int D, bool CAUSAL, int SPLIT>
-__device__ __forceinline__ void dq_item(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+__device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                         const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                         const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ, int Nq, int Nk,
                                         int qt, int bh, float scale, float scale_log2, uint32_t wait_limit) {
-    using C = DqCfg<D>;
+    using C = DqNarrowCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -769,10 +1449,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (role == 0) {
         const int r = idx / BH;
         const int kt = CAUSAL ? r : k_tiles - 1 - r;    // causal: the first key tiles see the most queries
-        dkdv_item<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, scale, scale_log2, wait_limit);
+        if constexpr (D == 64)
+            dkdv_item_wide<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, scale, scale_log2, wait_limit);
+        else
+            dkdv_item_narrow<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, scale, scale_log2,
+                                               wait_limit);
     } else {
         const int qt = q_tiles - 1 - idx / BH;           // causal: the last query tiles see the most keys
-        dq_item<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, scale, scale_log2, wait_limit);
+        if constexpr (D == 64)
+            dq_item_wide<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, scale, scale_log2, wait_limit);
+        else
+            dq_item_narrow<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, scale, scale_log2, wait_limit);
     }
 }
 
@@ -814,13 +1501,13 @@ int sm_count() {
 
 // Split an item over a two-CTA cluster when the longest item's loop is more than
 // 1.5x the average loop length per SM (it, not the total work, would set the time).
-bool worth_splitting(long long n_max, long long total) { return n_max >= 4 && 2 * n_max * sm_count() > 3 * total; }
+bool worth_splitting(long long n_max, long long total) { return n_max >= 2 && 2 * n_max * sm_count() > 3 * total; }
 
 bool dkdv_split(const FaProblem &p) {
-    const long long ktiles = (p.Nk + 127) / 128, i_end = (p.Nq + 63) / 64;
+    const long long ktiles = (p.Nk + 127) / 128, i_end = (p.Nq + 127) / 128;
     long long total = 0, n_max = 0;
     for (long long kt = 0; kt < ktiles; ++kt) {
-        const long long first = p.causal ? kt * 2 : 0;
+        const long long first = p.causal ? kt : 0;
         const long long n = i_end > first ? i_end - first : 0;
         total += n;
         n_max = std::max(n_max, n);
@@ -833,7 +1520,7 @@ bool dq_split(const FaProblem &p) {
     long long total = 0, n_max = 0;
     for (long long qt = 0; qt < qtiles; ++qt) {
         const long long kend = p.causal ? std::min<long long>(p.Nk, (qt + 1) * 128) : p.Nk;
-        const long long n = (kend + 63) / 64;
+        const long long n = (kend + 127) / 128;
         total += n;
         n_max = std::max(n_max, n);
     }
@@ -841,14 +1528,15 @@ bool dq_split(const FaProblem &p) {
 }
 
 struct Maps2 {
-    Maps a, b;   // a: dK/dV pass boxes (Q, dO 64 rows; K, V 128); b: dQ pass boxes (Q, dO 128; K, V 64)
+    Maps a, b;   // tensor maps of the dK/dV pass (a) and of the dQ pass (b)
 };
 
 template <int D, bool CAUSAL, int SPLIT>
 cudaError_t launch_bwd(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dQ, void *dK,
                        void *dV, bool do_kv, bool do_q, cudaStream_t st) {
-    constexpr uint32_t smem = DkdvCfg<D>::SMEM_BYTES > DqCfg<D>::SMEM_BYTES ? DkdvCfg<D>::SMEM_BYTES
-                                                                           : DqCfg<D>::SMEM_BYTES;
+    using KvC = std::conditional_t<D == 64, DkdvWideCfg<D>, DkdvNarrowCfg<D>>;
+    using QC = std::conditional_t<D == 64, DqWideCfg<D>, DqNarrowCfg<D>>;
+    constexpr uint32_t smem = KvC::SMEM_BYTES > QC::SMEM_BYTES ? KvC::SMEM_BYTES : QC::SMEM_BYTES;
     const int kt = (p.Nk + 127) / 128, qt = (p.Nq + 127) / 128;
     const long long na = do_kv ? (long long)kt * p.BH : 0, nb = do_q ? (long long)qt * p.BH : 0;
     return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q, m.a.k, m.a.v,
@@ -895,9 +1583,15 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
 cudaError_t tc_bwd_grads(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                          const float *Lp, const float *Dp, void *dQ, void *dK, void *dV, bool do_kv, bool do_q,
                          cudaStream_t st) {
+    // box heights: wide sub-tiles (d = 64) load 128-row tiles everywhere; narrow ones
+    // (d = 128) load 64-row sub-tiles of the looped-over operand
     Maps2 m;
-    if (!make_maps(p, Q, K, V, dO, 64, 128, &m.a) || !make_maps(p, Q, K, V, dO, 128, 64, &m.b))
+    if (p.d == 64) {
+        if (!make_maps(p, Q, K, V, dO, 128, 128, &m.a)) return cudaErrorInvalidValue;
+        m.b = m.a;
+    } else if (!make_maps(p, Q, K, V, dO, 64, 128, &m.a) || !make_maps(p, Q, K, V, dO, 128, 64, &m.b)) {
         return cudaErrorInvalidValue;
+    }
     if (p.d == 128) return p.causal ? launch_bwd_any<128, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
                                     : launch_bwd_any<128, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
     return p.causal ? launch_bwd_any<64, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
