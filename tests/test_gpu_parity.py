@@ -92,6 +92,25 @@ def test_parity_small(cuda_lib, bh, nq, nk, d, dt, causal):
     assert_close(got, oracle_all(t, causal, sc), TOL[dt], f"bh={bh} nq={nq} nk={nk} d={d} {dt} causal={causal}")
 
 
+# Many short query tiles (at least two per SM of a 152-SM part, at most 12 key
+# tiles each on average) run on persistent CTAs that carry their barrier
+# phases, ring slots and TMEM buffers from one unit into the next; these cases
+# put between 2 and 8 units on every CTA, with odd and even key-tile counts so
+# that the buffer parity flips at unit boundaries, and ragged tails.
+PERSISTENT = [
+    (320, 256, 256, 64, "bf16", True), (160, 200, 200, 128, "bf16", True),
+    (600, 256, 256, 64, "bf16", False), (310, 384, 384, 128, "bf16", False),
+]
+
+
+@pytest.mark.parametrize("bh,nq,nk,d,dt,causal", PERSISTENT)
+def test_parity_many_short_units(cuda_lib, bh, nq, nk, d, dt, causal):
+    t = inputs.make_custom(bh, nq, nk, d, dt, seed=2000 + bh + nq + d)
+    got = run_gpu(t, causal)
+    assert_close(got, oracle_all(t, causal, 1.0 / math.sqrt(d)), TOL[dt],
+                 f"bh={bh} nq={nq} nk={nk} d={d} {dt} causal={causal}")
+
+
 @pytest.mark.parametrize("scale", [0.05, 0.25])
 def test_parity_non_default_scale(cuda_lib, scale):
     t = inputs.make_custom(2, 256, 256, 64, "bf16", seed=77)

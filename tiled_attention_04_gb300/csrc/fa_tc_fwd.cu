@@ -78,9 +78,10 @@ struct FwdCfg {
     static constexpr uint32_t K_OFF = Q_OFF + TILE_BYTES;
     static constexpr uint32_t V_OFF = K_OFF + KST * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = V_OFF + VST * TILE_BYTES;
-    static constexpr int NBAR = 1 + KST + VST + R + 4 + 2 + 2;
+    static constexpr int NBAR = 1 + KST + VST + R + 11;
+    // per-row (m, l) of both warpgroups, double-buffered by work unit: 2 x (256 + 256) floats
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t MISC_OFF = STAT_OFF + 4 * 128 * 4;
+    static constexpr uint32_t MISC_OFF = STAT_OFF + 2 * 512 * 4;
     static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;                  // peer_ready, peer_done
     static constexpr uint32_t USED = PEER_BAR_OFF + 16;
     // split items: rank 1's partial O (fp32, rows padded by 4 floats) and its m, l, in the K ring
@@ -506,6 +507,415 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// Persistent form for many short query tiles: one CTA per SM walks a list of
+// work units (one 128-row query tile of one batch*head each).  Same roles,
+// TMEM layout and per-tile pipeline as fa_fwd_tc_kernel; what it adds is the
+// hand-over between units -- the next unit's Q and first K/V tiles load, and
+// its first S MMAs run, under the previous unit's last tiles and epilogue.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    fa_fwd_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
+                     float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
+                     uint32_t wait_limit, uint32_t force_stall) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // Work units are numbered longest first (high query tiles see the most keys
+    // under causal masking) and dealt to the CTAs in snake order: round r gives
+    // CTA b unit r*G + b when r is even and r*G + G-1-b when r is odd, which
+    // evens out the causal lengths.
+    const int num_units = num_q_tiles * BH;
+    const int G = (int)gridDim.x, cb = (int)blockIdx.x;
+    struct Unit {
+        int bh, q0, jb, n;   // batch*head, first query row, first key tile (0), key tiles
+    };
+    auto unit_of = [&](int r, Unit &w) -> bool {
+        const int u = r * G + ((r & 1) ? G - 1 - cb : cb);
+        if (u >= num_units) return false;
+        const int qt = num_q_tiles - 1 - u / BH;
+        w.bh = u % BH;
+        w.q0 = qt * BM;
+        const int kend = CAUSAL ? min(Nk, w.q0 + BM) : Nk;
+        w.jb = 0;
+        w.n = (kend + BN - 1) / BN;
+        return true;
+    };
+
+    // Tiles are numbered globally over this CTA's units (g); the two S / P / O
+    // buffers and softmax warpgroups alternate with g, and every ring index and
+    // barrier phase below follows from g, so one unit runs into the next: its
+    // Q and first K/V tiles load, and its first S MMAs run, under the previous
+    // unit's last tiles and epilogue.
+    auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
+    const uint32_t q_full = bar(0);
+    constexpr int RB = 1 + C::KST + C::VST + C::R;          // first non-ring barrier
+    auto k_full = [&](int s) { return bar(1 + s); };
+    auto v_full = [&](int s) { return bar(1 + C::KST + s); };
+    auto pv_done_bar = [&](int g) { return bar(1 + C::KST + C::VST + (int)((uint32_t)g % C::R)); };
+    auto pv_done_par = [&](int g) { return ((uint32_t)g / C::R) & 1u; };
+    auto s_full = [&](int t) { return bar(RB + t); };
+    auto p_full = [&](int t) { return bar(RB + 2 + t); };
+    const uint32_t drain = bar(RB + 4);
+    const uint32_t never = bar(RB + 5);   // fault injection: nothing ever arrives here
+    auto s_free = [&](int t) { return bar(RB + 6 + t); };   // softmax has read S_t (separate-P layout)
+    const uint32_t q_empty = bar(RB + 8);     // S MMAs of the unit done: the Q buffer may be refilled
+    const uint32_t o_free = bar(RB + 9);      // epilogue has read O_0, O_1: the next unit may overwrite them
+    const uint32_t merge_bar = bar(RB + 10);  // both warpgroups have published their (m, l)
+    float *stat_sm = reinterpret_cast<float *>(sb + C::STAT_OFF);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(q_full, 1);
+        for (int s = 0; s < C::KST; ++s) tc::mbar_init(k_full(s), 1);
+        for (int s = 0; s < C::VST; ++s) tc::mbar_init(v_full(s), 1);
+        for (int s = 0; s < C::R; ++s) tc::mbar_init(pv_done_bar(s), 1);
+        for (int t = 0; t < 2; ++t) {
+            tc::mbar_init(s_full(t), 1);
+            tc::mbar_init(p_full(t), 128);
+            tc::mbar_init(s_free(t), 128);
+        }
+        tc::mbar_init(drain, 1);
+        tc::mbar_init(never, 1);
+        tc::mbar_init(q_empty, 1);
+        tc::mbar_init(o_free, 256);
+        tc::mbar_init(merge_bar, 256);
+        *abort_flag = 0u;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const tc::Waiter W{abort_flag, &g_fa_fwd_status, wait_limit, 1u};
+
+    // registers: warpgroup 0 (producer, MMA issuer, two idle warps) hands its share
+    // to the two softmax warpgroups; each warpgroup changes its budget in one place
+    if (warp < 4) {
+    tc::regs_dec<56>();
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmQ);
+            tc::tma_prefetch_desc(&tmK);
+            tc::tma_prefetch_desc(&tmV);
+            int g0 = 0, k_issued = 0, v_issued = 0, q_issued = 0;
+            bool ok = true;
+            Unit w;
+            for (int u = 0; ok && unit_of(u, w); ++u) {
+                // the Q buffer is refilled once the previous unit's S MMAs have completed
+                if (u > 0 && !(ok = W.wait(q_empty, (u - 1) & 1))) break;
+                tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tc::tma_load_3d(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, w.q0, w.bh);
+                q_issued = u + 1;
+                auto load = [&](const CUtensorMap *m, uint32_t ring, uint32_t st, int g, int key0, uint32_t full) {
+                    // the slot last held tile g - st: wait until PV of that tile has completed
+                    if (g >= (int)st && !W.wait(pv_done_bar(g - (int)st), pv_done_par(g - (int)st))) return false;
+                    tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tc::tma_load_3d(ring + ((uint32_t)g % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full,
+                                        c * 64, key0, w.bh);
+                    return true;
+                };
+                // order K_0, K_1, V_0, K_2, V_1, ...: the MMA warp uses K_{j+1} before V_j
+                for (int j = 0; j <= w.n; ++j) {
+                    if (j < w.n) {
+                        const int g = g0 + j;
+                        if (!(ok = load(&tmK, base + C::K_OFF, C::KST, g, (w.jb + j) * BN, k_full((uint32_t)g % C::KST))))
+                            break;
+                        k_issued = g + 1;
+                    }
+                    if (j >= 1) {
+                        const int g = g0 + j - 1;
+                        if (!(ok = load(&tmV, base + C::V_OFF, C::VST, g, (w.jb + j - 1) * BN,
+                                        v_full((uint32_t)g % C::VST))))
+                            break;
+                        v_issued = g + 1;
+                    }
+                }
+                g0 += w.n;
+            }
+            if (*abort_flag) {
+                // let the copies already in flight land before the CTA exits
+                for (int g = k_issued - 1; g >= 0 && g >= k_issued - C::KST; --g)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(k_full(g % C::KST), (g / C::KST) & 1); ++i) {
+                    }
+                for (int g = v_issued - 1; g >= 0 && g >= v_issued - C::VST; --g)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(v_full(g % C::VST), (g / C::VST) & 1); ++i) {
+                    }
+                if (q_issued > 0)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, (q_issued - 1) & 1); ++i) {
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // The whole warp runs the loop so that descriptors stay warp-uniform and
+        // cheap to form; one elected lane issues the tcgen05 instructions.
+        const bool leader = tc::elect_one();
+        constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN, false, false);
+        constexpr uint32_t idesc_o = tc::idesc_bf16(BM, D, false, true);
+        const uint64_t qd = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);
+        const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);
+        const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, C::CHUNK_BYTES, 1024);
+        bool ok = true;
+        if (force_stall) ok = __all_sync(0xffffffffu, W.wait(never, 0));
+        auto wait_all = [&](uint32_t b, uint32_t par) { return __all_sync(0xffffffffu, W.wait(b, par)); };
+        // ring positions advance by one per S (K ring) and per PV (V ring); g_s and
+        // g_pv are the global indices of the next S and the next PV
+        int k_slot = 0, v_slot = 0, g_s = 0, g_pv = 0;
+        uint32_t k_par = 0, v_par = 0;
+        // S runs LAG tiles ahead of PV: with P in its own columns S_{j+2} can be
+        // computed while the softmax works on S_j; with P over S, S_{j+1} only
+        constexpr int LAG = C::SEP_P ? 2 : 1;
+        Unit w;
+        for (int u = 0; ok && unit_of(u, w); ++u) {
+            const int n = w.n;
+            if (!(ok = wait_all(q_full, u & 1))) break;
+            for (int i = 0; ok && i < n + LAG; ++i) {
+                if (i < n) {
+                    // S_g = Q K_g^T into S_{g&1}; with separate P, S_{g&1} is free once S_{g-2} has been read
+                    const int t = g_s & 1;
+                    if (C::SEP_P && g_s >= 2 && !(ok = wait_all(s_free(t), ((g_s - 2) >> 1) & 1))) break;
+                    if (!(ok = wait_all(k_full(k_slot), k_par))) break;
+                    tc::fence_after_sync();
+                    if (leader) {
+                        const uint64_t ks = kd + ((k_slot * C::TILE_BYTES) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                            tc::mma_ss(tmem + C::S_COL0 + t * 128, qd + off, ks + off, idesc_s, kk > 0 ? 1u : 0u);
+                        }
+                        tc::mma_commit(s_full(t));
+                        if (i == n - 1) tc::mma_commit(q_empty);   // last S of the unit: Q may be refilled
+                    }
+                    __syncwarp();
+                    ++g_s;
+                    if (++k_slot == C::KST) { k_slot = 0; k_par ^= 1u; }
+                }
+                if (i >= LAG) {
+                    // O_t (+)= P_g V_g; the first PV of a unit overwrites O, so the
+                    // previous unit's epilogue must have read it
+                    const int j = i - LAG, t = g_pv & 1;
+                    if (j == 0 && u > 0 && !(ok = wait_all(o_free, (u - 1) & 1))) break;
+                    if (!(ok = wait_all(p_full(t), (g_pv >> 1) & 1))) break;
+                    if (!(ok = wait_all(v_full(v_slot), v_par))) break;
+                    tc::fence_after_sync();
+                    if (leader) {
+                        const uint64_t vs = vd + ((v_slot * C::TILE_BYTES) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 16 rows of V = 2048 bytes per k-step
+                            tc::mma_ts(tmem + C::O_COL0 + t * D, tmem + C::P_COL0 + t * C::P_STRIDE + kk * 8,
+                                       vs + kk * 128, idesc_o, (j >= 2 || kk > 0) ? 1u : 0u);
+                        tc::mma_commit(pv_done_bar(g_pv));
+                    }
+                    __syncwarp();
+                    ++g_pv;
+                    if (++v_slot == C::VST) { v_slot = 0; v_par ^= 1u; }
+                }
+            }
+            if (ok && n == 0) {
+                if (leader) tc::mma_commit(q_empty);   // nothing reads Q: release it at once
+                __syncwarp();
+            }
+        }
+        if (!ok && leader) {
+            // wait (bounded) for the MMAs already issued before TMEM is released
+            tc::mma_commit(drain);
+            for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
+            }
+        }
+        __syncwarp();
+    }
+    } else {
+        tc::regs_inc<224>();
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = (warp - 4) >> 2;
+        const int r = ((warp & 3) << 5) + lane;            // row within the tile = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        const uint32_t tS = tmem + lane_base + C::S_COL0 + t * 128;
+        const uint32_t tP = tmem + lane_base + C::P_COL0 + t * C::P_STRIDE;
+        const uint32_t tO = tmem + lane_base + C::O_COL0 + t * D;
+        bool ok = true;
+        int g0 = 0;
+        Unit w;
+        for (int u = 0; ok && unit_of(u, w); ++u) {
+            const int n = w.n, bh = w.bh, row = w.q0 + r;
+            // this warpgroup's tiles of the unit: local j = jt, jt + 2, ... (global g = g0 + j has parity t)
+            const int j_0 = (0 - g0) & 1, j_1 = (1 - g0) & 1;
+            const int jt = t == 0 ? j_0 : j_1;
+            const int nt = n > jt ? (n - jt + 1) >> 1 : 0;
+            float m = -INFINITY, l = 0.f;
+            for (int k = 0; k < nt; ++k) {
+                const int j = jt + 2 * k, g = g0 + j;
+                const int k0 = (w.jb + j) * BN;
+                ok = W.wait(s_full(t), (g >> 1) & 1);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc::fence_after_sync();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_x32(tS + 32 * c, sr[c]);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) reg_fence_x32(sr[c]);
+                if constexpr (C::SEP_P) {
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(s_free(t));   // S_t may now be overwritten by S_{g+2}
+                }
+                float s[128];
+#pragma unroll
+                for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
+                const bool need_mask = (CAUSAL && k0 + BN - 1 > w.q0) || (k0 + BN > Nk);
+                if (need_mask) {
+                    const int lim = min(Nk - 1, CAUSAL ? row : Nk - 1) - k0;   // last visible column
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        if (i > lim) s[i] = -INFINITY;
+                }
+                // row max as four independent chains (short dependency paths)
+                float mq[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mq[q] = tc::fmax3(s[q], s[4 + q], s[8 + q]);
+#pragma unroll
+                for (int i = 12; i < 124; i += 8)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) mq[q] = tc::fmax3(mq[q], s[i + q], s[i + 4 + q]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mq[q] = fmaxf(mq[q], s[124 + q]);
+                const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+                const float m_cand = fmaxf(m, mx * scale_log2);
+                const bool rescale = m_cand > m + kRescaleThreshold;
+                float alpha = 1.f;
+                if (rescale) {
+                    alpha = tc::ex2(m - m_cand);
+                    m = m_cand;
+                }
+                l *= alpha;
+                const float nm = -m;
+                uint32_t p[64];
+                float rs[4][2] = {};
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    float x0, x1;
+                    tc::fma2(x0, x1, s[2 * i], s[2 * i + 1], scale_log2, scale_log2, nm, nm);
+                    const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
+                    tc::add2(rs[i & 3][0], rs[i & 3][1], rs[i & 3][0], rs[i & 3][1], e0, e1);
+                    p[i] = tc::pack_bf16(e0, e1);
+                }
+                l += ((rs[0][0] + rs[0][1]) + (rs[1][0] + rs[1][1])) + ((rs[2][0] + rs[2][1]) + (rs[3][0] + rs[3][1]));
+                if (C::SEP_P && g >= 2) {
+                    // P_t is still read by the PV of this warpgroup's previous tile until that completes
+                    ok = W.wait(pv_done_bar(g - 2), pv_done_par(g - 2));
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc::fence_after_sync();
+                }
+                tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+                tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                if (k > 0 && __any_sync(0xffffffffu, rescale)) {
+                    // O_t holds the sum up to this warpgroup's previous tile: rescale it in place
+                    ok = W.wait(pv_done_bar(g - 2), pv_done_par(g - 2));
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_x32(tO + 32 * c, o);
+                        tc::tmem_ld_wait();
+                        reg_fence_x32(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st_x32(tO + 32 * c, o);
+                    }
+                }
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+                tc::mbar_arrive(p_full(t));
+            }
+            // ---- merge the two warpgroups' partial results
+            float *m_sm = stat_sm + (u & 1) * 512;
+            float *l_sm = m_sm + 256;
+            m_sm[t * 128 + r] = m;
+            l_sm[t * 128 + r] = l;
+            tc::mbar_arrive(merge_bar);
+            bool fine = W.wait(merge_bar, u & 1) && ok;
+            if (fine && n > 0) fine = W.wait(pv_done_bar(g0 + n - 1), pv_done_par(g0 + n - 1));
+            fine = __all_sync(0xffffffffu, fine);
+            const bool has0 = n > j_0, has1 = n > j_1;
+            // this CTA's partial for row r, columns [t*D/2, (t+1)*D/2), relative to max Mc (unnormalised)
+            float v[D / 2];
+            float Mc = -INFINITY, lc = 0.f;
+#pragma unroll
+            for (int i = 0; i < D / 2; ++i) v[i] = 0.f;
+            if (fine && n > 0) {
+                tc::fence_after_sync();
+                const float m0 = m_sm[r], l0 = l_sm[r];
+                const float m1 = m_sm[128 + r], l1 = l_sm[128 + r];
+                Mc = fmaxf(m0, m1);
+                const float a0 = has0 ? exp2f(m0 - Mc) : 0.f;
+                const float a1 = has1 ? exp2f(m1 - Mc) : 0.f;
+                lc = l0 * a0 + l1 * a1;
+                const uint32_t tO0 = tmem + lane_base + C::O_COL0, tO1 = tO0 + D;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    const int col = t * (D / 2) + 32 * c;
+                    uint32_t o0[32] = {}, o1[32] = {};
+                    if (has0) tmem_ld_x32(tO0 + col, o0);
+                    if (has1) tmem_ld_x32(tO1 + col, o1);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(o0);
+                    reg_fence_x32(o1);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x = has0 ? __uint_as_float(o0[i]) * a0 : 0.f;
+                        if (has1) x = fmaf(__uint_as_float(o1[i]), a1, x);
+                        v[32 * c + i] = x;
+                    }
+                }
+            }
+            // O_0 and O_1 have been read: the next unit's first PV may overwrite them
+            tc::fence_before_sync();
+            tc::mbar_arrive(o_free);
+            auto store_row = [&](const float *vals, float Mrow, float lrow) {
+                const float inv = 1.f / lrow;
+                __nv_bfloat16 *orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
+                if (row < Nq) {
+#pragma unroll
+                    for (int c = 0; c < D / 16; ++c) {
+                        uint4 q;
+                        q.x = tc::pack_bf16(vals[8 * c + 0] * inv, vals[8 * c + 1] * inv);
+                        q.y = tc::pack_bf16(vals[8 * c + 2] * inv, vals[8 * c + 3] * inv);
+                        q.z = tc::pack_bf16(vals[8 * c + 4] * inv, vals[8 * c + 5] * inv);
+                        q.w = tc::pack_bf16(vals[8 * c + 6] * inv, vals[8 * c + 7] * inv);
+                        reinterpret_cast<uint4 *>(orow)[c] = q;
+                    }
+                    if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
+                }
+            };
+            if (fine) store_row(v, Mc, lc);
+            g0 += n;
+            if (!fine) ok = false;
+        }
+    }
+    // ------------------------------------------------------------ teardown
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -541,15 +951,28 @@ bool tc_fwd_supported(const FaProblem &p) {
     return p.dtype == FA_DTYPE_BF16 && (p.d == 64 || p.d == 128) && p.Nq >= 128 && p.Nk >= 128 && p.BH >= 1;
 }
 
-template <int D, bool CAUSAL, int SPLIT>
+static int sm_count() {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+template <int D, bool CAUSAL, int SPLIT, bool PERSIST>
 static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                               void *O, float *L, cudaStream_t st) {
+    static_assert(!(PERSIST && SPLIT > 1), "persistent units are not split");
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT>;
+    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, __nv_bfloat16 *, float *, int, int, int, int,
+                 float, uint32_t, uint32_t);
+    if constexpr (PERSIST) kern = fa_fwd_tc_persistent_kernel<D, CAUSAL>;
+    else kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int qtiles = (p.Nq + BM - 1) / BM;
-    const long long grid = (long long)qtiles * p.BH * SPLIT;
+    // persistent: one CTA per SM walking its share of the work units; otherwise
+    // one CTA (or cluster) per unit, handed out by the hardware as SMs free up
+    const long long units = (long long)qtiles * p.BH;
+    const long long grid = PERSIST ? std::min<long long>(units, sm_count()) : units * SPLIT;
     const float scale_log2 = p.scale * 1.4426950408889634f;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -569,13 +992,18 @@ static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const C
     return cudaGetLastError();
 }
 
-// Work items are split over a cluster of two CTAs when the longest item (a
-// whole row of key tiles) is more than 1.5x the average number of key tiles per
-// SM: then it, not the total work, would set the run time.
-static bool fwd_split(const FaProblem &p) {
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long qtiles = (p.Nq + BM - 1) / BM, ktiles = (p.Nk + BN - 1) / BN;
+enum class FwdMode { kStream, kSplit, kPersist };
+
+// Work units are split over a cluster of two CTAs when the longest one (a whole
+// row of key tiles) is more than 1.5x the average number of key tiles per SM:
+// then it, not the total work, would set the run time.  Many short units (at
+// least two per SM, at most 12 key tiles on average) run on persistent CTAs,
+// which overlap one unit's epilogue with the next unit's loads and first MMAs;
+// otherwise the hardware hands out one unit per CTA, which balances uneven
+// causal lengths by itself.
+static FwdMode fwd_mode(const FaProblem &p) {
+    const int sms = sm_count();
+    const long long qtiles = (p.Nq + BM - 1) / BM;
     long long total = 0, n_max = 0;
     for (long long qt = 0; qt < qtiles; ++qt) {
         const long long kend = p.causal ? std::min<long long>(p.Nk, (qt + 1) * BM) : p.Nk;
@@ -584,15 +1012,20 @@ static bool fwd_split(const FaProblem &p) {
         n_max = std::max(n_max, n);
     }
     total *= p.BH;
-    (void)ktiles;
-    return n_max >= 4 && 2 * n_max * sms > 3 * total;
+    const long long units = qtiles * p.BH;
+    if (n_max >= 4 && 2 * n_max * sms > 3 * total) return FwdMode::kSplit;
+    if (units >= 2LL * sms && total <= 12 * units) return FwdMode::kPersist;
+    return FwdMode::kStream;
 }
 
 template <int D, bool CAUSAL>
 static cudaError_t launch_fwd_any(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                   const CUtensorMap &mv, void *O, float *L, cudaStream_t st) {
-    return fwd_split(p) ? launch_fwd<D, CAUSAL, 2>(p, mq, mk, mv, O, L, st)
-                        : launch_fwd<D, CAUSAL, 1>(p, mq, mk, mv, O, L, st);
+    switch (fwd_mode(p)) {
+        case FwdMode::kSplit: return launch_fwd<D, CAUSAL, 2, false>(p, mq, mk, mv, O, L, st);
+        case FwdMode::kPersist: return launch_fwd<D, CAUSAL, 1, true>(p, mq, mk, mv, O, L, st);
+        default: return launch_fwd<D, CAUSAL, 1, false>(p, mq, mk, mv, O, L, st);
+    }
 }
 
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
