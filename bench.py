@@ -249,48 +249,61 @@ def run_gpu(args, w, rank, world):
     kf = kernel_flops(w, path)
     fwd_f, bwd_f = w.flops()
 
-    def step(ev):
-        ev[0].record(stream)
+    def launch_step():
         binding.fa_fwd(Qd, Kd, Vd, is_causal=w.causal, O=O, L=L)
-        ev[1].record(stream)
         binding.fa_bwd_preprocess(O, dOd, L, Qd, Kd, w.causal, ws)
-        ev[2].record(stream)
         binding.fa_bwd_grads(Qd, Kd, Vd, dOd, L, dQ, dK, dV, w.causal, ws)
-        ev[3].record(stream)
 
-    def new_events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        step(new_events())
+        launch_step()
     torch.cuda.synchronize()
     if binding.fa_get_device_status() != binding.FA_OK:
         raise RuntimeError("device status not ok after warm-up")
 
-    evs = [new_events() for _ in range(args.steps)]
+    # timed region: one event pair per step, so that each kernel may be scheduled
+    # onto SMs the previous one has vacated (programmatic dependent launch)
+    evs = [(ev(), ev()) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        for e in evs:
+        for a, b in evs:
             flush.fill_(1.0)
-            step(e)
+            a.record(stream)
+            launch_step()
+            b.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    names = ["fwd", "bwd_pre", "bwd_grads"]
-    per = {n: [] for n in names}
-    total = []
-    for e in evs:
-        for i, n in enumerate(names):
-            per[n].append(e[i].elapsed_time(e[i + 1]))
-        total.append(e[0].elapsed_time(e[3]))
+    total = [a.elapsed_time(b) for a, b in evs]
     step_ms = sum(total) / len(total)
     if world > 1:
         t = torch.tensor([step_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         step_ms = float(t.item())
+
+    # per-kernel durations (for the fwd / bwd split and the roofline of the dominant
+    # kernel): the same steps with an event between kernels, which serialises them
+    names = ["fwd", "bwd_pre", "bwd_grads"]
+    per = {n: [] for n in names}
+    kevs = [[ev() for _ in range(4)] for _ in range(min(args.steps, 50))]
+    for e in kevs:
+        flush.fill_(1.0)
+        e[0].record(stream)
+        binding.fa_fwd(Qd, Kd, Vd, is_causal=w.causal, O=O, L=L)
+        e[1].record(stream)
+        binding.fa_bwd_preprocess(O, dOd, L, Qd, Kd, w.causal, ws)
+        e[2].record(stream)
+        binding.fa_bwd_grads(Qd, Kd, Vd, dOd, L, dQ, dK, dV, w.causal, ws)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    for e in kevs:
+        for i, n in enumerate(names):
+            per[n].append(e[i].elapsed_time(e[i + 1]))
     if binding.fa_get_device_status() != binding.FA_OK:
         raise RuntimeError("device status not ok after timed steps")
 
@@ -344,6 +357,8 @@ def run_gpu(args, w, rank, world):
         "fwd": {"ms": round(avg["fwd"], 5), "tflops": round(fwd_tf, 2), "frac": round(fwd_tf / pk["bf16_tflops"], 4)},
         "bwd": {"ms": round(bwd_ms, 5), "tflops": round(bwd_tf, 2), "frac": round(bwd_tf / pk["bf16_tflops"], 4),
                 "kernels_ms": {n: round(avg[n], 5) for n in names[1:]}},
+        "breakdown": f"fwd and bwd from per-kernel CUDA events over {len(kevs)} further steps "
+                     "(an event between kernels serialises them; the timed steps carry one event pair each)",
         "path": path,
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(dom_tf, 2), "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(dom_tf / pk["bf16_tflops"], 4),

@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__
                                                          const float *__restrict__ L, float *__restrict__ Dp,
                                                          float *__restrict__ Lp, int BH, int Nq) {
     constexpr int TPR = D / 8;                      // threads per row
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();   // O (from the forward) and dO are complete
     const int nqp = padded_rows(Nq);
     const long long gr = ((long long)blockIdx.x * 256 + threadIdx.x) / TPR;
     const int sub = threadIdx.x % TPR;
@@ -1435,6 +1437,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH,
                      int k_tiles, int q_tiles, int n_kv_items, int n_q_items, float scale, float scale_log2,
                      uint32_t wait_limit) {
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();   // D and L staged by the preprocessing kernel are complete
     const int item = blockIdx.x / SPLIT;
     const int both = min(n_kv_items, n_q_items);
     int role, idx;
@@ -1481,13 +1485,15 @@ cudaError_t launch_cluster(Kern kern, uint32_t smem, long long grid, int split, 
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = split;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = split > 1 ? 1 : 0;
+    cfg.numAttrs = split > 1 ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, args...);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -1573,10 +1579,18 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
     if (rows == 0) return cudaSuccess;
     const auto *o = static_cast<const __nv_bfloat16 *>(O);
     const auto *g = static_cast<const __nv_bfloat16 *>(dO);
-    if (p.d == 128)
-        fa_bwd_pre_kernel<128><<<(unsigned)((rows * 16 + 255) / 256), 256, 0, st>>>(o, g, L, Dp, Lp, p.BH, p.Nq);
-    else
-        fa_bwd_pre_kernel<64><<<(unsigned)((rows * 8 + 255) / 256), 256, 0, st>>>(o, g, L, Dp, Lp, p.BH, p.Nq);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows * (p.d / 8) + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = p.d == 128 ? cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128>, o, g, L, Dp, Lp, p.BH, p.Nq)
+                                     : cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<64>, o, g, L, Dp, Lp, p.BH, p.Nq);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

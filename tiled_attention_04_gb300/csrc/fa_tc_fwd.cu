@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *sb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    tc::pdl_launch_dependents();
 
     // longest work first: high query tiles (more key tiles under causal) start first
     const int item = blockIdx.x / SPLIT;
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (SPLIT > 1) tc::cluster_sync_all();   // the peer's barriers are initialised before anyone arrives
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    tc::pdl_wait();   // the previous kernel's writes (Q, K, V; readers of O and L) are done
     const tc::Waiter W{abort_flag, &g_fa_fwd_status, wait_limit, 1u};
     // registers: warps 0-3 (producer, MMA issuer, two idle) give theirs to the softmax warpgroups
 
@@ -524,6 +526,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *sb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    tc::pdl_launch_dependents();
 
     // Work units are numbered longest first (high query tiles see the most keys
     // under causal masking) and dealt to the CTAs in snake order: round r gives
@@ -596,6 +599,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    tc::pdl_wait();   // the previous kernel's writes (Q, K, V; readers of O and L) are done
     const tc::Waiter W{abort_flag, &g_fa_fwd_status, wait_limit, 1u};
 
     // registers: warpgroup 0 (producer, MMA issuer, two idle warps) hands its share
@@ -979,13 +983,15 @@ static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const C
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = SPLIT;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = SPLIT;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = SPLIT > 1 ? 1 : 0;
+    cfg.numAttrs = SPLIT > 1 ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, static_cast<__nv_bfloat16 *>(O), L, p.Nq, p.Nk, p.BH, qtiles,
                            scale_log2, p.wait_limit, p.force_stall);
     if (e != cudaSuccess) return e;

@@ -137,6 +137,15 @@ __device__ __forceinline__ bool wait_peer(uint32_t bar, unsigned *status, uint32
     return false;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Lets the next kernel in the stream (launched with programmatic stream
+// serialization) be scheduled onto SMs this grid has vacated, once every CTA
+// of this grid has started.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Waits until the grids this one depends on have completed and their memory is
+// visible; every thread calls it before touching global memory they may share.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
