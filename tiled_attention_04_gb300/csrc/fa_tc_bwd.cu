@@ -11,19 +11,28 @@
 //   preprocess   -D and -L*log2(e), padded per batch*head to a multiple of
 //                128 rows (padding rows get -L = -inf, so their P is exactly
 //                zero), in the caller's workspace;
-//   dK/dV pass   one CTA per 128-key tile; loops over 64-query sub-tiles,
-//                recomputing S^T = K Q^T and dP^T = V dO^T in TMEM,
-//                P^T and dS^T (bf16) written back into TMEM, then
-//                dV += P^T dO and dK += dS^T Q with A read from TMEM;
-//   dQ pass      one CTA per 128-query tile; loops over 64-key sub-tiles,
-//                recomputing S = Q K^T and dP = dO V^T, dS into TMEM,
+//   dK/dV items  one per 128-key tile, looping over query sub-tiles:
+//                S^T = K Q^T and dP^T = V dO^T recomputed in TMEM, P^T and
+//                dS^T (bf16) written back into TMEM, then dV += P^T dO and
+//                dK += dS^T Q with A read from TMEM;
+//   dQ items     one per 128-query tile, looping over key sub-tiles:
+//                S = Q K^T and dP = dO V^T recomputed, dS into TMEM,
 //                dQ += dS K.
+// Both kinds of item run in one launch (fa_bwd_tc_kernel), interleaved
+// longest first; an item whose loop would dominate the run is split over a
+// two-CTA cluster and the two partial accumulators are added through
+// distributed shared memory.
 //
-// Both passes use the same warp roles as the forward: warp 0 TMA producer,
-// warp 1 MMA issuer / TMEM owner, warps 4-7 and 8-11 two element-wise
-// warpgroups that take alternate sub-tiles, so that one warpgroup's
-// exponentials overlap the tensor core's work on the other's sub-tile.  The
-// accumulators (dK and dV, or dQ) are shared: every MMA is issued by one
+// Warp roles as in the forward: warp 0 TMA producer, warp 1 MMA issuer and
+// TMEM owner, warps 4-7 and 8-11 two element-wise warpgroups.  Sub-tiles:
+//   d = 64   128 wide (MMA N = 128 for S and dP, which run at full rate);
+//            both warpgroups work on every sub-tile, each on 64 of its
+//            columns, and P^T / dS^T have TMEM columns of their own so the
+//            next sub-tile's S and dP are computed under the element-wise work;
+//   d = 128  64 wide, the warpgroups taking alternate sub-tiles with their
+//            own double-buffered S / dP columns (TMEM has no room for
+//            separate P^T / dS^T next to dK and dV at this head dimension).
+// The accumulators (dK and dV, or dQ) are shared: every MMA is issued by one
 // thread, in order, so the two warpgroups' contributions simply add up.
 // Causal: sub-tiles wholly on the masked side of the diagonal are skipped.
 #include <cuda.h>

@@ -38,6 +38,17 @@
 // shared memory; rank 0 reads it through distributed shared memory, merges it
 // exactly like the two warpgroups' halves, and writes O and L.  The hand-over
 // uses mbarriers arrived on from the other CTA and waited on with a bound.
+//
+// Many short units (at least two per SM, at most 12 key tiles on average):
+// fa_fwd_tc_persistent_kernel runs one CTA per SM over a snake-ordered list of
+// units, numbering tiles across units so that every ring slot, barrier phase
+// and TMEM buffer carries over; the next unit's Q and first K/V tiles load and
+// its first S MMAs run while the softmax warps finish the previous unit.
+//
+// Every kernel here is launched with programmatic stream serialisation: it
+// lets the next kernel be scheduled as soon as all of its CTAs have started,
+// and waits (griddepcontrol.wait) for the previous one before touching global
+// memory, so launch latency overlaps the previous kernel's tail.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
