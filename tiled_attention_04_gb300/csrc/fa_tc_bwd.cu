@@ -372,27 +372,35 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                 if (!__all_sync(0xffffffffu, ok)) break;
             }
             const float *lds = reinterpret_cast<const float *>(sb + C::LD_OFF + s * 1024) + 64 * t;   // -L*log2e
-            const bool need_mask = CAUSAL && (key > qc);
-            const int first_visible = key - qc;      // query columns c < key - qc cannot see this key
+            // causal: query columns c < key - qc cannot see this key.  Only the
+            // diagonal sub-tile has such columns; there S^T is set to -inf first
+            // (P = 2^-inf = 0 and dS = 0), so the main loop carries no mask test.
+            const int first_visible = key - qc;
+            if (CAUSAL && __any_sync(0xffffffffu, first_visible > 0)) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c < first_visible) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+            }
             uint32_t pp[32], dsp[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float2 nl = *reinterpret_cast<const float2 *>(lds + 2 * i);
-                const float2 nd = *reinterpret_cast<const float2 *>(lds + 128 + 2 * i);   // -D
-                const int c = 2 * i;
-                float x0, x1, g0, g1;
-                tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
-                         scale_log2, scale_log2, nl.x, nl.y);
-                float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-                if (need_mask) {
-                    if (c < first_visible) p0 = 0.f;
-                    if (c + 1 < first_visible) p1 = 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const float4 nl = *reinterpret_cast<const float4 *>(lds + 4 * i);
+                const float4 nd = *reinterpret_cast<const float4 *>(lds + 128 + 4 * i);   // -D
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = 4 * i + 2 * h;
+                    const float l0 = h ? nl.z : nl.x, l1 = h ? nl.w : nl.y;
+                    const float d0 = h ? nd.z : nd.x, d1 = h ? nd.w : nd.y;
+                    float x0, x1, g0, g1;
+                    tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
+                             scale_log2, scale_log2, l0, l1);
+                    const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+                    tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
+                             d0, d1);
+                    tc::mul2(g0, g1, g0, g1, p0, p1);
+                    pp[2 * i + h] = tc::pack_bf16(p0, p1);
+                    dsp[2 * i + h] = tc::pack_bf16(g0, g1);
                 }
-                tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
-                         nd.x, nd.y);
-                tc::mul2(g0, g1, g0, g1, p0, p1);
-                pp[i] = tc::pack_bf16(p0, p1);
-                dsp[i] = tc::pack_bf16(g0, g1);
             }
             if (C::SEP && it > 0) {
                 // P^T and dS^T are still read by the previous sub-tile's gradient MMAs until they complete
@@ -695,8 +703,14 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
             reg_fence_x32(dv[1]);
             tc::fence_before_sync();
             tc::mbar_arrive(sd_free);                         // S and dP may be overwritten
-            const bool need_mask = (CAUSAL && kc + 63 > row) || (kc + 64 > Nk);
+            // key columns past the diagonal (causal) or past Nk: S set to -inf first
+            // (P = 0, dS = 0), so the main loop carries no mask test
             const int lim = min(Nk - 1, CAUSAL ? row : Nk - 1) - kc;   // last visible key column
+            if (__any_sync(0xffffffffu, lim < 63)) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+            }
             uint32_t dsp[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -704,11 +718,7 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
                 float x0, x1, g0, g1;
                 tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
                          scale_log2, scale_log2, nlrow, nlrow);
-                float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-                if (need_mask) {
-                    if (c > lim) p0 = 0.f;
-                    if (c + 1 > lim) p1 = 0.f;
-                }
+                const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
                 tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
                          ndrow, ndrow);
                 tc::mul2(g0, g1, g0, g1, p0, p1);
