@@ -1037,27 +1037,34 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
             reg_fence_x32(dv[0]);
             reg_fence_x32(dv[1]);
             const float *lds = reinterpret_cast<const float *>(sb + C::LD_OFF + s * 512);   // -L*log2e, -D
-            const bool need_mask = CAUSAL && (k0 + 127 > q0);
-            const int first_visible = key - q0;      // query columns c < key - q0 cannot see this key
+            // causal: query columns c < key - q0 cannot see this key; where a sub-tile
+            // has such columns, S^T is set to -inf first (P = 0, dS = 0)
+            const int first_visible = key - q0;
+            if (CAUSAL && __any_sync(0xffffffffu, first_visible > 0)) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c < first_visible) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+            }
             uint32_t pp[32], dsp[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float2 nl = *reinterpret_cast<const float2 *>(lds + 2 * i);
-                const float2 nd = *reinterpret_cast<const float2 *>(lds + 64 + 2 * i);
-                const int c = 2 * i;
-                float x0, x1, g0, g1;
-                tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
-                         scale_log2, scale_log2, nl.x, nl.y);
-                float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-                if (need_mask) {
-                    if (c < first_visible) p0 = 0.f;
-                    if (c + 1 < first_visible) p1 = 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const float4 nl = *reinterpret_cast<const float4 *>(lds + 4 * i);
+                const float4 nd = *reinterpret_cast<const float4 *>(lds + 64 + 4 * i);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = 4 * i + 2 * h;
+                    const float l0 = h ? nl.z : nl.x, l1 = h ? nl.w : nl.y;
+                    const float d0 = h ? nd.z : nd.x, d1 = h ? nd.w : nd.y;
+                    float x0, x1, g0, g1;
+                    tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
+                             scale_log2, scale_log2, l0, l1);
+                    const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+                    tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
+                             d0, d1);
+                    tc::mul2(g0, g1, g0, g1, p0, p1);
+                    pp[2 * i + h] = tc::pack_bf16(p0, p1);
+                    dsp[2 * i + h] = tc::pack_bf16(g0, g1);
                 }
-                tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
-                         nd.x, nd.y);
-                tc::mul2(g0, g1, g0, g1, p0, p1);
-                pp[i] = tc::pack_bf16(p0, p1);
-                dsp[i] = tc::pack_bf16(g0, g1);
             }
             tmem_st_x32(tS, pp);
             tmem_st_x32(tP, dsp);
@@ -1344,8 +1351,13 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
             reg_fence_x32(sv[1]);
             reg_fence_x32(dv[0]);
             reg_fence_x32(dv[1]);
-            const bool need_mask = (CAUSAL && kb0 + C::BK - 1 > q0) || (kb0 + C::BK > Nk);
+            // key columns past the diagonal (causal) or past Nk: S set to -inf first (P = 0, dS = 0)
             const int lim = min(Nk - 1, CAUSAL ? row : Nk - 1) - kb0;   // last visible key column
+            if (__any_sync(0xffffffffu, lim < C::BK - 1)) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+            }
             uint32_t dsp[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -1353,11 +1365,7 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                 float x0, x1, g0, g1;
                 tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
                          scale_log2, scale_log2, nlrow, nlrow);
-                float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-                if (need_mask) {
-                    if (c > lim) p0 = 0.f;
-                    if (c + 1 > lim) p1 = 0.f;
-                }
+                const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
                 tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
                          ndrow, ndrow);
                 tc::mul2(g0, g1, g0, g1, p0, p1);
