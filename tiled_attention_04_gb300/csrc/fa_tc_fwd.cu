@@ -200,9 +200,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int c = 0; c < C::CHUNKS; ++c)
                 tc::tma_load_3d(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh);
             int k_issued = 0, v_issued = 0;
-            auto load = [&](const CUtensorMap *m, uint32_t ring, int st, int j, uint32_t full) {
-                // the slot last held tile j - st: wait until PV of that tile has completed
-                if (j >= st && !W.wait(pv_done_bar(j - st), ((j - st) / C::R) & 1)) return false;
+            // The slot of tile j last held tile j - st.  A V slot is free once PV of that
+            // tile has completed.  A K slot is read only by S of that tile; with P over S
+            // the MMA warp issues S_{x+1} before PV_x (and S_0, S_1 before PV_0), so the
+            // K slot is free once PV_{j-st-1} has completed.  (With P in its own columns
+            // the K ring is deep enough to keep waiting for PV_{j-st}.)
+            auto load = [&](const CUtensorMap *m, uint32_t ring, int st, int j, uint32_t full, int lag) {
+                const int g = j - st - lag < 0 ? 0 : j - st - lag;
+                if (j >= st && !W.wait(pv_done_bar(g), (g / C::R) & 1)) return false;
                 tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
                     tc::tma_load_3d(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64,
@@ -212,12 +217,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // order K_0, K_1, V_0, K_2, V_1, ...: the MMA warp uses K_{j+1} before V_j
             for (int j = 0; j <= n; ++j) {
                 if (j < n) {
-                    if (!load(&tmK, base + C::K_OFF, C::KST, j, k_full(j % C::KST))) break;
+                    if (!load(&tmK, base + C::K_OFF, C::KST, j, k_full(j % C::KST), C::SEP_P ? 0 : 1)) break;
                     k_issued = j + 1;
                 }
                 if (j >= 1) {
                     const int v = j - 1;
-                    if (!load(&tmV, base + C::V_OFF, C::VST, v, v_full(v % C::VST))) break;
+                    if (!load(&tmV, base + C::V_OFF, C::VST, v, v_full(v % C::VST), 0)) break;
                     v_issued = v + 1;
                 }
             }
