@@ -252,8 +252,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (force_stall) ok = __all_sync(0xffffffffu, W.wait(never, 0));
         auto pv = [&](int j) -> bool {
             const int s = j % C::VST, t = j & 1, k = j >> 1;
-            if (!__all_sync(0xffffffffu, W.wait(p_full(t), k & 1))) return false;
-            if (!__all_sync(0xffffffffu, W.wait(v_full(s), (j / C::VST) & 1))) return false;
+            if (!__all_sync(0xffffffffu, W.wait2(p_full(t), k & 1, v_full(s), (j / C::VST) & 1))) return false;
             tc::fence_after_sync();
             if (leader) {
                 const uint64_t vs = vd + ((s * C::TILE_BYTES) >> 4);
@@ -266,9 +265,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             return true;
         };
-        auto issue_s = [&](int j) -> bool {   // S_j = Q K_j^T into S_{j&1}
+        // S_j = Q K_j^T into S_{j&1}; with P in its own columns S_{j&1} must first have
+        // been read by the softmax (tile j - 2): both waits are polled together
+        auto issue_s = [&](int j) -> bool {
             const int s = j % C::KST, t = j & 1;
-            if (!__all_sync(0xffffffffu, W.wait(k_full(s), (j / C::KST) & 1))) return false;
+            const bool ok_k = (C::SEP_P && j >= 2)
+                                  ? W.wait2(s_free(t), ((j - 2) >> 1) & 1, k_full(s), (j / C::KST) & 1)
+                                  : W.wait(k_full(s), (j / C::KST) & 1);
+            if (!__all_sync(0xffffffffu, ok_k)) return false;
             if (leader) {
                 const uint64_t ks = kd + ((s * C::TILE_BYTES) >> 4);
 #pragma unroll
@@ -285,10 +289,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // S_0, S_1, then per tile: S_{j+2} once S_j has been read, then PV_j once P_j is ready
             for (int j = 0; ok && j < n && j < 2; ++j) ok = issue_s(j);
             for (int j = 0; ok && j < n; ++j) {
-                if (j + 2 < n) {
-                    if (!(ok = __all_sync(0xffffffffu, W.wait(s_free(j & 1), (j >> 1) & 1)))) break;
-                    if (!(ok = issue_s(j + 2))) break;
-                }
+                if (j + 2 < n && !(ok = issue_s(j + 2))) break;
                 ok = pv(j);
             }
         } else {

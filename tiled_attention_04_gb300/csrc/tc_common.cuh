@@ -118,6 +118,15 @@ struct Waiter {
         atomicOr(status, code);
         return false;
     }
+
+    // Two waits whose first polls are issued back to back, so that the common case
+    // (both phases already complete) costs one shared-memory round trip, not two.
+    __device__ __forceinline__ bool wait2(uint32_t bar0, uint32_t parity0, uint32_t bar1, uint32_t parity1) const {
+        const bool r0 = mbar_try_wait(bar0, parity0);
+        const bool r1 = mbar_try_wait(bar1, parity1);
+        if (r0 && r1) return true;
+        return (r0 || wait(bar0, parity0)) && (r1 || wait(bar1, parity1));
+    }
 };
 
 // Hand-over wait between the two CTAs of a split work item: bounded (two
