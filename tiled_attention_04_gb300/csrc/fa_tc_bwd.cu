@@ -278,9 +278,13 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
             const uint64_t qm = tc::sdesc_sw128(base + C::Q_OFF, C::QT::CHUNK, 1024);    // B of dK, MN-major
             const uint64_t gm = tc::sdesc_sw128(base + C::DO_OFF, C::QT::CHUNK, 1024);   // B of dV, MN-major
             bool ok = __all_sync(0xffffffffu, W.wait(kv_full, 0));
-            auto sdp = [&](int it) -> bool {   // S^T = K Q^T and dP^T = V dO^T for sub-tile `it`
+            // S^T = K Q^T and dP^T = V dO^T for sub-tile `it`; after the first, S^T / dP^T
+            // must also have been read for sub-tile it-1 (both waits polled together)
+            auto sdp = [&](int it) -> bool {
                 const int s = it % C::STAGES;
-                if (!__all_sync(0xffffffffu, W.wait(q_full(s), (it / C::STAGES) & 1))) return false;
+                const bool ready = it > 0 ? W.wait2(sd_free, (it - 1) & 1, q_full(s), (it / C::STAGES) & 1)
+                                          : W.wait(q_full(s), (it / C::STAGES) & 1);
+                if (!__all_sync(0xffffffffu, ready)) return false;
                 if (leader) {
                     const uint32_t st = (s * C::QT::BYTES) >> 4;
 #pragma unroll
@@ -316,10 +320,7 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
             for (int it = 0; ok && it < n; ++it) {
                 if constexpr (C::SEP) {
                     // the next scores once this sub-tile's have been read, then this sub-tile's gradients
-                    if (it + 1 < n) {
-                        if (!(ok = __all_sync(0xffffffffu, W.wait(sd_free, it & 1)))) break;
-                        if (!(ok = sdp(it + 1))) break;
-                    }
+                    if (it + 1 < n && !(ok = sdp(it + 1))) break;
                     ok = grads(it);
                 } else {
                     // P^T and dS^T live over S^T and dP^T: the next scores follow the gradients
@@ -349,9 +350,8 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         for (int it = 0; it < n; ++it) {
             const int s = it % C::STAGES;
             const int qc = (i_begin + it) * C::BQ + 64 * t;      // this warpgroup's first query column
-            bool ok = W.wait(sd_full, it & 1);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            ok = W.wait(q_full(s), (it / C::STAGES) & 1);      // L and D of this sub-tile are in smem
+            // S^T, dP^T of this sub-tile, and its L and D in shared memory
+            bool ok = W.wait2(sd_full, it & 1, q_full(s), (it / C::STAGES) & 1);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
             uint32_t sv[2][32], dv[2][32];
@@ -628,9 +628,13 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
         const uint64_t vk = tc::sdesc_sw128(base + C::V_OFF, 16, 1024);     // B of dP
         const uint64_t km = tc::sdesc_sw128(base + C::K_OFF, C::KT::CHUNK, 1024);   // B of dQ, MN-major
         bool ok = __all_sync(0xffffffffu, W.wait(q_full, 0));
-        auto sdp = [&](int j) -> bool {   // S = Q K_j^T and dP = dO V_j^T
+        // S = Q K_j^T and dP = dO V_j^T; after the first, S / dP must also have been read
+        // for sub-tile j-1 (both waits polled together)
+        auto sdp = [&](int j) -> bool {
             const int s = j % C::STAGES;
-            if (!__all_sync(0xffffffffu, W.wait(kv_full(s), (j / C::STAGES) & 1))) return false;
+            const bool ready = j > 0 ? W.wait2(sd_free, (j - 1) & 1, kv_full(s), (j / C::STAGES) & 1)
+                                     : W.wait(kv_full(s), (j / C::STAGES) & 1);
+            if (!__all_sync(0xffffffffu, ready)) return false;
             if (leader) {
                 const uint32_t st = (s * C::KT::BYTES) >> 4;
 #pragma unroll
@@ -662,10 +666,7 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
         };
         if (ok && n > 0) ok = sdp(0);
         for (int j = 0; ok && j < n; ++j) {
-            if (j + 1 < n) {
-                if (!(ok = __all_sync(0xffffffffu, W.wait(sd_free, j & 1)))) break;
-                if (!(ok = sdp(j + 1))) break;
-            }
+            if (j + 1 < n && !(ok = sdp(j + 1))) break;
             ok = grads(j);
         }
         if (!ok && leader) {
