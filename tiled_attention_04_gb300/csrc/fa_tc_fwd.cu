@@ -707,8 +707,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (i < n) {
                     // S_g = Q K_g^T into S_{g&1}; with separate P, S_{g&1} is free once S_{g-2} has been read
                     const int t = g_s & 1;
-                    if (C::SEP_P && g_s >= 2 && !(ok = wait_all(s_free(t), ((g_s - 2) >> 1) & 1))) break;
-                    if (!(ok = wait_all(k_full(k_slot), k_par))) break;
+                    const bool ready = (C::SEP_P && g_s >= 2)
+                                           ? W.wait2(s_free(t), ((g_s - 2) >> 1) & 1, k_full(k_slot), k_par)
+                                           : W.wait(k_full(k_slot), k_par);
+                    if (!(ok = __all_sync(0xffffffffu, ready))) break;
                     tc::fence_after_sync();
                     if (leader) {
                         const uint64_t ks = kd + ((k_slot * C::TILE_BYTES) >> 4);
@@ -729,8 +731,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // previous unit's epilogue must have read it
                     const int j = i - LAG, t = g_pv & 1;
                     if (j == 0 && u > 0 && !(ok = wait_all(o_free, (u - 1) & 1))) break;
-                    if (!(ok = wait_all(p_full(t), (g_pv >> 1) & 1))) break;
-                    if (!(ok = wait_all(v_full(v_slot), v_par))) break;
+                    if (!(ok = __all_sync(0xffffffffu, W.wait2(p_full(t), (g_pv >> 1) & 1, v_full(v_slot), v_par))))
+                        break;
                     tc::fence_after_sync();
                     if (leader) {
                         const uint64_t vs = vd + ((v_slot * C::TILE_BYTES) >> 4);
