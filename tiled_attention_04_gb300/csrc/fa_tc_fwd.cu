@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // registers: warpgroup 0 (producer, MMA issuer, two idle warps) hands its share
     // to the two softmax warpgroups; each warpgroup changes its budget in one place
     if (warp < 4) {
-    tc::regs_dec<56>();
+    tc::regs_dec<(SPLIT > 1 ? 72 : 56)>();   // split items keep cluster state: 72 avoids a spill
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
     }
     } else {
-        tc::regs_inc<224>();
+        tc::regs_inc<(SPLIT > 1 ? 216 : 224)>();
         // ------------------------------------------------------------ softmax warpgroups
         const int t = (warp - 4) >> 2;
         const int r = ((warp & 3) << 5) + lane;            // row within the tile = TMEM lane
