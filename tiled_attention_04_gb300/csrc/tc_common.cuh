@@ -82,6 +82,11 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t cluster_addr) {
                  : "memory");
     return v;
 }
+// remote store of 16 bytes into a peer CTA's shared memory (made visible by a later release arrive)
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
 __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
