@@ -34,10 +34,12 @@
 // Split work items (SPLIT = 2): when there are too few query tiles to fill the
 // GPU, or the longest causal row would dominate the run, a cluster of two CTAs
 // shares one query tile: rank 0 takes the first half of the key tiles, rank 1
-// the rest.  Rank 1 leaves its merged, unnormalised partial (O, m, l) in its
-// shared memory; rank 0 reads it through distributed shared memory, merges it
-// exactly like the two warpgroups' halves, and writes O and L.  The hand-over
-// uses mbarriers arrived on from the other CTA and waited on with a bound.
+// the rest.  Each rank then finalises half of the columns: it stores its
+// unnormalised partial of the other half, with the row's (m, l), into the
+// peer's shared memory with remote stores (once the peer's MMAs are done),
+// and merges the half it keeps exactly like the two warpgroups' halves.  The
+// hand-over uses mbarriers arrived on from the other CTA, waited on with a
+// bound.
 //
 // Many short units (at least two per SM, at most 12 key tiles on average):
 // fa_fwd_tc_persistent_kernel runs one CTA per SM over a snake-ordered list of
@@ -93,7 +95,7 @@ struct FwdCfg {
     // per-row (m, l) of both warpgroups, double-buffered by work unit: 2 x (256 + 256) floats
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t MISC_OFF = STAT_OFF + 2 * 512 * 4;
-    static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;                  // peer_ready, peer_done
+    static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;                  // peer_free, peer_ready
     static constexpr uint32_t USED = PEER_BAR_OFF + 16;
     // split items: rank 1's partial O (fp32, rows padded by 4 floats) and its m, l, in the K ring
     static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::mbar_init(drain, 1);
         tc::mbar_init(never, 1);
         if (SPLIT > 1) {
-            tc::mbar_init(base + C::PEER_BAR_OFF, 256);       // peer_ready: rank 1's 256 softmax threads
-            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 256);   // peer_done: rank 0's 256 softmax threads
+            tc::mbar_init(base + C::PEER_BAR_OFF, 256);       // peer_free: the peer's 256 softmax threads
+            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 128);   // peer_ready: the peer's 128 senders
         }
         *abort_flag = 0u;
         tc::fence_mbar_init();
@@ -479,32 +481,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if constexpr (SPLIT == 1) {
             if (fine) store_row(v, Mc, lc);
         } else {
-            const uint32_t peer_ready = base + C::PEER_BAR_OFF, peer_done = peer_ready + 8;
-            if (rank == 1) {
-                // leave the partial in this CTA's shared memory for rank 0, then wait until it has been read
-                float *part = reinterpret_cast<float *>(sb + C::PART_OFF + r * C::PART_STRIDE) + t * (D / 2);
+            // rank r finalises the columns of warpgroup r; the other warpgroup sends its
+            // half row and the row's (m, l) into the peer's shared memory with remote
+            // stores, once the peer's MMAs are done (its K ring holds the partials)
+            const uint32_t peer_free = base + C::PEER_BAR_OFF, peer_ready = peer_free + 8;
+            tc::mbar_arrive_remote(tc::map_to_rank(peer_free, rank ^ 1u));
+            if (t != (int)rank) {
+                const bool dst_ok = wait_peer(peer_free);
+                if (dst_ok) {
+                    const uint32_t prow = tc::map_to_rank(base + C::PART_OFF + r * C::PART_STRIDE, rank ^ 1u);
+                    const uint32_t pml = tc::map_to_rank(base + C::PART_ML_OFF, rank ^ 1u);
+                    const bool ok_part = fine && n > 0;
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c)
-                    reinterpret_cast<float4 *>(part)[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-                if (t == 0) {
-                    float *ml = reinterpret_cast<float *>(sb + C::PART_ML_OFF);
-                    ml[r] = Mc;
-                    ml[128 + r] = lc;
+                    for (int c = 0; c < D / 8; ++c)
+                        tc::st_cluster_v4(prow + 16 * c, __float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                                          __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+                    tc::st_cluster_f32(pml + r * 4, ok_part ? Mc : -INFINITY);
+                    tc::st_cluster_f32(pml + (128 + r) * 4, ok_part ? lc : 0.f);
                 }
-                tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, 0));
-                wait_peer(peer_done);   // rank 0 reads this CTA's shared memory until then
+                tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, rank ^ 1u));   // release: the stores above
             } else {
                 const bool got = wait_peer(peer_ready);
                 if (__all_sync(0xffffffffu, fine && got)) {
-                    const uint32_t prow = tc::map_to_rank(base + C::PART_OFF + r * C::PART_STRIDE, 1) + t * (D / 2) * 4;
-                    const uint32_t pml = tc::map_to_rank(base + C::PART_ML_OFF, 1);
-                    const float M1 = tc::ld_cluster_f32(pml + r * 4), l1 = tc::ld_cluster_f32(pml + (128 + r) * 4);
+                    const float *prow = reinterpret_cast<const float *>(sb + C::PART_OFF + r * C::PART_STRIDE);
+                    const float *ml = reinterpret_cast<const float *>(sb + C::PART_ML_OFF);
+                    const float M1 = ml[r], l1 = ml[128 + r];
                     const float M = fmaxf(Mc, M1);
-                    const float b0 = exp2f(Mc - M);
+                    const float b0 = Mc > -INFINITY ? exp2f(Mc - M) : 0.f;
                     const float b1 = l1 > 0.f ? exp2f(M1 - M) : 0.f;
 #pragma unroll
                     for (int c = 0; c < D / 8; ++c) {
-                        const float4 pv = tc::ld_cluster_v4(prow + 16 * c);
+                        const float4 pv = reinterpret_cast<const float4 *>(prow)[c];
                         v[4 * c + 0] = fmaf(pv.x, b1, v[4 * c + 0] * b0);
                         v[4 * c + 1] = fmaf(pv.y, b1, v[4 * c + 1] * b0);
                         v[4 * c + 2] = fmaf(pv.z, b1, v[4 * c + 2] * b0);
@@ -512,7 +519,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                     store_row(v, M, lc * b0 + l1 * b1);
                 }
-                tc::mbar_arrive_remote(tc::map_to_rank(peer_done, 1));
             }
         }
     }
