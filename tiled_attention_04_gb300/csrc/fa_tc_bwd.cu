@@ -207,8 +207,8 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         tc::mbar_init(p_full, 256);
         tc::mbar_init(drain, 1);
         if (SPLIT > 1) {
-            tc::mbar_init(base + C::PEER_BAR_OFF, 256);
-            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 256);
+            tc::mbar_init(base + C::PEER_BAR_OFF, 256);       // peer_free: the peer's 256 element-wise threads
+            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 128);   // peer_ready: the peer's 128 senders
         }
         *abort_flag = 0u;
         tc::fence_mbar_init();
@@ -425,59 +425,70 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         __nv_bfloat16 *dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
         const float mul = t == 0 ? 1.f : scale;
         const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
-        const uint32_t part = base + C::PART_OFF + (t * 128 + r) * C::PART_STRIDE;   // this thread's partial row
-        const uint32_t peer_ready = base + C::PEER_BAR_OFF, peer_done = peer_ready + 8;
+        // Split items: each rank finalises one tensor (rank 0 dV, rank 1 dK) and sends
+        // its partial of the other into the peer's shared memory with remote stores
+        // (streamed, no round trip per access), once the peer's own MMAs are done
+        // and its stages are free; the peer adds it to its own accumulator.
+        const bool mine = SPLIT == 1 || t == (int)rank;
+        const uint32_t peer_free = base + C::PEER_BAR_OFF, peer_ready = peer_free + 8;
+        const uint32_t part = base + C::PART_OFF + r * C::PART_STRIDE;   // partial row received here
+        if constexpr (SPLIT > 1) tc::mbar_arrive_remote(tc::map_to_rank(peer_free, rank ^ 1u));
         bool merge = false;
-        if constexpr (SPLIT > 1) {
-            if (rank == 0) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 2u);
-        }
-        const uint32_t rpart = SPLIT > 1 ? tc::map_to_rank(part, 1) : 0u;
+        if (SPLIT > 1 && !mine) {
+            const bool dst_ok = tc::wait_peer(peer_free, &g_fa_bwd_status, 2u);
+            const uint32_t rdst = tc::map_to_rank(part, rank ^ 1u);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t a[32];
-            if (fine && n > 0) {
-                tmem_ld_x32(tA + 32 * c, a);
-                tc::tmem_ld_wait();
-                reg_fence_x32(a);
-            } else {
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32];
+                if (fine && n > 0) {
+                    tmem_ld_x32(tA + 32 * c, a);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(a);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) a[i] = 0u;
-            }
-            if (SPLIT > 1 && rank == 1) {
-                float4 *pr = reinterpret_cast<float4 *>(sb + (part - base)) + 8 * c;
+                    for (int i = 0; i < 32; ++i) a[i] = 0u;
+                }
+                if (dst_ok) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    pr[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
-                                        __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
-                continue;
-            }
-            if (merge) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 q = tc::ld_cluster_v4(rpart + 128 * c + 16 * i);
-                    a[4 * i + 0] = __float_as_uint(__uint_as_float(a[4 * i + 0]) + q.x);
-                    a[4 * i + 1] = __float_as_uint(__uint_as_float(a[4 * i + 1]) + q.y);
-                    a[4 * i + 2] = __float_as_uint(__uint_as_float(a[4 * i + 2]) + q.z);
-                    a[4 * i + 3] = __float_as_uint(__uint_as_float(a[4 * i + 3]) + q.w);
+                    for (int i = 0; i < 8; ++i)
+                        tc::st_cluster_v4(rdst + 128 * c + 16 * i, a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
                 }
             }
-            uint32_t packed[16];
+            tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, rank ^ 1u));   // release: the stores above
+        } else {
+            if constexpr (SPLIT > 1) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 2u);
+            const float *pr = reinterpret_cast<const float *>(sb + (part - base));
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
-            if (fine && key < Nk) {
-                uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32];
+                if (fine && n > 0) {
+                    tmem_ld_x32(tA + 32 * c, a);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(a);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-            }
-        }
-        if constexpr (SPLIT > 1) {
-            if (rank == 1) {
-                tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, 0));
-                tc::wait_peer(peer_done, &g_fa_bwd_status, 2u);   // rank 0 reads this partial until then
-            } else {
-                tc::mbar_arrive_remote(tc::map_to_rank(peer_done, 1));
+                    for (int i = 0; i < 32; ++i) a[i] = 0u;
+                }
+                if (merge) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 q = reinterpret_cast<const float4 *>(pr + 32 * c)[i];
+                        a[4 * i + 0] = __float_as_uint(__uint_as_float(a[4 * i + 0]) + q.x);
+                        a[4 * i + 1] = __float_as_uint(__uint_as_float(a[4 * i + 1]) + q.y);
+                        a[4 * i + 2] = __float_as_uint(__uint_as_float(a[4 * i + 2]) + q.z);
+                        a[4 * i + 3] = __float_as_uint(__uint_as_float(a[4 * i + 3]) + q.w);
+                    }
+                }
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
+                if (fine && (SPLIT == 1 || merge) && key < Nk) {
+                    uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
             }
         }
     }
@@ -566,8 +577,8 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
         tc::mbar_init(p_full, 256);
         tc::mbar_init(drain, 1);
         if (SPLIT > 1) {
-            tc::mbar_init(base + C::PEER_BAR_OFF, 256);
-            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 256);
+            tc::mbar_init(base + C::PEER_BAR_OFF, 256);       // peer_free: the peer's 256 element-wise threads
+            tc::mbar_init(base + C::PEER_BAR_OFF + 8, 128);   // peer_ready: the peer's 128 senders
         }
         *abort_flag = 0u;
         tc::fence_mbar_init();
@@ -744,60 +755,71 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
         if (fine && n > 0) tc::fence_after_sync();
         __nv_bfloat16 *dst = dQ + ((size_t)bh * Nq + row) * D;
         const uint32_t tA = tmem + lane_base + C::DQ_COL;
-        const uint32_t part = base + C::PART_OFF + r * C::PART_STRIDE;
-        const uint32_t peer_ready = base + C::PEER_BAR_OFF, peer_done = peer_ready + 8;
-        bool merge = false;
-        if constexpr (SPLIT > 1) {
-            if (rank == 0) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 4u);
-        }
-        const uint32_t rpart = SPLIT > 1 ? tc::map_to_rank(part, 1) : 0u;
+        // Split items: rank r finalises the columns of warpgroup r and sends its partial
+        // of the other half into the peer's shared memory with remote stores, once the
+        // peer's own MMAs are done and its stages are free.
+        const bool mine = SPLIT == 1 || t == (int)rank;
+        const uint32_t peer_free = base + C::PEER_BAR_OFF, peer_ready = peer_free + 8;
+        const uint32_t part = base + C::PART_OFF + r * C::PART_STRIDE;   // half row received here
+        if constexpr (SPLIT > 1) tc::mbar_arrive_remote(tc::map_to_rank(peer_free, rank ^ 1u));
+        if (SPLIT > 1 && !mine) {
+            const bool dst_ok = tc::wait_peer(peer_free, &g_fa_bwd_status, 4u);
+            const uint32_t rdst = tc::map_to_rank(part, rank ^ 1u);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-            const int col = t * (D / 2) + 32 * c;
-            uint32_t a[32];
-            if (fine && n > 0) {
-                tmem_ld_x32(tA + col, a);
-                tc::tmem_ld_wait();
-                reg_fence_x32(a);
-            } else {
+            for (int c = 0; c < D / 64; ++c) {
+                const int col = t * (D / 2) + 32 * c;
+                uint32_t a[32];
+                if (fine && n > 0) {
+                    tmem_ld_x32(tA + col, a);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(a);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) a[i] = 0u;
-            }
-            if (SPLIT > 1 && rank == 1) {
-                float4 *pr = reinterpret_cast<float4 *>(sb + (part - base) + col * 4);
+                    for (int i = 0; i < 32; ++i) a[i] = 0u;
+                }
+                if (dst_ok) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    pr[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
-                                        __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
-                continue;
-            }
-            if (merge) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 q = tc::ld_cluster_v4(rpart + col * 4 + 16 * i);
-                    a[4 * i + 0] = __float_as_uint(__uint_as_float(a[4 * i + 0]) + q.x);
-                    a[4 * i + 1] = __float_as_uint(__uint_as_float(a[4 * i + 1]) + q.y);
-                    a[4 * i + 2] = __float_as_uint(__uint_as_float(a[4 * i + 2]) + q.z);
-                    a[4 * i + 3] = __float_as_uint(__uint_as_float(a[4 * i + 3]) + q.w);
+                    for (int i = 0; i < 8; ++i)
+                        tc::st_cluster_v4(rdst + 128 * c + 16 * i, a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
                 }
             }
-            uint32_t packed[16];
+            tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, rank ^ 1u));   // release: the stores above
+        } else {
+            bool merge = false;
+            if constexpr (SPLIT > 1) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 4u);
+            const float *pr = reinterpret_cast<const float *>(sb + (part - base));
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * scale, __uint_as_float(a[2 * i + 1]) * scale);
-            if (fine && row < Nq) {
-                uint4 *o = reinterpret_cast<uint4 *>(dst + col);
+            for (int c = 0; c < D / 64; ++c) {
+                const int col = t * (D / 2) + 32 * c;
+                uint32_t a[32];
+                if (fine && n > 0) {
+                    tmem_ld_x32(tA + col, a);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(a);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-            }
-        }
-        if constexpr (SPLIT > 1) {
-            if (rank == 1) {
-                tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, 0));
-                tc::wait_peer(peer_done, &g_fa_bwd_status, 4u);
-            } else {
-                tc::mbar_arrive_remote(tc::map_to_rank(peer_done, 1));
+                    for (int i = 0; i < 32; ++i) a[i] = 0u;
+                }
+                if (merge) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 q = reinterpret_cast<const float4 *>(pr + 32 * c)[i];
+                        a[4 * i + 0] = __float_as_uint(__uint_as_float(a[4 * i + 0]) + q.x);
+                        a[4 * i + 1] = __float_as_uint(__uint_as_float(a[4 * i + 1]) + q.y);
+                        a[4 * i + 2] = __float_as_uint(__uint_as_float(a[4 * i + 2]) + q.z);
+                        a[4 * i + 3] = __float_as_uint(__uint_as_float(a[4 * i + 3]) + q.w);
+                    }
+                }
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * scale, __uint_as_float(a[2 * i + 1]) * scale);
+                if (fine && (SPLIT == 1 || merge) && row < Nq) {
+                    uint4 *o = reinterpret_cast<uint4 *>(dst + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
             }
         }
     }
