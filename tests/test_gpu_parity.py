@@ -166,6 +166,32 @@ def test_misaligned_pointer_is_rejected_and_nothing_written(cuda_lib):
     assert (buf == 5.0).all()
 
 
+# The exported phases one by one (preprocessing, then the dK/dV and the dQ
+# launches separately instead of the fused gradient launch), on shapes that take
+# the unsplit path and both two-CTA split paths (d = 64 and d = 128).
+PHASE_CASES = [(2, 384, 64, True), (1, 1088, 64, True), (4, 1152, 128, True), (2, 512, 128, False)]
+
+
+@pytest.mark.parametrize("bh,n,d,causal", PHASE_CASES)
+def test_backward_phases_launched_separately(cuda_lib, bh, n, d, causal):
+    torch = _torch()
+    from tiled_attention_04_gb300 import binding
+    t = inputs.make_custom(bh, n, n, d, "bf16", seed=3000 + n + d)
+    Q, K, V, dO = (inputs.to_torch(x, torch.device("cuda")) for x in t)
+    O, L = binding.fa_fwd(Q, K, V, is_causal=causal)
+    ws = binding.alloc_workspace(Q, K, causal)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    binding.fa_bwd_preprocess(O, dO, L, Q, K, causal, ws)
+    binding.fa_bwd_dkdv(Q, K, V, dO, L, dQ, dK, dV, causal, ws)
+    binding.fa_bwd_dq(Q, K, V, dO, L, dQ, causal, ws)
+    torch.cuda.synchronize()
+    assert binding.fa_get_device_status() == binding.FA_OK
+    want = oracle_all(t, causal, 1.0 / math.sqrt(d))
+    got = {"O": O.double().cpu().numpy(), "L": L.double().cpu().numpy(), "dQ": dQ.double().cpu().numpy(),
+           "dK": dK.double().cpu().numpy(), "dV": dV.double().cpu().numpy()}
+    assert_close(got, want, 2e-2, f"phases bh={bh} n={n} d={d} causal={causal}")
+
+
 def test_forward_and_dkdv_are_deterministic(cuda_lib):
     t = inputs.make_custom(2, 1024, 1024, 128, "bf16", seed=9)
     a = run_gpu(t, True, canary=False)
