@@ -193,6 +193,16 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest per-rank value of x (the job takes as long as its slowest rank)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def config_of(w):
     return {"workload": w.name, "B": w.B, "H": w.H, "seq_len": w.N, "head_dim": w.d, "causal": w.causal,
             "input_dtype": w.dtype, "l2": "flushed between timed steps (512 MiB write)"}
@@ -282,11 +292,7 @@ def run_gpu(args, w, rank, world):
     if world > 1:
         torch.distributed.barrier()
     total = [a.elapsed_time(b) for a, b in evs]
-    step_ms = sum(total) / len(total)
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(sum(total) / len(total), world, dev)
 
     # fwd / bwd split: the same steps with one more event, between fa_fwd and the
     # backward (preprocessing + gradients, still overlapped by dependent launch)
@@ -394,7 +400,7 @@ def run_gpu(args, w, rank, world):
 
     run_e2e(max(4, args.warmup))
     n_e2e = max(4, min(args.steps, 100))
-    e2e_ms = run_e2e(n_e2e)
+    e2e_ms = max_over_ranks(run_e2e(n_e2e), world, dev)
     if binding.fa_get_device_status() != binding.FA_OK:
         raise RuntimeError("device status not ok after the end-to-end steps")
 
