@@ -167,6 +167,57 @@ FA_API fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V, con
 FA_API size_t fa_noalloc_scratch_bytes(void);
 
 /*
+ * Strided (B, H, N, d) views.  The field guide's "Systems and Parallelism"
+ * §1.3 builds every tile load from a base pointer, a shape and per-dimension
+ * strides, with batch and heads flattened into one batch stride.  Here batch
+ * and heads keep a stride each, so a view such as the (B, N, H, d) output of a
+ * projection, transposed to (B, H, N, d), is read and written in place with no
+ * reshape copy.
+ *
+ * Element (b, h, n, c) of a tensor with strides s sits at element index
+ * b*s.b + h*s.h + n*s.n + c from its base pointer: the head dimension d is
+ * contiguous; the other three strides are in elements, not bytes.  A NULL
+ * fa_strides pointer means the contiguous layout of the plain entry points,
+ * {H*N*d, N*d, d}.
+ *
+ * Rules (checked before anything is launched):
+ *  - for every dimension of extent > 1 (B, H, or N of that tensor) the stride
+ *    is positive, a multiple of 16 bytes (8 elements for bf16, 4 for fp32) and
+ *    below 2^40 bytes -- else FA_ERR_BAD_SHAPE (not positive or too large) or
+ *    FA_ERR_MISALIGNED (not a multiple of 16 bytes); the stride of a
+ *    dimension of extent 1 is ignored;
+ *  - input views (Q, K, V, O read by the backward, dO) may overlap each other
+ *    and themselves (for example two rows sharing elements);
+ *  - output views (O written by the forward, dQ, dK, dV) must not overlap
+ *    themselves: sorted by stride, each of the four dimensions' strides must be
+ *    at least the previous one times its extent -- else FA_ERR_BAD_SHAPE.  An
+ *    output must not overlap any input or another output (not checked);
+ *  - L stays a contiguous (B*H, Nq) fp32 array, and the workspace is the one
+ *    fa_bwd_workspace_size gives.
+ * Results are the same, bit for bit, as those of the plain entry points on
+ * contiguous copies of the same values.
+ */
+typedef struct {
+    int64_t b, h, n;
+} fa_strides;
+
+/* fa_fwd over strided views: reads Q, K, V through sQ, sK, sV; writes O through sO. */
+FA_API fa_status fa_fwd_strided(const void *Q, const fa_strides *sQ, const void *K, const fa_strides *sK,
+                                const void *V, const fa_strides *sV, void *O, const fa_strides *sO, float *L,
+                                int B, int H, int Nq, int Nk, int d, float scale, int is_causal, fa_dtype dtype,
+                                fa_stream_t stream);
+
+/* fa_bwd over strided views: reads Q, K, V, O, dO through their strides; writes
+ * dQ, dK, dV through sdQ, sdK, sdV. */
+FA_API fa_status fa_bwd_strided(const void *Q, const fa_strides *sQ, const void *K, const fa_strides *sK,
+                                const void *V, const fa_strides *sV, const void *O, const fa_strides *sO,
+                                const void *dO, const fa_strides *sdO, const float *L,
+                                void *dQ, const fa_strides *sdQ, void *dK, const fa_strides *sdK,
+                                void *dV, const fa_strides *sdV,
+                                int B, int H, int Nq, int Nk, int d, float scale, int is_causal, fa_dtype dtype,
+                                void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Name of the kernel family fa_fwd / fa_bwd would use for these arguments:
  * "tc" (tcgen05 tensor-core kernels) or "simt" (fp32 CUDA-core kernels), or
  * NULL for unsupported arguments.  Host-only; launches nothing.

@@ -99,3 +99,89 @@ def test_valid_call_without_a_device_reports_no_device(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert fwd(L) == 9
+
+
+# ------------------------------------------------------------------ strided views (fa_strides)
+
+def _st(b, h, n):
+    from tiled_attention_04_gb300 import binding
+    return ctypes.byref(binding.FaStrides(b, h, n))
+
+
+def fwd_strided(L, sQ=None, sK=None, sV=None, sO=None, B=2, H=4, Nq=256, Nk=256, d=64, dt=1):
+    return L.fa_fwd_strided(V16, sQ, V16, sK, V16, sV, V16, sO, V16, B, H, Nq, Nk, d, 0.125, 1, dt, None)
+
+
+def bwd_strided(L, s=None, B=2, H=4, Nq=256, Nk=256, d=64, dt=1):
+    s = s or {}
+    g = lambda k: s.get(k)   # noqa: E731
+    return L.fa_bwd_strided(V16, g("Q"), V16, g("K"), V16, g("V"), V16, g("O"), V16, g("dO"), V16,
+                            V16, g("dQ"), V16, g("dK"), V16, g("dV"), B, H, Nq, Nk, d, 0.125, 1, dt,
+                            V16, 1 << 30, None)
+
+
+# (B, H, N, d) = (2, 4, 256, 64): contiguous strides are (65536, 16384, 64); a transposed
+# (B, N, H, d) buffer gives (65536, 64, 256)
+@pytest.mark.parametrize("kw,status", [
+    (dict(sQ=(65536, 64, 256)), None),                  # transposed projection layout: accepted
+    (dict(sK=(3 * 65536, 64, 3 * 256)), None),          # one third of a fused QKV buffer
+    (dict(sQ=(65536, 16384, 72)), None),                # padded rows (inputs may have gaps)
+    (dict(sQ=(65536, 16384, 68)), 5),                   # row stride not a multiple of 16 bytes
+    (dict(sV=(65536, 20, 256)), 5),                     # head stride not a multiple of 16 bytes
+    (dict(sQ=(65536, 0, 64)), 2),                       # broadcast head: not supported
+    (dict(sK=(-65536, 16384, 64)), 2),                  # negative stride
+    (dict(sQ=(1 << 40, 16384, 64)), 2),                 # beyond the 2^40-byte stride limit
+    (dict(sO=(65536, 64, 256)), None),                  # dense transposed output
+    (dict(sO=(65536, 16384, 32)), 2),                   # output rows overlap (row stride < d)
+    (dict(sO=(65536, 64, 64)), 2),                      # output heads and rows collide
+    (dict(sO=(16384, 16384, 64)), 2),                   # output batches and heads collide
+    (dict(sQ=(65536, 16384, 32)), None),                # overlapping input rows are fine
+])
+def test_fwd_strided_checks_views(L, kw, status):
+    args = {k: _st(*v) for k, v in kw.items()}
+    got = fwd_strided(L, **args)
+    if status is None:
+        # accepted: the call goes on to find no device here (or runs, where one exists)
+        assert got in (0, 9)
+    else:
+        assert got == status
+
+
+def test_strided_extent_one_dimensions_ignore_their_stride(L):
+    # B = 1 and H = 1: the batch and head strides are never used, whatever they are
+    got = fwd_strided(L, sQ=_st(0, -7, 64), sO=_st(3, 5, 64), B=1, H=1)
+    assert got in (0, 9)
+
+
+def test_fp32_strides_need_multiples_of_4_elements(L):
+    assert fwd_strided(L, sQ=_st(65536, 16384, 68), dt=0) in (0, 9)
+    assert fwd_strided(L, sQ=_st(65536, 16384, 66), dt=0) == 5
+
+
+def test_bwd_strided_checks_every_view(L):
+    assert bwd_strided(L) in (0, 9)
+    assert bwd_strided(L, {"dO": _st(65536, 64, 256), "dQ": _st(65536, 64, 256)}) in (0, 9)
+    assert bwd_strided(L, {"dO": _st(65536, 16384, 60)}) == 5
+    assert bwd_strided(L, {"dK": _st(65536, 16384, 32)}) == 2      # overlapping gradient rows
+    assert bwd_strided(L, {"O": _st(65536, 16384, 32)}) in (0, 9)  # O is read, not written
+    assert bwd_strided(L, {"dV": _st(65536, 0, 64)}) == 2
+
+
+def test_binding_stride_helpers():
+    torch = pytest.importorskip("torch")
+    from tiled_attention_04_gb300 import binding
+    x = torch.empty(2, 256, 4, 64, dtype=torch.bfloat16)
+    q = x.transpose(1, 2)                                   # (B, H, N, d) view of a (B, N, H, d) buffer
+    s = binding._strides(q)
+    assert (s.b, s.h, s.n) == (65536, 64, 256)
+    assert binding._strides(q.contiguous()) is None
+    assert binding.accepts_view(q) == (q.data_ptr() % 16 == 0)
+    qkv = torch.empty(2, 256, 3, 4, 64, dtype=torch.bfloat16)
+    k = qkv.unbind(2)[1].transpose(1, 2)
+    s = binding._strides(k)
+    assert (s.b, s.h, s.n) == (3 * 65536, 64, 3 * 256)
+    assert not binding.accepts_view(q[..., ::2])              # last dimension not contiguous
+    assert not binding.accepts_view(q.expand(2, 4, 256, 64).as_strided((2, 4, 256, 64), (0, 64, 256, 1)))
+    o = binding._like_rows(q, (2, 4, 256, 64))
+    assert o.shape == (2, 4, 256, 64) and o.stride() == (65536, 64, 256, 1)
+    assert binding._like_rows(q.contiguous(), (2, 4, 256, 64)).is_contiguous()

@@ -4,7 +4,9 @@ Interface of CS336 A2 "Systems and Parallelism", problem flash_forward:
 ``forward(ctx, Q, K, V, is_causal=False)`` returns O, saves L with
 ``ctx.save_for_backward`` (the only saved tensor of shape (batch, n_queries))
 and stashes ``ctx.is_causal``; ``backward`` returns dQ, dK, dV (problem
-flash_backward).  Inputs are (..., N, d) CUDA tensors, fp32 or bf16.
+flash_backward).  Inputs are (..., N, d) CUDA tensors, fp32 or bf16; strided
+(B, H, N, d) views (a projection's (B, N, H, d) output transposed, or slices
+of a fused QKV projection) are read in place, without a reshape copy.
 
 ``scaled_dot_product_attention`` and ``patch_sdpa`` make it a drop-in for the
 module-level attention function a Transformer layer calls (the field guide's
@@ -20,10 +22,16 @@ import torch
 from . import binding
 
 
+def _in_place(t):
+    """t itself when the kernels can read it where it lies (contiguous, or a strided
+    (B, H, N, d) view such as a transposed projection output), else a contiguous copy."""
+    return t if binding.accepts_view(t) else t.contiguous()
+
+
 class FlashAttention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, Q, K, V, is_causal=False, scale=None):
-        Q, K, V = Q.contiguous(), K.contiguous(), V.contiguous()
+        Q, K, V = _in_place(Q), _in_place(K), _in_place(V)
         O, L = binding.fa_fwd(Q, K, V, is_causal=is_causal, scale=scale)
         ctx.save_for_backward(Q, K, V, O, L)
         ctx.is_causal = bool(is_causal)
@@ -33,7 +41,7 @@ class FlashAttention(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dO):
         Q, K, V, O, L = ctx.saved_tensors
-        dQ, dK, dV = binding.fa_bwd(Q, K, V, O, dO.contiguous(), L, is_causal=ctx.is_causal, scale=ctx.scale)
+        dQ, dK, dV = binding.fa_bwd(Q, K, V, O, _in_place(dO), L, is_causal=ctx.is_causal, scale=ctx.scale)
         return dQ, dK, dV, None, None
 
 

@@ -24,11 +24,16 @@ FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
 
 # every function include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq",
-           "fa_bwd_grads",
+           "fa_bwd_grads", "fa_fwd_strided", "fa_bwd_strided",
            "fa_bwd_noalloc", "fa_noalloc_scratch_bytes", "fa_path_name", "fa_get_device_status",
            "fa_reset_device_status", "fa_set_wait_limit", "fa_debug_force_stall", "fa_status_string")
 
 _lib = None
+
+
+class FaStrides(ctypes.Structure):
+    """fa_strides of include/fa.h: element strides (batch, head, row) of a (B, H, N, d) view."""
+    _fields_ = [("b", ctypes.c_int64), ("h", ctypes.c_int64), ("n", ctypes.c_int64)]
 
 
 class FaError(RuntimeError):
@@ -54,6 +59,10 @@ def lib() -> ctypes.CDLL:
     L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_bwd_grads.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
+    sp = ctypes.POINTER(FaStrides)
+    L.fa_fwd_strided.argtypes = [vp, sp, vp, sp, vp, sp, vp, sp, vp, i, i, i, i, i, f, i, i, vp]
+    L.fa_bwd_strided.argtypes = [vp, sp, vp, sp, vp, sp, vp, sp, vp, sp, vp, vp, sp, vp, sp, vp, sp,
+                                 i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     L.fa_bwd_noalloc.restype = ctypes.c_int
     L.fa_noalloc_scratch_bytes.argtypes = []
@@ -69,7 +78,7 @@ def lib() -> ctypes.CDLL:
     L.fa_status_string.argtypes = [i]
     L.fa_status_string.restype = ctypes.c_char_p
     for name in ("fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_grads",
-                 "fa_get_device_status",
+                 "fa_fwd_strided", "fa_bwd_strided", "fa_get_device_status",
                  "fa_reset_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -114,15 +123,58 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _check_inputs(*ts):
+def _check_inputs(*ts, strided=False):
     t0 = ts[0]
     for t in ts:
         if not t.is_cuda:
             raise ValueError("tensors must be on a CUDA device")
-        if not t.is_contiguous():
+        if not strided and not t.is_contiguous():
             raise ValueError("tensors must be contiguous (B, H, N, d) or (..., N, d)")
         if t.dtype != t0.dtype:
             raise ValueError("Q, K, V (and O, dO) must share a dtype")
+
+
+def _strides(t):
+    """fa_strides of a (B, H, N, d) or (B, N, d) view whose last dimension is contiguous,
+    or None for a contiguous tensor (the plain layout)."""
+    if t.is_contiguous():
+        return None
+    if t.dim() not in (3, 4) or (t.shape[-1] > 1 and t.stride(-1) != 1):
+        raise ValueError("a non-contiguous view must be (B, H, N, d) or (B, N, d) with the last dimension "
+                         "contiguous")
+    if t.dim() == 3:
+        return FaStrides(t.stride(0), t.stride(0), t.stride(1))
+    return FaStrides(t.stride(0), t.stride(1), t.stride(2))
+
+
+def accepts_view(t) -> bool:
+    """True when the library reads this tensor in place (the rules of fa_strides in
+    include/fa.h): contiguous, or a 3-/4-D view with a contiguous last dimension, a
+    16-byte aligned start and positive strides that are multiples of 16 bytes."""
+    if t.is_contiguous():
+        return t.data_ptr() % 16 == 0
+    if t.dim() not in (3, 4) or (t.shape[-1] > 1 and t.stride(-1) != 1) or t.data_ptr() % 16:
+        return False
+    eb = t.element_size()
+    for size, stride in zip(t.shape[:-1], t.stride()[:-1]):
+        if size > 1 and (stride <= 0 or (stride * eb) % 16):
+            return False
+    return True
+
+
+def _sp(st):
+    return ctypes.byref(st) if st is not None else None
+
+
+def _like_rows(Q, shape):
+    """An output with Q's order of heads and rows: a (B, N, H, d) buffer seen as
+    (B, H, N, d) when Q's rows are outer to its heads (a transposed projection),
+    else contiguous."""
+    torch = _torch()
+    if Q.dim() == 4 and not Q.is_contiguous() and Q.shape[1] > 1 and Q.stride(2) > Q.stride(1):
+        B, H, N, d = shape
+        return torch.empty((B, N, H, d), dtype=Q.dtype, device=Q.device).transpose(1, 2)
+    return torch.empty(shape, dtype=Q.dtype, device=Q.device)
 
 
 def path_name(Nq, Nk, d, is_causal, dtype_c) -> str | None:
@@ -133,19 +185,34 @@ def path_name(Nq, Nk, d, is_causal, dtype_c) -> str | None:
 # ------------------------------------------------------------------ entry points
 
 def fa_fwd(Q, K, V, is_causal=False, scale=None, O=None, L=None, stream=None):
-    """O (like Q) and L (Q.shape[:-1], fp32) of attention; see include/fa.h."""
+    """O (shaped like Q) and L (Q.shape[:-1], fp32) of attention; see include/fa.h.
+
+    Contiguous inputs go to fa_fwd.  Strided (B, H, N, d) views (for example a
+    (B, N, H, d) projection transposed to (B, H, N, d)) go to fa_fwd_strided and
+    are read in place; O then follows Q's order of heads and rows."""
     torch = _torch()
-    _check_inputs(Q, K, V)
+    strided = not all(t.is_contiguous() for t in (Q, K, V)) or (O is not None and not O.is_contiguous())
+    _check_inputs(Q, K, V, strided=strided)
     B, H = _bh(Q)
     Nq, d = Q.shape[-2], Q.shape[-1]
     Nk = K.shape[-2]
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    if O is None:
-        O = torch.empty_like(Q)
     if L is None:
         L = torch.empty(Q.shape[:-1], dtype=torch.float32, device=Q.device)
-    check(lib().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), B, H, Nq, Nk, d, sc, int(is_causal),
-                       dtype_code(Q), _stream(stream)), "fa_fwd")
+    if not strided:
+        if O is None:
+            O = torch.empty_like(Q)
+        check(lib().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), B, H, Nq, Nk, d, sc, int(is_causal),
+                           dtype_code(Q), _stream(stream)), "fa_fwd")
+        return O, L
+    if Q.shape[:-2] != K.shape[:-2] or K.shape[:-2] != V.shape[:-2]:
+        raise ValueError("Q, K and V need the same batch and head sizes")
+    if O is None:
+        O = _like_rows(Q, tuple(Q.shape))
+    sQ, sK, sV, sO = _strides(Q), _strides(K), _strides(V), _strides(O)
+    check(lib().fa_fwd_strided(_ptr(Q), _sp(sQ), _ptr(K), _sp(sK), _ptr(V), _sp(sV), _ptr(O), _sp(sO), _ptr(L),
+                               B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _stream(stream)),
+          "fa_fwd_strided")
     return O, L
 
 
@@ -163,9 +230,12 @@ def alloc_workspace(Q, K, is_causal=False):
 
 def fa_bwd(Q, K, V, O, dO, L, is_causal=False, scale=None, dQ=None, dK=None, dV=None, workspace=None,
            stream=None):
-    """dQ, dK, dV of attention given the forward's O and L; see include/fa.h."""
+    """dQ, dK, dV of attention given the forward's O and L; see include/fa.h.
+
+    Contiguous tensors go to fa_bwd; strided views to fa_bwd_strided, with each
+    gradient laid out like its input when that input is dense (else contiguous)."""
     torch = _torch()
-    _check_inputs(Q, K, V, O, dO)
+    _check_inputs(Q, K, V, O, dO, strided=True)
     B, H = _bh(Q)
     Nq, d = Q.shape[-2], Q.shape[-1]
     Nk = K.shape[-2]
@@ -174,9 +244,18 @@ def fa_bwd(Q, K, V, O, dO, L, is_causal=False, scale=None, dQ=None, dK=None, dV=
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
     ws = alloc_workspace(Q, K, is_causal) if workspace is None else workspace
-    check(lib().fa_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV),
-                       B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _ptr(ws), ws.numel(),
-                       _stream(stream)), "fa_bwd")
+    if all(t.is_contiguous() for t in (Q, K, V, O, dO, dQ, dK, dV)):
+        check(lib().fa_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV),
+                           B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _ptr(ws), ws.numel(),
+                           _stream(stream)), "fa_bwd")
+        return dQ, dK, dV
+    if not (Q.shape[:-2] == K.shape[:-2] == V.shape[:-2] == O.shape[:-2] == dO.shape[:-2]):
+        raise ValueError("Q, K, V, O and dO need the same batch and head sizes")
+    st = [_strides(t) for t in (Q, K, V, O, dO, dQ, dK, dV)]
+    check(lib().fa_bwd_strided(_ptr(Q), _sp(st[0]), _ptr(K), _sp(st[1]), _ptr(V), _sp(st[2]), _ptr(O), _sp(st[3]),
+                               _ptr(dO), _sp(st[4]), _ptr(L), _ptr(dQ), _sp(st[5]), _ptr(dK), _sp(st[6]), _ptr(dV),
+                               _sp(st[7]), B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _ptr(ws), ws.numel(),
+                               _stream(stream)), "fa_bwd_strided")
     return dQ, dK, dV
 
 

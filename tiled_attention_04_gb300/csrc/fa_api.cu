@@ -8,6 +8,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "fa.h"
@@ -34,6 +35,8 @@ fa_status check_common(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dt
     if (BH * (long long)(Nq > Nk ? Nq : Nk) > INT32_MAX) return FA_ERR_BAD_SHAPE;
     if (is_causal != 0 && is_causal != 1) return FA_ERR_BAD_ARG;
     if (check_scale && !isfinite(scale)) return FA_ERR_BAD_ARG;
+    out->B = B;
+    out->H = H;
     out->BH = (int)BH;
     out->Nq = Nq;
     out->Nk = Nk;
@@ -44,6 +47,9 @@ fa_status check_common(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dt
     const uint32_t w = g_wait_limit.load(std::memory_order_relaxed);
     out->wait_limit = w ? w : kDefaultWaitLimit;
     out->force_stall = g_force_stall.load(std::memory_order_relaxed);
+    const FaStrides q{(long long)H * Nq * d, (long long)Nq * d, d}, k{(long long)H * Nk * d, (long long)Nk * d, d};
+    out->sQ = out->sO = out->sdO = out->sdQ = q;
+    out->sK = out->sV = out->sdK = out->sdV = k;
     return FA_OK;
 }
 
@@ -72,6 +78,49 @@ fa_status device_ok() {
 }
 
 size_t elem_bytes(fa_dtype t) { return t == FA_DTYPE_F32 ? 4 : 2; }
+
+// Takes the strides of one (B, H, N, d) view (NULL: keep the contiguous ones
+// already in *s).  A dimension of extent 1 keeps its contiguous stride, whatever
+// the caller passed: its index is always 0.  The others must be positive
+// multiples of 16 bytes below 2^40 bytes (the limits of a TMA descriptor).  An
+// output view must not overlap itself.
+fa_status take_strides(const fa_strides *in, int B, int H, int N, int d, fa_dtype dt, bool output, FaStrides *s) {
+    if (!in) return FA_OK;
+    const long long eb = (long long)elem_bytes(dt);
+    const long long ext[3] = {B, H, N};
+    const long long given[3] = {in->b, in->h, in->n};
+    long long *dst[3] = {&s->b, &s->h, &s->n};
+    long long span = d - 1;   // largest element index the view reaches
+    for (int i = 0; i < 3; ++i) {
+        if (ext[i] <= 1) continue;
+        const long long v = given[i];
+        if (v <= 0 || v >= (1LL << 40) / eb) return FA_ERR_BAD_SHAPE;
+        if ((v * eb) % 16 != 0) return FA_ERR_MISALIGNED;
+        if (v > ((1LL << 48) / eb) / (ext[i] - 1)) return FA_ERR_BAD_SHAPE;
+        span += v * (ext[i] - 1);
+        if (span >= (1LL << 48) / eb) return FA_ERR_BAD_SHAPE;
+        *dst[i] = v;
+    }
+    if (output) {
+        // sorted by stride, every dimension must step past the whole span of the ones below it
+        long long st[4] = {1, 0, 0, 0}, ex[4] = {d, 0, 0, 0};
+        int n = 1;
+        for (int i = 0; i < 3; ++i)
+            if (ext[i] > 1) {
+                st[n] = *dst[i];
+                ex[n] = ext[i];
+                ++n;
+            }
+        for (int i = 1; i < n; ++i)   // insertion sort of at most four entries
+            for (int j = i; j > 0 && st[j] < st[j - 1]; --j) {
+                std::swap(st[j], st[j - 1]);
+                std::swap(ex[j], ex[j - 1]);
+            }
+        for (int i = 1; i < n; ++i)
+            if (st[i] / ex[i - 1] < st[i - 1]) return FA_ERR_BAD_SHAPE;
+    }
+    return FA_OK;
+}
 
 // Backward workspace.  CUDA-core path: D (BH*Nq fp32).  Tensor-core path:
 // D then L*log2(e), each BH * padded_rows(Nq) fp32 (see fa_tc_bwd.cu).
@@ -104,6 +153,87 @@ fa_status bwd_args(const void *Q, const void *K, const void *V, const void *dO, 
     if (!aligned16(workspace)) return FA_ERR_MISALIGNED;
     *w = workspace_layout(*p);
     if (workspace_bytes < w->total) return FA_ERR_WORKSPACE;
+    return FA_OK;
+}
+
+
+// ---- runners: arguments already checked (shape, strides, pointers, workspace)
+
+cudaStream_t as_stream(fa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+fa_status run_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
+                  fa_stream_t stream) {
+    if ((long long)p.BH * p.Nq == 0) return FA_OK;
+    fa_status s = device_ok();
+    if (s != FA_OK) return s;
+    const cudaStream_t st = as_stream(stream);
+    return map_cuda(tc_fwd_supported(p) ? tc_fwd(p, Q, K, V, O, L, st) : simt_fwd(p, Q, K, V, O, L, st));
+}
+
+fa_status run_preprocess(const FaProblem &p, const Workspace &w, const void *O, const void *dO, const float *L,
+                         void *workspace, fa_stream_t stream) {
+    if ((long long)p.BH * p.Nq == 0) return FA_OK;
+    fa_status s = device_ok();
+    if (s != FA_OK) return s;
+    char *ws = static_cast<char *>(workspace);
+    float *Dv = reinterpret_cast<float *>(ws + w.d_off);
+    const cudaStream_t st = as_stream(stream);
+    return map_cuda(w.tc ? tc_bwd_preprocess(p, O, dO, L, Dv, reinterpret_cast<float *>(ws + w.l_off), st)
+                         : simt_bwd_preprocess(p, O, dO, Dv, st));
+}
+
+fa_status run_dkdv(const FaProblem &p, const Workspace &w, const void *Q, const void *K, const void *V,
+                   const void *dO, const float *L, void *dK, void *dV, void *workspace, fa_stream_t stream) {
+    if ((long long)p.BH * p.Nk == 0) return FA_OK;
+    fa_status s = device_ok();
+    if (s != FA_OK) return s;
+    const cudaStream_t st = as_stream(stream);
+    if (p.Nq == 0) {   // no query sees any key: the gradients are zero
+        cudaError_t e = simt_zero_rows(p, dK, p.sdK, p.Nk, st);
+        if (e == cudaSuccess) e = simt_zero_rows(p, dV, p.sdV, p.Nk, st);
+        return map_cuda(e);
+    }
+    char *ws = static_cast<char *>(workspace);
+    const float *Dv = reinterpret_cast<const float *>(ws + w.d_off);
+    return map_cuda(w.tc ? tc_bwd_dkdv(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off), Dv, dK, dV, st)
+                         : simt_bwd_dkdv(p, Q, K, V, dO, L, Dv, dK, dV, st));
+}
+
+fa_status run_dq(const FaProblem &p, const Workspace &w, const void *Q, const void *K, const void *V,
+                 const void *dO, const float *L, void *dQ, void *workspace, fa_stream_t stream) {
+    if ((long long)p.BH * p.Nq == 0) return FA_OK;
+    fa_status s = device_ok();
+    if (s != FA_OK) return s;
+    char *ws = static_cast<char *>(workspace);
+    const float *Dv = reinterpret_cast<const float *>(ws + w.d_off);
+    const cudaStream_t st = as_stream(stream);
+    return map_cuda(w.tc ? tc_bwd_dq(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off), Dv, dQ, st)
+                         : simt_bwd_dq(p, Q, K, V, dO, L, Dv, dQ, st));
+}
+
+fa_status run_grads(const FaProblem &p, const Workspace &w, const void *Q, const void *K, const void *V,
+                    const void *dO, const float *L, void *dQ, void *dK, void *dV, void *workspace,
+                    fa_stream_t stream) {
+    const bool any_q = (long long)p.BH * p.Nq > 0;
+    if (!w.tc || !any_q) {   // CUDA-core kernels, or no queries (then dK = dV = 0)
+        fa_status s = run_dkdv(p, w, Q, K, V, dO, L, dK, dV, workspace, stream);
+        if (s != FA_OK) return s;
+        return run_dq(p, w, Q, K, V, dO, L, dQ, workspace, stream);
+    }
+    fa_status s = device_ok();
+    if (s != FA_OK) return s;
+    char *ws = static_cast<char *>(workspace);
+    return map_cuda(tc_bwd_grads(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off),
+                                 reinterpret_cast<const float *>(ws + w.d_off), dQ, dK, dV, true, true,
+                                 as_stream(stream)));
+}
+
+// pointer checks of a whole backward pass (fa_bwd, fa_bwd_strided)
+fa_status bwd_ptrs(const FaProblem &p, const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                   const float *L, const void *dQ, const void *dK, const void *dV) {
+    fa_status s = FA_OK;
+    if ((long long)p.BH * p.Nq > 0 && (s = check_ptrs({Q, K, V, O, dO, L, dQ})) != FA_OK) return s;
+    if ((long long)p.BH * p.Nk > 0 && (s = check_ptrs({dK, dV})) != FA_OK) return s;
     return FA_OK;
 }
 
@@ -140,15 +270,24 @@ const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype dtype) {
 
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H, int Nq, int Nk,
                  int d, float scale, int is_causal, fa_dtype dtype, fa_stream_t stream) {
+    return fa_fwd_strided(Q, nullptr, K, nullptr, V, nullptr, O, nullptr, L, B, H, Nq, Nk, d, scale, is_causal, dtype,
+                          stream);
+}
+
+fa_status fa_fwd_strided(const void *Q, const fa_strides *sQ, const void *K, const fa_strides *sK, const void *V,
+                         const fa_strides *sV, void *O, const fa_strides *sO, float *L, int B, int H, int Nq, int Nk,
+                         int d, float scale, int is_causal, fa_dtype dtype, fa_stream_t stream) {
     FaProblem p{};
     fa_status s = check_common(B, H, Nq, Nk, d, is_causal, dtype, scale, true, &p);
     if (s != FA_OK) return s;
     if ((long long)p.BH * p.Nq == 0) return FA_OK;
+    if ((s = take_strides(sQ, B, H, Nq, d, dtype, false, &p.sQ)) != FA_OK ||
+        (s = take_strides(sK, B, H, Nk, d, dtype, false, &p.sK)) != FA_OK ||
+        (s = take_strides(sV, B, H, Nk, d, dtype, false, &p.sV)) != FA_OK ||
+        (s = take_strides(sO, B, H, Nq, d, dtype, true, &p.sO)) != FA_OK)
+        return s;
     if ((s = check_ptrs({Q, K, V, O, L})) != FA_OK) return s;
-    if ((s = device_ok()) != FA_OK) return s;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = tc_fwd_supported(p) ? tc_fwd(p, Q, K, V, O, L, st) : simt_fwd(p, Q, K, V, O, L, st);
-    return map_cuda(e);
+    return run_fwd(p, Q, K, V, O, L, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype) {
@@ -167,13 +306,7 @@ fa_status fa_bwd_preprocess(const void *O, const void *dO, const float *L, int B
     if (s != FA_OK) return s;
     if ((long long)p.BH * p.Nq == 0) return FA_OK;
     if ((s = check_ptrs({O, dO, L})) != FA_OK) return s;
-    if ((s = device_ok()) != FA_OK) return s;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    char *ws = static_cast<char *>(workspace);
-    float *Dv = reinterpret_cast<float *>(ws + w.d_off);
-    cudaError_t e = w.tc ? tc_bwd_preprocess(p, O, dO, L, Dv, reinterpret_cast<float *>(ws + w.l_off), st)
-                         : simt_bwd_preprocess(p, O, dO, Dv, st);
-    return map_cuda(e);
+    return run_preprocess(p, w, O, dO, L, workspace, stream);
 }
 
 fa_status fa_bwd_dkdv(const void *Q, const void *K, const void *V, const void *dO, const float *L, void *dQ,
@@ -185,21 +318,9 @@ fa_status fa_bwd_dkdv(const void *Q, const void *K, const void *V, const void *d
                            workspace_bytes, &p, &w, false);
     if (s != FA_OK) return s;
     if ((long long)p.BH * p.Nk == 0) return FA_OK;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((s = check_ptrs({dK, dV})) != FA_OK) return s;
-    if ((s = device_ok()) != FA_OK) return s;
-    if (p.Nq == 0) {   // no query sees any key: the gradients are zero
-        const size_t bytes = (size_t)p.BH * p.Nk * p.d * elem_bytes(dtype);
-        cudaError_t e = cudaMemsetAsync(dK, 0, bytes, st);
-        if (e == cudaSuccess) e = cudaMemsetAsync(dV, 0, bytes, st);
-        return map_cuda(e);
-    }
-    if ((s = check_ptrs({Q, K, V, dO, L, dQ})) != FA_OK) return s;
-    char *ws = static_cast<char *>(workspace);
-    const float *Dv = reinterpret_cast<const float *>(ws + w.d_off);
-    cudaError_t e = w.tc ? tc_bwd_dkdv(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off), Dv, dK, dV, st)
-                         : simt_bwd_dkdv(p, Q, K, V, dO, L, Dv, dK, dV, st);
-    return map_cuda(e);
+    if (p.Nq > 0 && (s = check_ptrs({Q, K, V, dO, L, dQ})) != FA_OK) return s;
+    return run_dkdv(p, w, Q, K, V, dO, L, dK, dV, workspace, stream);
 }
 
 fa_status fa_bwd_dq(const void *Q, const void *K, const void *V, const void *dO, const float *L, void *dQ, int B,
@@ -212,13 +333,7 @@ fa_status fa_bwd_dq(const void *Q, const void *K, const void *V, const void *dO,
     if (s != FA_OK) return s;
     if ((long long)p.BH * p.Nq == 0) return FA_OK;
     if ((s = check_ptrs({Q, K, V, dO, L, dQ})) != FA_OK) return s;
-    if ((s = device_ok()) != FA_OK) return s;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    char *ws = static_cast<char *>(workspace);
-    const float *Dv = reinterpret_cast<const float *>(ws + w.d_off);
-    cudaError_t e = w.tc ? tc_bwd_dq(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off), Dv, dQ, st)
-                         : simt_bwd_dq(p, Q, K, V, dO, L, Dv, dQ, st);
-    return map_cuda(e);
+    return run_dq(p, w, Q, K, V, dO, L, dQ, workspace, stream);
 }
 
 fa_status fa_bwd_grads(const void *Q, const void *K, const void *V, const void *dO, const float *L, void *dQ,
@@ -233,38 +348,41 @@ fa_status fa_bwd_grads(const void *Q, const void *K, const void *V, const void *
     if (!any_q && !any_k) return FA_OK;
     if (any_q && (s = check_ptrs({Q, K, V, dO, L, dQ})) != FA_OK) return s;
     if (any_k && (s = check_ptrs({dK, dV})) != FA_OK) return s;
-    if (!w.tc || !any_q) {   // CUDA-core kernels, or no queries (then dK = dV = 0)
-        if ((s = fa_bwd_dkdv(Q, K, V, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace,
-                             workspace_bytes, stream)) != FA_OK)
-            return s;
-        return fa_bwd_dq(Q, K, V, dO, L, dQ, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace, workspace_bytes,
-                         stream);
-    }
-    if ((s = device_ok()) != FA_OK) return s;
-    char *ws = static_cast<char *>(workspace);
-    return map_cuda(tc_bwd_grads(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off),
-                                 reinterpret_cast<const float *>(ws + w.d_off), dQ, dK, dV, true, true,
-                                 reinterpret_cast<cudaStream_t>(stream)));
+    return run_grads(p, w, Q, K, V, dO, L, dQ, dK, dV, workspace, stream);
 }
 
 fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *L,
                  void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nk, int d, float scale, int is_causal,
                  fa_dtype dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    return fa_bwd_strided(Q, nullptr, K, nullptr, V, nullptr, O, nullptr, dO, nullptr, L, dQ, nullptr, dK, nullptr,
+                          dV, nullptr, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_strided(const void *Q, const fa_strides *sQ, const void *K, const fa_strides *sK, const void *V,
+                         const fa_strides *sV, const void *O, const fa_strides *sO, const void *dO,
+                         const fa_strides *sdO, const float *L, void *dQ, const fa_strides *sdQ, void *dK,
+                         const fa_strides *sdK, void *dV, const fa_strides *sdV, int B, int H, int Nq, int Nk, int d,
+                         float scale, int is_causal, fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                         fa_stream_t stream) {
     // validate everything up front so that a bad argument launches nothing at all
     FaProblem p{};
     Workspace w{};
     fa_status s = bwd_args(Q, K, V, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace,
                            workspace_bytes, &p, &w, false);
     if (s != FA_OK) return s;
-    const bool any_q = (long long)p.BH * p.Nq > 0, any_k = (long long)p.BH * p.Nk > 0;
-    if (!any_q && !any_k) return FA_OK;
-    if (any_q && (s = check_ptrs({Q, K, V, O, dO, L, dQ})) != FA_OK) return s;
-    if (any_k && (s = check_ptrs({dK, dV})) != FA_OK) return s;
-    if ((s = fa_bwd_preprocess(O, dO, L, B, H, Nq, Nk, d, is_causal, dtype, workspace, workspace_bytes, stream)) !=
-        FA_OK)
+    if ((long long)p.BH * p.Nq == 0 && (long long)p.BH * p.Nk == 0) return FA_OK;
+    if ((s = take_strides(sQ, B, H, Nq, d, dtype, false, &p.sQ)) != FA_OK ||
+        (s = take_strides(sK, B, H, Nk, d, dtype, false, &p.sK)) != FA_OK ||
+        (s = take_strides(sV, B, H, Nk, d, dtype, false, &p.sV)) != FA_OK ||
+        (s = take_strides(sO, B, H, Nq, d, dtype, false, &p.sO)) != FA_OK ||
+        (s = take_strides(sdO, B, H, Nq, d, dtype, false, &p.sdO)) != FA_OK ||
+        (s = take_strides(sdQ, B, H, Nq, d, dtype, true, &p.sdQ)) != FA_OK ||
+        (s = take_strides(sdK, B, H, Nk, d, dtype, true, &p.sdK)) != FA_OK ||
+        (s = take_strides(sdV, B, H, Nk, d, dtype, true, &p.sdV)) != FA_OK)
         return s;
-    return fa_bwd_grads(Q, K, V, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace,
-                        workspace_bytes, stream);
+    if ((s = bwd_ptrs(p, Q, K, V, O, dO, L, dQ, dK, dV)) != FA_OK) return s;
+    if ((s = run_preprocess(p, w, O, dO, L, workspace, stream)) != FA_OK) return s;
+    return run_grads(p, w, Q, K, V, dO, L, dQ, dK, dV, workspace, stream);
 }
 
 fa_status fa_get_device_status(fa_stream_t stream) {

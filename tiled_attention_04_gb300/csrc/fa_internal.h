@@ -7,7 +7,20 @@
 
 #include "fa.h"
 
+// Element strides of a (B, H, N, d) tensor s: element (b, h, n, c) is at index
+// b*s.b + h*s.h + n*s.n + c (the head dimension is contiguous).
+struct FaStrides {
+    long long b, h, n;
+};
+
+// index of the first element of row n of batch*head bh = b*H + h
+__host__ __device__ __forceinline__ long long fa_row_offset(const FaStrides &s, int H, int bh, int n) {
+    const int b = bh / H;
+    return (long long)b * s.b + (long long)(bh - b * H) * s.h + (long long)n * s.n;
+}
+
 struct FaProblem {
+    int B, H;        // batch, heads
     int BH;          // batch * heads
     int Nq, Nk;      // query / key sequence lengths
     int d;           // head dimension
@@ -16,6 +29,8 @@ struct FaProblem {
     fa_dtype dtype;  // element type of Q, K, V, O, dO, dQ, dK, dV
     uint32_t wait_limit;  // cap on device-side polling loops
     uint32_t force_stall; // fault injection: the forward's MMA issuer waits on a barrier nobody arrives on
+    // strides of every (B, H, N, d) tensor (contiguous unless a *_strided entry point set them)
+    FaStrides sQ, sK, sV, sO, sdO, sdQ, sdK, sdV;
 };
 
 // ---- fp32 CUDA-core kernels (fa_simt.cu): every dtype and head dim.
@@ -27,10 +42,15 @@ cudaError_t simt_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, cons
                           const float *L, const float *Dvec, void *dK, void *dV, cudaStream_t st);
 cudaError_t simt_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                         const float *L, const float *Dvec, void *dQ, cudaStream_t st);
+// writes zeros to the N rows of every batch*head of the (B, H, N, d) view X with strides s
+cudaError_t simt_zero_rows(const FaProblem &p, void *X, const FaStrides &s, int N, cudaStream_t st);
 
-// (B*H, N, d) bf16 tensor -> 3-D TMA map, boxes of 64 columns x box_rows rows, 128-byte swizzle
+// (B, H, N, d) bf16 tensor with strides s -> 4-D TMA map over (d, N, H, B), boxes of
+// 64 columns x box_rows rows, 128-byte swizzle; a load of batch*head bh uses
+// coordinates (column, row, bh % H, bh / H)
 struct CUtensorMap_st;
-bool tc_make_map_3d(CUtensorMap_st *m, const void *ptr, int BH, int N, int d, int box_rows);
+bool tc_make_map_4d(CUtensorMap_st *m, const void *ptr, int B, int H, int N, int d, const FaStrides &s,
+                    int box_rows);
 
 // ---- tcgen05 tensor-core kernels (fa_tc_fwd.cu, fa_tc_bwd.cu): bf16, d in {64, 128}.
 bool tc_fwd_supported(const FaProblem &p);

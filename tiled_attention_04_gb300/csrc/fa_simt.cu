@@ -22,6 +22,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "fa_internal.h"
 
 namespace {
@@ -37,13 +39,21 @@ template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-// rows [row0, row0+SB) of an (N, D) matrix into smem [SB][D+1] fp32, zero past N
+// Heads per batch and the element strides of every (B, H, N, d) tensor.
+struct Views {
+    int H;
+    FaStrides q, k, v, o, dO, dq, dk, dv;
+};
+
+Views views_of(const FaProblem &p) { return Views{p.H, p.sQ, p.sK, p.sV, p.sO, p.sdO, p.sdQ, p.sdK, p.sdV}; }
+
+// rows [row0, row0+SB) of an (N, D) matrix with row stride rs into smem [SB][D+1] fp32, zero past N
 template <typename T, int D>
-__device__ __forceinline__ void load_tile(float *s, const T *g, int row0, int N) {
+__device__ __forceinline__ void load_tile(float *s, const T *g, long long rs, int row0, int N) {
     for (int idx = threadIdx.x; idx < SB * D; idx += NT) {
         const int r = idx / D, c = idx % D;
         const int gr = row0 + r;
-        s[r * (D + 1) + c] = gr < N ? to_f(g[(size_t)gr * D + c]) : 0.f;
+        s[r * (D + 1) + c] = gr < N ? to_f(g[(long long)gr * rs + c]) : 0.f;
     }
 }
 
@@ -67,14 +77,15 @@ constexpr size_t bwd_smem() { return (size_t)(4 * SB * (D + 1) + SB * (SB + 1) +
 template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(NT) simt_fwd_kernel(const T *__restrict__ Q, const T *__restrict__ K,
                                                       const T *__restrict__ V, T *__restrict__ O,
-                                                      float *__restrict__ L, int Nq, int Nk, float scale_log2) {
+                                                      float *__restrict__ L, int Nq, int Nk, float scale_log2,
+                                                      Views vw) {
     extern __shared__ float sm[];
     float *Qs = sm, *Ks = Qs + SB * (D + 1), *Vs = Ks + SB * (D + 1), *Ps = Vs + SB * (D + 1);
     constexpr int OC = D / 16;
     const int bh = blockIdx.y, q0 = blockIdx.x * SB;
-    const T *Qg = Q + (size_t)bh * Nq * D;
-    const T *Kg = K + (size_t)bh * Nk * D;
-    const T *Vg = V + (size_t)bh * Nk * D;
+    const T *Qg = Q + fa_row_offset(vw.q, vw.H, bh, 0);
+    const T *Kg = K + fa_row_offset(vw.k, vw.H, bh, 0);
+    const T *Vg = V + fa_row_offset(vw.v, vw.H, bh, 0);
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
 
     float o[4][OC], m[4], l[4];
@@ -85,12 +96,12 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(const T *__restrict__ Q, c
 #pragma unroll
         for (int c = 0; c < OC; ++c) o[i][c] = 0.f;
     }
-    load_tile<T, D>(Qs, Qg, q0, Nq);
+    load_tile<T, D>(Qs, Qg, vw.q.n, q0, Nq);
     const int kend = CAUSAL ? min(Nk, q0 + SB) : Nk;   // keys beyond the tile's last query are never visible
     for (int k0 = 0; k0 < kend; k0 += SB) {
         __syncthreads();
-        load_tile<T, D>(Ks, Kg, k0, Nk);
-        load_tile<T, D>(Vs, Vg, k0, Nk);
+        load_tile<T, D>(Ks, Kg, vw.k.n, k0, Nk);
+        load_tile<T, D>(Vs, Vg, vw.v.n, k0, Nk);
         __syncthreads();
         float s[4][4];
 #pragma unroll
@@ -154,14 +165,14 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(const T *__restrict__ Q, c
                 for (int c = 0; c < OC; ++c) o[i][c] = fmaf(pv[i], vv[c], o[i][c]);
         }
     }
-    T *Og = O + (size_t)bh * Nq * D;
+    T *Og = O + fa_row_offset(vw.o, vw.H, bh, 0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int qi = q0 + ty * 4 + i;
         if (qi < Nq) {
             const float inv = 1.f / l[i];
 #pragma unroll
-            for (int c = 0; c < OC; ++c) Og[(size_t)qi * D + tx + 16 * c] = from_f<T>(o[i][c] * inv);
+            for (int c = 0; c < OC; ++c) Og[(long long)qi * vw.o.n + tx + 16 * c] = from_f<T>(o[i][c] * inv);
             if (tx == 0) L[(size_t)bh * Nq + qi] = m[i] * kLn2 + logf(l[i]);
         }
     }
@@ -170,12 +181,15 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(const T *__restrict__ Q, c
 // ------------------------------------------------------------------ D = rowsum(dO * O)
 template <typename T>
 __global__ void __launch_bounds__(NT) simt_preprocess_kernel(const T *__restrict__ O, const T *__restrict__ dO,
-                                                             float *__restrict__ Dvec, long long rows, int D) {
+                                                             float *__restrict__ Dvec, long long rows, int D,
+                                                             int Nq, Views vw) {
     const long long row = (long long)blockIdx.x * (NT / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
+    const int bh = (int)(row / Nq), q = (int)(row % Nq);
+    const T *o = O + fa_row_offset(vw.o, vw.H, bh, q), *g = dO + fa_row_offset(vw.dO, vw.H, bh, q);
     float acc = 0.f;
-    for (int c = lane; c < D; c += 32) acc = fmaf(to_f(O[row * D + c]), to_f(dO[row * D + c]), acc);
+    for (int c = lane; c < D; c += 32) acc = fmaf(to_f(o[c]), to_f(g[c]), acc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) Dvec[row] = acc;
@@ -187,14 +201,14 @@ __global__ void __launch_bounds__(NT) simt_dkdv_kernel(const T *__restrict__ Q, 
                                                        const T *__restrict__ V, const T *__restrict__ dO,
                                                        const float *__restrict__ L, const float *__restrict__ Dvec,
                                                        T *__restrict__ dK, T *__restrict__ dV, int Nq, int Nk,
-                                                       float scale, float scale_log2) {
+                                                       float scale, float scale_log2, Views vw) {
     extern __shared__ float sm[];
     float *Ks = sm, *Vs = Ks + SB * (D + 1), *Qs = Vs + SB * (D + 1), *dOs = Qs + SB * (D + 1);
     float *Ps = dOs + SB * (D + 1), *Ls = Ps + SB * (SB + 1), *Ds = Ls + SB;
     constexpr int OC = D / 16;
     const int bh = blockIdx.y, k0 = blockIdx.x * SB;
-    const T *Qg = Q + (size_t)bh * Nq * D, *dOg = dO + (size_t)bh * Nq * D;
-    const T *Kg = K + (size_t)bh * Nk * D, *Vg = V + (size_t)bh * Nk * D;
+    const T *Qg = Q + fa_row_offset(vw.q, vw.H, bh, 0), *dOg = dO + fa_row_offset(vw.dO, vw.H, bh, 0);
+    const T *Kg = K + fa_row_offset(vw.k, vw.H, bh, 0), *Vg = V + fa_row_offset(vw.v, vw.H, bh, 0);
     const float *Lg = L + (size_t)bh * Nq, *Dg = Dvec + (size_t)bh * Nq;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
 
@@ -203,13 +217,13 @@ __global__ void __launch_bounds__(NT) simt_dkdv_kernel(const T *__restrict__ Q, 
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int c = 0; c < OC; ++c) dk[i][c] = dv[i][c] = 0.f;
-    load_tile<T, D>(Ks, Kg, k0, Nk);
-    load_tile<T, D>(Vs, Vg, k0, Nk);
+    load_tile<T, D>(Ks, Kg, vw.k.n, k0, Nk);
+    load_tile<T, D>(Vs, Vg, vw.v.n, k0, Nk);
     const int qstart = CAUSAL ? k0 : 0;   // queries before this key tile never see it
     for (int q0 = qstart; q0 < Nq; q0 += SB) {
         __syncthreads();
-        load_tile<T, D>(Qs, Qg, q0, Nq);
-        load_tile<T, D>(dOs, dOg, q0, Nq);
+        load_tile<T, D>(Qs, Qg, vw.q.n, q0, Nq);
+        load_tile<T, D>(dOs, dOg, vw.dO.n, q0, Nq);
         if (tid < SB) {
             const int qi = q0 + tid;
             Ls[tid] = qi < Nq ? Lg[qi] * kLog2e : INFINITY;   // padding rows get P = 0
@@ -285,15 +299,15 @@ __global__ void __launch_bounds__(NT) simt_dkdv_kernel(const T *__restrict__ Q, 
                 for (int cc = 0; cc < OC; ++cc) dk[i][cc] = fmaf(sv[i], qv[cc], dk[i][cc]);
         }
     }
-    T *dKg = dK + (size_t)bh * Nk * D, *dVg = dV + (size_t)bh * Nk * D;
+    T *dKg = dK + fa_row_offset(vw.dk, vw.H, bh, 0), *dVg = dV + fa_row_offset(vw.dv, vw.H, bh, 0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int kj = k0 + ty * 4 + i;
         if (kj < Nk) {
 #pragma unroll
             for (int cc = 0; cc < OC; ++cc) {
-                dKg[(size_t)kj * D + tx + 16 * cc] = from_f<T>(dk[i][cc] * scale);
-                dVg[(size_t)kj * D + tx + 16 * cc] = from_f<T>(dv[i][cc]);
+                dKg[(long long)kj * vw.dk.n + tx + 16 * cc] = from_f<T>(dk[i][cc] * scale);
+                dVg[(long long)kj * vw.dv.n + tx + 16 * cc] = from_f<T>(dv[i][cc]);
             }
         }
     }
@@ -305,14 +319,14 @@ __global__ void __launch_bounds__(NT) simt_dq_kernel(const T *__restrict__ Q, co
                                                      const T *__restrict__ V, const T *__restrict__ dO,
                                                      const float *__restrict__ L, const float *__restrict__ Dvec,
                                                      T *__restrict__ dQ, int Nq, int Nk, float scale,
-                                                     float scale_log2) {
+                                                     float scale_log2, Views vw) {
     extern __shared__ float sm[];
     float *Qs = sm, *dOs = Qs + SB * (D + 1), *Ks = dOs + SB * (D + 1), *Vs = Ks + SB * (D + 1);
     float *Ps = Vs + SB * (D + 1);
     constexpr int OC = D / 16;
     const int bh = blockIdx.y, q0 = blockIdx.x * SB;
-    const T *Qg = Q + (size_t)bh * Nq * D, *dOg = dO + (size_t)bh * Nq * D;
-    const T *Kg = K + (size_t)bh * Nk * D, *Vg = V + (size_t)bh * Nk * D;
+    const T *Qg = Q + fa_row_offset(vw.q, vw.H, bh, 0), *dOg = dO + fa_row_offset(vw.dO, vw.H, bh, 0);
+    const T *Kg = K + fa_row_offset(vw.k, vw.H, bh, 0), *Vg = V + fa_row_offset(vw.v, vw.H, bh, 0);
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
 
     float dq[4][OC], lrow[4], drow[4];
@@ -324,13 +338,13 @@ __global__ void __launch_bounds__(NT) simt_dq_kernel(const T *__restrict__ Q, co
 #pragma unroll
         for (int c = 0; c < OC; ++c) dq[i][c] = 0.f;
     }
-    load_tile<T, D>(Qs, Qg, q0, Nq);
-    load_tile<T, D>(dOs, dOg, q0, Nq);
+    load_tile<T, D>(Qs, Qg, vw.q.n, q0, Nq);
+    load_tile<T, D>(dOs, dOg, vw.dO.n, q0, Nq);
     const int kend = CAUSAL ? min(Nk, q0 + SB) : Nk;
     for (int k0 = 0; k0 < kend; k0 += SB) {
         __syncthreads();
-        load_tile<T, D>(Ks, Kg, k0, Nk);
-        load_tile<T, D>(Vs, Vg, k0, Nk);
+        load_tile<T, D>(Ks, Kg, vw.k.n, k0, Nk);
+        load_tile<T, D>(Vs, Vg, vw.v.n, k0, Nk);
         __syncthreads();
         float s[4][4], dp[4][4];
 #pragma unroll
@@ -382,14 +396,24 @@ __global__ void __launch_bounds__(NT) simt_dq_kernel(const T *__restrict__ Q, co
                 for (int cc = 0; cc < OC; ++cc) dq[i][cc] = fmaf(sv[i], kv[cc], dq[i][cc]);
         }
     }
-    T *dQg = dQ + (size_t)bh * Nq * D;
+    T *dQg = dQ + fa_row_offset(vw.dq, vw.H, bh, 0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int qi = q0 + ty * 4 + i;
         if (qi < Nq) {
 #pragma unroll
-            for (int cc = 0; cc < OC; ++cc) dQg[(size_t)qi * D + tx + 16 * cc] = from_f<T>(dq[i][cc] * scale);
+            for (int cc = 0; cc < OC; ++cc) dQg[(long long)qi * vw.dq.n + tx + 16 * cc] = from_f<T>(dq[i][cc] * scale);
         }
+    }
+}
+
+// ------------------------------------------------------------------ zero rows of a strided view
+template <typename T>
+__global__ void __launch_bounds__(NT) simt_zero_kernel(T *__restrict__ X, FaStrides s, int H, int N, int D,
+                                                       long long total) {
+    for (long long i = (long long)blockIdx.x * NT + threadIdx.x; i < total; i += (long long)gridDim.x * NT) {
+        const long long row = i / D;
+        X[fa_row_offset(s, H, (int)(row / N), (int)(row % N)) + i % D] = from_f<T>(0.f);
     }
 }
 
@@ -407,21 +431,21 @@ cudaError_t fwd_t(const FaProblem &p, const void *Q, const void *K, const void *
                   cudaStream_t st) {
     dim3 grid((p.Nq + SB - 1) / SB, p.BH);
     return launch(simt_fwd_kernel<T, D, C>, grid, fwd_smem<D>(), st, (const T *)Q, (const T *)K, (const T *)V,
-                  (T *)O, L, p.Nq, p.Nk, p.scale * kLog2e);
+                  (T *)O, L, p.Nq, p.Nk, p.scale * kLog2e, views_of(p));
 }
 template <typename T, int D, bool C>
 cudaError_t dkdv_t(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                    const float *L, const float *Dv, void *dK, void *dV, cudaStream_t st) {
     dim3 grid((p.Nk + SB - 1) / SB, p.BH);
     return launch(simt_dkdv_kernel<T, D, C>, grid, bwd_smem<D>(), st, (const T *)Q, (const T *)K, (const T *)V,
-                  (const T *)dO, L, Dv, (T *)dK, (T *)dV, p.Nq, p.Nk, p.scale, p.scale * kLog2e);
+                  (const T *)dO, L, Dv, (T *)dK, (T *)dV, p.Nq, p.Nk, p.scale, p.scale * kLog2e, views_of(p));
 }
 template <typename T, int D, bool C>
 cudaError_t dq_t(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO, const float *L,
                  const float *Dv, void *dQ, cudaStream_t st) {
     dim3 grid((p.Nq + SB - 1) / SB, p.BH);
     return launch(simt_dq_kernel<T, D, C>, grid, bwd_smem<D>(), st, (const T *)Q, (const T *)K, (const T *)V,
-                  (const T *)dO, L, Dv, (T *)dQ, p.Nq, p.Nk, p.scale, p.scale * kLog2e);
+                  (const T *)dO, L, Dv, (T *)dQ, p.Nq, p.Nk, p.scale, p.scale * kLog2e, views_of(p));
 }
 
 // expands FN<T, D, C>(args) over dtype x head dim x causal
@@ -459,10 +483,23 @@ cudaError_t simt_bwd_preprocess(const FaProblem &p, const void *O, const void *d
     if (rows == 0) return cudaSuccess;
     dim3 grid((unsigned)((rows + NT / 32 - 1) / (NT / 32)));
     if (p.dtype == FA_DTYPE_F32)
-        simt_preprocess_kernel<float><<<grid, NT, 0, st>>>((const float *)O, (const float *)dO, Dvec, rows, p.d);
+        simt_preprocess_kernel<float><<<grid, NT, 0, st>>>((const float *)O, (const float *)dO, Dvec, rows, p.d,
+                                                           p.Nq, views_of(p));
     else
         simt_preprocess_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>((const __nv_bfloat16 *)O,
-                                                                  (const __nv_bfloat16 *)dO, Dvec, rows, p.d);
+                                                                  (const __nv_bfloat16 *)dO, Dvec, rows, p.d,
+                                                                  p.Nq, views_of(p));
+    return cudaGetLastError();
+}
+
+cudaError_t simt_zero_rows(const FaProblem &p, void *X, const FaStrides &s, int N, cudaStream_t st) {
+    const long long total = (long long)p.BH * N * p.d;
+    if (total == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)std::min<long long>((total + NT - 1) / NT, 4096);
+    if (p.dtype == FA_DTYPE_F32)
+        simt_zero_kernel<float><<<grid, NT, 0, st>>>((float *)X, s, p.H, N, p.d, total);
+    else
+        simt_zero_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>((__nv_bfloat16 *)X, s, p.H, N, p.d, total);
     return cudaGetLastError();
 }
 

@@ -66,7 +66,8 @@ template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
                                                          const __nv_bfloat16 *__restrict__ dO,
                                                          const float *__restrict__ L, float *__restrict__ Dp,
-                                                         float *__restrict__ Lp, int BH, int Nq) {
+                                                         float *__restrict__ Lp, int BH, int Nq, int H,
+                                                         FaStrides so, FaStrides sdo) {
     constexpr int TPR = D / 8;                      // threads per row
     tc::pdl_launch_dependents();
     tc::pdl_wait();   // O (from the forward) and dO are complete
@@ -77,9 +78,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__
     const int bh = live ? (int)(gr / nqp) : 0, q = live ? (int)(gr % nqp) : 0;
     float acc = 0.f;
     if (live && q < Nq) {
-        const size_t off = ((size_t)bh * Nq + q) * D + sub * 8;
-        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(O + off));
-        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + off));
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(O + fa_row_offset(so, H, bh, q) + sub * 8));
+        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + fa_row_offset(sdo, H, bh, q) + sub * 8));
         const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
         const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
 #pragma unroll
@@ -165,7 +165,8 @@ template <int D, bool CAUSAL, int SPLIT>
 __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                           const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                           const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
-                                          __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, float scale,
+                                          __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, int H,
+                                          const FaStrides &sdk, const FaStrides &sdv, float scale,
                                           float scale_log2, uint32_t wait_limit) {
     using C = DkdvWideCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -233,8 +234,8 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
             tc::tma_prefetch_desc(&tmdO);
             tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
             for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_3d(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh);
-                tc::tma_load_3d(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh);
+                tc::tma_load_bh(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
+                tc::tma_load_bh(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
             }
             int issued = 0;
             for (int it = 0; it < n; ++it) {
@@ -244,10 +245,10 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                 const int q0 = (i_begin + it) * C::BQ;
                 tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 1024);
                 for (int c = 0; c < D / 64; ++c) {
-                    tc::tma_load_3d(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
-                                    q0, bh);
-                    tc::tma_load_3d(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
-                                    c * 64, q0, bh);
+                    tc::tma_load_bh(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
+                                    q0, bh, H);
+                    tc::tma_load_bh(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
+                                    c * 64, q0, bh, H);
                 }
                 const size_t off = (size_t)bh * nqp + q0;
                 tc::bulk_load(base + C::LD_OFF + s * 1024, Lp + off, 512, q_full(s));
@@ -422,7 +423,8 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         if (fine && n > 0) fine = W.wait(q_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
-        __nv_bfloat16 *dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
+        __nv_bfloat16 *dst = t == 0 ? dV + fa_row_offset(sdv, tc::opaque(H), bh, key)
+                                         : dK + fa_row_offset(sdk, tc::opaque(H), bh, key);
         const float mul = t == 0 ? 1.f : scale;
         const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
         // Split items: each rank finalises one tensor (rank 0 dV, rank 1 dK) and sends
@@ -537,7 +539,8 @@ template <int D, bool CAUSAL, int SPLIT>
 __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                         const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                         const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ, int Nq, int Nk,
-                                        int qt, int bh, float scale, float scale_log2, uint32_t wait_limit) {
+                                        int qt, int bh, int H, const FaStrides &sdq, float scale, float scale_log2,
+                                        uint32_t wait_limit) {
     using C = DqWideCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -602,8 +605,8 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
             tc::tma_prefetch_desc(&tmV);
             tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
             for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_3d(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh);
-                tc::tma_load_3d(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh);
+                tc::tma_load_bh(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
+                tc::tma_load_bh(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
             }
             int issued = 0;
             for (int j = 0; j < n; ++j) {
@@ -611,10 +614,10 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
                 if (!W.wait(kv_empty(s), ((j / C::STAGES) & 1) ^ 1u)) break;
                 tc::mbar_arrive_expect_tx(kv_full(s), 2 * C::KT::BYTES);
                 for (int c = 0; c < D / 64; ++c) {
-                    tc::tma_load_3d(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
-                                    (jb + j) * C::BK, bh);
-                    tc::tma_load_3d(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
-                                    (jb + j) * C::BK, bh);
+                    tc::tma_load_bh(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
+                                    (jb + j) * C::BK, bh, H);
+                    tc::tma_load_bh(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
+                                    (jb + j) * C::BK, bh, H);
                 }
                 issued = j + 1;
             }
@@ -753,7 +756,7 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
         if (fine && n > 0) fine = W.wait(kv_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
-        __nv_bfloat16 *dst = dQ + ((size_t)bh * Nq + row) * D;
+        __nv_bfloat16 *dst = dQ + fa_row_offset(sdq, tc::opaque(H), bh, row);
         const uint32_t tA = tmem + lane_base + C::DQ_COL;
         // Split items: rank r finalises the columns of warpgroup r and sends its partial
         // of the other half into the peer's shared memory with remote stores, once the
@@ -872,7 +875,8 @@ template <int D, bool CAUSAL, int SPLIT>
 __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                           const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                           const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
-                                          __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, float scale,
+                                          __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, int H,
+                                          const FaStrides &sdk, const FaStrides &sdv, float scale,
                                           float scale_log2, uint32_t wait_limit) {
     using C = DkdvNarrowCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -942,8 +946,8 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
             tc::tma_prefetch_desc(&tmdO);
             tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
             for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_3d(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh);
-                tc::tma_load_3d(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh);
+                tc::tma_load_bh(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
+                tc::tma_load_bh(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
             }
             int issued = 0;
             for (int it = 0; it < n; ++it) {
@@ -953,10 +957,10 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                 const int q0 = (i_begin + it) * C::BQ;
                 tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 512);
                 for (int c = 0; c < D / 64; ++c) {
-                    tc::tma_load_3d(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
-                                    q0, bh);
-                    tc::tma_load_3d(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
-                                    c * 64, q0, bh);
+                    tc::tma_load_bh(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
+                                    q0, bh, H);
+                    tc::tma_load_bh(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
+                                    c * 64, q0, bh, H);
                 }
                 const size_t off = (size_t)bh * nqp + q0;
                 tc::bulk_load(base + C::LD_OFF + s * 512, Lp + off, 256, q_full(s));
@@ -1103,7 +1107,8 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
         if (fine && n > 0) fine = W.wait(q_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
-        __nv_bfloat16 *dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
+        __nv_bfloat16 *dst = t == 0 ? dV + fa_row_offset(sdv, tc::opaque(H), bh, key)
+                                         : dK + fa_row_offset(sdk, tc::opaque(H), bh, key);
         const float mul = t == 0 ? 1.f : scale;
         const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
         // Split items: each rank finalises one tensor (rank 0 dV, rank 1 dK) and sends
@@ -1214,7 +1219,8 @@ template <int D, bool CAUSAL, int SPLIT>
 __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                         const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                         const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ, int Nq, int Nk,
-                                        int qt, int bh, float scale, float scale_log2, uint32_t wait_limit) {
+                                        int qt, int bh, int H, const FaStrides &sdq, float scale, float scale_log2,
+                                        uint32_t wait_limit) {
     using C = DqNarrowCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -1281,8 +1287,8 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
             tc::tma_prefetch_desc(&tmV);
             tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
             for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_3d(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh);
-                tc::tma_load_3d(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh);
+                tc::tma_load_bh(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
+                tc::tma_load_bh(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
             }
             int issued = 0;
             for (int j = 0; j < n; ++j) {
@@ -1290,10 +1296,10 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                 if (!W.wait(kv_empty(s), ((j / C::STAGES) & 1) ^ 1u)) break;
                 tc::mbar_arrive_expect_tx(kv_full(s), 2 * C::KT::BYTES);
                 for (int c = 0; c < D / 64; ++c) {
-                    tc::tma_load_3d(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
-                                    (jb + j) * C::BK, bh);
-                    tc::tma_load_3d(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
-                                    (jb + j) * C::BK, bh);
+                    tc::tma_load_bh(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
+                                    (jb + j) * C::BK, bh, H);
+                    tc::tma_load_bh(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
+                                    (jb + j) * C::BK, bh, H);
                 }
                 issued = j + 1;
             }
@@ -1416,7 +1422,7 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
         if (fine && n > 0) fine = W.wait(kv_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
-        __nv_bfloat16 *dst = dQ + ((size_t)bh * Nq + row) * D;
+        __nv_bfloat16 *dst = dQ + fa_row_offset(sdq, tc::opaque(H), bh, row);
         const uint32_t tA = tmem + lane_base + C::DQ_COL;
         // Split items: rank r finalises the columns of warpgroup r and sends its partial
         // of the other half into the peer's shared memory with remote stores, once the
@@ -1508,7 +1514,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ,
                      __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH,
                      int k_tiles, int q_tiles, int n_kv_items, int n_q_items, float scale, float scale_log2,
-                     uint32_t wait_limit) {
+                     uint32_t wait_limit, int H, FaStrides sdq, FaStrides sdk, FaStrides sdv) {
     tc::pdl_launch_dependents();
     tc::pdl_wait();   // D and L staged by the preprocessing kernel are complete
     const int item = blockIdx.x / SPLIT;
@@ -1526,16 +1532,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int r = idx / BH;
         const int kt = CAUSAL ? r : k_tiles - 1 - r;    // causal: the first key tiles see the most queries
         if constexpr (D == 64)
-            dkdv_item_wide<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, scale, scale_log2, wait_limit);
+            dkdv_item_wide<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, sdk, sdv, scale,
+                                             scale_log2, wait_limit);
         else
-            dkdv_item_narrow<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, scale, scale_log2,
-                                               wait_limit);
+            dkdv_item_narrow<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, sdk, sdv, scale,
+                                               scale_log2, wait_limit);
     } else {
         const int qt = q_tiles - 1 - idx / BH;           // causal: the last query tiles see the most keys
         if constexpr (D == 64)
-            dq_item_wide<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, scale, scale_log2, wait_limit);
+            dq_item_wide<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, sdq, scale, scale_log2,
+                                           wait_limit);
         else
-            dq_item_narrow<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, scale, scale_log2, wait_limit);
+            dq_item_narrow<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, sdq, scale, scale_log2,
+                                             wait_limit);
     }
 }
 
@@ -1620,7 +1629,7 @@ cudaError_t launch_bwd(const FaProblem &p, const Maps2 &m, const float *Lp, cons
     return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q, m.a.k, m.a.v,
                           m.a.dO, m.b.q, m.b.k, m.b.v, m.b.dO, Lp, Dp, static_cast<__nv_bfloat16 *>(dQ),
                           static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt, qt,
-                          (int)na, (int)nb, p.scale, p.scale * kLog2e, p.wait_limit);
+                          (int)na, (int)nb, p.scale, p.scale * kLog2e, p.wait_limit, p.H, p.sdQ, p.sdK, p.sdV);
 }
 
 template <int D, bool CAUSAL>
@@ -1633,8 +1642,10 @@ cudaError_t launch_bwd_any(const FaProblem &p, const Maps2 &m, const float *Lp, 
 
 bool make_maps(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO, int q_rows,
                int k_rows, Maps *m) {
-    return tc_make_map_3d(&m->q, Q, p.BH, p.Nq, p.d, q_rows) && tc_make_map_3d(&m->dO, dO, p.BH, p.Nq, p.d, q_rows) &&
-           tc_make_map_3d(&m->k, K, p.BH, p.Nk, p.d, k_rows) && tc_make_map_3d(&m->v, V, p.BH, p.Nk, p.d, k_rows);
+    return tc_make_map_4d(&m->q, Q, p.B, p.H, p.Nq, p.d, p.sQ, q_rows) &&
+           tc_make_map_4d(&m->dO, dO, p.B, p.H, p.Nq, p.d, p.sdO, q_rows) &&
+           tc_make_map_4d(&m->k, K, p.B, p.H, p.Nk, p.d, p.sK, k_rows) &&
+           tc_make_map_4d(&m->v, V, p.B, p.H, p.Nk, p.d, p.sV, k_rows);
 }
 
 }  // namespace
@@ -1660,8 +1671,9 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = p.d == 128 ? cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128>, o, g, L, Dp, Lp, p.BH, p.Nq)
-                                     : cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<64>, o, g, L, Dp, Lp, p.BH, p.Nq);
+    const cudaError_t e =
+        p.d == 128 ? cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128>, o, g, L, Dp, Lp, p.BH, p.Nq, p.H, p.sO, p.sdO)
+                   : cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<64>, o, g, L, Dp, Lp, p.BH, p.Nq, p.H, p.sO, p.sdO);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

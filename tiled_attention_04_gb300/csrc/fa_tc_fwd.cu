@@ -96,7 +96,9 @@ struct FwdCfg {
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t MISC_OFF = STAT_OFF + 2 * 512 * 4;
     static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;                  // peer_free, peer_ready
-    static constexpr uint32_t USED = PEER_BAR_OFF + 16;
+    // persistent kernel: per softmax thread, the element offset of its output row in the current unit
+    static constexpr uint32_t OROW_OFF = PEER_BAR_OFF + 16;
+    static constexpr uint32_t USED = OROW_OFF + 256 * 8;
     // split items: rank 1's partial O (fp32, rows padded by 4 floats) and its m, l, in the K ring
     static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
     static constexpr uint32_t PART_OFF = K_OFF;
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
-                     uint32_t wait_limit, uint32_t force_stall) {
+                     uint32_t wait_limit, uint32_t force_stall, int H, FaStrides so) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::tma_prefetch_desc(&tmV);
             tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c)
-                tc::tma_load_3d(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh);
+                tc::tma_load_bh(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh, H);
             int k_issued = 0, v_issued = 0;
             // The slot of tile j last held tile j - st.  A V slot is free once PV of that
             // tile has completed.  A K slot is read only by S of that tile; with P over S
@@ -212,8 +214,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (j >= st && !W.wait(pv_done_bar(g), (g / C::R) & 1)) return false;
                 tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
-                    tc::tma_load_3d(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64,
-                                    (jb + j) * BN, bh);
+                    tc::tma_load_bh(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64,
+                                    (jb + j) * BN, bh, H);
                 return true;
             };
             // order K_0, K_1, V_0, K_2, V_1, ...: the MMA warp uses K_{j+1} before V_j
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         auto store_row = [&](const float *vals, float Mrow, float lrow) {
             const float inv = 1.f / lrow;
-            __nv_bfloat16 *orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
+            __nv_bfloat16 *orow = O + fa_row_offset(so, tc::opaque(H), bh, row) + t * (D / 2);
             if (row < Nq) {
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c) {
@@ -542,7 +544,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
-                     uint32_t wait_limit, uint32_t force_stall) {
+                     uint32_t wait_limit, uint32_t force_stall, int H, FaStrides so) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -643,15 +645,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (u > 0 && !(ok = W.wait(q_empty, (u - 1) & 1))) break;
                 tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
-                    tc::tma_load_3d(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, w.q0, w.bh);
+                    tc::tma_load_bh(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, w.q0, w.bh, H);
                 q_issued = u + 1;
                 auto load = [&](const CUtensorMap *m, uint32_t ring, uint32_t st, int g, int key0, uint32_t full) {
                     // the slot last held tile g - st: wait until PV of that tile has completed
                     if (g >= (int)st && !W.wait(pv_done_bar(g - (int)st), pv_done_par(g - (int)st))) return false;
                     tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
                     for (int c = 0; c < C::CHUNKS; ++c)
-                        tc::tma_load_3d(ring + ((uint32_t)g % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full,
-                                        c * 64, key0, w.bh);
+                        tc::tma_load_bh(ring + ((uint32_t)g % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full,
+                                        c * 64, key0, w.bh, H);
                     return true;
                 };
                 // order K_0, K_1, V_0, K_2, V_1, ...: the MMA warp uses K_{j+1} before V_j
@@ -780,6 +782,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Unit w;
         for (int u = 0; ok && unit_of(u, w); ++u) {
             const int n = w.n, bh = w.bh, row = w.q0 + r;
+            // the output row's offset, taken now and parked in shared memory: computed at
+            // the epilogue it would compete for registers with the row being stored
+            volatile long long *orow_sm = reinterpret_cast<volatile long long *>(sb + C::OROW_OFF) + (threadIdx.x - 128);
+            *orow_sm = fa_row_offset(so, H, bh, row);
             // this warpgroup's tiles of the unit: local j = jt, jt + 2, ... (global g = g0 + j has parity t)
             const int j_0 = (0 - g0) & 1, j_1 = (1 - g0) & 1;
             const int jt = t == 0 ? j_0 : j_1;
@@ -916,7 +922,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_arrive(o_free);
             auto store_row = [&](const float *vals, float Mrow, float lrow) {
                 const float inv = 1.f / lrow;
-                __nv_bfloat16 *orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
+                __nv_bfloat16 *orow = O + *orow_sm + t * (D / 2);
                 if (row < Nq) {
 #pragma unroll
                     for (int c = 0; c < D / 16; ++c) {
@@ -962,16 +968,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// (BH, N, d) bf16 tensor -> 3-D map with 64 x rows x 1 boxes, 128-byte swizzle.
-// Rows past N in a batch*head read as zero.
-bool tc_make_map_3d(CUtensorMap_st *m, const void *ptr, int BH, int N, int d, int box_rows) {
+// (B, H, N, d) bf16 view -> 4-D map over (d, N, H, B) with 64 x rows x 1 x 1 boxes,
+// 128-byte swizzle.  Rows past N in a batch*head read as zero.  The strides are
+// the view's own (positive multiples of 16 bytes below 2^40 bytes), in any order.
+bool tc_make_map_4d(CUtensorMap_st *m, const void *ptr, int B, int H, int N, int d, const FaStrides &s,
+                    int box_rows) {
     auto enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)s.n * 2, (cuuint64_t)s.h * 2, (cuuint64_t)s.b * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -992,7 +1000,7 @@ static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const C
     static_assert(!(PERSIST && SPLIT > 1), "persistent units are not split");
     using C = FwdCfg<D>;
     void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, __nv_bfloat16 *, float *, int, int, int, int,
-                 float, uint32_t, uint32_t);
+                 float, uint32_t, uint32_t, int, FaStrides);
     if constexpr (PERSIST) kern = fa_fwd_tc_persistent_kernel<D, CAUSAL>;
     else kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
@@ -1018,7 +1026,7 @@ static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const C
     cfg.attrs = attr;
     cfg.numAttrs = SPLIT > 1 ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, static_cast<__nv_bfloat16 *>(O), L, p.Nq, p.Nk, p.BH, qtiles,
-                           scale_log2, p.wait_limit, p.force_stall);
+                           scale_log2, p.wait_limit, p.force_stall, p.H, p.sO);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1062,8 +1070,9 @@ static cudaError_t launch_fwd_any(const FaProblem &p, const CUtensorMap &mq, con
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
                    cudaStream_t st) {
     CUtensorMap mq, mk, mv;
-    if (!tc_make_map_3d(&mq, Q, p.BH, p.Nq, p.d, BM) || !tc_make_map_3d(&mk, K, p.BH, p.Nk, p.d, BN) ||
-        !tc_make_map_3d(&mv, V, p.BH, p.Nk, p.d, BN))
+    if (!tc_make_map_4d(&mq, Q, p.B, p.H, p.Nq, p.d, p.sQ, BM) ||
+        !tc_make_map_4d(&mk, K, p.B, p.H, p.Nk, p.d, p.sK, BN) ||
+        !tc_make_map_4d(&mv, V, p.B, p.H, p.Nk, p.d, p.sV, BN))
         return cudaErrorInvalidValue;
     if (p.d == 128) return p.causal ? launch_fwd_any<128, true>(p, mq, mk, mv, O, L, st)
                                     : launch_fwd_any<128, false>(p, mq, mk, mv, O, L, st);

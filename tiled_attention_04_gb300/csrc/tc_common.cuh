@@ -167,13 +167,31 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
-// 3-D tiled load of one box into shared memory, completing on `bar` (tx bytes)
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y, int z) {
+// x, unchanged, but opaque to the compiler: what is computed from the result is
+// computed here, not hoisted ahead of earlier volatile asm (keeps such values out
+// of registers through the main loops)
+__device__ __forceinline__ int opaque(int x) {
+    asm volatile("" : "+r"(x));
+    return x;
+}
+
+// 4-D tiled TMA load (coordinates innermost first), completing on `bar`
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y, int z,
+                                            int w) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
-        "[%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+        "%6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
         : "memory");
+}
+
+// tiled load from a 4-D (d, N, H, B) map for batch*head bh = b*H + h; the head
+// and batch coordinates are recomputed at each call rather than kept live
+__device__ __forceinline__ void tma_load_bh(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y, int bh,
+                                            int H) {
+    const int h = opaque(H);
+    const int b = bh / h;
+    tma_load_4d(dst, m, bar, x, y, bh - b * h, b);
 }
 
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16), completing on `bar`
