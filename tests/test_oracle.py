@@ -303,3 +303,17 @@ def test_planted_mask_mistakes_are_caught(monkeypatch, mistake):
     O, _ = oracle.attn_fwd_ref(Q, K, V, 0.35, True)
     tO = _torch_sdpa(Q, K, V, dO, 0.35, True)[0]
     assert not np.allclose(O, tO, rtol=1e-6, atol=1e-6)
+
+
+def test_sweep_vanilla_baseline_matches_oracle():
+    """The vanilla attention the latency sweep compares against computes the same
+    attention (checked here on the CPU in fp64, causal and not)."""
+    torch = pytest.importorskip("torch")
+    from tiled_attention_04_gb300.sweep import vanilla
+    rng = np.random.default_rng(11)
+    for causal in (False, True):
+        Q, K, V = (rng.standard_normal((2, 1, 12, 8)) for _ in range(3))
+        got = vanilla(*(torch.from_numpy(x) for x in (Q, K, V)), causal, 0.3).numpy()
+        for b in range(2):
+            O, L = oracle.attn_fwd_ref(Q[b], K[b], V[b], 0.3, causal)
+            np.testing.assert_allclose(got[b], O, rtol=1e-12, atol=1e-12)

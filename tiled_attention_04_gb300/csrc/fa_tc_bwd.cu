@@ -61,23 +61,29 @@ __host__ __device__ inline int padded_rows(int n) { return (n + 127) / 128 * 128
 // d/8 threads per query row (each reads 16 bytes of O and of dO, so a row is
 // one contiguous, coalesced segment), rows reduced with shuffles.  Writes the
 // negated row constants the passes add: Dn = -rowsum(dO * O), Ln = -L*log2(e);
-// padding rows: Dn = 0, Ln = -inf (so their P = 2^(-inf) = 0).
+// padding rows: Dn = 0, Ln = -inf (so their P = 2^(-inf) = 0).  A block takes
+// 256/(d/8) consecutive rows of one batch*head (the padded row count is a
+// multiple of 128, so no block straddles two), which leaves one 32-bit
+// division per thread to find them.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
                                                          const __nv_bfloat16 *__restrict__ dO,
                                                          const float *__restrict__ L, float *__restrict__ Dp,
-                                                         float *__restrict__ Lp, int BH, int Nq, int H,
-                                                         FaStrides so, FaStrides sdo) {
-    constexpr int TPR = D / 8;                      // threads per row
+                                                         float *__restrict__ Lp, int Nq, int H, FaStrides so,
+                                                         FaStrides sdo) {
+    constexpr int TPR = D / 8;          // threads per row
+    constexpr int RPB = 256 / TPR;      // rows per block
+    static_assert(128 % RPB == 0, "a block stays within one batch*head");
     tc::pdl_launch_dependents();
     tc::pdl_wait();   // O (from the forward) and dO are complete
     const int nqp = padded_rows(Nq);
-    const long long gr = ((long long)blockIdx.x * 256 + threadIdx.x) / TPR;
+    const int bpb = nqp / RPB;                                  // blocks per batch*head
+    const int bh = (int)blockIdx.x / bpb;
+    const int q = ((int)blockIdx.x - bh * bpb) * RPB + (int)threadIdx.x / TPR;
     const int sub = threadIdx.x % TPR;
-    const bool live = gr < (long long)BH * nqp;
-    const int bh = live ? (int)(gr / nqp) : 0, q = live ? (int)(gr % nqp) : 0;
+    const long long gr = (long long)bh * nqp + q;
     float acc = 0.f;
-    if (live && q < Nq) {
+    if (q < Nq) {
         const uint4 a = __ldg(reinterpret_cast<const uint4 *>(O + fa_row_offset(so, H, bh, q) + sub * 8));
         const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + fa_row_offset(sdo, H, bh, q) + sub * 8));
         const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
@@ -91,10 +97,10 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__
     }
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (live && sub == 0) {
+    if (sub == 0) {
         if (q < Nq) {
             Dp[gr] = -acc;
-            Lp[gr] = -L[(size_t)bh * Nq + q] * kLog2e;
+            Lp[gr] = -L[(long long)bh * Nq + q] * kLog2e;
         } else {
             Dp[gr] = 0.f;
             Lp[gr] = -INFINITY;
@@ -1663,7 +1669,7 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
     const auto *o = static_cast<const __nv_bfloat16 *>(O);
     const auto *g = static_cast<const __nv_bfloat16 *>(dO);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((rows * (p.d / 8) + 255) / 256));
+    cfg.gridDim = dim3((unsigned)(rows / (256 / (p.d / 8))));   // rows is a multiple of 128
     cfg.blockDim = dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1672,8 +1678,8 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e =
-        p.d == 128 ? cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128>, o, g, L, Dp, Lp, p.BH, p.Nq, p.H, p.sO, p.sdO)
-                   : cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<64>, o, g, L, Dp, Lp, p.BH, p.Nq, p.H, p.sO, p.sdO);
+        p.d == 128 ? cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO)
+                   : cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<64>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
