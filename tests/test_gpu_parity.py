@@ -81,6 +81,10 @@ RAGGED = [
     (1, 192, 64, 64, "bf16", True), (1, 300, 1000, 128, "bf16", False), (1, 1000, 300, 64, "f32", True),
     (2, 384, 384, 64, "bf16", True), (1, 640, 640, 128, "bf16", True), (1, 512, 512, 64, "bf16", False),
     (4, 1152, 1152, 128, "bf16", True), (1, 1088, 1088, 64, "bf16", True),
+    # bf16 head dims 16 and 32 on the d = 64 tensor-core kernels (columns past d are
+    # zero-filled padding, never stored): ragged, Nq != Nk, split and persistent launches
+    (1, 200, 200, 16, "bf16", True), (2, 333, 129, 32, "bf16", False), (1, 129, 400, 16, "bf16", True),
+    (1, 1152, 1152, 16, "bf16", True), (1, 1152, 1152, 32, "bf16", False), (160, 200, 200, 32, "bf16", True),
 ]
 
 

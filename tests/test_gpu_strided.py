@@ -81,7 +81,7 @@ def run_both(t, B, H, causal, layout, out_layout=None):
 
 
 CASES = [
-    # B, H, N, d, dtype, causal, layout           (tensor-core path: bf16, d 64/128, N >= 128)
+    # B, H, N, d, dtype, causal, layout           (tensor-core path: bf16 and N >= 128)
     (2, 3, 256, 64, "bf16", True, "bnhd"),
     (2, 3, 200, 128, "bf16", False, "bnhd"),
     (1, 4, 333, 64, "bf16", True, "qkv"),
@@ -89,7 +89,9 @@ CASES = [
     (3, 2, 256, 64, "bf16", False, "padded"),
     (1, 2, 1152, 128, "bf16", True, "bnhd"),     # long rows: work split over a CTA pair
     (4, 40, 256, 64, "bf16", True, "bnhd"),      # many short units: persistent CTAs
-    # fp32 CUDA-core path, and bf16 head dims the tensor cores do not take
+    (2, 3, 256, 32, "bf16", True, "bnhd"),       # head dims below 64 on the tensor cores
+    (1, 2, 300, 16, "bf16", False, "qkv"),
+    # fp32 CUDA-core path, and a bf16 shape shorter than one 128-row tile
     (2, 3, 130, 32, "f32", True, "bnhd"),
     (1, 3, 100, 64, "f32", False, "qkv"),
     (2, 2, 96, 16, "bf16", True, "padded"),

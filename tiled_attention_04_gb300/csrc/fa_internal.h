@@ -51,6 +51,13 @@ cudaError_t simt_zero_rows(const FaProblem &p, void *X, const FaStrides &s, int 
 struct CUtensorMap_st;
 bool tc_make_map_4d(CUtensorMap_st *m, const void *ptr, int B, int H, int N, int d, const FaStrides &s,
                     int box_rows);
+// (B*H, N, d) contiguous bf16 tensor -> 3-D TMA map over (d, N, B*H), same boxes
+bool tc_make_map_3d(CUtensorMap_st *m, const void *ptr, int BH, int N, int d, int box_rows);
+// true when s is the contiguous layout of a (B, H, N, d) tensor (dimensions of extent 1 aside)
+bool tc_plain_layout(const FaProblem &p, const FaStrides &s, int N);
+// the 4-D map (view4) or the 3-D map of one tensor of the problem
+bool tc_make_map(CUtensorMap_st *m, const void *ptr, const FaProblem &p, const FaStrides &s, int N, int box_rows,
+                 bool view4);
 
 // ---- tcgen05 tensor-core kernels (fa_tc_fwd.cu, fa_tc_bwd.cu): bf16, d in {64, 128}.
 bool tc_fwd_supported(const FaProblem &p);

@@ -167,12 +167,12 @@ struct DkdvWideCfg {
 };
 
 // one dK/dV work item: key tile kt of batch*head bh (a half of its queries when SPLIT = 2)
-template <int D, bool CAUSAL, int SPLIT>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
 __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                           const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                           const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
                                           __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, int H,
-                                          const FaStrides &sdk, const FaStrides &sdv, float scale,
+                                          int dv, const FaStrides &sdk, const FaStrides &sdv, float scale,
                                           float scale_log2, uint32_t wait_limit) {
     using C = DkdvWideCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -240,8 +240,8 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
             tc::tma_prefetch_desc(&tmdO);
             tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
             for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_bh(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
-                tc::tma_load_bh(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
+                tc::tma_load_rows<VIEW4>(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
+                tc::tma_load_rows<VIEW4>(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
             }
             int issued = 0;
             for (int it = 0; it < n; ++it) {
@@ -251,9 +251,9 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                 const int q0 = (i_begin + it) * C::BQ;
                 tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 1024);
                 for (int c = 0; c < D / 64; ++c) {
-                    tc::tma_load_bh(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
+                    tc::tma_load_rows<VIEW4>(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
                                     q0, bh, H);
-                    tc::tma_load_bh(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
+                    tc::tma_load_rows<VIEW4>(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
                                     c * 64, q0, bh, H);
                 }
                 const size_t off = (size_t)bh * nqp + q0;
@@ -429,8 +429,11 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         if (fine && n > 0) fine = W.wait(q_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
-        __nv_bfloat16 *dst = t == 0 ? dV + fa_row_offset(sdv, tc::opaque(H), bh, key)
-                                         : dK + fa_row_offset(sdk, tc::opaque(H), bh, key);
+        __nv_bfloat16 *dst;
+        if constexpr (VIEW4)
+            dst = t == 0 ? dV + fa_row_offset(sdv, tc::opaque(H), bh, key) : dK + fa_row_offset(sdk, tc::opaque(H), bh, key);
+        else
+            dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
         const float mul = t == 0 ? 1.f : scale;
         const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
         // Split items: each rank finalises one tensor (rank 0 dV, rank 1 dK) and sends
@@ -495,7 +498,8 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                     uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                        if (!VIEW4 || 32 * c + 8 * i < dv)   // columns past a head dim below 64 are padding
+                            o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
                 }
             }
         }
@@ -541,11 +545,12 @@ struct DqWideCfg {
 };
 
 // one dQ work item: query tile qt of batch*head bh (a half of its keys when SPLIT = 2)
-template <int D, bool CAUSAL, int SPLIT>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
 __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                         const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                         const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ, int Nq, int Nk,
-                                        int qt, int bh, int H, const FaStrides &sdq, float scale, float scale_log2,
+                                        int qt, int bh, int H, int dv, const FaStrides &sdq, float scale,
+                                        float scale_log2,
                                         uint32_t wait_limit) {
     using C = DqWideCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -611,8 +616,8 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
             tc::tma_prefetch_desc(&tmV);
             tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
             for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_bh(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
-                tc::tma_load_bh(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
+                tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
+                tc::tma_load_rows<VIEW4>(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
             }
             int issued = 0;
             for (int j = 0; j < n; ++j) {
@@ -620,9 +625,9 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
                 if (!W.wait(kv_empty(s), ((j / C::STAGES) & 1) ^ 1u)) break;
                 tc::mbar_arrive_expect_tx(kv_full(s), 2 * C::KT::BYTES);
                 for (int c = 0; c < D / 64; ++c) {
-                    tc::tma_load_bh(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
+                    tc::tma_load_rows<VIEW4>(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
                                     (jb + j) * C::BK, bh, H);
-                    tc::tma_load_bh(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
+                    tc::tma_load_rows<VIEW4>(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
                                     (jb + j) * C::BK, bh, H);
                 }
                 issued = j + 1;
@@ -762,7 +767,9 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
         if (fine && n > 0) fine = W.wait(kv_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
-        __nv_bfloat16 *dst = dQ + fa_row_offset(sdq, tc::opaque(H), bh, row);
+        __nv_bfloat16 *dst;
+        if constexpr (VIEW4) dst = dQ + fa_row_offset(sdq, tc::opaque(H), bh, row);
+        else dst = dQ + ((size_t)bh * Nq + row) * D;
         const uint32_t tA = tmem + lane_base + C::DQ_COL;
         // Split items: rank r finalises the columns of warpgroup r and sends its partial
         // of the other half into the peer's shared memory with remote stores, once the
@@ -827,7 +834,8 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
                     uint4 *o = reinterpret_cast<uint4 *>(dst + col);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                        if (!VIEW4 || col + 8 * i < dv)   // columns past a head dim below 64 are padding
+                            o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
                 }
             }
         }
@@ -877,12 +885,12 @@ struct DkdvNarrowCfg {
 };
 
 // one dK/dV work item: key tile kt of batch*head bh (a half of it when SPLIT = 2)
-template <int D, bool CAUSAL, int SPLIT>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
 __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                           const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                           const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
                                           __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, int H,
-                                          const FaStrides &sdk, const FaStrides &sdv, float scale,
+                                          int dv, const FaStrides &sdk, const FaStrides &sdv, float scale,
                                           float scale_log2, uint32_t wait_limit) {
     using C = DkdvNarrowCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -952,8 +960,8 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
             tc::tma_prefetch_desc(&tmdO);
             tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
             for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_bh(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
-                tc::tma_load_bh(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
+                tc::tma_load_rows<VIEW4>(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
+                tc::tma_load_rows<VIEW4>(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
             }
             int issued = 0;
             for (int it = 0; it < n; ++it) {
@@ -963,9 +971,9 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                 const int q0 = (i_begin + it) * C::BQ;
                 tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 512);
                 for (int c = 0; c < D / 64; ++c) {
-                    tc::tma_load_bh(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
+                    tc::tma_load_rows<VIEW4>(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
                                     q0, bh, H);
-                    tc::tma_load_bh(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
+                    tc::tma_load_rows<VIEW4>(base + C::DO_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmdO, q_full(s),
                                     c * 64, q0, bh, H);
                 }
                 const size_t off = (size_t)bh * nqp + q0;
@@ -1113,8 +1121,11 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
         if (fine && n > 0) fine = W.wait(q_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
-        __nv_bfloat16 *dst = t == 0 ? dV + fa_row_offset(sdv, tc::opaque(H), bh, key)
-                                         : dK + fa_row_offset(sdk, tc::opaque(H), bh, key);
+        __nv_bfloat16 *dst;
+        if constexpr (VIEW4)
+            dst = t == 0 ? dV + fa_row_offset(sdv, tc::opaque(H), bh, key) : dK + fa_row_offset(sdk, tc::opaque(H), bh, key);
+        else
+            dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
         const float mul = t == 0 ? 1.f : scale;
         const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
         // Split items: each rank finalises one tensor (rank 0 dV, rank 1 dK) and sends
@@ -1179,7 +1190,8 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                     uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                        if (!VIEW4 || 32 * c + 8 * i < dv)   // columns past a head dim below 64 are padding
+                            o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
                 }
             }
         }
@@ -1221,11 +1233,12 @@ struct DqNarrowCfg {
 };
 
 // one dQ work item: query tile qt of batch*head bh (a half of its keys when SPLIT = 2)
-template <int D, bool CAUSAL, int SPLIT>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
 __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                         const CUtensorMap &tmdO, const float *__restrict__ Lp,
                                         const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ, int Nq, int Nk,
-                                        int qt, int bh, int H, const FaStrides &sdq, float scale, float scale_log2,
+                                        int qt, int bh, int H, int dv, const FaStrides &sdq, float scale,
+                                        float scale_log2,
                                         uint32_t wait_limit) {
     using C = DqNarrowCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -1293,8 +1306,8 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
             tc::tma_prefetch_desc(&tmV);
             tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
             for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_bh(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
-                tc::tma_load_bh(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
+                tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
+                tc::tma_load_rows<VIEW4>(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
             }
             int issued = 0;
             for (int j = 0; j < n; ++j) {
@@ -1302,9 +1315,9 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                 if (!W.wait(kv_empty(s), ((j / C::STAGES) & 1) ^ 1u)) break;
                 tc::mbar_arrive_expect_tx(kv_full(s), 2 * C::KT::BYTES);
                 for (int c = 0; c < D / 64; ++c) {
-                    tc::tma_load_bh(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
+                    tc::tma_load_rows<VIEW4>(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
                                     (jb + j) * C::BK, bh, H);
-                    tc::tma_load_bh(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
+                    tc::tma_load_rows<VIEW4>(base + C::V_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmV, kv_full(s), c * 64,
                                     (jb + j) * C::BK, bh, H);
                 }
                 issued = j + 1;
@@ -1428,7 +1441,9 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
         if (fine && n > 0) fine = W.wait(kv_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
-        __nv_bfloat16 *dst = dQ + fa_row_offset(sdq, tc::opaque(H), bh, row);
+        __nv_bfloat16 *dst;
+        if constexpr (VIEW4) dst = dQ + fa_row_offset(sdq, tc::opaque(H), bh, row);
+        else dst = dQ + ((size_t)bh * Nq + row) * D;
         const uint32_t tA = tmem + lane_base + C::DQ_COL;
         // Split items: rank r finalises the columns of warpgroup r and sends its partial
         // of the other half into the peer's shared memory with remote stores, once the
@@ -1493,7 +1508,8 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                     uint4 *o = reinterpret_cast<uint4 *>(dst + col);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                        if (!VIEW4 || col + 8 * i < dv)   // columns past a head dim below 64 are padding
+                            o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
                 }
             }
         }
@@ -1511,7 +1527,7 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
 // key tile, dQ per query tile; each longest first) are interleaved so that the
 // long items of both start first and the short ones of both fill the end --
 // one kernel tail instead of two, and the passes balance each other's load.
-template <int D, bool CAUSAL, int SPLIT>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap qA, const __grid_constant__ CUtensorMap kA,
                      const __grid_constant__ CUtensorMap vA, const __grid_constant__ CUtensorMap dOA,
@@ -1520,7 +1536,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ,
                      __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH,
                      int k_tiles, int q_tiles, int n_kv_items, int n_q_items, float scale, float scale_log2,
-                     uint32_t wait_limit, int H, FaStrides sdq, FaStrides sdk, FaStrides sdv) {
+                     uint32_t wait_limit, int H, int dv, FaStrides sdq, FaStrides sdk, FaStrides sdv) {
     tc::pdl_launch_dependents();
     tc::pdl_wait();   // D and L staged by the preprocessing kernel are complete
     const int item = blockIdx.x / SPLIT;
@@ -1538,18 +1554,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int r = idx / BH;
         const int kt = CAUSAL ? r : k_tiles - 1 - r;    // causal: the first key tiles see the most queries
         if constexpr (D == 64)
-            dkdv_item_wide<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, sdk, sdv, scale,
+            dkdv_item_wide<D, CAUSAL, SPLIT, VIEW4>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, dv, sdk, sdv, scale,
                                              scale_log2, wait_limit);
         else
-            dkdv_item_narrow<D, CAUSAL, SPLIT>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, sdk, sdv, scale,
+            dkdv_item_narrow<D, CAUSAL, SPLIT, VIEW4>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, dv, sdk, sdv, scale,
                                                scale_log2, wait_limit);
     } else {
         const int qt = q_tiles - 1 - idx / BH;           // causal: the last query tiles see the most keys
         if constexpr (D == 64)
-            dq_item_wide<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, sdq, scale, scale_log2,
+            dq_item_wide<D, CAUSAL, SPLIT, VIEW4>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, dv, sdq, scale, scale_log2,
                                            wait_limit);
         else
-            dq_item_narrow<D, CAUSAL, SPLIT>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, sdq, scale, scale_log2,
+            dq_item_narrow<D, CAUSAL, SPLIT, VIEW4>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, dv, sdq, scale, scale_log2,
                                              wait_limit);
     }
 }
@@ -1622,9 +1638,10 @@ bool dq_split(const FaProblem &p) {
 
 struct Maps2 {
     Maps a, b;   // tensor maps of the dK/dV pass (a) and of the dQ pass (b)
+    bool view4;  // 4-D maps over strided views (else 3-D maps over contiguous tensors)
 };
 
-template <int D, bool CAUSAL, int SPLIT>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
 cudaError_t launch_bwd(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dQ, void *dK,
                        void *dV, bool do_kv, bool do_q, cudaStream_t st) {
     using KvC = std::conditional_t<D == 64, DkdvWideCfg<D>, DkdvNarrowCfg<D>>;
@@ -1632,33 +1649,32 @@ cudaError_t launch_bwd(const FaProblem &p, const Maps2 &m, const float *Lp, cons
     constexpr uint32_t smem = KvC::SMEM_BYTES > QC::SMEM_BYTES ? KvC::SMEM_BYTES : QC::SMEM_BYTES;
     const int kt = (p.Nk + 127) / 128, qt = (p.Nq + 127) / 128;
     const long long na = do_kv ? (long long)kt * p.BH : 0, nb = do_q ? (long long)qt * p.BH : 0;
-    return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q, m.a.k, m.a.v,
+    return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q, m.a.k, m.a.v,
                           m.a.dO, m.b.q, m.b.k, m.b.v, m.b.dO, Lp, Dp, static_cast<__nv_bfloat16 *>(dQ),
                           static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt, qt,
-                          (int)na, (int)nb, p.scale, p.scale * kLog2e, p.wait_limit, p.H, p.sdQ, p.sdK, p.sdV);
+                          (int)na, (int)nb, p.scale, p.scale * kLog2e, p.wait_limit, p.H, p.d, p.sdQ, p.sdK, p.sdV);
 }
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_any(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dQ, void *dK,
                            void *dV, bool do_kv, bool do_q, cudaStream_t st) {
     const bool split = (do_kv && dkdv_split(p)) || (do_q && dq_split(p));
-    return split ? launch_bwd<D, CAUSAL, 2>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
-                 : launch_bwd<D, CAUSAL, 1>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+    if (m.view4)
+        return split ? launch_bwd<D, CAUSAL, 2, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                     : launch_bwd<D, CAUSAL, 1, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+    return split ? launch_bwd<D, CAUSAL, 2, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                 : launch_bwd<D, CAUSAL, 1, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
 }
 
 bool make_maps(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO, int q_rows,
-               int k_rows, Maps *m) {
-    return tc_make_map_4d(&m->q, Q, p.B, p.H, p.Nq, p.d, p.sQ, q_rows) &&
-           tc_make_map_4d(&m->dO, dO, p.B, p.H, p.Nq, p.d, p.sdO, q_rows) &&
-           tc_make_map_4d(&m->k, K, p.B, p.H, p.Nk, p.d, p.sK, k_rows) &&
-           tc_make_map_4d(&m->v, V, p.B, p.H, p.Nk, p.d, p.sV, k_rows);
+               int k_rows, bool view4, Maps *m) {
+    return tc_make_map(&m->q, Q, p, p.sQ, p.Nq, q_rows, view4) && tc_make_map(&m->dO, dO, p, p.sdO, p.Nq, q_rows, view4) &&
+           tc_make_map(&m->k, K, p, p.sK, p.Nk, k_rows, view4) && tc_make_map(&m->v, V, p, p.sV, p.Nk, k_rows, view4);
 }
 
 }  // namespace
 
-bool tc_bwd_supported(const FaProblem &p) {
-    return p.dtype == FA_DTYPE_BF16 && (p.d == 64 || p.d == 128) && p.Nq >= 128 && p.Nk >= 128 && p.BH >= 1;
-}
+bool tc_bwd_supported(const FaProblem &p) { return tc_fwd_supported(p); }
 
 size_t tc_bwd_ld_rows(const FaProblem &p) { return (size_t)p.BH * padded_rows(p.Nq); }
 
@@ -1677,9 +1693,13 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e =
-        p.d == 128 ? cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO)
-                   : cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<64>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO);
+    cudaError_t e;
+    switch (p.d) {
+        case 128: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO); break;
+        case 64: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<64>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO); break;
+        case 32: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<32>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO); break;
+        default: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<16>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO); break;
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1687,13 +1707,22 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
 cudaError_t tc_bwd_grads(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                          const float *Lp, const float *Dp, void *dQ, void *dK, void *dV, bool do_kv, bool do_q,
                          cudaStream_t st) {
-    // box heights: wide sub-tiles (d = 64) load 128-row tiles everywhere; narrow ones
-    // (d = 128) load 64-row sub-tiles of the looped-over operand
+    // Contiguous tensors keep 3-D (d, N, B*H) maps and plain row addressing; any
+    // strided view, or a head dim below 64 (run on the d = 64 kernels with the
+    // columns past d read as zero and never stored), switches the whole launch to
+    // 4-D maps and strided rows.
     Maps2 m;
-    if (p.d == 64) {
-        if (!make_maps(p, Q, K, V, dO, 128, 128, &m.a)) return cudaErrorInvalidValue;
+    m.view4 = p.d < 64 || !tc_plain_layout(p, p.sQ, p.Nq) || !tc_plain_layout(p, p.sK, p.Nk) ||
+              !tc_plain_layout(p, p.sV, p.Nk) || !tc_plain_layout(p, p.sdO, p.Nq) ||
+              !tc_plain_layout(p, p.sdQ, p.Nq) || !tc_plain_layout(p, p.sdK, p.Nk) ||
+              !tc_plain_layout(p, p.sdV, p.Nk);
+    // box heights: wide sub-tiles (d <= 64) load 128-row tiles everywhere; narrow ones
+    // (d = 128) load 64-row sub-tiles of the looped-over operand
+    if (p.d <= 64) {
+        if (!make_maps(p, Q, K, V, dO, 128, 128, m.view4, &m.a)) return cudaErrorInvalidValue;
         m.b = m.a;
-    } else if (!make_maps(p, Q, K, V, dO, 64, 128, &m.a) || !make_maps(p, Q, K, V, dO, 128, 64, &m.b)) {
+    } else if (!make_maps(p, Q, K, V, dO, 64, 128, m.view4, &m.a) ||
+               !make_maps(p, Q, K, V, dO, 128, 64, m.view4, &m.b)) {
         return cudaErrorInvalidValue;
     }
     if (p.d == 128) return p.causal ? launch_bwd_any<128, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)

@@ -115,12 +115,12 @@ struct FwdCfg {
     static constexpr uint32_t P_STRIDE = SEP_P ? 64 : 128;
 };
 
-template <int D, bool CAUSAL, int SPLIT>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
-                     uint32_t wait_limit, uint32_t force_stall, int H, FaStrides so) {
+                     uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::tma_prefetch_desc(&tmV);
             tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c)
-                tc::tma_load_bh(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh, H);
+                tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh, H);
             int k_issued = 0, v_issued = 0;
             // The slot of tile j last held tile j - st.  A V slot is free once PV of that
             // tile has completed.  A K slot is read only by S of that tile; with P over S
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (j >= st && !W.wait(pv_done_bar(g), (g / C::R) & 1)) return false;
                 tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
-                    tc::tma_load_bh(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64,
+                    tc::tma_load_rows<VIEW4>(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64,
                                     (jb + j) * BN, bh, H);
                 return true;
             };
@@ -451,7 +451,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         auto store_row = [&](const float *vals, float Mrow, float lrow) {
             const float inv = 1.f / lrow;
-            __nv_bfloat16 *orow = O + fa_row_offset(so, tc::opaque(H), bh, row) + t * (D / 2);
+            __nv_bfloat16 *orow;
+            if constexpr (VIEW4) orow = O + fa_row_offset(so, tc::opaque(H), bh, row) + t * (D / 2);
+            else orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
             if (row < Nq) {
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c) {
@@ -460,7 +462,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     q.y = tc::pack_bf16(vals[8 * c + 2] * inv, vals[8 * c + 3] * inv);
                     q.z = tc::pack_bf16(vals[8 * c + 4] * inv, vals[8 * c + 5] * inv);
                     q.w = tc::pack_bf16(vals[8 * c + 6] * inv, vals[8 * c + 7] * inv);
-                    reinterpret_cast<uint4 *>(orow)[c] = q;
+                    if (!VIEW4 || t * (D / 2) + 8 * c < dv)   // columns past a head dim below 64 are padding
+                        reinterpret_cast<uint4 *>(orow)[c] = q;
                 }
                 if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
             }
@@ -539,12 +542,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // TMEM layout and per-tile pipeline as fa_fwd_tc_kernel; what it adds is the
 // hand-over between units -- the next unit's Q and first K/V tiles load, and
 // its first S MMAs run, under the previous unit's last tiles and epilogue.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VIEW4>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
-                     uint32_t wait_limit, uint32_t force_stall, int H, FaStrides so) {
+                     uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -645,14 +648,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (u > 0 && !(ok = W.wait(q_empty, (u - 1) & 1))) break;
                 tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
-                    tc::tma_load_bh(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, w.q0, w.bh, H);
+                    tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, w.q0, w.bh, H);
                 q_issued = u + 1;
                 auto load = [&](const CUtensorMap *m, uint32_t ring, uint32_t st, int g, int key0, uint32_t full) {
                     // the slot last held tile g - st: wait until PV of that tile has completed
                     if (g >= (int)st && !W.wait(pv_done_bar(g - (int)st), pv_done_par(g - (int)st))) return false;
                     tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
                     for (int c = 0; c < C::CHUNKS; ++c)
-                        tc::tma_load_bh(ring + ((uint32_t)g % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full,
+                        tc::tma_load_rows<VIEW4>(ring + ((uint32_t)g % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full,
                                         c * 64, key0, w.bh, H);
                     return true;
                 };
@@ -782,10 +785,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Unit w;
         for (int u = 0; ok && unit_of(u, w); ++u) {
             const int n = w.n, bh = w.bh, row = w.q0 + r;
-            // the output row's offset, taken now and parked in shared memory: computed at
-            // the epilogue it would compete for registers with the row being stored
+            // a strided output row's offset, taken now and parked in shared memory:
+            // computed at the epilogue it would compete for registers with the row
             volatile long long *orow_sm = reinterpret_cast<volatile long long *>(sb + C::OROW_OFF) + (threadIdx.x - 128);
-            *orow_sm = fa_row_offset(so, H, bh, row);
+            if constexpr (VIEW4) *orow_sm = fa_row_offset(so, H, bh, row);
             // this warpgroup's tiles of the unit: local j = jt, jt + 2, ... (global g = g0 + j has parity t)
             const int j_0 = (0 - g0) & 1, j_1 = (1 - g0) & 1;
             const int jt = t == 0 ? j_0 : j_1;
@@ -922,7 +925,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_arrive(o_free);
             auto store_row = [&](const float *vals, float Mrow, float lrow) {
                 const float inv = 1.f / lrow;
-                __nv_bfloat16 *orow = O + *orow_sm + t * (D / 2);
+                __nv_bfloat16 *orow;
+                if constexpr (VIEW4) orow = O + *orow_sm + t * (D / 2);
+                else orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
                 if (row < Nq) {
 #pragma unroll
                     for (int c = 0; c < D / 16; ++c) {
@@ -931,7 +936,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         q.y = tc::pack_bf16(vals[8 * c + 2] * inv, vals[8 * c + 3] * inv);
                         q.z = tc::pack_bf16(vals[8 * c + 4] * inv, vals[8 * c + 5] * inv);
                         q.w = tc::pack_bf16(vals[8 * c + 6] * inv, vals[8 * c + 7] * inv);
-                        reinterpret_cast<uint4 *>(orow)[c] = q;
+                        if (!VIEW4 || t * (D / 2) + 8 * c < dv)   // columns past a head dim below 64 are padding
+                            reinterpret_cast<uint4 *>(orow)[c] = q;
                     }
                     if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
                 }
@@ -968,6 +974,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+// (B*H, N, d) contiguous bf16 tensor -> 3-D map with 64 x rows x 1 boxes, 128-byte
+// swizzle.  Rows past N in a batch*head read as zero.
+bool tc_make_map_3d(CUtensorMap_st *m, const void *ptr, int BH, int N, int d, int box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_plain_layout(const FaProblem &p, const FaStrides &s, int N) {
+    const long long n = p.d, h = (long long)N * p.d, b = (long long)p.H * N * p.d;
+    return (N <= 1 || s.n == n) && (p.H <= 1 || s.h == h) && (p.B <= 1 || s.b == b);
+}
+
+bool tc_make_map(CUtensorMap_st *m, const void *ptr, const FaProblem &p, const FaStrides &s, int N, int box_rows,
+                 bool view4) {
+    return view4 ? tc_make_map_4d(m, ptr, p.B, p.H, N, p.d, s, box_rows)
+                 : tc_make_map_3d(m, ptr, p.BH, N, p.d, box_rows);
+}
+
 // (B, H, N, d) bf16 view -> 4-D map over (d, N, H, B) with 64 x rows x 1 x 1 boxes,
 // 128-byte swizzle.  Rows past N in a batch*head read as zero.  The strides are
 // the view's own (positive multiples of 16 bytes below 2^40 bytes), in any order.
@@ -984,8 +1015,12 @@ bool tc_make_map_4d(CUtensorMap_st *m, const void *ptr, int B, int H, int N, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 with d in {16, 32, 64, 128}.  Head dims 16 and 32 run the d = 64 kernels:
+// their TMA boxes are 64 columns wide and the columns past d read as zero, which
+// adds nothing to Q K^T and leaves zero output columns that are never stored.
 bool tc_fwd_supported(const FaProblem &p) {
-    return p.dtype == FA_DTYPE_BF16 && (p.d == 64 || p.d == 128) && p.Nq >= 128 && p.Nk >= 128 && p.BH >= 1;
+    return p.dtype == FA_DTYPE_BF16 && (p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128) && p.Nq >= 128 &&
+           p.Nk >= 128 && p.BH >= 1;
 }
 
 static int sm_count() {
@@ -994,15 +1029,15 @@ static int sm_count() {
     return sms;
 }
 
-template <int D, bool CAUSAL, int SPLIT, bool PERSIST>
+template <int D, bool CAUSAL, int SPLIT, bool PERSIST, bool VIEW4>
 static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                               void *O, float *L, cudaStream_t st) {
     static_assert(!(PERSIST && SPLIT > 1), "persistent units are not split");
     using C = FwdCfg<D>;
     void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, __nv_bfloat16 *, float *, int, int, int, int,
-                 float, uint32_t, uint32_t, int, FaStrides);
-    if constexpr (PERSIST) kern = fa_fwd_tc_persistent_kernel<D, CAUSAL>;
-    else kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT>;
+                 float, uint32_t, uint32_t, int, int, FaStrides);
+    if constexpr (PERSIST) kern = fa_fwd_tc_persistent_kernel<D, CAUSAL, VIEW4>;
+    else kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int qtiles = (p.Nq + BM - 1) / BM;
@@ -1026,7 +1061,7 @@ static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const C
     cfg.attrs = attr;
     cfg.numAttrs = SPLIT > 1 ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, static_cast<__nv_bfloat16 *>(O), L, p.Nq, p.Nk, p.BH, qtiles,
-                           scale_log2, p.wait_limit, p.force_stall, p.H, p.sO);
+                           scale_log2, p.wait_limit, p.force_stall, p.H, p.d, p.sO);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1057,27 +1092,38 @@ static FwdMode fwd_mode(const FaProblem &p) {
     return FwdMode::kStream;
 }
 
+template <int D, bool CAUSAL, bool VIEW4>
+static cudaError_t launch_fwd_mode(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                                   const CUtensorMap &mv, void *O, float *L, cudaStream_t st) {
+    switch (fwd_mode(p)) {
+        case FwdMode::kSplit: return launch_fwd<D, CAUSAL, 2, false, VIEW4>(p, mq, mk, mv, O, L, st);
+        case FwdMode::kPersist: return launch_fwd<D, CAUSAL, 1, true, VIEW4>(p, mq, mk, mv, O, L, st);
+        default: return launch_fwd<D, CAUSAL, 1, false, VIEW4>(p, mq, mk, mv, O, L, st);
+    }
+}
+
 template <int D, bool CAUSAL>
 static cudaError_t launch_fwd_any(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                                  const CUtensorMap &mv, void *O, float *L, cudaStream_t st) {
-    switch (fwd_mode(p)) {
-        case FwdMode::kSplit: return launch_fwd<D, CAUSAL, 2, false>(p, mq, mk, mv, O, L, st);
-        case FwdMode::kPersist: return launch_fwd<D, CAUSAL, 1, true>(p, mq, mk, mv, O, L, st);
-        default: return launch_fwd<D, CAUSAL, 1, false>(p, mq, mk, mv, O, L, st);
-    }
+                                  const CUtensorMap &mv, void *O, float *L, bool view4, cudaStream_t st) {
+    return view4 ? launch_fwd_mode<D, CAUSAL, true>(p, mq, mk, mv, O, L, st)
+                 : launch_fwd_mode<D, CAUSAL, false>(p, mq, mk, mv, O, L, st);
 }
 
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
                    cudaStream_t st) {
+    // contiguous tensors keep 3-D (d, N, B*H) maps and plain row addressing; any
+    // strided view, or a head dim below 64 (whose rows are narrower than the
+    // kernel's), switches the whole launch to 4-D maps and strided rows
+    const bool view4 = p.d < 64 || !tc_plain_layout(p, p.sQ, p.Nq) || !tc_plain_layout(p, p.sK, p.Nk) ||
+                       !tc_plain_layout(p, p.sV, p.Nk) || !tc_plain_layout(p, p.sO, p.Nq);
     CUtensorMap mq, mk, mv;
-    if (!tc_make_map_4d(&mq, Q, p.B, p.H, p.Nq, p.d, p.sQ, BM) ||
-        !tc_make_map_4d(&mk, K, p.B, p.H, p.Nk, p.d, p.sK, BN) ||
-        !tc_make_map_4d(&mv, V, p.B, p.H, p.Nk, p.d, p.sV, BN))
+    if (!tc_make_map(&mq, Q, p, p.sQ, p.Nq, BM, view4) || !tc_make_map(&mk, K, p, p.sK, p.Nk, BN, view4) ||
+        !tc_make_map(&mv, V, p, p.sV, p.Nk, BN, view4))
         return cudaErrorInvalidValue;
-    if (p.d == 128) return p.causal ? launch_fwd_any<128, true>(p, mq, mk, mv, O, L, st)
-                                    : launch_fwd_any<128, false>(p, mq, mk, mv, O, L, st);
-    return p.causal ? launch_fwd_any<64, true>(p, mq, mk, mv, O, L, st)
-                    : launch_fwd_any<64, false>(p, mq, mk, mv, O, L, st);
+    if (p.d == 128) return p.causal ? launch_fwd_any<128, true>(p, mq, mk, mv, O, L, view4, st)
+                                    : launch_fwd_any<128, false>(p, mq, mk, mv, O, L, view4, st);
+    return p.causal ? launch_fwd_any<64, true>(p, mq, mk, mv, O, L, view4, st)
+                    : launch_fwd_any<64, false>(p, mq, mk, mv, O, L, view4, st);
 }
 
 cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st) {

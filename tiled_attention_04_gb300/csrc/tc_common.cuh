@@ -175,6 +175,15 @@ __device__ __forceinline__ int opaque(int x) {
     return x;
 }
 
+// 3-D tiled load of one box into shared memory, completing on `bar` (tx bytes)
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+        "[%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // 4-D tiled TMA load (coordinates innermost first), completing on `bar`
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y, int z,
                                             int w) {
@@ -192,6 +201,15 @@ __device__ __forceinline__ void tma_load_bh(uint32_t dst, const CUtensorMap *m, 
     const int h = opaque(H);
     const int b = bh / h;
     tma_load_4d(dst, m, bar, x, y, bh - b * h, b);
+}
+
+// rows y.. of batch*head bh, columns x..: from a 3-D (d, N, B*H) map for contiguous
+// tensors (VIEW4 false), from a 4-D (d, N, H, B) map for strided views
+template <bool VIEW4>
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y, int bh,
+                                              int H) {
+    if constexpr (VIEW4) tma_load_bh(dst, m, bar, x, y, bh, H);
+    else tma_load_3d(dst, m, bar, x, y, bh);
 }
 
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16), completing on `bar`
