@@ -113,25 +113,45 @@ def _bh(t):
     return math.prod(t.shape[:-2]), 1
 
 
-def _stream(stream):
+_raw_stream = None
+
+
+def _stream(stream, t=None):
+    """The CUDA stream handle (an int) to launch on: `stream`, else the current
+    stream of t's device (through torch's raw-stream query when it has one, which
+    skips building a Stream object on every call)."""
+    global _raw_stream
+    if stream is not None:
+        return stream.cuda_stream
     torch = _torch()
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if t is not None:
+        if _raw_stream is None:
+            _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+        if _raw_stream:
+            return _raw_stream(t.get_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+    return t.data_ptr() if t is not None else None
 
 
 def _check_inputs(*ts, strided=False):
-    t0 = ts[0]
+    dt = ts[0].dtype
     for t in ts:
         if not t.is_cuda:
             raise ValueError("tensors must be on a CUDA device")
+        if t.dtype != dt:
+            raise ValueError("Q, K, V (and O, dO) must share a dtype")
         if not strided and not t.is_contiguous():
             raise ValueError("tensors must be contiguous (B, H, N, d) or (..., N, d)")
-        if t.dtype != t0.dtype:
-            raise ValueError("Q, K, V (and O, dO) must share a dtype")
+
+
+def _on_gpu(*ts):
+    """Every tensor handed to the kernels must live in device memory."""
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
 
 
 def _strides(t):
@@ -191,19 +211,21 @@ def fa_fwd(Q, K, V, is_causal=False, scale=None, O=None, L=None, stream=None):
     (B, N, H, d) projection transposed to (B, H, N, d)) go to fa_fwd_strided and
     are read in place; O then follows Q's order of heads and rows."""
     torch = _torch()
-    strided = not all(t.is_contiguous() for t in (Q, K, V)) or (O is not None and not O.is_contiguous())
+    strided = not (Q.is_contiguous() and K.is_contiguous() and V.is_contiguous()
+                   and (O is None or O.is_contiguous()))
     _check_inputs(Q, K, V, strided=strided)
     B, H = _bh(Q)
-    Nq, d = Q.shape[-2], Q.shape[-1]
+    shape = Q.shape
+    Nq, d = shape[-2], shape[-1]
     Nk = K.shape[-2]
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if L is None:
-        L = torch.empty(Q.shape[:-1], dtype=torch.float32, device=Q.device)
+        L = torch.empty(shape[:-1], dtype=torch.float32, device=Q.device)
     if not strided:
         if O is None:
             O = torch.empty_like(Q)
-        check(lib().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), B, H, Nq, Nk, d, sc, int(is_causal),
-                           dtype_code(Q), _stream(stream)), "fa_fwd")
+        check(lib().fa_fwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), L.data_ptr(), B, H, Nq, Nk, d,
+                           sc, int(is_causal), dtype_code(Q), _stream(stream, Q)), "fa_fwd")
         return O, L
     if Q.shape[:-2] != K.shape[:-2] or K.shape[:-2] != V.shape[:-2]:
         raise ValueError("Q, K and V need the same batch and head sizes")
@@ -211,7 +233,7 @@ def fa_fwd(Q, K, V, is_causal=False, scale=None, O=None, L=None, stream=None):
         O = _like_rows(Q, tuple(Q.shape))
     sQ, sK, sV, sO = _strides(Q), _strides(K), _strides(V), _strides(O)
     check(lib().fa_fwd_strided(_ptr(Q), _sp(sQ), _ptr(K), _sp(sK), _ptr(V), _sp(sV), _ptr(O), _sp(sO), _ptr(L),
-                               B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _stream(stream)),
+                               B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _stream(stream, Q)),
           "fa_fwd_strided")
     return O, L
 
@@ -247,7 +269,7 @@ def fa_bwd(Q, K, V, O, dO, L, is_causal=False, scale=None, dQ=None, dK=None, dV=
     if all(t.is_contiguous() for t in (Q, K, V, O, dO, dQ, dK, dV)):
         check(lib().fa_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV),
                            B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _ptr(ws), ws.numel(),
-                           _stream(stream)), "fa_bwd")
+                           _stream(stream, Q)), "fa_bwd")
         return dQ, dK, dV
     if not (Q.shape[:-2] == K.shape[:-2] == V.shape[:-2] == O.shape[:-2] == dO.shape[:-2]):
         raise ValueError("Q, K, V, O and dO need the same batch and head sizes")
@@ -255,7 +277,7 @@ def fa_bwd(Q, K, V, O, dO, L, is_causal=False, scale=None, dQ=None, dK=None, dV=
     check(lib().fa_bwd_strided(_ptr(Q), _sp(st[0]), _ptr(K), _sp(st[1]), _ptr(V), _sp(st[2]), _ptr(O), _sp(st[3]),
                                _ptr(dO), _sp(st[4]), _ptr(L), _ptr(dQ), _sp(st[5]), _ptr(dK), _sp(st[6]), _ptr(dV),
                                _sp(st[7]), B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _ptr(ws), ws.numel(),
-                               _stream(stream)), "fa_bwd_strided")
+                               _stream(stream, Q)), "fa_bwd_strided")
     return dQ, dK, dV
 
 
@@ -271,43 +293,47 @@ def fa_bwd_noalloc(Q, K, V, O, dO, L, is_causal=False, scale=None, dQ=None, dK=N
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
     check(lib().fa_bwd_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK),
-                               _ptr(dV), B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _stream(stream)),
+                               _ptr(dV), B, H, Nq, Nk, d, sc, int(is_causal), dtype_code(Q), _stream(stream, Q)),
           "fa_bwd_noalloc")
     return dQ, dK, dV
 
 
 def fa_bwd_preprocess(O, dO, L, Q, K, is_causal, workspace, stream=None):
+    _on_gpu(O, dO, L, workspace)
     B, H = _bh(Q)
     check(lib().fa_bwd_preprocess(_ptr(O), _ptr(dO), _ptr(L), B, H, Q.shape[-2], K.shape[-2], Q.shape[-1],
                                   int(is_causal), dtype_code(Q), _ptr(workspace), workspace.numel(),
-                                  _stream(stream)), "fa_bwd_preprocess")
+                                  _stream(stream, Q)), "fa_bwd_preprocess")
 
 
 def fa_bwd_dkdv(Q, K, V, dO, L, dQ, dK, dV, is_causal, workspace, scale=None, stream=None):
+    _on_gpu(Q, K, V, dO, L, dQ, dK, dV, workspace)
     B, H = _bh(Q)
     d = Q.shape[-1]
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
     check(lib().fa_bwd_dkdv(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV), B, H,
                             Q.shape[-2], K.shape[-2], d, sc, int(is_causal), dtype_code(Q), _ptr(workspace),
-                            workspace.numel(), _stream(stream)), "fa_bwd_dkdv")
+                            workspace.numel(), _stream(stream, Q)), "fa_bwd_dkdv")
 
 
 def fa_bwd_dq(Q, K, V, dO, L, dQ, is_causal, workspace, scale=None, stream=None):
+    _on_gpu(Q, K, V, dO, L, dQ, workspace)
     B, H = _bh(Q)
     d = Q.shape[-1]
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
     check(lib().fa_bwd_dq(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(dQ), B, H, Q.shape[-2],
                           K.shape[-2], d, sc, int(is_causal), dtype_code(Q), _ptr(workspace), workspace.numel(),
-                          _stream(stream)), "fa_bwd_dq")
+                          _stream(stream, Q)), "fa_bwd_dq")
 
 
 def fa_bwd_grads(Q, K, V, dO, L, dQ, dK, dV, is_causal, workspace, scale=None, stream=None):
+    _on_gpu(Q, K, V, dO, L, dQ, dK, dV, workspace)
     B, H = _bh(Q)
     d = Q.shape[-1]
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
     check(lib().fa_bwd_grads(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV), B, H,
                              Q.shape[-2], K.shape[-2], d, sc, int(is_causal), dtype_code(Q), _ptr(workspace),
-                             workspace.numel(), _stream(stream)), "fa_bwd_grads")
+                             workspace.numel(), _stream(stream, Q)), "fa_bwd_grads")
 
 
 def fa_get_device_status(stream=None) -> int:

@@ -59,7 +59,13 @@ bool tc_plain_layout(const FaProblem &p, const FaStrides &s, int N);
 bool tc_make_map(CUtensorMap_st *m, const void *ptr, const FaProblem &p, const FaStrides &s, int N, int box_rows,
                  bool view4);
 
-// ---- tcgen05 tensor-core kernels (fa_tc_fwd.cu, fa_tc_bwd.cu): bf16, d in {64, 128}.
+// host-side launch helpers (fa_tc_fwd.cu): the dynamic shared-memory attribute set
+// once per kernel and device, and the multiprocessor count cached per device
+cudaError_t tc_set_smem_once(const void *kernel, int bytes);
+int tc_sm_count();
+
+// ---- tcgen05 tensor-core kernels (fa_tc_fwd.cu, fa_tc_bwd.cu): bf16, d in {16, 32, 64, 128}
+// (16 and 32 run the d = 64 kernels with zero-filled columns).
 bool tc_fwd_supported(const FaProblem &p);
 bool tc_bwd_supported(const FaProblem &p);
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,

@@ -1572,7 +1572,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 template <typename Kern>
 cudaError_t set_smem(Kern k, uint32_t bytes) {
-    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    return tc_set_smem_once(reinterpret_cast<const void *>(k), (int)bytes);
 }
 
 struct Maps {
@@ -1602,11 +1602,7 @@ cudaError_t launch_cluster(Kern kern, uint32_t smem, long long grid, int split, 
     return cudaGetLastError();
 }
 
-int sm_count() {
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    return sms;
-}
+int sm_count() { return tc_sm_count(); }
 
 // Split an item over a two-CTA cluster when the longest item's loop is more than
 // 1.5x the average loop length per SM (it, not the total work, would set the time).

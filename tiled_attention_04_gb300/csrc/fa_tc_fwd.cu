@@ -57,6 +57,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "fa_internal.h"
@@ -993,10 +994,84 @@ bool tc_plain_layout(const FaProblem &p, const FaStrides &s, int N) {
     return (N <= 1 || s.n == n) && (p.H <= 1 || s.h == h) && (p.B <= 1 || s.b == b);
 }
 
+// Encoded maps are kept in a small table keyed by everything they encode (pointer,
+// sizes, strides, box, rank): a step's launches reuse the same few tensors, and a
+// hit costs a short scan instead of a descriptor encode.  A map holds only the
+// address and geometry, so an entry never goes stale.
+namespace {
+struct MapKey {
+    const void *ptr;
+    long long b, h, n, sb, sh, sn;
+    int d, box_rows, view4;
+    bool operator==(const MapKey &o) const {
+        return ptr == o.ptr && b == o.b && h == o.h && n == o.n && sb == o.sb && sh == o.sh && sn == o.sn &&
+               d == o.d && box_rows == o.box_rows && view4 == o.view4;
+    }
+};
+constexpr int kMapCache = 32;
+std::mutex g_map_mu;
+MapKey g_map_key[kMapCache];
+CUtensorMap g_map_val[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+}  // namespace
+
 bool tc_make_map(CUtensorMap_st *m, const void *ptr, const FaProblem &p, const FaStrides &s, int N, int box_rows,
                  bool view4) {
-    return view4 ? tc_make_map_4d(m, ptr, p.B, p.H, N, p.d, s, box_rows)
-                 : tc_make_map_3d(m, ptr, p.BH, N, p.d, box_rows);
+    const MapKey key{ptr, p.B, p.H, N, s.b, s.h, s.n, p.d, box_rows, view4 ? 1 : 0};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        for (int i = 0; i < g_map_used; ++i)
+            if (g_map_key[i] == key) {
+                *reinterpret_cast<CUtensorMap *>(m) = g_map_val[i];
+                return true;
+            }
+    }
+    const bool ok = view4 ? tc_make_map_4d(m, ptr, p.B, p.H, N, p.d, s, box_rows)
+                          : tc_make_map_3d(m, ptr, p.BH, N, p.d, box_rows);
+    if (ok) {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        const int i = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
+        g_map_key[i] = key;
+        g_map_val[i] = *reinterpret_cast<CUtensorMap *>(m);
+    }
+    return ok;
+}
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and device
+cudaError_t tc_set_smem_once(const void *kernel, int bytes) {
+    static std::mutex mu;
+    static const void *fn[128];
+    static unsigned long long mask[128];
+    static int used = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    std::lock_guard<std::mutex> lock(mu);
+    int i = 0;
+    while (i < used && fn[i] != kernel) ++i;
+    if (i < used && bit && (mask[i] & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) {
+        if (i == used && used < 128) fn[used++] = kernel;
+        if (i < used) mask[i] |= bit;
+    }
+    return e;
+}
+
+// multiprocessor count of the current device, looked up once per device
+int tc_sm_count() {
+    static std::atomic<int> sms[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64) {
+        const int v = sms[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 148;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && dev < 64) sms[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 // (B, H, N, d) bf16 view -> 4-D map over (d, N, H, B) with 64 x rows x 1 x 1 boxes,
@@ -1023,11 +1098,7 @@ bool tc_fwd_supported(const FaProblem &p) {
            p.Nk >= 128 && p.BH >= 1;
 }
 
-static int sm_count() {
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    return sms;
-}
+static int sm_count() { return tc_sm_count(); }
 
 template <int D, bool CAUSAL, int SPLIT, bool PERSIST, bool VIEW4>
 static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
@@ -1038,7 +1109,7 @@ static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const C
                  float, uint32_t, uint32_t, int, int, FaStrides);
     if constexpr (PERSIST) kern = fa_fwd_tc_persistent_kernel<D, CAUSAL, VIEW4>;
     else kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+    cudaError_t e = tc_set_smem_once(reinterpret_cast<const void *>(kern), (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int qtiles = (p.Nq + BM - 1) / BM;
     // persistent: one CTA per SM walking its share of the work units; otherwise
