@@ -232,10 +232,10 @@ EXECUTED_FACTOR = {"fwd": 1.0, "bwd_pre": 0.0, "bwd_grads": 3.5 / 2.5}
 # `ncu --set full` capture of the current kernels (profiles/fa_tc_kernels_*.md);
 # None where no capture of the current build exists for that workload.
 NCU_TRAFFIC = {
-    ("bench_b8_n4096_d64_causal", "fwd"): 12626176,
-    ("bench_b8_n4096_d64_causal", "bwd_grads"): 17094912,
-    ("long_n16384_d128_causal", "fwd"): 12634880,
-    ("long_n16384_d128_causal", "bwd_grads"): 16977408,
+    ("bench_b8_n4096_d64_causal", "fwd"): 12625664,
+    ("bench_b8_n4096_d64_causal", "bwd_grads"): 17095168,
+    ("long_n16384_d128_causal", "fwd"): 12634624,
+    ("long_n16384_d128_causal", "bwd_grads"): 16977664,
 }
 
 
