@@ -335,9 +335,14 @@ def run_gpu(args, w, rank, world):
 
     # ---- end to end through the public API with host buffers: every step copies its
     # inputs from pinned host memory, runs fa_fwd and fa_bwd and copies O, L, dQ, dK,
-    # dV back.  Two buffer sets, each step captured once as a CUDA graph and the two
-    # graphs replayed alternately on two streams, so one step's copies overlap the
-    # other's kernels (as a data loader would); per-step work is unchanged.
+    # dV back.  Three buffer sets, each step captured once as a CUDA graph and the
+    # graphs replayed in turn on three streams, so the copies of two steps overlap the
+    # kernels of a third (as a data loader would); per-step work is unchanged.  The
+    # copy engines move about 190 GB/s each way from pinned memory here, so with the
+    # short steps the copies, not the kernels, set this number; a third set hides
+    # the copy-in of one step behind the copy-out of another (two sets left the
+    # batch-8 step at 157 us against 130 us with three; a fourth adds nothing, and
+    # splitting the copies over parallel graph branches was slower).
     def make_set():
         dev_in = [torch.empty_like(x) for x in (Qd, Kd, Vd, dOd)]
         o, l_ = torch.empty_like(O), torch.empty_like(L)
@@ -346,7 +351,8 @@ def run_gpu(args, w, rank, world):
         return {"in": dev_in, "out": outs, "ws": binding.alloc_workspace(Qd, Kd, w.causal),
                 "host_out": [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]}
 
-    sets = [make_set(), make_set()]
+    n_sets = 3
+    sets = [make_set() for _ in range(n_sets)]
     h2d = sum(x.numel() * x.element_size() for x in host)
     d2h = sum(x.numel() * x.element_size() for x in sets[0]["host_out"])
 
@@ -360,8 +366,9 @@ def run_gpu(args, w, rank, world):
         for dst, src in zip(st["host_out"], st["out"]):
             dst.copy_(src, non_blocking=True)
 
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
-    e2e_method = "two CUDA graphs of (H2D inputs, fa_fwd, fa_bwd, D2H outputs) replayed alternately on two streams"
+    streams = [torch.cuda.Stream() for _ in range(n_sets)]
+    e2e_method = (f"{n_sets} CUDA graphs of (H2D inputs, fa_fwd, fa_bwd, D2H outputs) replayed in turn on "
+                  f"{n_sets} streams")
     graphs = []
     try:
         for st, sm in zip(sets, streams):
@@ -374,9 +381,9 @@ def run_gpu(args, w, rank, world):
             with torch.cuda.graph(g, stream=sm):
                 e2e_step(st)
             graphs.append(g)
-    except Exception as exc:   # capture refused: the same steps issued eagerly on the two streams
+    except Exception as exc:   # capture refused: the same steps issued eagerly on the streams
         graphs = []
-        e2e_method = f"eager on two alternating streams (graph capture failed: {type(exc).__name__})"
+        e2e_method = f"eager on {n_sets} streams in turn (graph capture failed: {type(exc).__name__})"
     torch.cuda.synchronize()
 
     def run_e2e(n):
@@ -386,12 +393,12 @@ def run_gpu(args, w, rank, world):
         for sm in streams:
             sm.wait_stream(cur)
         for i in range(n):
-            sm = streams[i % 2]
+            sm = streams[i % n_sets]
             with torch.cuda.stream(sm):
                 if graphs:
-                    graphs[i % 2].replay()
+                    graphs[i % n_sets].replay()
                 else:
-                    e2e_step(sets[i % 2])
+                    e2e_step(sets[i % n_sets])
         for sm in streams:
             cur.wait_stream(sm)
         b.record(cur)
