@@ -261,10 +261,8 @@ def run_gpu(args, w, rank, world):
     kf = kernel_flops(w, path)
     fwd_f, bwd_f = w.flops()
 
-    def launch_step():
-        binding.fa_fwd(Qd, Kd, Vd, is_causal=w.causal, O=O, L=L)
-        binding.fa_bwd_preprocess(O, dOd, L, Qd, Kd, w.causal, ws)
-        binding.fa_bwd_grads(Qd, Kd, Vd, dOd, L, dQ, dK, dV, w.causal, ws)
+    def launch_step():   # forward + backward in one library call (fa_fwd_bwd: three kernels)
+        binding.fa_fwd_bwd(Qd, Kd, Vd, dOd, is_causal=w.causal, O=O, L=L, dQ=dQ, dK=dK, dV=dV, workspace=ws)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
@@ -334,7 +332,7 @@ def run_gpu(args, w, rank, world):
         raise RuntimeError("device status not ok after timed steps")
 
     # ---- end to end through the public API with host buffers: every step copies its
-    # inputs from pinned host memory, runs fa_fwd and fa_bwd and copies O, L, dQ, dK,
+    # inputs from pinned host memory, runs fa_fwd_bwd and copies O, L, dQ, dK,
     # dV back.  Three buffer sets, each step captured once as a CUDA graph and the
     # graphs replayed in turn on three streams, so the copies of two steps overlap the
     # kernels of a third (as a data loader would); per-step work is unchanged.  The
@@ -361,13 +359,12 @@ def run_gpu(args, w, rank, world):
         o, l_, dq, dk, dv = st["out"]
         for dst, src in zip(st["in"], host):
             dst.copy_(src, non_blocking=True)
-        binding.fa_fwd(q, k, v, is_causal=w.causal, O=o, L=l_)
-        binding.fa_bwd(q, k, v, o, g, l_, is_causal=w.causal, dQ=dq, dK=dk, dV=dv, workspace=st["ws"])
+        binding.fa_fwd_bwd(q, k, v, g, is_causal=w.causal, O=o, L=l_, dQ=dq, dK=dk, dV=dv, workspace=st["ws"])
         for dst, src in zip(st["host_out"], st["out"]):
             dst.copy_(src, non_blocking=True)
 
     streams = [torch.cuda.Stream() for _ in range(n_sets)]
-    e2e_method = (f"{n_sets} CUDA graphs of (H2D inputs, fa_fwd, fa_bwd, D2H outputs) replayed in turn on "
+    e2e_method = (f"{n_sets} CUDA graphs of (H2D inputs, fa_fwd_bwd, D2H outputs) replayed in turn on "
                   f"{n_sets} streams")
     graphs = []
     try:

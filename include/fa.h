@@ -135,6 +135,20 @@ FA_API fa_status fa_bwd_grads(const void *Q, const void *K, const void *V, const
                        void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * Forward then backward in one call: the unit the field guide's §1.3.3
+ * leaderboard times (a forward plus backward at a fixed configuration, with a
+ * given dO).  Writes O and L, then dQ, dK and dV; the same results, bit for
+ * bit, as fa_fwd followed by fa_bwd on the same stream, but every argument of
+ * both passes is checked before the first launch, and the three kernels
+ * (forward, D-preprocess, gradients) go out back to back, each starting while
+ * its predecessor drains.  Contiguous layout; `workspace` as for fa_bwd.
+ */
+FA_API fa_status fa_fwd_bwd(const void *Q, const void *K, const void *V, const void *dO,
+                            void *O, float *L, void *dQ, void *dK, void *dV,
+                            int B, int H, int Nq, int Nk, int d, float scale, int is_causal, fa_dtype dtype,
+                            void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * fa_bwd without a caller-supplied workspace.  (No counterpart in the method's
  * description: this exists for callers, not for the algorithm.)
  *

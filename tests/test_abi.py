@@ -189,3 +189,21 @@ def test_binding_stride_helpers():
     o = binding._like_rows(q, (2, 4, 256, 64))
     assert o.shape == (2, 4, 256, 64) and o.stride() == (65536, 64, 256, 1)
     assert binding._like_rows(q.contiguous(), (2, 4, 256, 64)).is_contiguous()
+
+
+def fwd_bwd(L, O=V16, ws=V16, ws_bytes=1 << 30, **kw):
+    a = dict(B=1, H=1, Nq=128, Nk=128, d=64, scale=0.125, causal=1, dt=1)
+    a.update(kw)
+    return L.fa_fwd_bwd(V16, V16, V16, V16, O, V16, V16, V16, V16, a["B"], a["H"], a["Nq"], a["Nk"], a["d"],
+                        a["scale"], a["causal"], a["dt"], ws, ws_bytes, None)
+
+
+def test_fwd_bwd_checks_both_passes_before_launching(L):
+    assert fwd_bwd(L, ws=VP(0)) == 6           # the backward's workspace, checked before the forward runs
+    assert fwd_bwd(L, ws_bytes=16) == 6
+    assert fwd_bwd(L, O=VP(0)) == 1
+    assert fwd_bwd(L, O=VP(24)) == 5
+    assert fwd_bwd(L, d=100) == 3
+    assert fwd_bwd(L, causal=3) == 10
+    assert fwd_bwd(L, B=0) == 0                # empty
+    assert fwd_bwd(L) in (0, 9)

@@ -196,6 +196,25 @@ def test_backward_phases_launched_separately(cuda_lib, bh, n, d, causal):
     assert_close(got, want, 2e-2, f"phases bh={bh} n={n} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("bh,n,d,dt,causal", [(8, 512, 64, "bf16", True), (2, 1152, 128, "bf16", True),
+                                               (3, 300, 32, "bf16", False), (2, 200, 64, "f32", True)])
+def test_fwd_bwd_in_one_call(cuda_lib, bh, n, d, dt, causal):
+    """fa_fwd_bwd gives fa_fwd followed by fa_bwd, bit for bit, and matches the oracle."""
+    torch = _torch()
+    from tiled_attention_04_gb300 import binding
+    t = inputs.make_custom(bh, n, n, d, dt, seed=500 + n + d)
+    Q, K, V, dO = (inputs.to_torch(x, torch.device("cuda")) for x in t)
+    O, L, dQ, dK, dV = binding.fa_fwd_bwd(Q, K, V, dO, is_causal=causal)
+    O2, L2 = binding.fa_fwd(Q, K, V, is_causal=causal)
+    dQ2, dK2, dV2 = binding.fa_bwd(Q, K, V, O2, dO, L2, is_causal=causal)
+    torch.cuda.synchronize()
+    assert binding.fa_get_device_status() == binding.FA_OK
+    for name, a, b in (("O", O, O2), ("L", L, L2), ("dQ", dQ, dQ2), ("dK", dK, dK2), ("dV", dV, dV2)):
+        assert torch.equal(a, b), name
+    got = {k: v.double().cpu().numpy() for k, v in (("O", O), ("L", L), ("dQ", dQ), ("dK", dK), ("dV", dV))}
+    assert_close(got, oracle_all(t, causal, 1.0 / math.sqrt(d)), TOL[dt], f"fwd_bwd bh={bh} n={n} d={d} {dt}")
+
+
 def test_forward_and_dkdv_are_deterministic(cuda_lib):
     t = inputs.make_custom(2, 1024, 1024, 128, "bf16", seed=9)
     a = run_gpu(t, True, canary=False)

@@ -385,6 +385,22 @@ fa_status fa_bwd_strided(const void *Q, const fa_strides *sQ, const void *K, con
     return run_grads(p, w, Q, K, V, dO, L, dQ, dK, dV, workspace, stream);
 }
 
+fa_status fa_fwd_bwd(const void *Q, const void *K, const void *V, const void *dO, void *O, float *L, void *dQ,
+                     void *dK, void *dV, int B, int H, int Nq, int Nk, int d, float scale, int is_causal,
+                     fa_dtype dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    // both passes' arguments first, so that a bad one launches nothing at all
+    FaProblem p{};
+    Workspace w{};
+    fa_status s = bwd_args(Q, K, V, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, workspace,
+                           workspace_bytes, &p, &w, false);
+    if (s != FA_OK) return s;
+    if ((long long)p.BH * p.Nq == 0 && (long long)p.BH * p.Nk == 0) return FA_OK;
+    if ((s = bwd_ptrs(p, Q, K, V, O, dO, L, dQ, dK, dV)) != FA_OK) return s;
+    if ((s = run_fwd(p, Q, K, V, O, L, stream)) != FA_OK) return s;
+    if ((s = run_preprocess(p, w, O, dO, L, workspace, stream)) != FA_OK) return s;
+    return run_grads(p, w, Q, K, V, dO, L, dQ, dK, dV, workspace, stream);
+}
+
 fa_status fa_get_device_status(fa_stream_t stream) {
     if (device_ok() != FA_OK) return FA_ERR_NO_DEVICE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
