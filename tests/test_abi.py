@@ -207,3 +207,21 @@ def test_fwd_bwd_checks_both_passes_before_launching(L):
     assert fwd_bwd(L, causal=3) == 10
     assert fwd_bwd(L, B=0) == 0                # empty
     assert fwd_bwd(L) in (0, 9)
+
+
+def test_autograd_copies_views_the_kernels_cannot_read():
+    torch = pytest.importorskip("torch")
+    from tiled_attention_04_gb300 import binding
+    from tiled_attention_04_gb300.autograd import _in_place
+    base = torch.zeros(2 * 256 * 64 + 1, dtype=torch.bfloat16)
+    odd = base[1:].view(2, 1, 256, 64)                 # contiguous, but 2 bytes off a 16-byte boundary
+    assert odd.is_contiguous() and not binding.accepts_view(odd)
+    fixed = _in_place(odd)
+    assert fixed.data_ptr() % 16 == 0 and torch.equal(fixed, odd)
+    x = torch.zeros(2, 4, 256, 64, dtype=torch.bfloat16)
+    assert _in_place(x) is x                            # contiguous and aligned: used in place
+    t = x.transpose(1, 2).contiguous().transpose(1, 2)  # (B, N, H, d) buffer seen as (B, H, N, d)
+    assert _in_place(t) is t
+    bcast = torch.zeros(1, 1, 256, 64, dtype=torch.bfloat16).expand(2, 4, 256, 64)
+    c = _in_place(bcast)                                # stride-0 heads: copied
+    assert c is not bcast and c.is_contiguous()

@@ -24,8 +24,9 @@ from . import binding
 
 def _in_place(t):
     """t itself when the kernels can read it where it lies (contiguous, or a strided
-    (B, H, N, d) view such as a transposed projection output), else a contiguous copy."""
-    return t if binding.accepts_view(t) else t.contiguous()
+    (B, H, N, d) view such as a transposed projection output), else a fresh
+    contiguous copy (a fresh allocation, so also 16-byte aligned)."""
+    return t if binding.accepts_view(t) else t.clone(memory_format=torch.contiguous_format)
 
 
 class FlashAttention(torch.autograd.Function):
