@@ -35,6 +35,11 @@
 // The accumulators (dK and dV, or dQ) are shared: every MMA is issued by one
 // thread, in order, so the two warpgroups' contributions simply add up.
 // Causal: sub-tiles wholly on the masked side of the diagonal are skipped.
+// Layouts as in the forward (template argument VIEW4): contiguous tensors load
+// through 3-D maps and store gradient rows at (bh*N + row)*d; strided views,
+// and head dims 16 and 32 on the d = 64 items, load through 4-D (d, N, H, B)
+// maps and store through the gradients' own strides, skipping the zero
+// columns past d.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>

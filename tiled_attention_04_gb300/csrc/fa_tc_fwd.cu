@@ -51,6 +51,15 @@
 // lets the next kernel be scheduled as soon as all of its CTAs have started,
 // and waits (griddepcontrol.wait) for the previous one before touching global
 // memory, so launch latency overlaps the previous kernel's tail.
+//
+// Layouts (template argument VIEW4): contiguous (B*H, N, d) tensors load
+// through 3-D tensor maps (d, N, B*H) and store O rows at (bh*Nq + row)*d.
+// Strided (B, H, N, d) views -- the method's block pointers keep one stride per
+// dimension, and here batch and heads keep theirs -- load through 4-D maps
+// (d, N, H, B) at coordinates (col, row, bh % H, bh / H) and store through O's
+// own strides.  Head dims 16 and 32 run the d = 64 kernels in this form: the
+// 64-column boxes read zeros past d, so Q K^T is unchanged and the zero output
+// columns past d are never stored.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
