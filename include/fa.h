@@ -21,7 +21,8 @@
  * with batch and heads flattened in front (problem flash_forward (b)).
  * K, V, dK, dV: (B, H, Nk, d).  L: (B*H, Nq) fp32.  All tensors but L and the
  * workspace share one element type (fa_dtype); O, dQ, dK, dV are written in
- * that type; accumulation is always fp32.
+ * that type; accumulation is always fp32.  fa_fwd_strided / fa_bwd_strided
+ * (below) take any of these tensors as a strided (B, H, N, d) view instead.
  *
  * Causal alignment: top-left.  Key j is visible to query i iff j <= i
  * (absolute indices), so every query row sees key 0 and no row is empty.
