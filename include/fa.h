@@ -140,9 +140,10 @@ FA_API fa_status fa_bwd_grads(const void *Q, const void *K, const void *V, const
  * leaderboard times (a forward plus backward at a fixed configuration, with a
  * given dO).  Writes O and L, then dQ, dK and dV; the same results, bit for
  * bit, as fa_fwd followed by fa_bwd on the same stream, but every argument of
- * both passes is checked before the first launch, and the three kernels
- * (forward, D-preprocess, gradients) go out back to back, each starting while
- * its predecessor drains.  Contiguous layout; `workspace` as for fa_bwd.
+ * both passes is checked before the first launch, and the kernels (forward,
+ * D-preprocess, gradients: three on the tensor-core path, four on the CUDA-core
+ * one) go out back to back, each starting while its predecessor drains.
+ * Contiguous layout; `workspace` as for fa_bwd.
  */
 FA_API fa_status fa_fwd_bwd(const void *Q, const void *K, const void *V, const void *dO,
                             void *O, float *L, void *dQ, void *dK, void *dV,
