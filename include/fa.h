@@ -142,8 +142,8 @@ FA_API fa_status fa_bwd_grads(const void *Q, const void *K, const void *V, const
  * bit, as fa_fwd followed by fa_bwd on the same stream, but every argument of
  * both passes is checked before the first launch, and the kernels (forward,
  * D-preprocess, gradients: three on the tensor-core path, four on the CUDA-core
- * one) go out back to back, each starting while its predecessor drains.
- * Contiguous layout; `workspace` as for fa_bwd.
+ * one) go out back to back -- on the tensor-core path each starting while its
+ * predecessor drains.  Contiguous layout; `workspace` as for fa_bwd.
  */
 FA_API fa_status fa_fwd_bwd(const void *Q, const void *K, const void *V, const void *dO,
                             void *O, float *L, void *dQ, void *dK, void *dV,
