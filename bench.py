@@ -1,11 +1,22 @@
 """Attention fwd+bwd throughput on GB300 through the C ABI (libfa.so).
 
-One step = one forward (fa_fwd) and one backward (fa_bwd_preprocess, then
-fa_bwd_grads for dK, dV and dQ) over one batch of the workload, inputs
-resident in HBM.
-FLOP convention: forward 4*B*H*Nq*Nk*d, backward 2.5x that, both halved when
-causal.  L2 (129 MB) is flushed by writing a 512 MiB buffer between timed
-steps; each step is timed with CUDA events on the launching stream.
+One step = one forward plus one backward over one batch of the workload
+(fa_fwd_bwd: the forward, D-preprocess and gradient kernels), inputs resident
+in HBM.  FLOP convention: forward 4*B*H*Nq*Nk*d, backward 2.5x that, both
+halved when causal.  L2 (129 MB) is flushed by writing a 512 MiB buffer
+between timed steps; each step is timed with CUDA events on the launching
+stream.
+
+Besides the K timed steps of the headline workload the JSON line carries:
+  sustained   the same step repeated for about a second (clock coverage);
+  workloads   the other four full-size workloads, each timed forward alone,
+              backward alone and forward + backward, with its own clocks;
+  e2e         through the public call with pinned host buffers: throughput
+              with three buffer sets in flight, and the latency of one call
+              (copies in, fa_fwd_bwd, copies out, synchronised) on one stream;
+  cpu_baseline the fp64 oracle on the host cores (forward and forward +
+              backward timed separately; one-thread numbers for the tiny and
+              the batch-8 shapes).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -146,29 +157,76 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- CPU oracle timing
 
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
+    except Exception:
+        return os.cpu_count()
+
+
 def oracle_sample(w, budget_s: float, max_units=None):
-    """Time the oracle on whole batch*head units of the workload until ~budget_s has passed."""
+    """Time the oracle on whole batch*head units of the workload until ~budget_s has passed.
+
+    Each unit is timed twice: the oracle's forward alone (attn_fwd_ref) and its
+    forward + backward (attn_bwd_ref, which rebuilds P itself)."""
     import oracle
     from tiled_attention_04_gb300 import inputs
     Q, K, V, dO = inputs.make_inputs(w)
     fwd, bwd = w.flops()
-    per_unit = (fwd + bwd) / w.BH
-    units, t = 0, 0.0
+    units, t_fb, t_f = 0, 0.0, 0.0
     limit = max_units or w.BH
-    while units < limit and (t < budget_s or units == 0):
+    while units < limit and (t_fb + t_f < budget_s or units == 0):
         b = units % w.BH
         t0 = time.perf_counter()
+        oracle.attn_fwd_ref(Q.exact[b:b + 1], K.exact[b:b + 1], V.exact[b:b + 1], w.scale, w.causal)
+        t1 = time.perf_counter()
         oracle.attn_bwd_ref(Q.exact[b:b + 1], K.exact[b:b + 1], V.exact[b:b + 1], dO.exact[b:b + 1],
                             w.scale, w.causal)
-        t += time.perf_counter() - t0
+        t2 = time.perf_counter()
+        t_f += t1 - t0
+        t_fb += t2 - t1
         units += 1
-    try:
-        from threadpoolctl import threadpool_info
-        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
-    except Exception:
-        cores = os.cpu_count()
-    return {"value": per_unit * units / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{units} of {w.BH} batch*head units of {w.name} (full rows, fwd+bwd), {t:.1f} s"}
+    per_fwd, per_fb = fwd / w.BH, (fwd + bwd) / w.BH
+    return {"value": per_fb * units / t_fb / 1e12, "unit": "TFLOP/s", "cores": _blas_threads(), "kind": "oracle",
+            "fwd_tflops": per_fwd * units / t_f / 1e12,
+            "bwd_tflops": (per_fb - per_fwd) * units / max(t_fb - t_f, 1e-9) / 1e12,
+            "host_cores": os.cpu_count(),
+            "sample": f"{units} of {w.BH} batch*head units of {w.name} (full rows): forward alone {t_f:.1f} s, "
+                      f"forward + backward {t_fb:.1f} s; bwd_tflops from the difference"}
+
+
+_ONE_THREAD = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import oracle
+from tiled_attention_04_gb300 import inputs
+w = inputs.WORKLOADS[sys.argv[2]]
+Q, K, V, dO = inputs.make_inputs(w)
+t0 = time.perf_counter()
+oracle.attn_fwd_ref(Q.exact[:1], K.exact[:1], V.exact[:1], w.scale, w.causal)
+t1 = time.perf_counter()
+oracle.attn_bwd_ref(Q.exact[:1], K.exact[:1], V.exact[:1], dO.exact[:1], w.scale, w.causal)
+t2 = time.perf_counter()
+f, b = w.flops()
+print(json.dumps({"workload": w.name, "units": 1, "fwd_s": t1 - t0, "fwd_bwd_s": t2 - t1,
+                  "fwd_tflops": f / w.BH / (t1 - t0) / 1e12, "fwd_bwd_tflops": (f + b) / w.BH / (t2 - t1) / 1e12}))
+"""
+
+
+def oracle_one_thread(names):
+    """The oracle on one batch*head unit with one BLAS thread (a child process whose
+    thread-count variables are set before numpy loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = []
+    for n in names:
+        r = subprocess.run([sys.executable, "-c", _ONE_THREAD, ROOT, n], env=env, capture_output=True, text=True,
+                           timeout=300)
+        if r.returncode == 0 and r.stdout.strip():
+            out.append(json.loads(r.stdout.strip().splitlines()[-1]))
+        else:
+            out.append({"workload": n, "error": (r.stderr or "no output").strip().splitlines()[-1][:200]})
+    return out
 
 
 def run_reference(args, w, rank, world):
@@ -212,12 +270,11 @@ def config_of(w):
 def kernel_flops(w, path):
     """Algorithmic FLOP per launch of each kernel, by the FLOP convention above.
 
-    The backward's algorithmic count (2.5x the forward: the five N x N x d
-    matmuls dS recomputation aside) is credited to the launch that forms the
-    gradients.  Both kernel families execute more than that -- the dK/dV pass
-    recomputes S and dP and forms dV and dK (four matmuls), the dQ pass
-    recomputes S and dP again and forms dQ (three) -- so the tensor pipes run
-    at 3.5/2.5 = 1.4x the achieved rate reported for fa_bwd_grads.
+    The backward's algorithmic count (2.5x the forward: five N x N x d matmuls)
+    is credited to the launch that forms the gradients.  That launch executes
+    more: its dK/dV work items recompute S and dP and form dV and dK (four
+    matmuls), its dQ items recompute S and dP again and form dQ (three), so the
+    tensor pipes run at 3.5/2.5 = 1.4x the achieved rate reported for it.
     """
     f = 4.0 * w.BH * w.N * w.N * w.d * (0.5 if w.causal else 1.0)   # two N x N x d matmuls
     return {"fwd": f, "bwd_pre": 0.0, "bwd_grads": 2.5 * f}
@@ -226,56 +283,154 @@ def kernel_flops(w, path):
 # matmul FLOP per launch that the kernels actually execute (recomputation included)
 EXECUTED_FACTOR = {"fwd": 1.0, "bwd_pre": 0.0, "bwd_grads": 3.5 / 2.5}
 
+# Kernel source of each launch: a DRAM traffic figure below is reported only while
+# that source is unchanged since the capture it came from (else the key is null).
+KERNEL_SOURCE = {"fwd": "fa_tc_fwd.cu", "bwd_pre": "fa_tc_bwd.cu", "bwd_grads": "fa_tc_bwd.cu"}
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from one
-# `ncu --set full` capture of the current kernels (profiles/fa_tc_kernels_*.md);
-# None where no capture of the current build exists for that workload.
-NCU_TRAFFIC = {
-    ("bench_b8_n4096_d64_causal", "fwd"): 12625664,
-    ("bench_b8_n4096_d64_causal", "bwd_grads"): 17095168,
-    ("long_n16384_d128_causal", "fwd"): 12634624,
-    ("long_n16384_d128_causal", "bwd_grads"): 16977664,
-}
+# DRAM bytes (read + write) per launch, from one `ncu` capture per workload of the
+# kernel built from the source whose SHA-256 prefix is given.
+NCU_TRAFFIC = {}
+
+
+def _source_sha(kernel):
+    import hashlib
+    path = os.path.join(ROOT, "tiled_attention_04_gb300", "csrc", KERNEL_SOURCE[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_of(workload, kernel):
+    rec = NCU_TRAFFIC.get((workload, kernel))
+    if rec is None:
+        return None, "no capture of this kernel at this workload"
+    nbytes, sha = rec
+    if sha != _source_sha(kernel):
+        return None, "kernel source changed since the capture"
+    return nbytes, f"ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch, source {sha}"
+
+
+def _ev():
+    import torch
+    return torch.cuda.Event(enable_timing=True)
+
+
+def timed(fn, n, flush, stream):
+    """Per-call device times (ms) of n calls of fn, each after an L2 flush, one
+    event pair per call on the launching stream."""
+    import torch
+    evs = [(_ev(), _ev()) for _ in range(n)]
+    for a, b in evs:
+        flush.fill_(1.0)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+class Problem:
+    """Device buffers of one workload and the library calls on them."""
+
+    def __init__(self, w, dev):
+        import torch
+        from tiled_attention_04_gb300 import binding, inputs
+        self.w, self.b = w, binding
+        self.tens = inputs.make_inputs(w)
+        self.Q, self.K, self.V, self.dO = (inputs.to_torch(t, dev) for t in self.tens)
+        self.O = torch.empty_like(self.Q)
+        self.L = torch.empty(self.Q.shape[:-1], dtype=torch.float32, device=dev)
+        self.dQ, self.dK, self.dV = torch.empty_like(self.Q), torch.empty_like(self.K), torch.empty_like(self.V)
+        self.ws = binding.alloc_workspace(self.Q, self.K, w.causal)
+        self.path = binding.path_name(w.N, w.N, w.d, w.causal, binding.dtype_code(self.Q))
+
+    def step(self):   # forward + backward in one library call
+        self.b.fa_fwd_bwd(self.Q, self.K, self.V, self.dO, is_causal=self.w.causal, O=self.O, L=self.L,
+                          dQ=self.dQ, dK=self.dK, dV=self.dV, workspace=self.ws)
+
+    def fwd(self):
+        self.b.fa_fwd(self.Q, self.K, self.V, is_causal=self.w.causal, O=self.O, L=self.L)
+
+    def pre(self):
+        self.b.fa_bwd_preprocess(self.O, self.dO, self.L, self.Q, self.K, self.w.causal, self.ws)
+
+    def grads(self):
+        self.b.fa_bwd_grads(self.Q, self.K, self.V, self.dO, self.L, self.dQ, self.dK, self.dV, self.w.causal,
+                            self.ws)
+
+    def bwd(self):
+        self.pre()
+        self.grads()
+
+    def per_kernel(self, n, flush, stream):
+        """Mean device time of each kernel (an event between every two kernels)."""
+        import torch
+        names = ["fwd", "bwd_pre", "bwd_grads"]
+        kevs = [[_ev() for _ in range(4)] for _ in range(n)]
+        for e in kevs:
+            flush.fill_(1.0)
+            e[0].record(stream)
+            self.fwd()
+            e[1].record(stream)
+            self.pre()
+            e[2].record(stream)
+            self.grads()
+            e[3].record(stream)
+        torch.cuda.synchronize()
+        return {k: sum(e[i].elapsed_time(e[i + 1]) for e in kevs) / n for i, k in enumerate(names)}
+
+
+def summarize(w, pk, step_ms, fwd_ms, bwd_ms, kern_ms):
+    fwd_f, bwd_f = w.flops()
+    kf = kernel_flops(w, None)
+    tf = lambda f, ms: f / (ms * 1e-3) / 1e12   # noqa: E731
+    dom = max(kern_ms, key=lambda n: kern_ms[n])
+    traffic, note = traffic_of(w.name, dom)
+    r = {
+        "fwd_bwd": {"ms": round(step_ms, 5), "tflops": round(tf(fwd_f + bwd_f, step_ms), 2),
+                    "frac": round(tf(fwd_f + bwd_f, step_ms) / pk["bf16_tflops"], 4)},
+        "fwd": {"ms": round(fwd_ms, 5), "tflops": round(tf(fwd_f, fwd_ms), 2),
+                "frac": round(tf(fwd_f, fwd_ms) / pk["bf16_tflops"], 4)},
+        "bwd": {"ms": round(bwd_ms, 5), "tflops": round(tf(bwd_f, bwd_ms), 2),
+                "frac": round(tf(bwd_f, bwd_ms) / pk["bf16_tflops"], 4)},
+        "kernels_ms": {k: round(v, 5) for k, v in kern_ms.items()},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(tf(kf[dom], kern_ms[dom]), 2),
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(tf(kf[dom], kern_ms[dom]) / pk["bf16_tflops"], 4), "traffic": traffic,
+                     "traffic_source": note,
+                     "executed_tflops": round(tf(kf[dom], kern_ms[dom]) * EXECUTED_FACTOR[dom], 2),
+                     "peak_source": f"{pk['source']} bf16 dense burst"},
+    }
+    return r
 
 
 def run_gpu(args, w, rank, world):
     import torch
 
-    from tiled_attention_04_gb300 import binding, build, inputs
+    from tiled_attention_04_gb300 import binding, build
     build.build()
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     binding.lib()
-    tens = inputs.make_inputs(w)
-    Qd, Kd, Vd, dOd = (inputs.to_torch(t, dev) for t in tens)
-    host = [inputs.to_torch(t).pin_memory() for t in tens]
-    O = torch.empty_like(Qd)
-    L = torch.empty(Qd.shape[:-1], dtype=torch.float32, device=dev)
-    dQ, dK, dV = torch.empty_like(Qd), torch.empty_like(Kd), torch.empty_like(Vd)
-    ws = binding.alloc_workspace(Qd, Kd, w.causal)
+    pk = peaks()
+    prob = Problem(w, dev)
+    from tiled_attention_04_gb300 import inputs
+    host = [inputs.to_torch(t).pin_memory() for t in prob.tens]
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    path = binding.path_name(w.N, w.N, w.d, w.causal, binding.dtype_code(Qd))
-    kf = kernel_flops(w, path)
     fwd_f, bwd_f = w.flops()
-
-    def launch_step():   # forward + backward in one library call (fa_fwd_bwd: three kernels)
-        binding.fa_fwd_bwd(Qd, Kd, Vd, dOd, is_causal=w.causal, O=O, L=L, dQ=dQ, dK=dK, dV=dV, workspace=ws)
-
-    def ev():
-        return torch.cuda.Event(enable_timing=True)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        launch_step()
+        prob.step()
     torch.cuda.synchronize()
     if binding.fa_get_device_status() != binding.FA_OK:
         raise RuntimeError("device status not ok after warm-up")
 
-    # timed region: one event pair per step, so that each kernel may be scheduled
-    # onto SMs the previous one has vacated (programmatic dependent launch)
-    evs = [(ev(), ev()) for _ in range(args.steps)]
+    # ---- timed region: exactly K steps, one event pair per step, so that each
+    # kernel may be scheduled onto SMs the previous one has vacated (programmatic
+    # dependent launch)
+    evs = [(_ev(), _ev()) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -283,7 +438,7 @@ def run_gpu(args, w, rank, world):
         for a, b in evs:
             flush.fill_(1.0)
             a.record(stream)
-            launch_step()
+            prob.step()
             b.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -291,61 +446,65 @@ def run_gpu(args, w, rank, world):
     total = [a.elapsed_time(b) for a, b in evs]
     step_ms = max_over_ranks(sum(total) / len(total), world, dev)
 
-    # fwd / bwd split: the same steps with one more event, between fa_fwd and the
-    # backward (preprocessing + gradients, still overlapped by dependent launch)
-    nb = min(args.steps, 50)
-    split = {"fwd": [], "bwd": []}
-    sevs = [[ev() for _ in range(3)] for _ in range(nb)]
-    for e in sevs:
-        flush.fill_(1.0)
-        e[0].record(stream)
-        binding.fa_fwd(Qd, Kd, Vd, is_causal=w.causal, O=O, L=L)
-        e[1].record(stream)
-        binding.fa_bwd_preprocess(O, dOd, L, Qd, Kd, w.causal, ws)
-        binding.fa_bwd_grads(Qd, Kd, Vd, dOd, L, dQ, dK, dV, w.causal, ws)
-        e[2].record(stream)
-    torch.cuda.synchronize()
-    for e in sevs:
-        split["fwd"].append(e[0].elapsed_time(e[1]))
-        split["bwd"].append(e[1].elapsed_time(e[2]))
+    # ---- the same step repeated for about a second: clocks under sustained load
+    t_end = time.perf_counter() + args.sustain_s
+    sus = []
+    with ClockSampler(local) as clk_s:
+        while time.perf_counter() < t_end:
+            sus += timed(prob.step, 200, flush, stream)
+    sus_ms = sum(sus) / len(sus)
 
-    # per-kernel durations (roofline of the dominant kernel): an event between every
-    # two kernels, which serialises them
-    names = ["fwd", "bwd_pre", "bwd_grads"]
-    per = {n: [] for n in names}
-    kevs = [[ev() for _ in range(4)] for _ in range(nb)]
-    for e in kevs:
-        flush.fill_(1.0)
-        e[0].record(stream)
-        binding.fa_fwd(Qd, Kd, Vd, is_causal=w.causal, O=O, L=L)
-        e[1].record(stream)
-        binding.fa_bwd_preprocess(O, dOd, L, Qd, Kd, w.causal, ws)
-        e[2].record(stream)
-        binding.fa_bwd_grads(Qd, Kd, Vd, dOd, L, dQ, dK, dV, w.causal, ws)
-        e[3].record(stream)
-    torch.cuda.synchronize()
-    for e in kevs:
-        for i, n in enumerate(names):
-            per[n].append(e[i].elapsed_time(e[i + 1]))
+    # ---- fwd / bwd split and per-kernel times of the headline workload
+    nb = min(max(args.steps, 20), 50)
+    fwd_ms = sum(timed(prob.fwd, nb, flush, stream)) / nb
+    bwd_ms = sum(timed(prob.bwd, nb, flush, stream)) / nb
+    kern = prob.per_kernel(nb, flush, stream)
     if binding.fa_get_device_status() != binding.FA_OK:
         raise RuntimeError("device status not ok after timed steps")
+    head = summarize(w, pk, step_ms, fwd_ms, bwd_ms, kern)
+
+    # ---- the other full-size workloads (same kernels, same timing rules)
+    others = {}
+    if not args.no_workloads:
+        for name in OTHER_WORKLOADS:
+            if name == w.name:
+                continue
+            wo = inputs.WORKLOADS[name]
+            po = Problem(wo, dev)
+            for _ in range(3):
+                flush.fill_(1.0)
+                po.step()
+            torch.cuda.synchronize()
+            n = 20
+            with ClockSampler(local) as clk_o:
+                st = timed(po.step, n, flush, stream)
+                fo = timed(po.fwd, n, flush, stream)
+                bo = timed(po.bwd, n, flush, stream)
+            ko = po.per_kernel(n, flush, stream)
+            if binding.fa_get_device_status() != binding.FA_OK:
+                raise RuntimeError(f"device status not ok after {name}")
+            rec = summarize(wo, pk, sum(st) / n, sum(fo) / n, sum(bo) / n, ko)
+            rec["config"] = config_of(wo)
+            rec["steps"] = n
+            rec["clocks"] = clk_o.summary()
+            others[name] = rec
+            del po
+            torch.cuda.empty_cache()
 
     # ---- end to end through the public API with host buffers: every step copies its
-    # inputs from pinned host memory, runs fa_fwd_bwd and copies O, L, dQ, dK,
-    # dV back.  Three buffer sets, each step captured once as a CUDA graph and the
-    # graphs replayed in turn on three streams, so the copies of two steps overlap the
-    # kernels of a third (as a data loader would); per-step work is unchanged.  The
-    # copy engines move about 190 GB/s each way from pinned memory here, so with the
-    # short steps the copies, not the kernels, set this number; a third set hides
-    # the copy-in of one step behind the copy-out of another (two sets left the
-    # batch-8 step at 157 us against 130 us with three; a fourth adds nothing, and
-    # splitting the copies over parallel graph branches was slower).
+    # inputs from pinned host memory, runs fa_fwd_bwd and copies O, L, dQ, dK, dV
+    # back.  Throughput: three buffer sets, each step captured once as a CUDA graph
+    # and the graphs replayed in turn on three streams, so the copies of two steps
+    # overlap the kernels of a third (as a data loader would); per-step work is
+    # unchanged.  The copy engines move about 190 GB/s each way from pinned memory
+    # here, so with the short steps the copies, not the kernels, set this number.
+    # Latency: one buffer set on one stream, each call synchronised before the next.
     def make_set():
-        dev_in = [torch.empty_like(x) for x in (Qd, Kd, Vd, dOd)]
-        o, l_ = torch.empty_like(O), torch.empty_like(L)
-        g = [torch.empty_like(x) for x in (dQ, dK, dV)]
+        dev_in = [torch.empty_like(x) for x in (prob.Q, prob.K, prob.V, prob.dO)]
+        o, l_ = torch.empty_like(prob.O), torch.empty_like(prob.L)
+        g = [torch.empty_like(x) for x in (prob.dQ, prob.dK, prob.dV)]
         outs = [o, l_, *g]
-        return {"in": dev_in, "out": outs, "ws": binding.alloc_workspace(Qd, Kd, w.causal),
+        return {"in": dev_in, "out": outs, "ws": binding.alloc_workspace(prob.Q, prob.K, w.causal),
                 "host_out": [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]}
 
     n_sets = 3
@@ -384,7 +543,7 @@ def run_gpu(args, w, rank, world):
 
     def run_e2e(n):
         cur = torch.cuda.current_stream()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b = _ev(), _ev()
         a.record(cur)
         for sm in streams:
             sm.wait_stream(cur)
@@ -404,48 +563,59 @@ def run_gpu(args, w, rank, world):
     run_e2e(max(4, args.warmup))
     n_e2e = max(4, min(args.steps, 100))
     e2e_ms = max_over_ranks(run_e2e(n_e2e), world, dev)
+
+    # latency of one call: copies in, fa_fwd_bwd, copies out, then wait for it
+    lat = []
+    st0 = sets[0]
+    for i in range(args.warmup + max(10, min(args.steps, 50))):
+        t0 = time.perf_counter()
+        e2e_step(st0)
+        torch.cuda.current_stream().synchronize()
+        if i >= args.warmup:
+            lat.append((time.perf_counter() - t0) * 1e3)
+    lat_ms = max_over_ranks(statistics.median(lat), world, dev)
     if binding.fa_get_device_status() != binding.FA_OK:
         raise RuntimeError("device status not ok after the end-to-end steps")
 
     if rank != 0:
         return
-    pk = peaks()
-    avg = {n: sum(v) / len(v) for n, v in per.items()}
-    dom = max(names, key=lambda n: avg[n])
-    dom_tf = kf[dom] / (avg[dom] * 1e-3) / 1e12
     value = world * (fwd_f + bwd_f) / (step_ms * 1e-3) / 1e12
-    fwd_ms = sum(split["fwd"]) / nb
-    bwd_ms = sum(split["bwd"]) / nb
-    fwd_tf = fwd_f / (fwd_ms * 1e-3) / 1e12
-    bwd_tf = bwd_f / (bwd_ms * 1e-3) / 1e12
-    launches_per_step = 3 if path == "tc" else 4
+    launches_per_step = 3 if prob.path == "tc" else 4
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": config_of(w),
         "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
-        "fwd": {"ms": round(fwd_ms, 5), "tflops": round(fwd_tf, 2), "frac": round(fwd_tf / pk["bf16_tflops"], 4)},
-        "bwd": {"ms": round(bwd_ms, 5), "tflops": round(bwd_tf, 2), "frac": round(bwd_tf / pk["bf16_tflops"], 4),
-                "kernels_ms": {n: round(avg[n], 5) for n in names[1:]}},
-        "breakdown": f"fwd and bwd from {nb} further steps with an event between fa_fwd and the backward; "
-                     "kernels_ms and the roofline from another pass with an event between every two kernels",
-        "path": path,
-        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(dom_tf, 2), "peak": pk["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": round(dom_tf / pk["bf16_tflops"], 4),
-                     "traffic": NCU_TRAFFIC.get((w.name, dom)),
-                     "executed_tflops": round(dom_tf * EXECUTED_FACTOR[dom], 2),
-                     "peak_source": f"{pk['source']} bf16 dense burst"},
+        "fwd": head["fwd"],
+        "bwd": {**head["bwd"], "kernels_ms": {k: v for k, v in head["kernels_ms"].items() if k != "fwd"}},
+        "breakdown": f"fwd and bwd from {nb} further calls of each (L2 flushed before each); kernels_ms and "
+                     "the roofline from another pass with an event between every two kernels",
+        "path": prob.path,
+        "roofline": head["roofline"],
+        "sustained": {"ms_per_step": round(sus_ms, 5), "steps": len(sus),
+                      "tflops": round((fwd_f + bwd_f) / (sus_ms * 1e-3) / 1e12, 2),
+                      "seconds": args.sustain_s, "clocks": clk_s.summary()},
+        "workloads": others,
         "e2e": {"value": round(world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": n_e2e, "method": e2e_method,
+                "latency_ms_per_call": round(lat_ms, 4),
+                "latency_method": "one buffer set on one stream: H2D copies, fa_fwd_bwd, D2H copies, stream "
+                                  "synchronised, host wall clock, median",
                 "l2": "not flushed: each step's inputs are rewritten by its own host-to-device copy"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = oracle_sample(w, budget_s=args.cpu_budget)
+        cb = oracle_sample(w, budget_s=args.cpu_budget)
+        cb["one_thread"] = oracle_one_thread(["tiny_f32_causal", w.name])
+        line["cpu_baseline"] = cb
     print(json.dumps(line), flush=True)
+
+
+OTHER_WORKLOADS = ["long_n16384_d128_causal", "vlong_n65536_d64_causal", "layer_xl_b4_h25_n1024_causal",
+                   "layer_xl_b4_h25_n1024_full"]
 
 
 def main():
@@ -457,6 +627,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other four workloads")
+    ap.add_argument("--sustain-s", type=float, default=1.0, help="seconds of the sustained pass")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -2,10 +2,18 @@
 
 Tolerances (elementwise |got - want| <= tol + tol*|want|): 1e-4 for fp32
 inputs, 2e-2 for bf16 inputs, on O, L, dQ, dK and dV.  Small shapes are
-compared in full (several tiles plus ragged tails); the full-size workloads
-are compared at sampled rows against values the oracle wrote ahead of time
-(tests/golden/samples_*.npz, made by tests/golden/make_samples.py), after
-checking that the inputs drawn here hash to the same digests.
+compared in full (several tiles plus ragged tails).  The five full-size
+workloads are compared on every element of every output against the oracle,
+computed on the host's cores while the test runs (tests/fullsize_oracle.py),
+after a fast check of sampled rows against values the oracle wrote ahead of
+time (tests/golden/samples_*.npz, tests/golden/make_samples.py).
+
+Large softmax scales: the bf16 backward rounds the stored O (from which D is
+formed, as problem flash_backward defines D = rowsum(dO * O) from the forward's
+output) and dS (before its tensor-core products) to bf16.  Their effect on dQ
+and dK grows with the scale and passes 2e-2 near scale 1 at d = 64; there
+these two outputs are held to the first-order bound of those roundings
+(``rounding_bound``), every other output to the plain tolerance.
 """
 import math
 import os
@@ -14,6 +22,7 @@ import numpy as np
 import pytest
 
 import oracle
+from bf16_bound import rounding_bound
 from tiled_attention_04_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -62,8 +71,8 @@ def oracle_all(tensors, causal, scale):
     return {"O": O, "L": L, "dQ": dQ, "dK": dK, "dV": dV}
 
 
-def assert_close(got, want, tol, tag):
-    for k in ("O", "L", "dQ", "dK", "dV"):
+def assert_close(got, want, tol, tag, keys=("O", "L", "dQ", "dK", "dV")):
+    for k in keys:
         g, w = got[k], want[k]
         assert np.isfinite(g).all(), f"{tag}: non-finite {k}"
         bad = np.abs(g - w) > tol + tol * np.abs(w)
@@ -120,6 +129,34 @@ def test_parity_non_default_scale(cuda_lib, scale):
     t = inputs.make_custom(2, 256, 256, 64, "bf16", seed=77)
     got = run_gpu(t, True, scale=scale)
     assert_close(got, oracle_all(t, True, scale), 2e-2, f"scale={scale}")
+
+
+def assert_within_bound(got, want, bound, tag):
+    for k in ("dQ", "dK"):
+        g, w = got[k], want[k]
+        lim = bound[k] + 1e-3 * (1 + np.abs(w))
+        bad = np.abs(g - w) > lim
+        assert not bad.any(), (f"{tag}: {k} outside the bf16 rounding bound at {bad.sum()} of {bad.size} "
+                               f"elements (max ratio {(np.abs(g - w) / lim).max():.3g})")
+
+
+@pytest.mark.parametrize("scale,d", [(1.0, 64), (1.0, 128), (2.0, 64)])
+def test_parity_large_scale_within_rounding_bound(cuda_lib, scale, d):
+    """scale >= 1: O, L and dV within 2e-2; dQ and dK within the derived bound."""
+    t = inputs.make_custom(2, 256, 256, d, "bf16", seed=77)
+    got = run_gpu(t, True, scale=scale)
+    want = oracle_all(t, True, scale)
+    assert_close({k: got[k] for k in ("O", "L", "dV")}, {k: want[k] for k in ("O", "L", "dV")}, 2e-2,
+                 f"scale={scale} d={d}", keys=("O", "L", "dV"))
+    EQ, EK = rounding_bound(t, True, scale)
+    assert_within_bound(got, want, {"dQ": EQ, "dK": EK}, f"scale={scale} d={d}")
+
+
+def test_parity_large_scale_f32(cuda_lib):
+    """fp32 inputs keep fp32 arithmetic throughout: scale 1.0 meets the plain 1e-4."""
+    t = inputs.make_custom(2, 200, 200, 64, "f32", seed=78)
+    got = run_gpu(t, True, scale=1.0)
+    assert_close(got, oracle_all(t, True, 1.0), 1e-4, "f32 scale=1.0")
 
 
 def test_tiny_f32_workload_full(cuda_lib):
@@ -215,13 +252,15 @@ def test_fwd_bwd_in_one_call(cuda_lib, bh, n, d, dt, causal):
     assert_close(got, oracle_all(t, causal, 1.0 / math.sqrt(d)), TOL[dt], f"fwd_bwd bh={bh} n={n} d={d} {dt}")
 
 
-def test_forward_and_dkdv_are_deterministic(cuda_lib):
+def test_outputs_are_deterministic(cuda_lib):
+    """No launch adds into memory another program also writes (the backward's two
+    passes each own their outputs, and split items merge in a fixed order), so two
+    runs on the same inputs agree bit for bit, split launches included."""
     t = inputs.make_custom(2, 1024, 1024, 128, "bf16", seed=9)
     a = run_gpu(t, True, canary=False)
     b = run_gpu(t, True, canary=False)
-    for k in ("O", "L", "dK", "dV"):
+    for k in ("O", "L", "dQ", "dK", "dV"):
         assert np.array_equal(a[k], b[k]), k
-    np.testing.assert_allclose(a["dQ"], b["dQ"], rtol=1e-2, atol=1e-2)
 
 
 def test_autograd_function_saves_only_L_with_query_shape(cuda_lib):
@@ -245,8 +284,7 @@ FULL = ["bench_b8_n4096_d64_causal", "long_n16384_d128_causal", "vlong_n65536_d6
         "layer_xl_b4_h25_n1024_causal", "layer_xl_b4_h25_n1024_full"]
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(cuda_lib, name):
+def _digests_match(name):
     path = os.path.join(GOLDEN, f"samples_{name}.npz")
     if not os.path.exists(path):
         pytest.fail(f"missing oracle samples {path} (run tests/golden/make_samples.py)")
@@ -255,6 +293,13 @@ def test_full_size_sampled(cuda_lib, name):
     t = inputs.make_inputs(w)
     digests = [inputs.storage_digest(x) for x in t]
     assert digests == list(ref["digest"]), "inputs drawn here differ from the ones the oracle saw"
+    return ref, w, t
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(cuda_lib, name):
+    """Fast pre-check: sampled rows against values the oracle stored ahead of time."""
+    ref, w, t = _digests_match(name)
     got = run_gpu(t, w.causal, canary=False)
     for k in got:
         assert np.isfinite(got[k]).all(), f"{name}: non-finite {k}"
@@ -263,3 +308,22 @@ def test_full_size_sampled(cuda_lib, name):
            "dK": got["dK"][bh][:, cols], "dV": got["dV"][bh][:, cols]}
     want = {k: ref[k] for k in sub}
     assert_close(sub, want, TOL[w.dtype], name)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_every_element(cuda_lib, name):
+    """Every element of O, L, dQ, dK and dV at the full workload size, in the
+    launch configuration the bench times (fa_fwd_bwd), against the oracle
+    computed on all host cores."""
+    import fullsize_oracle
+    torch = _torch()
+    from tiled_attention_04_gb300 import binding
+    _, w, t = _digests_match(name)
+    want = fullsize_oracle.full_oracle(name)
+    dev = torch.device("cuda")
+    Q, K, V, dO = (inputs.to_torch(x, dev) for x in t)
+    O, L, dQ, dK, dV = binding.fa_fwd_bwd(Q, K, V, dO, is_causal=w.causal)
+    torch.cuda.synchronize()
+    assert binding.fa_get_device_status() == binding.FA_OK
+    got = {k: v.double().cpu().numpy() for k, v in (("O", O), ("L", L), ("dQ", dQ), ("dK", dK), ("dV", dV))}
+    assert_close(got, want, TOL[w.dtype], f"{name} (every element)")

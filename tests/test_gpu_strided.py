@@ -13,6 +13,7 @@ import math
 import numpy as np
 import pytest
 
+import oracle
 from tiled_attention_04_gb300 import inputs
 from test_gpu_parity import TOL, assert_close, oracle_all
 
@@ -121,8 +122,10 @@ def test_output_layout_follows_query_and_padded_output(cuda_lib, d, dt):
 
 def test_transformer_layer_qkv_projection_without_copies(cuda_lib):
     """An xl-shaped attention block (d_model 1600 = 25 heads of 64, N 256): the fused
-    QKV projection is viewed as Q, K, V with no reshape copy, and the gradients of x
-    and of the weights equal those of the same block fed contiguous copies."""
+    QKV projection is viewed as Q, K, V with no reshape copy; the gradients of x
+    and of the weights equal those of the same block fed contiguous copies, and
+    the attention's output and the gradients of its inputs match the oracle on
+    the exact bf16 values the block produced."""
     torch = _torch()
     from tiled_attention_04_gb300 import binding
     from tiled_attention_04_gb300.autograd import flash_attention
@@ -133,6 +136,7 @@ def test_transformer_layer_qkv_projection_without_copies(cuda_lib):
     w0 = torch.from_numpy(inputs.uniform(5, 1, (D, 3 * D), -math.sqrt(6 / (4 * D)), math.sqrt(6 / (4 * D))))
     w0 = w0.to(dev, torch.bfloat16)
     g0 = torch.from_numpy(inputs.normal(5, 2, (B, N, D))).to(dev, torch.bfloat16)
+    seen = {}
 
     def block(copies):
         x = x0.clone().requires_grad_(True)
@@ -143,7 +147,12 @@ def test_transformer_layer_qkv_projection_without_copies(cuda_lib):
             q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
         else:
             assert all(binding.accepts_view(z) for z in (q, k, v))
+            for z in (q, k, v):
+                z.retain_grad()
         o = flash_attention(q, k, v, is_causal=True)
+        if not copies:
+            seen.update(q=q, k=k, v=v, o=o)
+            o.register_hook(lambda grad: seen.__setitem__("dO", grad.detach().clone()))
         y = o.transpose(1, 2).reshape(B, N, D)
         y.backward(g0)
         return y.detach(), x.grad, w.grad
@@ -151,3 +160,9 @@ def test_transformer_layer_qkv_projection_without_copies(cuda_lib):
     a, b = block(False), block(True)
     for name, u, w in zip(("y", "dx", "dW"), a, b):
         assert torch.equal(u, w), f"{name} differs between the strided and the copied block"
+    f64 = lambda z: z.detach().double().cpu().numpy().reshape(B * H, N, d)   # noqa: E731
+    Q, K, V, dO = f64(seen["q"]), f64(seen["k"]), f64(seen["v"]), f64(seen["dO"])
+    dQ, dK, dV, O, L, _ = oracle.attn_bwd_ref(Q, K, V, dO, 1.0 / math.sqrt(d), True)
+    got = {"O": f64(seen["o"]), "L": L, "dQ": f64(seen["q"].grad), "dK": f64(seen["k"].grad),
+           "dV": f64(seen["v"].grad)}
+    assert_close(got, {"O": O, "L": L, "dQ": dQ, "dK": dK, "dV": dV}, 2e-2, "xl block, strided views")

@@ -317,3 +317,54 @@ def test_sweep_vanilla_baseline_matches_oracle():
         for b in range(2):
             O, L = oracle.attn_fwd_ref(Q[b], K[b], V[b], 0.3, causal)
             np.testing.assert_allclose(got[b], O, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- bf16 rounding bound
+
+def _bf16(x):
+    """Round fp64 values to bf16 (nearest even, via fp32) and back to fp64."""
+    return inputs.bf16_bits_to_f64(inputs.to_bf16_bits(x))
+
+
+def _rounded_backward(t, causal, scale, mistake=None):
+    """dQ, dK with the two bf16 roundings of the kernel's backward modelled in fp64:
+    D from the bf16-rounded O, dS rounded to bf16 before its two products.
+    `mistake` plants an error a kernel could make (on the CPU, in this model)."""
+    Q, K, V, dO = (x.exact for x in t)
+    _, _, _, O, _, _ = oracle.attn_bwd_ref(Q, K, V, dO, scale, causal)
+    dQ, dK = np.empty_like(Q), np.empty_like(K)
+    for b in range(Q.shape[0]):
+        P, _ = oracle.attn_probs_ref(Q[b], K[b], scale, causal)
+        D = (dO[b] * _bf16(O[b])).sum(axis=1)
+        if mistake == "no_D":
+            D = np.zeros_like(D)
+        dS = _bf16(P * (dO[b] @ V[b].T - D[:, None]))
+        s = scale * scale if mistake == "double_scale" else scale
+        dQ[b] = s * (dS @ K[b])
+        dK[b] = scale * (dS.T @ Q[b])
+    return dQ, dK
+
+
+@pytest.mark.parametrize("scale,d", [(0.25, 64), (1.0, 64), (1.0, 16), (2.0, 128)])
+def test_bf16_rounding_bound_holds_for_the_rounding_model(scale, d):
+    """The bound used by the bf16 large-scale GPU parity test contains the error of
+    the two roundings it models, at a margin (the bound is worst-case)."""
+    from bf16_bound import rounding_bound
+    t = inputs.make_custom(2, 160, 160, d, "bf16", seed=60 + d)
+    dQ, dK, _, _, _, _ = oracle.attn_bwd_ref(*(x.exact for x in t), scale, True)
+    gQ, gK = _rounded_backward(t, True, scale)
+    EQ, EK = rounding_bound(t, True, scale)
+    assert (np.abs(gQ - dQ) <= EQ + 1e-12).all()
+    assert (np.abs(gK - dK) <= EK + 1e-12).all()
+    assert np.abs(gQ - dQ).max() > 0.05 * EQ.max()   # the bound is not vacuous
+
+
+@pytest.mark.parametrize("mistake", ["no_D", "double_scale"])
+def test_bf16_rounding_bound_catches_planted_mistakes(mistake):
+    from bf16_bound import rounding_bound
+    t = inputs.make_custom(2, 160, 160, 64, "bf16", seed=61)
+    dQ, dK, _, _, _, _ = oracle.attn_bwd_ref(*(x.exact for x in t), 0.5, True)
+    gQ, gK = _rounded_backward(t, True, 0.5, mistake=mistake)
+    EQ, EK = rounding_bound(t, True, 0.5)
+    outside = (np.abs(gQ - dQ) > EQ + 1e-3 * (1 + np.abs(dQ))).sum()
+    assert outside > 0.01 * dQ.size
