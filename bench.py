@@ -271,17 +271,21 @@ def kernel_flops(w, path):
     """Algorithmic FLOP per launch of each kernel, by the FLOP convention above.
 
     The backward's algorithmic count (2.5x the forward: five N x N x d matmuls)
-    is credited to the launch that forms the gradients.  That launch executes
-    more: its dK/dV work items recompute S and dP and form dV and dK (four
-    matmuls), its dQ items recompute S and dP again and form dQ (three), so the
-    tensor pipes run at 3.5/2.5 = 1.4x the achieved rate reported for it.
+    is credited to the launch that forms the gradients (with dQ by reduction,
+    that launch plus its short conversion kernel, timed together).
     """
     f = 4.0 * w.BH * w.N * w.N * w.d * (0.5 if w.causal else 1.0)   # two N x N x d matmuls
     return {"fwd": f, "bwd_pre": 0.0, "bwd_grads": 2.5 * f}
 
 
-# matmul FLOP per launch that the kernels actually execute (recomputation included)
-EXECUTED_FACTOR = {"fwd": 1.0, "bwd_pre": 0.0, "bwd_grads": 3.5 / 2.5}
+def executed_factor(kernel, strategy):
+    """Matmul FLOP the kernels execute per algorithmic FLOP.  dQ by a separate pass:
+    the dK/dV items recompute S and dP and form dV and dK (four matmuls), the dQ
+    items recompute S and dP again and form dQ (three): 3.5/2.5.  dQ by reduction:
+    the five matmuls of the method, once each."""
+    if kernel == "bwd_grads":
+        return 1.0 if strategy == "reduction" else 3.5 / 2.5
+    return 1.0 if kernel == "fwd" else 0.0
 
 # Kernel source of each launch: a DRAM traffic figure below is reported only while
 # that source is unchanged since the capture it came from (else the key is null).
@@ -343,6 +347,42 @@ class Problem:
         self.ws = binding.alloc_workspace(self.Q, self.K, w.causal)
         self.path = binding.path_name(w.N, w.N, w.d, w.causal, binding.dtype_code(self.Q))
 
+    @property
+    def strategy(self):
+        s = self.b.dq_strategy(self.Q, self.K, self.w.causal)
+        return "reduction" if s == self.b.FA_DQ_REDUCTION else "separate"
+
+    def launches(self):
+        """Kernel launches of one fa_fwd_bwd step."""
+        if self.path != "tc":
+            return 4
+        return 4 if self.strategy == "reduction" else 3
+
+    def compare_strategies(self, n, flush, stream):
+        """Backward and per-kernel times under each dQ strategy (forced), then back to
+        the library's own choice: the measurement the choice rests on."""
+        import torch
+        out = {}
+        for name, mode in (("separate", self.b.FA_DQ_SEPARATE_PASS), ("reduction", self.b.FA_DQ_REDUCTION)):
+            prev = self.b.set_dq_strategy(mode)
+            try:
+                self.ws = self.b.alloc_workspace(self.Q, self.K, self.w.causal)
+                if self.b.dq_strategy(self.Q, self.K, self.w.causal) != mode:
+                    out[name] = None   # no such form for this shape
+                    continue
+                for _ in range(3):
+                    self.step()
+                torch.cuda.synchronize()
+                st = timed(self.step, n, flush, stream)
+                bw = timed(self.bwd, n, flush, stream)
+                kern = self.per_kernel(n, flush, stream)
+                out[name] = {"fwd_bwd_ms": round(sum(st) / n, 5), "bwd_ms": round(sum(bw) / n, 5),
+                             "kernels_ms": {k: round(v, 5) for k, v in kern.items()}}
+            finally:
+                self.b.set_dq_strategy(prev)
+        self.ws = self.b.alloc_workspace(self.Q, self.K, self.w.causal)
+        return out
+
     def step(self):   # forward + backward in one library call
         self.b.fa_fwd_bwd(self.Q, self.K, self.V, self.dO, is_causal=self.w.causal, O=self.O, L=self.L,
                           dQ=self.dQ, dK=self.dK, dV=self.dV, workspace=self.ws)
@@ -379,7 +419,7 @@ class Problem:
         return {k: sum(e[i].elapsed_time(e[i + 1]) for e in kevs) / n for i, k in enumerate(names)}
 
 
-def summarize(w, pk, step_ms, fwd_ms, bwd_ms, kern_ms):
+def summarize(w, pk, step_ms, fwd_ms, bwd_ms, kern_ms, strategy):
     fwd_f, bwd_f = w.flops()
     kf = kernel_flops(w, None)
     tf = lambda f, ms: f / (ms * 1e-3) / 1e12   # noqa: E731
@@ -393,11 +433,12 @@ def summarize(w, pk, step_ms, fwd_ms, bwd_ms, kern_ms):
         "bwd": {"ms": round(bwd_ms, 5), "tflops": round(tf(bwd_f, bwd_ms), 2),
                 "frac": round(tf(bwd_f, bwd_ms) / pk["bf16_tflops"], 4)},
         "kernels_ms": {k: round(v, 5) for k, v in kern_ms.items()},
+        "dq_strategy": strategy,
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(tf(kf[dom], kern_ms[dom]), 2),
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(tf(kf[dom], kern_ms[dom]) / pk["bf16_tflops"], 4), "traffic": traffic,
                      "traffic_source": note,
-                     "executed_tflops": round(tf(kf[dom], kern_ms[dom]) * EXECUTED_FACTOR[dom], 2),
+                     "executed_tflops": round(tf(kf[dom], kern_ms[dom]) * executed_factor(dom, strategy), 2),
                      "peak_source": f"{pk['source']} bf16 dense burst"},
     }
     return r
@@ -412,6 +453,8 @@ def run_gpu(args, w, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     binding.lib()
+    binding.set_dq_strategy({"auto": binding.FA_DQ_AUTO, "separate": binding.FA_DQ_SEPARATE_PASS,
+                             "reduction": binding.FA_DQ_REDUCTION}[args.dq_strategy])
     pk = peaks()
     prob = Problem(w, dev)
     from tiled_attention_04_gb300 import inputs
@@ -450,7 +493,7 @@ def run_gpu(args, w, rank, world):
     t_end = time.perf_counter() + args.sustain_s
     sus = []
     with ClockSampler(local) as clk_s:
-        while time.perf_counter() < t_end:
+        while not sus or time.perf_counter() < t_end:
             sus += timed(prob.step, 200, flush, stream)
     sus_ms = sum(sus) / len(sus)
 
@@ -461,7 +504,8 @@ def run_gpu(args, w, rank, world):
     kern = prob.per_kernel(nb, flush, stream)
     if binding.fa_get_device_status() != binding.FA_OK:
         raise RuntimeError("device status not ok after timed steps")
-    head = summarize(w, pk, step_ms, fwd_ms, bwd_ms, kern)
+    head = summarize(w, pk, step_ms, fwd_ms, bwd_ms, kern, prob.strategy)
+    head_cmp = prob.compare_strategies(nb, flush, stream) if not args.no_workloads else None
 
     # ---- the other full-size workloads (same kernels, same timing rules)
     others = {}
@@ -483,7 +527,8 @@ def run_gpu(args, w, rank, world):
             ko = po.per_kernel(n, flush, stream)
             if binding.fa_get_device_status() != binding.FA_OK:
                 raise RuntimeError(f"device status not ok after {name}")
-            rec = summarize(wo, pk, sum(st) / n, sum(fo) / n, sum(bo) / n, ko)
+            rec = summarize(wo, pk, sum(st) / n, sum(fo) / n, sum(bo) / n, ko, po.strategy)
+            rec["dq_strategies"] = po.compare_strategies(n, flush, stream)
             rec["config"] = config_of(wo)
             rec["steps"] = n
             rec["clocks"] = clk_o.summary()
@@ -580,7 +625,7 @@ def run_gpu(args, w, rank, world):
     if rank != 0:
         return
     value = world * (fwd_f + bwd_f) / (step_ms * 1e-3) / 1e12
-    launches_per_step = 3 if prob.path == "tc" else 4
+    launches_per_step = prob.launches()
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -593,6 +638,8 @@ def run_gpu(args, w, rank, world):
                      "the roofline from another pass with an event between every two kernels",
         "path": prob.path,
         "roofline": head["roofline"],
+        "dq_strategy": head["dq_strategy"],
+        "dq_strategies": head_cmp,
         "sustained": {"ms_per_step": round(sus_ms, 5), "steps": len(sus),
                       "tflops": round((fwd_f + bwd_f) / (sus_ms * 1e-3) / 1e12, 2),
                       "seconds": args.sustain_s, "clocks": clk_s.summary()},
@@ -629,6 +676,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other four workloads")
     ap.add_argument("--sustain-s", type=float, default=1.0, help="seconds of the sustained pass")
+    ap.add_argument("--dq-strategy", default="auto", choices=["auto", "separate", "reduction"],
+                    help="how the backward forms dQ (fa_set_dq_strategy)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -241,6 +241,38 @@ FA_API fa_status fa_bwd_strided(const void *Q, const fa_strides *sQ, const void 
 FA_API const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype dtype);
 
 /*
+ * How the backward forms dQ = scale * dS K (problem flash_backward; the field
+ * guide's §1.3.3 names both options: a separate pass, or adding partial sums
+ * into one buffer):
+ *   FA_DQ_SEPARATE_PASS  one program per query tile loops over the key tiles,
+ *                        recomputing S and dP (seven N x N x d products for the
+ *                        five of the method; bit-reproducible);
+ *   FA_DQ_REDUCTION      each key tile's program also forms dS K for every query
+ *                        tile it visits and adds it into an fp32 dQ accumulator
+ *                        in the workspace (TMA reductions in L2), then a short
+ *                        kernel writes dQ = scale * accumulator in the input
+ *                        dtype (five products; dQ's fp32 sums are added in a
+ *                        run-dependent order, so dQ can differ between runs in
+ *                        the last bit of its fp32 sum, about one bf16 rounding
+ *                        step at most; dK, dV, O and L stay bit-reproducible);
+ *   FA_DQ_AUTO           per shape, the faster form as measured on GB300: the
+ *                        reduction for causal attention with head dims up to 64
+ *                        on the tensor-core path, the separate pass otherwise.
+ * The CUDA-core (fp32) path always uses the separate pass.
+ */
+#define FA_DQ_AUTO 0
+#define FA_DQ_SEPARATE_PASS 1
+#define FA_DQ_REDUCTION 2
+/* Sets the process-wide dQ strategy and returns the previous one (-1 for an
+ * unknown value, which changes nothing).  The workspace size depends on it:
+ * query fa_bwd_workspace_size after setting it, and do not change it while a
+ * backward pass is queued on a stream. */
+FA_API int fa_set_dq_strategy(int strategy);
+/* The strategy fa_bwd would use for these arguments (FA_DQ_SEPARATE_PASS or
+ * FA_DQ_REDUCTION), or -1 for unsupported arguments.  Host-only. */
+FA_API int fa_bwd_dq_strategy(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype);
+
+/*
  * Synchronises `stream`, then returns FA_ERR_TIMEOUT if any kernel since the
  * last fa_reset_device_status() gave up a bounded wait, else the stream's
  * CUDA status mapped to FA_OK / FA_ERR_LAUNCH.

@@ -15,6 +15,7 @@ and dK grows with the scale and passes 2e-2 near scale 1 at d = 64; there
 these two outputs are held to the first-order bound of those roundings
 (``rounding_bound``), every other output to the plain tolerance.
 """
+import contextlib
 import math
 import os
 
@@ -63,6 +64,30 @@ def run_gpu(tensors, causal, scale=None, canary=True):
                 assert (part.float() == -7.25).all(), f"write outside {name}"
     return {k: v.double().cpu().numpy() for k, v in
             (("O", O), ("L", L), ("dQ", dQ), ("dK", dK), ("dV", dV))}
+
+
+@contextlib.contextmanager
+def forced_dq(strategy):
+    """Within the block the library forms dQ with `strategy` (binding.FA_DQ_*)."""
+    from tiled_attention_04_gb300 import binding
+    prev = binding.set_dq_strategy(strategy)
+    try:
+        yield
+    finally:
+        binding.set_dq_strategy(prev)
+
+
+def same_dq(a, b):
+    """dQ of two runs or of the two strategies.  Each is an fp32 sum of the same
+    bf16 products rounded once to bf16, but the reduction adds its fp32 partial
+    sums in another (and run-dependent) order, so the two fp32 sums differ by a
+    few fp32 roundings of the partial sums' size and may land on either side of a
+    bf16 rounding boundary: allowed are one bf16 step (2^-7 relative) plus 2^-16
+    of the tensor's largest value (fp32 roundings of partial sums that cancel)."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    big = max(np.abs(a).max(initial=0.0), np.abs(b).max(initial=0.0))
+    return bool((np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 2.0 ** -16 * big).all())
 
 
 def oracle_all(tensors, causal, scale):
@@ -236,7 +261,8 @@ def test_backward_phases_launched_separately(cuda_lib, bh, n, d, causal):
 @pytest.mark.parametrize("bh,n,d,dt,causal", [(8, 512, 64, "bf16", True), (2, 1152, 128, "bf16", True),
                                                (3, 300, 32, "bf16", False), (2, 200, 64, "f32", True)])
 def test_fwd_bwd_in_one_call(cuda_lib, bh, n, d, dt, causal):
-    """fa_fwd_bwd gives fa_fwd followed by fa_bwd, bit for bit, and matches the oracle."""
+    """fa_fwd_bwd gives fa_fwd followed by fa_bwd (bit for bit, dQ under the
+    reduction aside: see same_dq), and matches the oracle."""
     torch = _torch()
     from tiled_attention_04_gb300 import binding
     t = inputs.make_custom(bh, n, n, d, dt, seed=500 + n + d)
@@ -246,21 +272,61 @@ def test_fwd_bwd_in_one_call(cuda_lib, bh, n, d, dt, causal):
     dQ2, dK2, dV2 = binding.fa_bwd(Q, K, V, O2, dO, L2, is_causal=causal)
     torch.cuda.synchronize()
     assert binding.fa_get_device_status() == binding.FA_OK
-    for name, a, b in (("O", O, O2), ("L", L, L2), ("dQ", dQ, dQ2), ("dK", dK, dK2), ("dV", dV, dV2)):
+    for name, a, b in (("O", O, O2), ("L", L, L2), ("dK", dK, dK2), ("dV", dV, dV2)):
         assert torch.equal(a, b), name
+    if binding.dq_strategy(Q, K, causal) == binding.FA_DQ_SEPARATE_PASS:
+        assert torch.equal(dQ, dQ2), "dQ"
+    else:
+        assert same_dq(dQ.double().cpu().numpy(), dQ2.double().cpu().numpy()), "dQ"
     got = {k: v.double().cpu().numpy() for k, v in (("O", O), ("L", L), ("dQ", dQ), ("dK", dK), ("dV", dV))}
     assert_close(got, oracle_all(t, causal, 1.0 / math.sqrt(d)), TOL[dt], f"fwd_bwd bh={bh} n={n} d={d} {dt}")
 
 
-def test_outputs_are_deterministic(cuda_lib):
-    """No launch adds into memory another program also writes (the backward's two
-    passes each own their outputs, and split items merge in a fixed order), so two
-    runs on the same inputs agree bit for bit, split launches included."""
-    t = inputs.make_custom(2, 1024, 1024, 128, "bf16", seed=9)
-    a = run_gpu(t, True, canary=False)
-    b = run_gpu(t, True, canary=False)
-    for k in ("O", "L", "dQ", "dK", "dV"):
+@pytest.mark.parametrize("d,strategy", [(128, "auto"), (64, "separate"), (64, "reduction")])
+def test_outputs_are_deterministic(cuda_lib, d, strategy):
+    """Two runs on the same inputs agree bit for bit, split launches included:
+    the passes own their outputs and split items merge in a fixed order.  The one
+    exception is dQ formed by reduction (additions into one fp32 buffer in a
+    run-dependent order), which agrees to one bf16 rounding step."""
+    from tiled_attention_04_gb300 import binding
+    mode = {"auto": binding.FA_DQ_AUTO, "separate": binding.FA_DQ_SEPARATE_PASS,
+            "reduction": binding.FA_DQ_REDUCTION}[strategy]
+    t = inputs.make_custom(2, 1024, 1024, d, "bf16", seed=9)
+    with forced_dq(mode):
+        a = run_gpu(t, True, canary=False)
+        b = run_gpu(t, True, canary=False)
+    for k in ("O", "L", "dK", "dV"):
         assert np.array_equal(a[k], b[k]), k
+    if strategy == "reduction":
+        assert same_dq(a["dQ"], b["dQ"])
+    else:
+        assert np.array_equal(a["dQ"], b["dQ"]), "dQ"
+
+
+# Both dQ strategies on the shapes that exercise their different code: plain and
+# split launches, persistent-size batches, head dims 16/32 on the d = 64 items,
+# ragged lengths and Nq != Nk.  Each must match the oracle; dK, dV, O and L do not
+# depend on the strategy (bit for bit), and dQ agrees to one bf16 rounding step.
+STRATEGY_CASES = [
+    (2, 512, 512, 64, True), (1, 1088, 1088, 64, True), (3, 384, 384, 64, False), (1, 200, 333, 64, True),
+    (2, 333, 129, 32, False), (1, 1152, 1152, 16, True), (160, 256, 256, 64, True), (1, 4096, 4096, 64, True),
+]
+
+
+@pytest.mark.parametrize("bh,nq,nk,d,causal", STRATEGY_CASES)
+def test_dq_strategies_match_oracle_and_each_other(cuda_lib, bh, nq, nk, d, causal):
+    from tiled_attention_04_gb300 import binding
+    t = inputs.make_custom(bh, nq, nk, d, "bf16", seed=4000 + bh + nq + nk + d)
+    want = oracle_all(t, causal, 1.0 / math.sqrt(d))
+    got = {}
+    for mode in (binding.FA_DQ_SEPARATE_PASS, binding.FA_DQ_REDUCTION):
+        with forced_dq(mode):
+            got[mode] = run_gpu(t, causal)
+        assert_close(got[mode], want, 2e-2, f"strategy {mode} bh={bh} nq={nq} nk={nk} d={d} causal={causal}")
+    a, b = got[binding.FA_DQ_SEPARATE_PASS], got[binding.FA_DQ_REDUCTION]
+    for k in ("O", "L", "dK", "dV"):
+        assert np.array_equal(a[k], b[k]), k
+    assert same_dq(a["dQ"], b["dQ"])
 
 
 def test_autograd_function_saves_only_L_with_query_shape(cuda_lib):

@@ -4,7 +4,8 @@ Such callers (code handed raw pointers by a host framework with no allocator
 of its own, or code that must not call cudaMalloc/cudaFree because they can
 synchronise the device) get the scratch from a fixed array inside the library
 instead of a workspace argument.  It runs the same kernels as fa_bwd, so these
-tests call it through the C ABI and require bit-identical results to fa_bwd,
+tests call it through the C ABI and require the results of fa_bwd (bit for bit;
+for dQ formed by reduction, to one bf16 rounding step, as between two fa_bwd runs),
 twice in a row on different inputs, after a larger call has left its own data
 in the shared scratch, and on an empty shape; plus the refusal of unsupported
 arguments and of a shape that needs more scratch than the array holds.  This file is
@@ -15,6 +16,10 @@ import pytest
 from tiled_attention_04_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
+
+
+def t_q(t, dev, i=0):
+    return inputs.to_torch(t[i], dev)
 
 
 def _both(torch, binding, t, causal):
@@ -33,14 +38,22 @@ def _both(torch, binding, t, causal):
 def test_noalloc_matches_fa_bwd_twice(cuda_lib, bh, n, d, dt, causal):
     import torch
     from tiled_attention_04_gb300 import binding
+    dev = torch.device("cuda")
     # a larger call first, so that the scratch holds another problem's rows
     big = inputs.make_custom(4, 2048, 2048, 64, "bf16", seed=30)
     _both(torch, binding, big, True)
     for seed in (31, 32):   # two calls in a row, different inputs
         t = inputs.make_custom(bh, n, n, d, dt, seed=seed)
         got, ref = _both(torch, binding, t, causal)
-        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        for name, g, r in zip(("dK", "dV"), got[1:], ref[1:]):
             assert torch.equal(g, r), f"{name} differs from fa_bwd (seed {seed})"
+        # dQ formed by reduction adds fp32 partial sums in a run-dependent order, so two
+        # runs may differ by one bf16 rounding step; the separate pass is bit-exact
+        a, b = got[0].double(), ref[0].double()
+        if binding.dq_strategy(t_q(t, dev), t_q(t, dev, 1), causal) == binding.FA_DQ_SEPARATE_PASS:
+            assert torch.equal(a, b), f"dQ differs from fa_bwd (seed {seed})"
+        else:
+            assert bool(((a - b).abs() <= 2.0 ** -7 * torch.maximum(a.abs(), b.abs())).all()), f"dQ (seed {seed})"
 
 
 def test_noalloc_empty_queries_zero_gradients(cuda_lib):

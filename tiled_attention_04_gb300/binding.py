@@ -21,11 +21,13 @@ STATUS = {
     8: "FA_ERR_TIMEOUT", 9: "FA_ERR_NO_DEVICE", 10: "FA_ERR_BAD_ARG",
 }
 FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
+FA_DQ_AUTO, FA_DQ_SEPARATE_PASS, FA_DQ_REDUCTION = 0, 1, 2
 
 # every function include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq",
            "fa_bwd_grads", "fa_fwd_strided", "fa_bwd_strided", "fa_fwd_bwd",
-           "fa_bwd_noalloc", "fa_noalloc_scratch_bytes", "fa_path_name", "fa_get_device_status",
+           "fa_bwd_noalloc", "fa_noalloc_scratch_bytes", "fa_path_name", "fa_set_dq_strategy",
+           "fa_bwd_dq_strategy", "fa_get_device_status",
            "fa_reset_device_status", "fa_set_wait_limit", "fa_debug_force_stall", "fa_status_string")
 
 _lib = None
@@ -70,6 +72,10 @@ def lib() -> ctypes.CDLL:
     L.fa_noalloc_scratch_bytes.restype = sz
     L.fa_path_name.argtypes = [i, i, i, i, i]
     L.fa_path_name.restype = ctypes.c_char_p
+    L.fa_set_dq_strategy.argtypes = [i]
+    L.fa_set_dq_strategy.restype = i
+    L.fa_bwd_dq_strategy.argtypes = [i, i, i, i, i, i, i]
+    L.fa_bwd_dq_strategy.restype = i
     L.fa_get_device_status.argtypes = [vp]
     L.fa_reset_device_status.argtypes = [vp]
     L.fa_set_wait_limit.argtypes = [ctypes.c_uint32]
@@ -196,6 +202,21 @@ def _like_rows(Q, shape):
         B, H, N, d = shape
         return torch.empty((B, N, H, d), dtype=Q.dtype, device=Q.device).transpose(1, 2)
     return torch.empty(shape, dtype=Q.dtype, device=Q.device)
+
+
+def set_dq_strategy(strategy: int) -> int:
+    """fa_set_dq_strategy: FA_DQ_AUTO, FA_DQ_SEPARATE_PASS or FA_DQ_REDUCTION; returns the previous one."""
+    prev = int(lib().fa_set_dq_strategy(int(strategy)))
+    if prev < 0:
+        raise ValueError(f"unknown dQ strategy {strategy}")
+    return prev
+
+
+def dq_strategy(Q, K, is_causal=False) -> int:
+    """The dQ strategy fa_bwd uses for these tensors (FA_DQ_SEPARATE_PASS or FA_DQ_REDUCTION)."""
+    B, H = _bh(Q)
+    return int(lib().fa_bwd_dq_strategy(B, H, Q.shape[-2], K.shape[-2], Q.shape[-1], int(is_causal),
+                                        dtype_code(Q)))
 
 
 def path_name(Nq, Nk, d, is_causal, dtype_c) -> str | None:

@@ -123,19 +123,24 @@ fa_status take_strides(const fa_strides *in, int B, int H, int N, int d, fa_dtyp
 }
 
 // Backward workspace.  CUDA-core path: D (BH*Nq fp32).  Tensor-core path:
-// D then L*log2(e), each BH * padded_rows(Nq) fp32 (see fa_tc_bwd.cu).
+// D then L*log2(e), each BH * padded_rows(Nq) fp32, then (dQ by reduction) the
+// fp32 dQ accumulator (see fa_tc_bwd.cu).
 struct Workspace {
     bool tc;
-    size_t d_off, l_off, total;
+    size_t d_off, l_off, dqa_off, total;
+    bool red;   // dQ by fp32 reduction into the accumulator at dqa_off
 };
 Workspace workspace_layout(const FaProblem &p) {
     Workspace w{};
     w.tc = tc_bwd_supported(p);
     const size_t rows = w.tc ? tc_bwd_ld_rows(p) : (size_t)p.BH * p.Nq;
     const size_t bytes = align_up(rows * sizeof(float), 256);
+    const size_t dqa = w.tc ? tc_bwd_dqa_floats(p) * sizeof(float) : 0;
+    w.red = dqa > 0;
     w.d_off = 0;
     w.l_off = bytes;
-    w.total = w.tc ? 2 * bytes : bytes;
+    w.dqa_off = 2 * bytes;
+    w.total = w.tc ? 2 * bytes + align_up(dqa, 256) : bytes;
     if (w.total == 0) w.total = 256;
     return w;
 }
@@ -178,7 +183,8 @@ fa_status run_preprocess(const FaProblem &p, const Workspace &w, const void *O, 
     char *ws = static_cast<char *>(workspace);
     float *Dv = reinterpret_cast<float *>(ws + w.d_off);
     const cudaStream_t st = as_stream(stream);
-    return map_cuda(w.tc ? tc_bwd_preprocess(p, O, dO, L, Dv, reinterpret_cast<float *>(ws + w.l_off), st)
+    float *dqa = w.red ? reinterpret_cast<float *>(ws + w.dqa_off) : nullptr;
+    return map_cuda(w.tc ? tc_bwd_preprocess(p, O, dO, L, Dv, reinterpret_cast<float *>(ws + w.l_off), dqa, st)
                          : simt_bwd_preprocess(p, O, dO, Dv, st));
 }
 
@@ -223,9 +229,9 @@ fa_status run_grads(const FaProblem &p, const Workspace &w, const void *Q, const
     fa_status s = device_ok();
     if (s != FA_OK) return s;
     char *ws = static_cast<char *>(workspace);
+    float *dqa = w.red ? reinterpret_cast<float *>(ws + w.dqa_off) : nullptr;
     return map_cuda(tc_bwd_grads(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off),
-                                 reinterpret_cast<const float *>(ws + w.d_off), dQ, dK, dV, true, true,
-                                 as_stream(stream)));
+                                 reinterpret_cast<const float *>(ws + w.d_off), dqa, dQ, dK, dV, as_stream(stream)));
 }
 
 // pointer checks of a whole backward pass (fa_bwd, fa_bwd_strided)
@@ -266,6 +272,19 @@ const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype dtype) {
     FaProblem p{};
     if (check_common(1, 1, Nq, Nk, d, is_causal, dtype, 1.f, false, &p) != FA_OK) return nullptr;
     return tc_fwd_supported(p) ? "tc" : "simt";
+}
+
+int fa_set_dq_strategy(int strategy) {
+    if (strategy < FA_DQ_AUTO || strategy > FA_DQ_REDUCTION) return -1;
+    const int prev = static_cast<int>(tc_get_dq_strategy());
+    tc_set_dq_strategy(static_cast<DqStrategy>(strategy));
+    return prev;
+}
+
+int fa_bwd_dq_strategy(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype) {
+    FaProblem p{};
+    if (check_common(B, H, Nq, Nk, d, is_causal, dtype, 1.f, false, &p) != FA_OK) return -1;
+    return tc_bwd_dq_by_reduction(p) ? FA_DQ_REDUCTION : FA_DQ_SEPARATE_PASS;
 }
 
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H, int Nq, int Nk,

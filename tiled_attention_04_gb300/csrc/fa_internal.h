@@ -53,6 +53,9 @@ bool tc_make_map_4d(CUtensorMap_st *m, const void *ptr, int B, int H, int N, int
                     int box_rows);
 // (B*H, N, d) contiguous bf16 tensor -> 3-D TMA map over (d, N, B*H), same boxes
 bool tc_make_map_3d(CUtensorMap_st *m, const void *ptr, int BH, int N, int d, int box_rows);
+// (BH, rows, cols) contiguous fp32 accumulator -> 3-D TMA map over (cols, rows, BH), boxes of
+// 32 columns x 128 rows, 128-byte swizzle (the target of the dQ reductions)
+bool tc_make_map_acc(CUtensorMap_st *m, const void *ptr, int BH, int rows, int cols);
 // true when s is the contiguous layout of a (B, H, N, d) tensor (dimensions of extent 1 aside)
 bool tc_plain_layout(const FaProblem &p, const FaStrides &s, int N);
 // the 4-D map (view4) or the 3-D map of one tensor of the problem
@@ -70,17 +73,28 @@ bool tc_fwd_supported(const FaProblem &p);
 bool tc_bwd_supported(const FaProblem &p);
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
                    cudaStream_t st);
-// backward workspace on this path: per batch*head, padded_rows(Nq) fp32 D then the same of L*log2(e)
+// backward workspace on this path: per batch*head, padded_rows(Nq) fp32 D then the same
+// of L*log2(e); when dQ is formed by reduction, then an fp32 dQ accumulator of
+// padded_rows(Nq) x max(d, 64) per batch*head
 size_t tc_bwd_ld_rows(const FaProblem &p);
+// dQ strategy: a separate pass over query tiles (recomputing S and dP), or fp32
+// reduction by the dK/dV items (no recomputation) followed by a conversion kernel
+enum class DqStrategy { kAuto = 0, kSeparatePass = 1, kReduction = 2 };
+void tc_set_dq_strategy(DqStrategy s);
+DqStrategy tc_get_dq_strategy();
+bool tc_bwd_dq_by_reduction(const FaProblem &p);
+size_t tc_bwd_dqa_floats(const FaProblem &p);   // 0 unless tc_bwd_dq_by_reduction(p)
+// D, L staged (and the dQ accumulator, when dQa is not NULL, cleared)
 cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO, const float *L, float *Dp,
-                              float *Lp, cudaStream_t st);
+                              float *Lp, float *dQa, cudaStream_t st);
 cudaError_t tc_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                         const float *Lp, const float *Dp, void *dK, void *dV, cudaStream_t st);
 cudaError_t tc_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                       const float *Lp, const float *Dp, void *dQ, cudaStream_t st);
-// dK, dV and dQ in one launch (either pass may be switched off)
+// dK, dV and dQ: one launch of both kinds of work item (dQa NULL), or the dK/dV
+// items adding dQ into dQa (cleared by the preprocess) plus the conversion kernel
 cudaError_t tc_bwd_grads(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
-                         const float *Lp, const float *Dp, void *dQ, void *dK, void *dV, bool do_kv, bool do_q,
+                         const float *Lp, const float *Dp, float *dQa, void *dQ, void *dK, void *dV,
                          cudaStream_t st);
 
 // device-side status words of the tensor-core translation units

@@ -46,6 +46,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "fa_internal.h"
@@ -69,13 +70,14 @@ __host__ __device__ inline int padded_rows(int n) { return (n + 127) / 128 * 128
 // padding rows: Dn = 0, Ln = -inf (so their P = 2^(-inf) = 0).  A block takes
 // 256/(d/8) consecutive rows of one batch*head (the padded row count is a
 // multiple of 128, so no block straddles two), which leaves one 32-bit
-// division per thread to find them.
+// division per thread to find them.  When dQ is formed by reduction (dQa not
+// NULL), the row's fp32 accumulator (max(D, 64) columns) is cleared here too.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
                                                          const __nv_bfloat16 *__restrict__ dO,
                                                          const float *__restrict__ L, float *__restrict__ Dp,
-                                                         float *__restrict__ Lp, int Nq, int H, FaStrides so,
-                                                         FaStrides sdo) {
+                                                         float *__restrict__ Lp, float *__restrict__ dQa, int Nq,
+                                                         int H, FaStrides so, FaStrides sdo) {
     constexpr int TPR = D / 8;          // threads per row
     constexpr int RPB = 256 / TPR;      // rows per block
     static_assert(128 % RPB == 0, "a block stays within one batch*head");
@@ -87,29 +89,71 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__
     const int q = ((int)blockIdx.x - bh * bpb) * RPB + (int)threadIdx.x / TPR;
     const int sub = threadIdx.x % TPR;
     const long long gr = (long long)bh * nqp + q;
-    float acc = 0.f;
+    // every load goes out before anything waits on one: the row's L with O and dO,
+    // so the kernel pays one memory latency, not two
+    const float lrow = (sub == 0 && q < Nq) ? __ldg(L + (long long)bh * Nq + q) : 0.f;
+    uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
     if (q < Nq) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(O + fa_row_offset(so, H, bh, q) + sub * 8));
-        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + fa_row_offset(sdo, H, bh, q) + sub * 8));
-        const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
-        const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+        a = __ldg(reinterpret_cast<const uint4 *>(O + fa_row_offset(so, H, bh, q) + sub * 8));
+        b = __ldg(reinterpret_cast<const uint4 *>(dO + fa_row_offset(sdo, H, bh, q) + sub * 8));
+    }
+    if (dQa) {
+        constexpr int DK = D < 64 ? 64 : D;   // accumulator columns (head dims below 64 ride the d = 64 items)
+        float4 *row = reinterpret_cast<float4 *>(dQa + gr * DK);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
-            acc = fmaf(fa.x, fb.x, acc);
-            acc = fmaf(fa.y, fb.y, acc);
-        }
+        for (int i = sub; i < DK / 4; i += TPR) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float acc = 0.f;
+    const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+    const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
     }
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (sub == 0) {
         if (q < Nq) {
             Dp[gr] = -acc;
-            Lp[gr] = -L[(long long)bh * Nq + q] * kLog2e;
+            Lp[gr] = -lrow * kLog2e;
         } else {
             Dp[gr] = 0.f;
             Lp[gr] = -INFINITY;
         }
+    }
+}
+
+// ------------------------------------------------------------------ dQ from its fp32 accumulator
+// dQ = scale * dQa, rounded to bf16: 8 columns per thread (two 16-byte loads,
+// one 16-byte store), grid-stride over the BH * Nq rows' d / 8 column groups.
+template <int DK, bool VIEW4>
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float *__restrict__ dQa,
+                                                                __nv_bfloat16 *__restrict__ dQ, int Nq, int H,
+                                                                int dv, float scale, FaStrides sdq,
+                                                                long long groups) {
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();   // every reduction into dQa has completed
+    const int gpr = dv / 8;                      // column groups per row
+    const int nqp = padded_rows(Nq);
+    for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < groups;
+         g += (long long)gridDim.x * blockDim.x) {
+        const long long row = g / gpr;           // bh * Nq + q
+        const int c = (int)(g - row * gpr) * 8;
+        const int bh = (int)(row / Nq);
+        const int q = (int)(row - (long long)bh * Nq);
+        const float4 *src = reinterpret_cast<const float4 *>(dQa + ((long long)bh * nqp + q) * DK + c);
+        const float4 a = src[0], b = src[1];
+        uint4 o;
+        o.x = tc::pack_bf16(a.x * scale, a.y * scale);
+        o.y = tc::pack_bf16(a.z * scale, a.w * scale);
+        o.z = tc::pack_bf16(b.x * scale, b.y * scale);
+        o.w = tc::pack_bf16(b.z * scale, b.w * scale);
+        __nv_bfloat16 *dst;
+        if constexpr (VIEW4) dst = dQ + fa_row_offset(sdq, H, bh, q) + c;
+        else dst = dQ + row * dv + c;
+        *reinterpret_cast<uint4 *>(dst) = o;
     }
 }
 
@@ -138,7 +182,7 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
 // sub-tiles (MMA N = 128 for S^T and dP^T, which run at full rate; K = 128 for
 // dV and dK).  Both element-wise warpgroups work on every sub-tile, warpgroup t
 // on query columns [64t, 64t + 64).
-template <int D>
+template <int D, bool RED = false>
 struct DkdvWideCfg {
     static constexpr int BK = 128;                 // keys per CTA (MMA M)
     static constexpr int BQ = 128;                 // queries per sub-tile
@@ -154,32 +198,49 @@ struct DkdvWideCfg {
     static constexpr uint32_t Q_OFF = V_OFF + KT::BYTES;                 // stages of Q sub-tiles
     static constexpr uint32_t DO_OFF = Q_OFF + STAGES * QT::BYTES;       // stages of dO sub-tiles
     static constexpr uint32_t LD_OFF = DO_OFF + STAGES * QT::BYTES;      // stages of 128 -L*log2e + 128 -D floats
-    static constexpr uint32_t BAR_OFF = LD_OFF + STAGES * 1024;
-    // kv_full, q_full[S], q_empty[S], sd_full, sd_free, p_full, drain
-    static constexpr int NBAR = 1 + 2 * STAGES + 4;
+    // RED (dQ added into an fp32 accumulator in global memory): dS^T of the current
+    // sub-tile in shared memory (bf16, [128 keys x 128 B] per 64 queries, swizzled),
+    // read by two MMAs -- as dS^T (K-major A of dK) and as dS (MN-major A of dQ) --
+    // and the dQ partial of a sub-tile staged as fp32 [128 rows x 32 columns] boxes
+    // for the TMA reduction.  (A second staging buffer, which costs a stage of the
+    // Q / dO ring, measured slower: 54.9 -> 60.9 us at batch 8, N = 4096.)
+    static constexpr uint32_t DS_OFF = LD_OFF + STAGES * 1024;
+    static constexpr uint32_t DQS_OFF = DS_OFF + (RED ? 2 * 128 * 128 : 0);
+    static constexpr uint32_t DQS_BOX = 128 * 128;                       // bytes of one staged box
+    static constexpr uint32_t BAR_OFF = DQS_OFF + (RED ? (D / 32) * DQS_BOX : 0);
+    // kv_full, q_full[S], q_empty[S], sd_full, sd_free, p_full, drain (+ dq_staged, dq_free)
+    static constexpr int NBAR = 1 + 2 * STAGES + 4 + (RED ? 2 : 0);
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;
     static constexpr uint32_t SMEM_BYTES = (PEER_BAR_OFF + 16 + 1024 > 120u * 1024u ? PEER_BAR_OFF + 16 + 1024 : 120u * 1024u);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(DS_OFF % 1024 == 0 && DQS_OFF % 1024 == 0, "swizzled tiles sit on 1024-byte boundaries");
     // split items: rank 1's partial dV (rows 0..127) and dK (rows 128..255), fp32, over the tile rings
     static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
     static constexpr uint32_t PART_OFF = 0;
-    static_assert(PART_OFF + 256 * PART_STRIDE <= BAR_OFF, "partial fits the rings");
+    static_assert(PART_OFF + 256 * PART_STRIDE <= DS_OFF, "partial fits the rings");
     // TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D);
-    // P^T and dS^T (bf16, 64 columns each) at [384,448) and [448,512), or over S^T / dP^T
+    // P^T and dS^T (bf16, 64 columns each) at [384,448) and [448,512), or over S^T / dP^T.
+    // RED: dS^T lives in shared memory and the sub-tile's dQ partial (fp32) takes [448,512).
     static constexpr uint32_t ST_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
     static constexpr uint32_t PT_COL = SEP ? 384 : 0, DS_COL = SEP ? 448 : 128;
+    static constexpr uint32_t DQ_COL = 448;
+    static_assert(!RED || (D == 64 && SEP), "the dQ reduction form exists for the d = 64 wide items");
 };
 
-// one dK/dV work item: key tile kt of batch*head bh (a half of its queries when SPLIT = 2)
-template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
+// one dK/dV work item: key tile kt of batch*head bh (a half of its queries when SPLIT = 2).
+// RED: the item also forms each sub-tile's dQ partial, dS K, and adds it into the
+// fp32 accumulator behind tmdQa (a TMA reduction issued by warp 2), so that no
+// separate dQ pass recomputes S and dP.
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool RED>
 __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                                          const CUtensorMap &tmdO, const float *__restrict__ Lp,
+                                          const CUtensorMap &tmdO, const CUtensorMap *tmdQa,
+                                          const float *__restrict__ Lp,
                                           const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
                                           __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, int H,
                                           int dv, const FaStrides &sdk, const FaStrides &sdv, float scale,
                                           float scale_log2, uint32_t wait_limit) {
-    using C = DkdvWideCfg<D>;
+    using C = DkdvWideCfg<D, RED>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -205,6 +266,8 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
     const uint32_t sd_free = bar(2 + 2 * C::STAGES);
     const uint32_t p_full = bar(3 + 2 * C::STAGES);
     const uint32_t drain = bar(4 + 2 * C::STAGES);
+    const uint32_t dq_staged = bar(5 + 2 * C::STAGES);   // RED: the element-wise threads staged a dQ partial
+    const uint32_t dq_free = bar(6 + 2 * C::STAGES);     // RED: the reduction has read the staged partial
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -218,6 +281,10 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         tc::mbar_init(sd_free, 256);
         tc::mbar_init(p_full, 256);
         tc::mbar_init(drain, 1);
+        if constexpr (RED) {
+            tc::mbar_init(dq_staged, 256);
+            tc::mbar_init(dq_free, 1);
+        }
         if (SPLIT > 1) {
             tc::mbar_init(base + C::PEER_BAR_OFF, 256);       // peer_free: the peer's 256 element-wise threads
             tc::mbar_init(base + C::PEER_BAR_OFF + 8, 128);   // peer_ready: the peer's 128 senders
@@ -276,6 +343,23 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                 }
             }
         }
+    } else if (RED && warp == 2) {
+        // ------------------------------------------------------------ dQ reduction (RED)
+        // each sub-tile's staged dQ partial is added into the fp32 accumulator in
+        // global memory (rows q0.. of this batch*head) by one TMA reduction per box
+        if (lane == 0 && n > 0) {
+            for (int it = 0; it < n; ++it) {
+                if (!W.wait(dq_staged, it & 1)) break;
+                const int q0 = (i_begin + it) * C::BQ;
+#pragma unroll
+                for (int x = 0; x < D / 32; ++x)
+                    tc::tma_reduce_add_3d(tmdQa, base + C::DQS_OFF + x * C::DQS_BOX, 32 * x, q0, bh);
+                tc::bulk_commit_group();
+                tc::bulk_wait_read_all();   // the staging boxes may be rewritten
+                tc::mbar_arrive(dq_free);
+            }
+            tc::bulk_wait_all();            // the additions have landed before the CTA exits
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // whole warp in the loop (uniform descriptors), one elected lane issues
@@ -289,6 +373,12 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
             const uint64_t gk = tc::sdesc_sw128(base + C::DO_OFF, 16, 1024);    // B of dP^T
             const uint64_t qm = tc::sdesc_sw128(base + C::Q_OFF, C::QT::CHUNK, 1024);    // B of dK, MN-major
             const uint64_t gm = tc::sdesc_sw128(base + C::DO_OFF, C::QT::CHUNK, 1024);   // B of dV, MN-major
+            // RED: dQ = dS K with A = dS (queries x keys, MN-major: the dS^T rows are keys)
+            // and B = K (keys x d, MN-major), both from shared memory
+            constexpr uint32_t idesc_q = tc::idesc_bf16(128, D, true, true);
+            const uint64_t dsk = tc::sdesc_sw128(base + C::DS_OFF, 16, 1024);              // A of dK, K-major
+            const uint64_t dsm = tc::sdesc_sw128(base + C::DS_OFF, 128 * 128, 1024);       // A of dQ, MN-major
+            const uint64_t km = tc::sdesc_sw128(base + C::K_OFF, C::KT::CHUNK, 1024);      // B of dQ, MN-major
             bool ok = __all_sync(0xffffffffu, W.wait(kv_full, 0));
             // S^T = K Q^T and dP^T = V dO^T for sub-tile `it`; after the first, S^T / dP^T
             // must also have been read for sub-tile it-1 (both waits polled together)
@@ -321,7 +411,16 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                     for (int kk = 0; kk < C::BQ / 16; ++kk) {
                         const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
                         tc::mma_ts(tmem + C::DV_COL, tmem + C::PT_COL + kk * 8, gm + st + kk * 128, idesc_g, acc);
-                        tc::mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8, qm + st + kk * 128, idesc_g, acc);
+                        if constexpr (RED)
+                            tc::mma_ss(tmem + C::DK_COL, dsk + (((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4),
+                                       qm + st + kk * 128, idesc_g, acc);
+                        else
+                            tc::mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8, qm + st + kk * 128, idesc_g, acc);
+                    }
+                    if constexpr (RED) {
+#pragma unroll
+                        for (int kk = 0; kk < C::BK / 16; ++kk)   // 16 keys per step
+                            tc::mma_ss(tmem + C::DQ_COL, dsm + kk * 128, km + kk * 128, idesc_q, kk > 0 ? 1u : 0u);
                     }
                     tc::mma_commit(q_empty(s));   // sub-tile done: its stage is free
                 }
@@ -359,6 +458,29 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         const uint32_t tD = tmem + lane_base + C::DP_COL + 64 * t;
         const uint32_t tPT = tmem + lane_base + C::PT_COL + 32 * t;
         const uint32_t tDS = tmem + lane_base + C::DS_COL + 32 * t;
+        const uint32_t tDQ = tmem + lane_base + C::DQ_COL + 32 * t;   // RED: query row r, columns [32t, 32t+32)
+        // RED: this thread's 64 dS^T values (key r, queries [64t, 64t+64)) into the
+        // swizzled shared tile the dK and dQ MMAs read
+        auto store_ds = [&](const uint32_t (&v)[32]) {
+            uint8_t *row = sb + C::DS_OFF + t * (128 * 128) + r * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<uint4 *>(row + ((u ^ (r & 7)) << 4)) =
+                    make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        };
+        // RED: stage sub-tile j's dQ partial (row r, columns [32t, 32t+32)) once the
+        // reduction has read sub-tile j-1's, then hand it to the reducing warp
+        auto stage_dq = [&](int j, const uint32_t (&v)[32]) -> bool {
+            if (j > 0 && !__all_sync(0xffffffffu, W.wait(dq_free, (j - 1) & 1))) return false;
+            uint8_t *row = sb + C::DQS_OFF + t * C::DQS_BOX + r * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<uint4 *>(row + ((u ^ (r & 7)) << 4)) =
+                    make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(dq_staged);
+            return true;
+        };
         for (int it = 0; it < n; ++it) {
             const int s = it % C::STAGES;
             const int qc = (i_begin + it) * C::BQ + 64 * t;      // this warpgroup's first query column
@@ -420,11 +542,22 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                 if (!__all_sync(0xffffffffu, ok)) break;
                 tc::fence_after_sync();
             }
+            uint32_t dq[32];
+            if (RED && it > 0) tmem_ld_x32(tDQ, dq);   // sub-tile it-1's dQ, before this sub-tile's MMA rewrites it
             tmem_st_x32(tPT, pp);
-            tmem_st_x32(tDS, dsp);
+            if constexpr (RED) store_ds(dsp);
+            else tmem_st_x32(tDS, dsp);
             tc::tmem_st_wait();
+            if constexpr (RED) {
+                if (it > 0) {
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(dq);
+                }
+                tc::fence_proxy_async_smem();   // dS^T is read by the tensor core
+            }
             tc::fence_before_sync();
             tc::mbar_arrive(p_full);
+            if (RED && it > 0 && !stage_dq(it - 1, dq)) break;
         }
         // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (rows = keys);
         // a split item's rank 1 leaves its partial sums for rank 0 to add
@@ -434,6 +567,15 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         if (fine && n > 0) fine = W.wait(q_empty((n - 1) % C::STAGES), ((n - 1) / C::STAGES) & 1);
         fine = __all_sync(0xffffffffu, fine);
         if (fine && n > 0) tc::fence_after_sync();
+        if constexpr (RED) {
+            if (fine && n > 0) {   // the last sub-tile's dQ partial
+                uint32_t dq[32];
+                tmem_ld_x32(tDQ, dq);
+                tc::tmem_ld_wait();
+                reg_fence_x32(dq);
+                fine = stage_dq(n - 1, dq);
+            }
+        }
         __nv_bfloat16 *dst;
         if constexpr (VIEW4)
             dst = t == 0 ? dV + fa_row_offset(sdv, tc::opaque(H), bh, key) : dK + fa_row_offset(sdk, tc::opaque(H), bh, key);
@@ -1532,13 +1674,15 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
 // key tile, dQ per query tile; each longest first) are interleaved so that the
 // long items of both start first and the short ones of both fill the end --
 // one kernel tail instead of two, and the passes balance each other's load.
-template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
+// RED: dK/dV items only, each adding its dQ partials into the fp32 accumulator
+// behind dqa (no dQ items; a short kernel converts the accumulator afterwards).
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool RED>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap qA, const __grid_constant__ CUtensorMap kA,
                      const __grid_constant__ CUtensorMap vA, const __grid_constant__ CUtensorMap dOA,
                      const __grid_constant__ CUtensorMap qB, const __grid_constant__ CUtensorMap kB,
                      const __grid_constant__ CUtensorMap vB, const __grid_constant__ CUtensorMap dOB,
-                     const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ,
+                     const __grid_constant__ CUtensorMap dqa, const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ,
                      __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH,
                      int k_tiles, int q_tiles, int n_kv_items, int n_q_items, float scale, float scale_log2,
                      uint32_t wait_limit, int H, int dv, FaStrides sdq, FaStrides sdk, FaStrides sdv) {
@@ -1559,12 +1703,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int r = idx / BH;
         const int kt = CAUSAL ? r : k_tiles - 1 - r;    // causal: the first key tiles see the most queries
         if constexpr (D == 64)
-            dkdv_item_wide<D, CAUSAL, SPLIT, VIEW4>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, dv, sdk, sdv, scale,
-                                             scale_log2, wait_limit);
+            dkdv_item_wide<D, CAUSAL, SPLIT, VIEW4, RED>(qA, kA, vA, dOA, &dqa, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, dv,
+                                                         sdk, sdv, scale, scale_log2, wait_limit);
         else
             dkdv_item_narrow<D, CAUSAL, SPLIT, VIEW4>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, dv, sdk, sdv, scale,
                                                scale_log2, wait_limit);
-    } else {
+    } else if constexpr (!RED) {
         const int qt = q_tiles - 1 - idx / BH;           // causal: the last query tiles see the most keys
         if constexpr (D == 64)
             dq_item_wide<D, CAUSAL, SPLIT, VIEW4>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, dv, sdq, scale, scale_log2,
@@ -1638,33 +1782,36 @@ bool dq_split(const FaProblem &p) {
 }
 
 struct Maps2 {
-    Maps a, b;   // tensor maps of the dK/dV pass (a) and of the dQ pass (b)
-    bool view4;  // 4-D maps over strided views (else 3-D maps over contiguous tensors)
+    Maps a, b;        // tensor maps of the dK/dV pass (a) and of the dQ pass (b)
+    CUtensorMap dqa;  // the fp32 dQ accumulator (dQ by reduction), else unused
+    bool view4;       // 4-D maps over strided views (else 3-D maps over contiguous tensors)
 };
 
-template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool RED>
 cudaError_t launch_bwd(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dQ, void *dK,
                        void *dV, bool do_kv, bool do_q, cudaStream_t st) {
-    using KvC = std::conditional_t<D == 64, DkdvWideCfg<D>, DkdvNarrowCfg<D>>;
+    static_assert(!RED || D == 64, "the dQ reduction form exists for the d = 64 items");
+    using KvC = std::conditional_t<D == 64, DkdvWideCfg<D, RED>, DkdvNarrowCfg<D>>;
     using QC = std::conditional_t<D == 64, DqWideCfg<D>, DqNarrowCfg<D>>;
     constexpr uint32_t smem = KvC::SMEM_BYTES > QC::SMEM_BYTES ? KvC::SMEM_BYTES : QC::SMEM_BYTES;
     const int kt = (p.Nk + 127) / 128, qt = (p.Nq + 127) / 128;
-    const long long na = do_kv ? (long long)kt * p.BH : 0, nb = do_q ? (long long)qt * p.BH : 0;
-    return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q, m.a.k, m.a.v,
-                          m.a.dO, m.b.q, m.b.k, m.b.v, m.b.dO, Lp, Dp, static_cast<__nv_bfloat16 *>(dQ),
-                          static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt, qt,
-                          (int)na, (int)nb, p.scale, p.scale * kLog2e, p.wait_limit, p.H, p.d, p.sdQ, p.sdK, p.sdV);
+    const long long na = do_kv ? (long long)kt * p.BH : 0, nb = (do_q && !RED) ? (long long)qt * p.BH : 0;
+    return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4, RED>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q,
+                          m.a.k, m.a.v, m.a.dO, m.b.q, m.b.k, m.b.v, m.b.dO, m.dqa, Lp, Dp,
+                          static_cast<__nv_bfloat16 *>(dQ), static_cast<__nv_bfloat16 *>(dK),
+                          static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt, qt, (int)na, (int)nb, p.scale,
+                          p.scale * kLog2e, p.wait_limit, p.H, p.d, p.sdQ, p.sdK, p.sdV);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool RED>
 cudaError_t launch_bwd_any(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dQ, void *dK,
                            void *dV, bool do_kv, bool do_q, cudaStream_t st) {
-    const bool split = (do_kv && dkdv_split(p)) || (do_q && dq_split(p));
+    const bool split = (do_kv && dkdv_split(p)) || (do_q && !RED && dq_split(p));
     if (m.view4)
-        return split ? launch_bwd<D, CAUSAL, 2, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
-                     : launch_bwd<D, CAUSAL, 1, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
-    return split ? launch_bwd<D, CAUSAL, 2, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
-                 : launch_bwd<D, CAUSAL, 1, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+        return split ? launch_bwd<D, CAUSAL, 2, true, RED>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                     : launch_bwd<D, CAUSAL, 1, true, RED>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+    return split ? launch_bwd<D, CAUSAL, 2, false, RED>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                 : launch_bwd<D, CAUSAL, 1, false, RED>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
 }
 
 bool make_maps(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO, int q_rows,
@@ -1679,8 +1826,35 @@ bool tc_bwd_supported(const FaProblem &p) { return tc_fwd_supported(p); }
 
 size_t tc_bwd_ld_rows(const FaProblem &p) { return (size_t)p.BH * padded_rows(p.Nq); }
 
+namespace {
+std::atomic<int> g_dq_strategy{0};
+}
+
+void tc_set_dq_strategy(DqStrategy s) { g_dq_strategy.store(static_cast<int>(s)); }
+DqStrategy tc_get_dq_strategy() { return static_cast<DqStrategy>(g_dq_strategy.load()); }
+
+// dQ by fp32 reduction inside the dK/dV items exists for head dims up to 64 (the
+// 128-wide items).  Measured on GB300 (gradient launch, reduction / separate pass):
+// batch 8 x N 4096 causal 54.9 / 58.6 us, N 65536 causal 1204 / 1279 us, the
+// 4 x 25 x 1024 layer causal 75.6 / 78.2 us but non-causal 103.8 / 101.0 us -- the
+// reductions (32 KB per key tile and query tile) cost more where every key tile
+// meets every query tile.  So: the reduction for causal shapes, the separate pass
+// otherwise.  A forced strategy overrides the choice.
+bool tc_bwd_dq_by_reduction(const FaProblem &p) {
+    if (!tc_bwd_supported(p) || p.d > 64) return false;
+    switch (tc_get_dq_strategy()) {
+        case DqStrategy::kSeparatePass: return false;
+        case DqStrategy::kReduction: return true;
+        default: return p.causal != 0;
+    }
+}
+
+size_t tc_bwd_dqa_floats(const FaProblem &p) {
+    return tc_bwd_dq_by_reduction(p) ? (size_t)p.BH * padded_rows(p.Nq) * (p.d < 64 ? 64 : p.d) : 0;
+}
+
 cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO, const float *L, float *Dp,
-                              float *Lp, cudaStream_t st) {
+                              float *Lp, float *dQa, cudaStream_t st) {
     const long long rows = (long long)p.BH * padded_rows(p.Nq);
     if (rows == 0) return cudaSuccess;
     const auto *o = static_cast<const __nv_bfloat16 *>(O);
@@ -1696,18 +1870,44 @@ cudaError_t tc_bwd_preprocess(const FaProblem &p, const void *O, const void *dO,
     cfg.numAttrs = 1;
     cudaError_t e;
     switch (p.d) {
-        case 128: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO); break;
-        case 64: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<64>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO); break;
-        case 32: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<32>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO); break;
-        default: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<16>, o, g, L, Dp, Lp, p.Nq, p.H, p.sO, p.sdO); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<128>, o, g, L, Dp, Lp, dQa, p.Nq, p.H, p.sO, p.sdO); break;
+        case 64: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<64>, o, g, L, Dp, Lp, dQa, p.Nq, p.H, p.sO, p.sdO); break;
+        case 32: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<32>, o, g, L, Dp, Lp, dQa, p.Nq, p.H, p.sO, p.sdO); break;
+        default: e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_kernel<16>, o, g, L, Dp, Lp, dQa, p.Nq, p.H, p.sO, p.sdO); break;
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-cudaError_t tc_bwd_grads(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
-                         const float *Lp, const float *Dp, void *dQ, void *dK, void *dV, bool do_kv, bool do_q,
-                         cudaStream_t st) {
+namespace {
+
+template <int DK>
+cudaError_t launch_dq_convert(const FaProblem &p, const float *dQa, void *dQ, bool view4, cudaStream_t st) {
+    const long long groups = (long long)p.BH * p.Nq * (p.d / 8);
+    if (groups == 0) return cudaSuccess;
+    const long long blocks = std::min<long long>((groups + 255) / 256, (long long)sm_count() * 8);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    auto *q = static_cast<__nv_bfloat16 *>(dQ);
+    const cudaError_t e =
+        view4 ? cudaLaunchKernelEx(&cfg, fa_bwd_dq_convert_kernel<DK, true>, dQa, q, p.Nq, p.H, p.d, p.scale, p.sdQ, groups)
+              : cudaLaunchKernelEx(&cfg, fa_bwd_dq_convert_kernel<DK, false>, dQa, q, p.Nq, p.H, p.d, p.scale, p.sdQ,
+                                   groups);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+// the whole backward's gradient launches; dQa != NULL selects dQ by reduction
+cudaError_t grads_impl(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                       const float *Lp, const float *Dp, float *dQa, void *dQ, void *dK, void *dV, bool do_kv,
+                       bool do_q, cudaStream_t st) {
     // Contiguous tensors keep 3-D (d, N, B*H) maps and plain row addressing; any
     // strided view, or a head dim below 64 (run on the d = 64 kernels with the
     // columns past d read as zero and never stored), switches the whole launch to
@@ -1726,20 +1926,39 @@ cudaError_t tc_bwd_grads(const FaProblem &p, const void *Q, const void *K, const
                !make_maps(p, Q, K, V, dO, 128, 64, m.view4, &m.b)) {
         return cudaErrorInvalidValue;
     }
-    if (p.d == 128) return p.causal ? launch_bwd_any<128, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
-                                    : launch_bwd_any<128, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
-    return p.causal ? launch_bwd_any<64, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
-                    : launch_bwd_any<64, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+    const bool red = dQa != nullptr && do_kv && do_q;
+    if (red) {
+        if (p.d > 64) return cudaErrorInvalidValue;
+        if (!tc_make_map_acc(reinterpret_cast<CUtensorMap_st *>(&m.dqa), dQa, p.BH, padded_rows(p.Nq), 64))
+            return cudaErrorInvalidValue;
+        cudaError_t e = p.causal ? launch_bwd_any<64, true, true>(p, m, Lp, Dp, dQ, dK, dV, true, true, st)
+                                 : launch_bwd_any<64, false, true>(p, m, Lp, Dp, dQ, dK, dV, true, true, st);
+        if (e != cudaSuccess) return e;
+        return launch_dq_convert<64>(p, dQa, dQ, !tc_plain_layout(p, p.sdQ, p.Nq), st);
+    }
+    m.dqa = m.a.q;   // unused by the two-pass launch
+    if (p.d == 128) return p.causal ? launch_bwd_any<128, true, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                                    : launch_bwd_any<128, false, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+    return p.causal ? launch_bwd_any<64, true, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                    : launch_bwd_any<64, false, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+}
+
+}  // namespace
+
+cudaError_t tc_bwd_grads(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
+                         const float *Lp, const float *Dp, float *dQa, void *dQ, void *dK, void *dV,
+                         cudaStream_t st) {
+    return grads_impl(p, Q, K, V, dO, Lp, Dp, dQa, dQ, dK, dV, true, true, st);
 }
 
 cudaError_t tc_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                         const float *Lp, const float *Dp, void *dK, void *dV, cudaStream_t st) {
-    return tc_bwd_grads(p, Q, K, V, dO, Lp, Dp, nullptr, dK, dV, true, false, st);
+    return grads_impl(p, Q, K, V, dO, Lp, Dp, nullptr, nullptr, dK, dV, true, false, st);
 }
 
 cudaError_t tc_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                       const float *Lp, const float *Dp, void *dQ, cudaStream_t st) {
-    return tc_bwd_grads(p, Q, K, V, dO, Lp, Dp, dQ, nullptr, nullptr, false, true, st);
+    return grads_impl(p, Q, K, V, dO, Lp, Dp, nullptr, dQ, nullptr, nullptr, false, true, st);
 }
 
 cudaError_t tc_bwd_read_status(unsigned *out, cudaStream_t st) {

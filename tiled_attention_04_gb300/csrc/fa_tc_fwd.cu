@@ -1046,6 +1046,36 @@ bool tc_make_map(CUtensorMap_st *m, const void *ptr, const FaProblem &p, const F
     return ok;
 }
 
+// (BH, rows, cols) contiguous fp32 accumulator -> 3-D map with 32 x 128 x 1 boxes
+// (one 128-byte swizzled row of 32 floats per row), for TMA reductions into it
+bool tc_make_map_acc(CUtensorMap_st *m, const void *ptr, int BH, int rows, int cols) {
+    const MapKey key{ptr, BH, 0, rows, 0, 0, 0, cols, 128, 2};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        for (int i = 0; i < g_map_used; ++i)
+            if (g_map_key[i] == key) {
+                *reinterpret_cast<CUtensorMap *>(m) = g_map_val[i];
+                return true;
+            }
+    }
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)rows * cols * 4};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const bool ok = enc(reinterpret_cast<CUtensorMap *>(m), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (ok) {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        const int i = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
+        g_map_key[i] = key;
+        g_map_val[i] = *reinterpret_cast<CUtensorMap *>(m);
+    }
+    return ok;
+}
+
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and device
 cudaError_t tc_set_smem_once(const void *kernel, int bytes) {
     static std::mutex mu;
