@@ -1,8 +1,8 @@
 """Attention fwd+bwd throughput on GB300 through the C ABI (libfa.so).
 
 One step = one forward plus one backward over one batch of the workload
-(fa_fwd_bwd: the forward, D-preprocess and gradient kernels), inputs resident
-in HBM.  FLOP convention: forward 4*B*H*Nq*Nk*d, backward 2.5x that, both
+(fa_fwd_bwd: the forward kernel, whose epilogue also forms D, then the
+gradient kernels), inputs resident in HBM.  FLOP convention: forward 4*B*H*Nq*Nk*d, backward 2.5x that, both
 halved when causal.  L2 (129 MB) is flushed by writing a 512 MiB buffer
 between timed steps; each step is timed with CUDA events on the launching
 stream.
@@ -353,10 +353,12 @@ class Problem:
         return "reduction" if s == self.b.FA_DQ_REDUCTION else "separate"
 
     def launches(self):
-        """Kernel launches of one fa_fwd_bwd step."""
+        """Kernel launches of one fa_fwd_bwd step: on the tensor-core path the forward
+        (which also does the backward's preprocessing) and the gradient launch, plus
+        the dQ conversion when dQ is formed by reduction."""
         if self.path != "tc":
             return 4
-        return 4 if self.strategy == "reduction" else 3
+        return 3 if self.strategy == "reduction" else 2
 
     def compare_strategies(self, n, flush, stream):
         """Backward and per-kernel times under each dQ strategy (forced), then back to
@@ -634,8 +636,10 @@ def run_gpu(args, w, rank, world):
         "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
         "fwd": head["fwd"],
         "bwd": {**head["bwd"], "kernels_ms": {k: v for k, v in head["kernels_ms"].items() if k != "fwd"}},
-        "breakdown": f"fwd and bwd from {nb} further calls of each (L2 flushed before each); kernels_ms and "
-                     "the roofline from another pass with an event between every two kernels",
+        "breakdown": f"fwd (fa_fwd) and bwd (fa_bwd_preprocess + fa_bwd_grads) from {nb} further calls of "
+                     "each, L2 flushed before each; kernels_ms and the roofline from another pass of the same "
+                     "calls with an event between every two kernels.  The timed step (fa_fwd_bwd) does the "
+                     "preprocessing in the forward's epilogue instead of bwd_pre",
         "path": prob.path,
         "roofline": head["roofline"],
         "dq_strategy": head["dq_strategy"],

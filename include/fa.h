@@ -72,7 +72,8 @@ typedef enum {
     FA_ERR_LAUNCH = 7,               /* CUDA launch or descriptor error                 */
     FA_ERR_TIMEOUT = 8,              /* a device-side bounded wait ran out              */
     FA_ERR_NO_DEVICE = 9,            /* no usable CUDA device                           */
-    FA_ERR_BAD_ARG = 10              /* other invalid argument (is_causal, scale)       */
+    FA_ERR_BAD_ARG = 10,             /* other invalid argument (is_causal, scale)       */
+    FA_ERR_BOUNDS = 11               /* debug build: an in-kernel bounds check failed   */
 } fa_status;
 
 typedef enum {
@@ -138,12 +139,16 @@ FA_API fa_status fa_bwd_grads(const void *Q, const void *K, const void *V, const
 /*
  * Forward then backward in one call: the unit the field guide's §1.3.3
  * leaderboard times (a forward plus backward at a fixed configuration, with a
- * given dO).  Writes O and L, then dQ, dK and dV; the same results, bit for
- * bit, as fa_fwd followed by fa_bwd on the same stream, but every argument of
- * both passes is checked before the first launch, and the kernels (forward,
- * D-preprocess, gradients: three on the tensor-core path, four on the CUDA-core
- * one) go out back to back -- on the tensor-core path each starting while its
- * predecessor drains.  Contiguous layout; `workspace` as for fa_bwd.
+ * given dO).  Writes O and L, then dQ, dK and dV.  Every argument of both
+ * passes is checked before the first launch.  On the tensor-core path dO is
+ * known to the forward, so its epilogue also forms D = rowsum(dO * O) from the
+ * unrounded fp32 O (not from O rounded to the input dtype, as fa_bwd must) and
+ * stages the backward's row constants: no preprocessing kernel runs, and the
+ * kernels (forward, gradients, plus the dQ conversion when dQ is formed by
+ * reduction) go out back to back, each starting while its predecessor drains.
+ * O, L and dV are bit for bit those of fa_fwd followed by fa_bwd; dQ and dK
+ * differ from them only through that more accurate D.  The CUDA-core path runs
+ * fa_fwd then fa_bwd (four kernels).  Contiguous layout; `workspace` as for fa_bwd.
  */
 FA_API fa_status fa_fwd_bwd(const void *Q, const void *K, const void *V, const void *dO,
                             void *O, float *L, void *dQ, void *dK, void *dV,
@@ -297,6 +302,26 @@ FA_API void fa_set_wait_limit(uint32_t spins);
  * undefined.  For testing the failure path without faulting the GPU.
  */
 FA_API void fa_debug_force_stall(int on);
+
+/*
+ * Debug build.  libfa_debug.so is the same library compiled with FA_DEBUG: its
+ * kernels check, before each tile load and each store of a row, that the index
+ * lies inside its tensor and (causal) on or below the diagonal; a failed check
+ * records a bit that fa_get_device_status reports as FA_ERR_BOUNDS, skips the
+ * access and ends the kernel's waits (never a trap).  It also counts the tile
+ * rows that the kernels load.  The release library (libfa.so) carries neither.
+ */
+FA_API int fa_debug_build(void);   /* 1 in libfa_debug.so, 0 in libfa.so */
+/*
+ * Rows of tiles loaded since the last reset (debug build; zeros otherwise):
+ *   out[0]  key rows the forward loaded (K; V follows tile for tile),
+ *   out[1]  query rows the backward's dK/dV work items loaded (Q; dO alike),
+ *   out[2]  key rows the backward's dQ work items loaded (K; V alike).
+ * A tile counts with its full height (128 rows; 64 for the d = 128 backward's
+ * sub-tiles), ragged ends included.  Synchronises `stream`; n entries (at most 3).
+ */
+FA_API fa_status fa_debug_tile_rows(unsigned long long *out, int n, fa_stream_t stream);
+FA_API fa_status fa_debug_reset_tile_rows(fa_stream_t stream);
 
 FA_API const char *fa_status_string(fa_status s);
 

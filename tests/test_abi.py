@@ -34,8 +34,21 @@ def test_library_exports_every_declared_symbol(L):
     assert not hasattr(L, "simt_fwd")
 
 
+def test_debug_library_exports_the_same_symbols_and_says_so(L):
+    """libfa_debug.so (FA_DEBUG: in-kernel bounds checks, tile-load counters) exports
+    the same functions; fa_debug_build tells the two apart."""
+    from tiled_attention_04_gb300 import binding
+    with binding.debug_library() as D:
+        for name in declared_functions():
+            assert hasattr(D, name), name
+        assert not hasattr(D, "simt_fwd")
+        assert D.fa_debug_build() == 1
+    assert L.fa_debug_build() == 0
+    assert binding.lib() is L
+
+
 def test_status_strings(L):
-    for s in range(11):
+    for s in range(12):
         assert L.fa_status_string(s)
     assert L.fa_status_string(99) == b"unknown status"
 

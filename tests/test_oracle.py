@@ -326,16 +326,19 @@ def _bf16(x):
     return inputs.bf16_bits_to_f64(inputs.to_bf16_bits(x))
 
 
-def _rounded_backward(t, causal, scale, mistake=None):
-    """dQ, dK with the two bf16 roundings of the kernel's backward modelled in fp64:
-    D from the bf16-rounded O, dS rounded to bf16 before its two products.
-    `mistake` plants an error a kernel could make (on the CPU, in this model)."""
+def _rounded_backward(t, causal, scale, mistake=None, o_rounded=True):
+    """dQ, dK with the bf16 roundings of the kernels modelled in fp64: P rounded
+    before O = P V, D from that O (rounded to bf16 when o_rounded), dS rounded to
+    bf16 before its two products.  `mistake` plants an error a kernel could make
+    (on the CPU, in this model)."""
     Q, K, V, dO = (x.exact for x in t)
-    _, _, _, O, _, _ = oracle.attn_bwd_ref(Q, K, V, dO, scale, causal)
     dQ, dK = np.empty_like(Q), np.empty_like(K)
     for b in range(Q.shape[0]):
         P, _ = oracle.attn_probs_ref(Q[b], K[b], scale, causal)
-        D = (dO[b] * _bf16(O[b])).sum(axis=1)
+        O = _bf16(P) @ V[b]
+        if o_rounded:
+            O = _bf16(O)
+        D = (dO[b] * O).sum(axis=1)
         if mistake == "no_D":
             D = np.zeros_like(D)
         dS = _bf16(P * (dO[b] @ V[b].T - D[:, None]))
@@ -345,15 +348,17 @@ def _rounded_backward(t, causal, scale, mistake=None):
     return dQ, dK
 
 
+@pytest.mark.parametrize("o_rounded", [True, False])
 @pytest.mark.parametrize("scale,d", [(0.25, 64), (1.0, 64), (1.0, 16), (2.0, 128)])
-def test_bf16_rounding_bound_holds_for_the_rounding_model(scale, d):
-    """The bound used by the bf16 large-scale GPU parity test contains the error of
-    the two roundings it models, at a margin (the bound is worst-case)."""
+def test_bf16_rounding_bound_holds_for_the_rounding_model(scale, d, o_rounded):
+    """The bound used by the bf16 large-scale GPU parity tests contains the error of
+    the roundings it models, at a margin (the bound is worst-case), for D from
+    the stored bf16 O (fa_bwd) and from the forward's fp32 O (fused call)."""
     from bf16_bound import rounding_bound
     t = inputs.make_custom(2, 160, 160, d, "bf16", seed=60 + d)
     dQ, dK, _, _, _, _ = oracle.attn_bwd_ref(*(x.exact for x in t), scale, True)
-    gQ, gK = _rounded_backward(t, True, scale)
-    EQ, EK = rounding_bound(t, True, scale)
+    gQ, gK = _rounded_backward(t, True, scale, o_rounded=o_rounded)
+    EQ, EK = rounding_bound(t, True, scale, o_rounded=o_rounded)
     assert (np.abs(gQ - dQ) <= EQ + 1e-12).all()
     assert (np.abs(gK - dK) <= EK + 1e-12).all()
     assert np.abs(gQ - dQ).max() > 0.05 * EQ.max()   # the bound is not vacuous

@@ -7,18 +7,20 @@ there is no fallback of any kind, and a missing library is an error.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfa.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "libfa_debug.so")
 
 FA_OK = 0
 STATUS = {
     0: "FA_OK", 1: "FA_ERR_NULL_PTR", 2: "FA_ERR_BAD_SHAPE", 3: "FA_ERR_UNSUPPORTED_HEAD_DIM",
     4: "FA_ERR_UNSUPPORTED_DTYPE", 5: "FA_ERR_MISALIGNED", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_LAUNCH",
-    8: "FA_ERR_TIMEOUT", 9: "FA_ERR_NO_DEVICE", 10: "FA_ERR_BAD_ARG",
+    8: "FA_ERR_TIMEOUT", 9: "FA_ERR_NO_DEVICE", 10: "FA_ERR_BAD_ARG", 11: "FA_ERR_BOUNDS",
 }
 FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
 FA_DQ_AUTO, FA_DQ_SEPARATE_PASS, FA_DQ_REDUCTION = 0, 1, 2
@@ -28,7 +30,8 @@ EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa
            "fa_bwd_grads", "fa_fwd_strided", "fa_bwd_strided", "fa_fwd_bwd",
            "fa_bwd_noalloc", "fa_noalloc_scratch_bytes", "fa_path_name", "fa_set_dq_strategy",
            "fa_bwd_dq_strategy", "fa_get_device_status",
-           "fa_reset_device_status", "fa_set_wait_limit", "fa_debug_force_stall", "fa_status_string")
+           "fa_reset_device_status", "fa_set_wait_limit", "fa_debug_force_stall", "fa_debug_build",
+           "fa_debug_tile_rows", "fa_debug_reset_tile_rows", "fa_status_string")
 
 _lib = None
 
@@ -45,13 +48,37 @@ class FaError(RuntimeError):
 
 
 def lib() -> ctypes.CDLL:
-    """Load the in-tree libfa.so (built by __graft_entry__.build())."""
+    """The library every call of this module goes to: the in-tree libfa.so (built by
+    __graft_entry__.build()), or libfa_debug.so inside a debug_library() block."""
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
-    L = ctypes.CDLL(LIB_PATH)
+    _lib = _load(LIB_PATH)
+    return _lib
+
+
+_debug_lib = None
+
+
+@contextlib.contextmanager
+def debug_library():
+    """Within the block, this module's calls go to libfa_debug.so (the same library
+    built with FA_DEBUG: in-kernel bounds checks and tile-load counters)."""
+    global _lib, _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _load(DEBUG_LIB_PATH)
+    prev = lib()
+    _lib = _debug_lib
+    try:
+        yield _debug_lib
+    finally:
+        _lib = prev
+
+
+def _load(path) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build()")
+    L = ctypes.CDLL(path)
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     L.fa_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
@@ -84,11 +111,16 @@ def lib() -> ctypes.CDLL:
     L.fa_debug_force_stall.restype = None
     L.fa_status_string.argtypes = [i]
     L.fa_status_string.restype = ctypes.c_char_p
+    L.fa_debug_build.argtypes = []
+    L.fa_debug_build.restype = i
+    L.fa_debug_tile_rows.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i, vp]
+    L.fa_debug_tile_rows.restype = i
+    L.fa_debug_reset_tile_rows.argtypes = [vp]
+    L.fa_debug_reset_tile_rows.restype = i
     for name in ("fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_grads",
                  "fa_fwd_strided", "fa_bwd_strided", "fa_fwd_bwd", "fa_get_device_status",
                  "fa_reset_device_status"):
         getattr(L, name).restype = ctypes.c_int
-    _lib = L
     return L
 
 
@@ -396,3 +428,14 @@ def fa_set_wait_limit(spins: int):
 
 def fa_debug_force_stall(on: bool):
     lib().fa_debug_force_stall(1 if on else 0)
+
+
+def debug_tile_rows(stream=None):
+    """fa_debug_tile_rows: [forward key rows, dK/dV-item query rows, dQ-item key rows] loaded."""
+    out = (ctypes.c_ulonglong * 3)()
+    check(lib().fa_debug_tile_rows(out, 3, _stream(stream)), "fa_debug_tile_rows")
+    return [int(x) for x in out]
+
+
+def debug_reset_tile_rows(stream=None):
+    check(lib().fa_debug_reset_tile_rows(_stream(stream)), "fa_debug_reset_tile_rows")

@@ -260,6 +260,7 @@ const char *fa_status_string(fa_status s) {
         case FA_ERR_TIMEOUT: return "device-side wait timed out";
         case FA_ERR_NO_DEVICE: return "no CUDA device";
         case FA_ERR_BAD_ARG: return "bad argument";
+        case FA_ERR_BOUNDS: return "debug build: a kernel bounds check failed";
     }
     return "unknown status";
 }
@@ -415,8 +416,23 @@ fa_status fa_fwd_bwd(const void *Q, const void *K, const void *V, const void *dO
     if (s != FA_OK) return s;
     if ((long long)p.BH * p.Nq == 0 && (long long)p.BH * p.Nk == 0) return FA_OK;
     if ((s = bwd_ptrs(p, Q, K, V, O, dO, L, dQ, dK, dV)) != FA_OK) return s;
-    if ((s = run_fwd(p, Q, K, V, O, L, stream)) != FA_OK) return s;
-    if ((s = run_preprocess(p, w, O, dO, L, workspace, stream)) != FA_OK) return s;
+    bool prep_done = false;
+    if (w.tc && (long long)p.BH * p.Nq > 0) {
+        // tensor-core path: the forward's epilogue also forms D = rowsum(dO * O) from
+        // the unrounded O and stages the backward's row constants (no preprocessing kernel)
+        if ((s = device_ok()) != FA_OK) return s;
+        char *ws = static_cast<char *>(workspace);
+        FwdPrep prep{};
+        prep.dO = dO;
+        prep.sdo = p.sdO;
+        prep.Dp = reinterpret_cast<float *>(ws + w.d_off);
+        prep.Lp = reinterpret_cast<float *>(ws + w.l_off);
+        prep.dQa = w.red ? reinterpret_cast<float *>(ws + w.dqa_off) : nullptr;
+        if ((s = map_cuda(tc_fwd(p, Q, K, V, O, L, as_stream(stream), &prep, &prep_done))) != FA_OK) return s;
+    } else if ((s = run_fwd(p, Q, K, V, O, L, stream)) != FA_OK) {
+        return s;
+    }
+    if (!prep_done && (s = run_preprocess(p, w, O, dO, L, workspace, stream)) != FA_OK) return s;
     return run_grads(p, w, Q, K, V, dO, L, dQ, dK, dV, workspace, stream);
 }
 
@@ -427,7 +443,35 @@ fa_status fa_get_device_status(fa_stream_t stream) {
     if (e != cudaSuccess) return FA_ERR_LAUNCH;
     unsigned a = 0, b = 0;
     if (tc_fwd_read_status(&a, st) != cudaSuccess || tc_bwd_read_status(&b, st) != cudaSuccess) return FA_ERR_LAUNCH;
+    if ((a | b) & 0x100u) return FA_ERR_BOUNDS;   // a failed check also ends the kernel's waits
     return (a | b) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+int fa_debug_build(void) {
+#ifdef FA_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+fa_status fa_debug_tile_rows(unsigned long long *out, int n, fa_stream_t stream) {
+    if (!out || n < 0) return FA_ERR_BAD_ARG;
+    if (device_ok() != FA_OK) return FA_ERR_NO_DEVICE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    unsigned long long v[3] = {0, 0, 0};
+    if (tc_fwd_read_rows(&v[0], st) != cudaSuccess || tc_bwd_read_rows(&v[1], st) != cudaSuccess) return FA_ERR_LAUNCH;
+    for (int i = 0; i < n && i < 3; ++i) out[i] = v[i];
+    return FA_OK;
+}
+
+fa_status fa_debug_reset_tile_rows(fa_stream_t stream) {
+    if (device_ok() != FA_OK) return FA_ERR_NO_DEVICE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = tc_fwd_reset_rows(st);
+    if (e == cudaSuccess) e = tc_bwd_reset_rows(st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return map_cuda(e);
 }
 
 fa_status fa_reset_device_status(fa_stream_t stream) {

@@ -71,8 +71,20 @@ int tc_sm_count();
 // (16 and 32 run the d = 64 kernels with zero-filled columns).
 bool tc_fwd_supported(const FaProblem &p);
 bool tc_bwd_supported(const FaProblem &p);
+// The backward's preprocessing done by the forward's epilogue when dO is known
+// up front (the fused forward + backward call): D = rowsum(dO * O) from the
+// unrounded fp32 O, and -D, -L*log2(e) written to the tensor-core backward's
+// workspace rows (padding rows 0 and -inf), the dQ accumulator rows cleared.
+struct FwdPrep {
+    const void *dO;   // NULL: no preprocessing
+    FaStrides sdo;
+    float *Dp, *Lp;   // per batch*head, padded_rows(Nq) rows
+    float *dQa;       // NULL unless dQ is formed by reduction
+};
+// Forward.  With prep (dO not NULL) the forward's epilogue also does the
+// backward's preprocessing (*prep_done tells whether it did).
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
-                   cudaStream_t st);
+                   cudaStream_t st, const FwdPrep *prep = nullptr, bool *prep_done = nullptr);
 // backward workspace on this path: per batch*head, padded_rows(Nq) fp32 D then the same
 // of L*log2(e); when dQ is formed by reduction, then an fp32 dQ accumulator of
 // padded_rows(Nq) x max(d, 64) per batch*head
@@ -102,3 +114,9 @@ cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st);
 cudaError_t tc_bwd_read_status(unsigned *out, cudaStream_t st);
 cudaError_t tc_fwd_reset_status(cudaStream_t st);
 cudaError_t tc_bwd_reset_status(cudaStream_t st);
+// debug build: tile rows loaded (forward: key rows; backward: query rows of the
+// dK/dV items, key rows of the dQ items), read (synchronising) and reset
+cudaError_t tc_fwd_read_rows(unsigned long long *out, cudaStream_t st);
+cudaError_t tc_fwd_reset_rows(cudaStream_t st);
+cudaError_t tc_bwd_read_rows(unsigned long long *out, cudaStream_t st);
+cudaError_t tc_bwd_reset_rows(cudaStream_t st);

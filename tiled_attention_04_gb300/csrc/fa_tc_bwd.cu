@@ -53,6 +53,8 @@
 #include "tc_common.cuh"
 
 __device__ unsigned g_fa_bwd_status;
+// debug build: query rows the dK/dV items loaded, key rows the dQ items loaded
+__device__ unsigned long long g_fa_bwd_rows[2];
 
 namespace {
 
@@ -202,8 +204,10 @@ struct DkdvWideCfg {
     // sub-tile in shared memory (bf16, [128 keys x 128 B] per 64 queries, swizzled),
     // read by two MMAs -- as dS^T (K-major A of dK) and as dS (MN-major A of dQ) --
     // and the dQ partial of a sub-tile staged as fp32 [128 rows x 32 columns] boxes
-    // for the TMA reduction.  (A second staging buffer, which costs a stage of the
-    // Q / dO ring, measured slower: 54.9 -> 60.9 us at batch 8, N = 4096.)
+    // for the TMA reduction.  Measured alternatives at batch 8, N = 4096 (gradient
+    // launch 54.9 us as built): a second staging buffer, which costs a stage of the
+    // Q / dO ring, 60.9 us; the two idle warps issuing red.global.add.v4.f32 from
+    // the staged rows instead of the TMA reduction, 58.2 us.
     static constexpr uint32_t DS_OFF = LD_OFF + STAGES * 1024;
     static constexpr uint32_t DQS_OFF = DS_OFF + (RED ? 2 * 128 * 128 : 0);
     static constexpr uint32_t DQS_BOX = 128 * 128;                       // bytes of one staged box
@@ -310,17 +314,23 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         if (lane == 0 && n > 0) {
             tc::tma_prefetch_desc(&tmQ);
             tc::tma_prefetch_desc(&tmdO);
-            tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
-            for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_rows<VIEW4>(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
-                tc::tma_load_rows<VIEW4>(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
+            const bool kv_ok = tc::in_bounds(k0 < Nk, &g_fa_bwd_status, abort_flag);
+            if (kv_ok) {
+                tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
+                for (int c = 0; c < D / 64; ++c) {
+                    tc::tma_load_rows<VIEW4>(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
+                    tc::tma_load_rows<VIEW4>(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
+                }
             }
             int issued = 0;
-            for (int it = 0; it < n; ++it) {
+            for (int it = 0; kv_ok && it < n; ++it) {
                 const int s = it % C::STAGES;
                 const uint32_t ph = (it / C::STAGES) & 1;
                 if (!W.wait(q_empty(s), ph ^ 1u)) break;
                 const int q0 = (i_begin + it) * C::BQ;
+                // debug build: a query sub-tile past the queries, or wholly on the
+                // masked side of the diagonal, is never loaded
+                if (!tc::in_bounds(q0 < Nq && (!CAUSAL || q0 + C::BQ - 1 >= k0), &g_fa_bwd_status, abort_flag)) break;
                 tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 1024);
                 for (int c = 0; c < D / 64; ++c) {
                     tc::tma_load_rows<VIEW4>(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
@@ -333,14 +343,16 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                 tc::bulk_load(base + C::LD_OFF + s * 1024 + 512, Dp + off, 512, q_full(s));
                 issued = it + 1;
             }
+            if constexpr (tc::kDebug) atomicAdd(&g_fa_bwd_rows[0], (unsigned long long)issued * C::BQ);
             if (*abort_flag) {
                 for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it) {
                     const int s = it % C::STAGES;
                     for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full(s), (it / C::STAGES) & 1); ++i) {
                     }
                 }
-                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full, 0); ++i) {
-                }
+                if (kv_ok)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full, 0); ++i) {
+                    }
             }
         }
     } else if (RED && warp == 2) {
@@ -351,6 +363,7 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
             for (int it = 0; it < n; ++it) {
                 if (!W.wait(dq_staged, it & 1)) break;
                 const int q0 = (i_begin + it) * C::BQ;
+                if (!tc::in_bounds(q0 + C::BQ <= nqp, &g_fa_bwd_status, abort_flag)) break;
 #pragma unroll
                 for (int x = 0; x < D / 32; ++x)
                     tc::tma_reduce_add_3d(tmdQa, base + C::DQS_OFF + x * C::DQS_BOX, 32 * x, q0, bh);
@@ -761,15 +774,21 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
         if (lane == 0) {
             tc::tma_prefetch_desc(&tmK);
             tc::tma_prefetch_desc(&tmV);
-            tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
-            for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
-                tc::tma_load_rows<VIEW4>(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
+            const bool q_ok = tc::in_bounds(q0 < Nq, &g_fa_bwd_status, abort_flag);
+            if (q_ok) {
+                tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
+                for (int c = 0; c < D / 64; ++c) {
+                    tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
+                    tc::tma_load_rows<VIEW4>(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
+                }
             }
             int issued = 0;
-            for (int j = 0; j < n; ++j) {
+            for (int j = 0; q_ok && j < n; ++j) {
                 const int s = j % C::STAGES;
                 if (!W.wait(kv_empty(s), ((j / C::STAGES) & 1) ^ 1u)) break;
+                // debug build: a key sub-tile past the keys, or wholly above the diagonal, is never loaded
+                const int kj = (jb + j) * C::BK;
+                if (!tc::in_bounds(kj < Nk && (!CAUSAL || kj <= q0 + C::BQ - 1), &g_fa_bwd_status, abort_flag)) break;
                 tc::mbar_arrive_expect_tx(kv_full(s), 2 * C::KT::BYTES);
                 for (int c = 0; c < D / 64; ++c) {
                     tc::tma_load_rows<VIEW4>(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
@@ -779,14 +798,16 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
                 }
                 issued = j + 1;
             }
+            if constexpr (tc::kDebug) atomicAdd(&g_fa_bwd_rows[1], (unsigned long long)issued * C::BK);
             if (*abort_flag) {
                 for (int j = issued - 1; j >= 0 && j >= issued - C::STAGES; --j) {
                     const int s = j % C::STAGES;
                     for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full(s), (j / C::STAGES) & 1); ++i) {
                     }
                 }
-                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
-                }
+                if (q_ok)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
+                    }
             }
         }
     } else if (warp == 1) {
@@ -1105,17 +1126,23 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
         if (lane == 0 && n > 0) {
             tc::tma_prefetch_desc(&tmQ);
             tc::tma_prefetch_desc(&tmdO);
-            tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
-            for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_rows<VIEW4>(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
-                tc::tma_load_rows<VIEW4>(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
+            const bool kv_ok = tc::in_bounds(k0 < Nk, &g_fa_bwd_status, abort_flag);
+            if (kv_ok) {
+                tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
+                for (int c = 0; c < D / 64; ++c) {
+                    tc::tma_load_rows<VIEW4>(base + C::K_OFF + c * C::KT::CHUNK, &tmK, kv_full, c * 64, k0, bh, H);
+                    tc::tma_load_rows<VIEW4>(base + C::V_OFF + c * C::KT::CHUNK, &tmV, kv_full, c * 64, k0, bh, H);
+                }
             }
             int issued = 0;
-            for (int it = 0; it < n; ++it) {
+            for (int it = 0; kv_ok && it < n; ++it) {
                 const int s = it % C::STAGES;
                 const uint32_t ph = (it / C::STAGES) & 1;
                 if (!W.wait(q_empty(s), ph ^ 1u)) break;
                 const int q0 = (i_begin + it) * C::BQ;
+                // debug build: a query sub-tile past the queries, or wholly on the
+                // masked side of the diagonal, is never loaded
+                if (!tc::in_bounds(q0 < Nq && (!CAUSAL || q0 + C::BQ - 1 >= k0), &g_fa_bwd_status, abort_flag)) break;
                 tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 512);
                 for (int c = 0; c < D / 64; ++c) {
                     tc::tma_load_rows<VIEW4>(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
@@ -1128,14 +1155,16 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                 tc::bulk_load(base + C::LD_OFF + s * 512 + 256, Dp + off, 256, q_full(s));
                 issued = it + 1;
             }
+            if constexpr (tc::kDebug) atomicAdd(&g_fa_bwd_rows[0], (unsigned long long)issued * C::BQ);
             if (*abort_flag) {
                 for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it) {
                     const int s = it % C::STAGES;
                     for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full(s), (it / C::STAGES) & 1); ++i) {
                     }
                 }
-                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full, 0); ++i) {
-                }
+                if (kv_ok)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full, 0); ++i) {
+                    }
             }
         }
     } else if (warp == 1) {
@@ -1451,15 +1480,21 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
         if (lane == 0) {
             tc::tma_prefetch_desc(&tmK);
             tc::tma_prefetch_desc(&tmV);
-            tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
-            for (int c = 0; c < D / 64; ++c) {
-                tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
-                tc::tma_load_rows<VIEW4>(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
+            const bool q_ok = tc::in_bounds(q0 < Nq, &g_fa_bwd_status, abort_flag);
+            if (q_ok) {
+                tc::mbar_arrive_expect_tx(q_full, 2 * C::QT::BYTES);
+                for (int c = 0; c < D / 64; ++c) {
+                    tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::QT::CHUNK, &tmQ, q_full, c * 64, q0, bh, H);
+                    tc::tma_load_rows<VIEW4>(base + C::DO_OFF + c * C::QT::CHUNK, &tmdO, q_full, c * 64, q0, bh, H);
+                }
             }
             int issued = 0;
-            for (int j = 0; j < n; ++j) {
+            for (int j = 0; q_ok && j < n; ++j) {
                 const int s = j % C::STAGES;
                 if (!W.wait(kv_empty(s), ((j / C::STAGES) & 1) ^ 1u)) break;
+                // debug build: a key sub-tile past the keys, or wholly above the diagonal, is never loaded
+                const int kj = (jb + j) * C::BK;
+                if (!tc::in_bounds(kj < Nk && (!CAUSAL || kj <= q0 + C::BQ - 1), &g_fa_bwd_status, abort_flag)) break;
                 tc::mbar_arrive_expect_tx(kv_full(s), 2 * C::KT::BYTES);
                 for (int c = 0; c < D / 64; ++c) {
                     tc::tma_load_rows<VIEW4>(base + C::K_OFF + s * C::KT::BYTES + c * C::KT::CHUNK, &tmK, kv_full(s), c * 64,
@@ -1469,14 +1504,16 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                 }
                 issued = j + 1;
             }
+            if constexpr (tc::kDebug) atomicAdd(&g_fa_bwd_rows[1], (unsigned long long)issued * C::BK);
             if (*abort_flag) {
                 for (int j = issued - 1; j >= 0 && j >= issued - C::STAGES; --j) {
                     const int s = j % C::STAGES;
                     for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full(s), (j / C::STAGES) & 1); ++i) {
                     }
                 }
-                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
-                }
+                if (q_ok)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
+                    }
             }
         }
     } else if (warp == 1) {
@@ -1965,6 +2002,18 @@ cudaError_t tc_bwd_read_status(unsigned *out, cudaStream_t st) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fa_bwd_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     return e;
+}
+
+cudaError_t tc_bwd_read_rows(unsigned long long *out, cudaStream_t st) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fa_bwd_rows, 2 * sizeof(unsigned long long), 0,
+                                              cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e;
+}
+
+cudaError_t tc_bwd_reset_rows(cudaStream_t st) {
+    static const unsigned long long zero[2] = {0, 0};
+    return cudaMemcpyToSymbolAsync(g_fa_bwd_rows, zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
 }
 
 cudaError_t tc_bwd_reset_status(cudaStream_t st) {

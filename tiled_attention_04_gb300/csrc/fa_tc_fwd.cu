@@ -73,6 +73,7 @@
 #include "tc_common.cuh"
 
 __device__ unsigned g_fa_fwd_status;
+__device__ unsigned long long g_fa_fwd_rows;   // debug build: key rows the forward loaded
 
 namespace {
 
@@ -81,6 +82,7 @@ constexpr int BN = 128;          // keys per tile
 constexpr int NTHREADS = 384;    // 12 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int D>
@@ -101,14 +103,18 @@ struct FwdCfg {
     static constexpr uint32_t K_OFF = Q_OFF + TILE_BYTES;
     static constexpr uint32_t V_OFF = K_OFF + KST * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = V_OFF + VST * TILE_BYTES;
-    static constexpr int NBAR = 1 + KST + VST + R + 11;
+    static constexpr int NBAR = 1 + KST + VST + R + 12;
     // per-row (m, l) of both warpgroups, double-buffered by work unit: 2 x (256 + 256) floats
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t MISC_OFF = STAT_OFF + 2 * 512 * 4;
-    static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;                  // peer_free, peer_ready
+    static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;                  // peer_free, peer_ready, peer_d
     // persistent kernel: per softmax thread, the element offset of its output row in the current unit
-    static constexpr uint32_t OROW_OFF = PEER_BAR_OFF + 16;
-    static constexpr uint32_t USED = OROW_OFF + 256 * 8;
+    static constexpr uint32_t OROW_OFF = PEER_BAR_OFF + 32;
+    // fused backward preprocessing: the two halves of each row's rowsum(dO * O)
+    // (double-buffered by work unit in the persistent kernel; the split form's
+    // rank 1 stores its half into rank 0's copy)
+    static constexpr uint32_t DSUM_OFF = OROW_OFF + 256 * 8;
+    static constexpr uint32_t USED = DSUM_OFF + 2 * 256 * 4;
     // split items: rank 1's partial O (fp32, rows padded by 4 floats) and its m, l, in the K ring
     static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
     static constexpr uint32_t PART_OFF = K_OFF;
@@ -125,12 +131,65 @@ struct FwdCfg {
     static constexpr uint32_t P_STRIDE = SEP_P ? 64 : 128;
 };
 
+// ------------------------------------------------------------------ fused backward preprocessing
+// Half of rowsum(dO * O) for one query row: this thread's D/2 output columns of
+// the unrounded fp32 O (vals * inv) against the same columns of dO.
+template <int D, bool VIEW4>
+__device__ __forceinline__ float prep_half_rowsum(const FwdPrep &prep, const float *vals, float inv, int bh, int row,
+                                                  int Nq, int H, int dv, int t) {
+    const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(prep.dO);
+    if constexpr (VIEW4) g += fa_row_offset(prep.sdo, H, bh, row) + t * (D / 2);
+    else g += ((size_t)bh * Nq + row) * D + t * (D / 2);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+        if (!VIEW4 || t * (D / 2) + 8 * c < dv) {   // columns past a head dim below 64 are padding
+            const uint4 x = __ldg(reinterpret_cast<const uint4 *>(g) + c);
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&x);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = __bfloat1622float2(h[k]);
+                acc = fmaf(vals[8 * c + 2 * k] * inv, f.x, acc);
+                acc = fmaf(vals[8 * c + 2 * k + 1] * inv, f.y, acc);
+            }
+        }
+    }
+    return acc;
+}
+
+// The backward's per-row constants from the forward's epilogue: -D (half0 +
+// half1) and -L*log2(e), L exactly as stored (padding rows: 0 and -inf, so
+// their P is exactly zero); and this warpgroup's half of the row's dQ
+// accumulator cleared (d <= 64 kernels, when dQ is formed by reduction).
+template <int D>
+__device__ __forceinline__ void prep_row_finish(const FwdPrep &prep, float half0, float half1, bool write_consts,
+                                                float Mrow, float lrow, int bh, int row, int Nq, int t) {
+    const size_t gr = (size_t)bh * ((Nq + 127) / 128 * 128) + row;
+    if (write_consts) {
+        if (row < Nq) {
+            const float L = Mrow * kLn2 + logf(lrow);
+            prep.Dp[gr] = -(half0 + half1);
+            prep.Lp[gr] = -L * kLog2e;
+        } else {
+            prep.Dp[gr] = 0.f;
+            prep.Lp[gr] = -INFINITY;
+        }
+    }
+    if constexpr (D == 64) {
+        if (prep.dQa) {
+            float4 *z = reinterpret_cast<float4 *>(prep.dQa + gr * 64 + t * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
 template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
-                     uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so) {
+                     uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so, FwdPrep prep) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -183,6 +242,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (SPLIT > 1) {
             tc::mbar_init(base + C::PEER_BAR_OFF, 256);       // peer_free: the peer's 256 softmax threads
             tc::mbar_init(base + C::PEER_BAR_OFF + 8, 128);   // peer_ready: the peer's 128 senders
+            tc::mbar_init(base + C::PEER_BAR_OFF + 16, 128);  // peer_d: rank 1's half rowsums (fused preprocessing)
         }
         *abort_flag = 0u;
         tc::fence_mbar_init();
@@ -210,9 +270,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::tma_prefetch_desc(&tmQ);
             tc::tma_prefetch_desc(&tmK);
             tc::tma_prefetch_desc(&tmV);
-            tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
-            for (int c = 0; c < C::CHUNKS; ++c)
-                tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh, H);
+            const bool q_ok = tc::in_bounds(q0 < Nq && bh < BH, &g_fa_fwd_status, abort_flag);
+            if (q_ok) {
+                tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, q0, bh, H);
+            }
             int k_issued = 0, v_issued = 0;
             // The slot of tile j last held tile j - st.  A V slot is free once PV of that
             // tile has completed.  A K slot is read only by S of that tile; with P over S
@@ -220,6 +283,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // K slot is free once PV_{j-st-1} has completed.  (With P in its own columns
             // the K ring is deep enough to keep waiting for PV_{j-st}.)
             auto load = [&](const CUtensorMap *m, uint32_t ring, int st, int j, uint32_t full, int lag) {
+                // debug build: a key tile past the keys, or wholly above the diagonal, is never loaded
+                const int key0 = (jb + j) * BN;
+                if (!tc::in_bounds(key0 < Nk && (!CAUSAL || key0 <= q0 + BM - 1), &g_fa_fwd_status, abort_flag))
+                    return false;
                 const int g = j - st - lag < 0 ? 0 : j - st - lag;
                 if (j >= st && !W.wait(pv_done_bar(g), (g / C::R) & 1)) return false;
                 tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
@@ -229,7 +296,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 return true;
             };
             // order K_0, K_1, V_0, K_2, V_1, ...: the MMA warp uses K_{j+1} before V_j
-            for (int j = 0; j <= n; ++j) {
+            for (int j = 0; q_ok && j <= n; ++j) {
                 if (j < n) {
                     if (!load(&tmK, base + C::K_OFF, C::KST, j, k_full(j % C::KST), C::SEP_P ? 0 : 1)) break;
                     k_issued = j + 1;
@@ -240,6 +307,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     v_issued = v + 1;
                 }
             }
+            if constexpr (tc::kDebug) atomicAdd(&g_fa_fwd_rows, (unsigned long long)k_issued * BN);
             if (*abort_flag) {
                 // let the copies already in flight land before the CTA exits
                 for (int j = k_issued - 1; j >= 0 && j >= k_issued - C::KST; --j)
@@ -248,8 +316,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int j = v_issued - 1; j >= 0 && j >= v_issued - C::VST; --j)
                     for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(v_full(j % C::VST), (j / C::VST) & 1); ++i) {
                     }
-                for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
-                }
+                if (q_ok)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
+                    }
             }
         }
     } else if (warp == 1) {
@@ -459,11 +528,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-        auto store_row = [&](const float *vals, float Mrow, float lrow) {
+        // stores this thread's half row of O (and L); returns the half's part of
+        // rowsum(dO * O) from the unrounded O when the preprocessing is fused
+        auto store_row = [&](const float *vals, float Mrow, float lrow) -> float {
             const float inv = 1.f / lrow;
             __nv_bfloat16 *orow;
             if constexpr (VIEW4) orow = O + fa_row_offset(so, tc::opaque(H), bh, row) + t * (D / 2);
             else orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
+            float part = 0.f;
             if (row < Nq) {
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c) {
@@ -476,7 +548,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         reinterpret_cast<uint4 *>(orow)[c] = q;
                 }
                 if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
+                if (prep.dO) part = prep_half_rowsum<D, VIEW4>(prep, vals, inv, bh, row, Nq, H, dv, t);
             }
+            return part;
         };
         // hand-over waits: bounded, but not cut short by this CTA's own abort flag, so
         // that neither CTA exits while the other may still touch its shared memory
@@ -494,7 +568,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             return false;
         };
         if constexpr (SPLIT == 1) {
-            if (fine) store_row(v, Mc, lc);
+            const float part = fine ? store_row(v, Mc, lc) : 0.f;
+            if (prep.dO) {   // the same for every thread: all 256 reach the barrier
+                float *dsum = reinterpret_cast<float *>(sb + C::DSUM_OFF);
+                dsum[t * 128 + r] = part;
+                tc::named_bar_sync(1, 256);
+                if (fine) prep_row_finish<D>(prep, part, t == 0 ? dsum[128 + r] : 0.f, t == 0, Mc, lc, bh, row, Nq, t);
+            }
         } else {
             // rank r finalises the columns of warpgroup r; the other warpgroup sends its
             // half row and the row's (m, l) into the peer's shared memory with remote
@@ -517,11 +597,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, rank ^ 1u));   // release: the stores above
             } else {
                 const bool got = wait_peer(peer_ready);
-                if (__all_sync(0xffffffffu, fine && got)) {
+                const bool both = __all_sync(0xffffffffu, fine && got);
+                float part = 0.f, M = Mc, lrow = lc;
+                if (both) {
                     const float *prow = reinterpret_cast<const float *>(sb + C::PART_OFF + r * C::PART_STRIDE);
                     const float *ml = reinterpret_cast<const float *>(sb + C::PART_ML_OFF);
                     const float M1 = ml[r], l1 = ml[128 + r];
-                    const float M = fmaxf(Mc, M1);
+                    M = fmaxf(Mc, M1);
                     const float b0 = Mc > -INFINITY ? exp2f(Mc - M) : 0.f;
                     const float b1 = l1 > 0.f ? exp2f(M1 - M) : 0.f;
 #pragma unroll
@@ -532,7 +614,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         v[4 * c + 2] = fmaf(pv.z, b1, v[4 * c + 2] * b0);
                         v[4 * c + 3] = fmaf(pv.w, b1, v[4 * c + 3] * b0);
                     }
-                    store_row(v, M, lc * b0 + l1 * b1);
+                    lrow = lc * b0 + l1 * b1;
+                    part = store_row(v, M, lrow);
+                }
+                if (prep.dO) {
+                    // The row's other half was finalised by the other rank: rank 1 hands
+                    // its half rowsum to rank 0 (always, so that rank 0 never waits in
+                    // vain nor exits before the store lands), and rank 0 writes the
+                    // row's constants.
+                    const uint32_t peer_d = base + C::PEER_BAR_OFF + 16;
+                    if (rank == 1) {
+                        tc::st_cluster_f32(tc::map_to_rank(base + C::DSUM_OFF + 4u * r, 0u), part);
+                        tc::mbar_arrive_remote(tc::map_to_rank(peer_d, 0u));   // release: the store above
+                        if (both) prep_row_finish<D>(prep, part, 0.f, false, M, lrow, bh, row, Nq, t);
+                    } else {
+                        const bool got_d = wait_peer(peer_d);
+                        if (both) {
+                            const float other = got_d ? reinterpret_cast<const float *>(sb + C::DSUM_OFF)[r] : 0.f;
+                            prep_row_finish<D>(prep, part, other, got_d, M, lrow, bh, row, Nq, t);
+                        }
+                    }
                 }
             }
         }
@@ -557,7 +658,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
-                     uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so) {
+                     uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so, FwdPrep prep) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -607,6 +708,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t q_empty = bar(RB + 8);     // S MMAs of the unit done: the Q buffer may be refilled
     const uint32_t o_free = bar(RB + 9);      // epilogue has read O_0, O_1: the next unit may overwrite them
     const uint32_t merge_bar = bar(RB + 10);  // both warpgroups have published their (m, l)
+    const uint32_t dsum_bar = bar(RB + 11);   // both warpgroups have published their half rowsums (fused preprocessing)
     float *stat_sm = reinterpret_cast<float *>(sb + C::STAT_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
     volatile uint32_t *abort_flag = tmem_slot + 1;
@@ -626,6 +728,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::mbar_init(q_empty, 1);
         tc::mbar_init(o_free, 256);
         tc::mbar_init(merge_bar, 256);
+        tc::mbar_init(dsum_bar, 256);
         *abort_flag = 0u;
         tc::fence_mbar_init();
     }
@@ -656,11 +759,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int u = 0; ok && unit_of(u, w); ++u) {
                 // the Q buffer is refilled once the previous unit's S MMAs have completed
                 if (u > 0 && !(ok = W.wait(q_empty, (u - 1) & 1))) break;
+                if (!(ok = tc::in_bounds(w.q0 < Nq && w.bh < BH, &g_fa_fwd_status, abort_flag))) break;
                 tc::mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
                     tc::tma_load_rows<VIEW4>(base + C::Q_OFF + c * C::CHUNK_BYTES, &tmQ, q_full, c * 64, w.q0, w.bh, H);
                 q_issued = u + 1;
                 auto load = [&](const CUtensorMap *m, uint32_t ring, uint32_t st, int g, int key0, uint32_t full) {
+                    // debug build: a key tile past the keys, or wholly above the diagonal, is never loaded
+                    if (!tc::in_bounds(key0 < Nk && (!CAUSAL || key0 <= w.q0 + BM - 1), &g_fa_fwd_status, abort_flag))
+                        return false;
                     // the slot last held tile g - st: wait until PV of that tile has completed
                     if (g >= (int)st && !W.wait(pv_done_bar(g - (int)st), pv_done_par(g - (int)st))) return false;
                     tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
@@ -687,6 +794,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 g0 += w.n;
             }
+            if constexpr (tc::kDebug) atomicAdd(&g_fa_fwd_rows, (unsigned long long)k_issued * BN);
             if (*abort_flag) {
                 // let the copies already in flight land before the CTA exits
                 for (int g = k_issued - 1; g >= 0 && g >= k_issued - C::KST; --g)
@@ -933,11 +1041,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // O_0 and O_1 have been read: the next unit's first PV may overwrite them
             tc::fence_before_sync();
             tc::mbar_arrive(o_free);
-            auto store_row = [&](const float *vals, float Mrow, float lrow) {
+            auto store_row = [&](const float *vals, float Mrow, float lrow) -> float {
                 const float inv = 1.f / lrow;
                 __nv_bfloat16 *orow;
                 if constexpr (VIEW4) orow = O + *orow_sm + t * (D / 2);
                 else orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
+                float part = 0.f;
                 if (row < Nq) {
 #pragma unroll
                     for (int c = 0; c < D / 16; ++c) {
@@ -950,9 +1059,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             reinterpret_cast<uint4 *>(orow)[c] = q;
                     }
                     if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
+                    if (prep.dO) part = prep_half_rowsum<D, VIEW4>(prep, vals, inv, bh, row, Nq, H, dv, t);
                 }
+                return part;
             };
-            if (fine) store_row(v, Mc, lc);
+            const float part = fine ? store_row(v, Mc, lc) : 0.f;
+            if (prep.dO) {
+                // the two halves of the row meet in shared memory (double-buffered by
+                // unit: the merge barrier keeps the warpgroups within one unit)
+                float *dsum = reinterpret_cast<float *>(sb + C::DSUM_OFF) + (u & 1) * 256;
+                dsum[t * 128 + r] = part;
+                tc::mbar_arrive(dsum_bar);
+                const bool got = t == 0 ? W.wait(dsum_bar, u & 1) : true;
+                if (fine) prep_row_finish<D>(prep, part, got && t == 0 ? dsum[128 + r] : 0.f, got && t == 0, Mc, lc, bh,
+                                             row, Nq, t);
+            }
             g0 += n;
             if (!fine) ok = false;
         }
@@ -1141,11 +1262,11 @@ static int sm_count() { return tc_sm_count(); }
 
 template <int D, bool CAUSAL, int SPLIT, bool PERSIST, bool VIEW4>
 static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                              void *O, float *L, cudaStream_t st) {
+                              void *O, float *L, const FwdPrep &prep, cudaStream_t st) {
     static_assert(!(PERSIST && SPLIT > 1), "persistent units are not split");
     using C = FwdCfg<D>;
     void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, __nv_bfloat16 *, float *, int, int, int, int,
-                 float, uint32_t, uint32_t, int, int, FaStrides);
+                 float, uint32_t, uint32_t, int, int, FaStrides, FwdPrep);
     if constexpr (PERSIST) kern = fa_fwd_tc_persistent_kernel<D, CAUSAL, VIEW4>;
     else kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4>;
     cudaError_t e = tc_set_smem_once(reinterpret_cast<const void *>(kern), (int)C::SMEM_BYTES);
@@ -1171,7 +1292,7 @@ static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const C
     cfg.attrs = attr;
     cfg.numAttrs = SPLIT > 1 ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, static_cast<__nv_bfloat16 *>(O), L, p.Nq, p.Nk, p.BH, qtiles,
-                           scale_log2, p.wait_limit, p.force_stall, p.H, p.d, p.sO);
+                           scale_log2, p.wait_limit, p.force_stall, p.H, p.d, p.sO, prep);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1204,42 +1325,59 @@ static FwdMode fwd_mode(const FaProblem &p) {
 
 template <int D, bool CAUSAL, bool VIEW4>
 static cudaError_t launch_fwd_mode(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                                   const CUtensorMap &mv, void *O, float *L, cudaStream_t st) {
+                                   const CUtensorMap &mv, void *O, float *L, const FwdPrep &prep, cudaStream_t st) {
     switch (fwd_mode(p)) {
-        case FwdMode::kSplit: return launch_fwd<D, CAUSAL, 2, false, VIEW4>(p, mq, mk, mv, O, L, st);
-        case FwdMode::kPersist: return launch_fwd<D, CAUSAL, 1, true, VIEW4>(p, mq, mk, mv, O, L, st);
-        default: return launch_fwd<D, CAUSAL, 1, false, VIEW4>(p, mq, mk, mv, O, L, st);
+        case FwdMode::kSplit: return launch_fwd<D, CAUSAL, 2, false, VIEW4>(p, mq, mk, mv, O, L, prep, st);
+        case FwdMode::kPersist: return launch_fwd<D, CAUSAL, 1, true, VIEW4>(p, mq, mk, mv, O, L, prep, st);
+        default: return launch_fwd<D, CAUSAL, 1, false, VIEW4>(p, mq, mk, mv, O, L, prep, st);
     }
 }
 
 template <int D, bool CAUSAL>
 static cudaError_t launch_fwd_any(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                                  const CUtensorMap &mv, void *O, float *L, bool view4, cudaStream_t st) {
-    return view4 ? launch_fwd_mode<D, CAUSAL, true>(p, mq, mk, mv, O, L, st)
-                 : launch_fwd_mode<D, CAUSAL, false>(p, mq, mk, mv, O, L, st);
+                                  const CUtensorMap &mv, void *O, float *L, bool view4, const FwdPrep &prep,
+                                  cudaStream_t st) {
+    return view4 ? launch_fwd_mode<D, CAUSAL, true>(p, mq, mk, mv, O, L, prep, st)
+                 : launch_fwd_mode<D, CAUSAL, false>(p, mq, mk, mv, O, L, prep, st);
 }
 
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
-                   cudaStream_t st) {
+                   cudaStream_t st, const FwdPrep *prep, bool *prep_done) {
     // contiguous tensors keep 3-D (d, N, B*H) maps and plain row addressing; any
     // strided view, or a head dim below 64 (whose rows are narrower than the
     // kernel's), switches the whole launch to 4-D maps and strided rows
     const bool view4 = p.d < 64 || !tc_plain_layout(p, p.sQ, p.Nq) || !tc_plain_layout(p, p.sK, p.Nk) ||
-                       !tc_plain_layout(p, p.sV, p.Nk) || !tc_plain_layout(p, p.sO, p.Nq);
+                       !tc_plain_layout(p, p.sV, p.Nk) || !tc_plain_layout(p, p.sO, p.Nq) ||
+                       (prep && prep->dO && !tc_plain_layout(p, prep->sdo, p.Nq));
     CUtensorMap mq, mk, mv;
     if (!tc_make_map(&mq, Q, p, p.sQ, p.Nq, BM, view4) || !tc_make_map(&mk, K, p, p.sK, p.Nk, BN, view4) ||
         !tc_make_map(&mv, V, p, p.sV, p.Nk, BN, view4))
         return cudaErrorInvalidValue;
-    if (p.d == 128) return p.causal ? launch_fwd_any<128, true>(p, mq, mk, mv, O, L, view4, st)
-                                    : launch_fwd_any<128, false>(p, mq, mk, mv, O, L, view4, st);
-    return p.causal ? launch_fwd_any<64, true>(p, mq, mk, mv, O, L, view4, st)
-                    : launch_fwd_any<64, false>(p, mq, mk, mv, O, L, view4, st);
+    FwdPrep none{};
+    const FwdPrep &pr = (prep && prep->dO) ? *prep : none;
+    if (prep_done) *prep_done = pr.dO != nullptr;   // every kernel form does it
+    if (p.d == 128) return p.causal ? launch_fwd_any<128, true>(p, mq, mk, mv, O, L, view4, pr, st)
+                                    : launch_fwd_any<128, false>(p, mq, mk, mv, O, L, view4, pr, st);
+    return p.causal ? launch_fwd_any<64, true>(p, mq, mk, mv, O, L, view4, pr, st)
+                    : launch_fwd_any<64, false>(p, mq, mk, mv, O, L, view4, pr, st);
 }
 
 cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fa_fwd_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     return e;
+}
+
+cudaError_t tc_fwd_read_rows(unsigned long long *out, cudaStream_t st) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fa_fwd_rows, sizeof(unsigned long long), 0,
+                                              cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e;
+}
+
+cudaError_t tc_fwd_reset_rows(cudaStream_t st) {
+    static const unsigned long long zero = 0;
+    return cudaMemcpyToSymbolAsync(g_fa_fwd_rows, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
 }
 
 cudaError_t tc_fwd_reset_status(cudaStream_t st) {

@@ -21,6 +21,30 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// ------------------------------------------------------------------ debug build
+// FA_DEBUG builds (libfa_debug.so) check tile indices in the kernels and count
+// the tile rows they load; release builds compile both away.
+#ifdef FA_DEBUG
+constexpr bool kDebug = true;
+#else
+constexpr bool kDebug = false;
+#endif
+constexpr unsigned kStatusBounds = 0x100u;   // status-word bit of a failed bounds check
+
+// Debug builds: when cond fails, record the failure in the kernel's status word,
+// raise the CTA's abort flag (so that every bounded wait ends at once) and return
+// false, so that the caller skips the access.  Release builds: always true.
+__device__ __forceinline__ bool in_bounds(bool cond, unsigned *status, volatile uint32_t *abort_flag) {
+    if constexpr (kDebug) {
+        if (!cond) {
+            atomicOr(status, kStatusBounds);
+            if (abort_flag) *abort_flag = 1u;
+            return false;
+        }
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
