@@ -291,9 +291,14 @@ def executed_factor(kernel, strategy):
 # that source is unchanged since the capture it came from (else the key is null).
 KERNEL_SOURCE = {"fwd": "fa_tc_fwd.cu", "bwd_pre": "fa_tc_bwd.cu", "bwd_grads": "fa_tc_bwd.cu"}
 
-# DRAM bytes (read + write) per launch, from one `ncu` capture per workload of the
-# kernel built from the source whose SHA-256 prefix is given.
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per launch, from one `ncu --set full` capture per
+# workload of the kernel built from the source whose SHA-256 prefix is given.
+NCU_TRAFFIC = {
+    ("bench_b8_n4096_d64_causal", "bwd_grads"): (25470976, "2a9c2fe0277c320e"),
+    ("bench_b8_n4096_d64_causal", "fwd"): (16823040, "1c58d8e54de19951"),
+    ("long_n16384_d128_causal", "bwd_grads"): (16977408, "2a9c2fe0277c320e"),
+    ("long_n16384_d128_causal", "fwd"): (16833536, "1c58d8e54de19951"),
+}
 
 
 def _source_sha(kernel):

@@ -168,15 +168,20 @@ FA_API fa_status fa_fwd_bwd(const void *Q, const void *K, const void *V, const v
  * still owns and passes every input and output.  Same arguments, layout and
  * results as fa_bwd.
  *
- *  - Shapes needing more than FA_NOALLOC_SCRATCH_BYTES of workspace (see
- *    fa_bwd_workspace_size) return FA_ERR_WORKSPACE and launch nothing; 8 MiB
- *    covers about one million query rows (B*H*Nq).
+ *  - Where fa_bwd would form dQ by reduction (FA_DQ_REDUCTION: an fp32 dQ
+ *    accumulator of 256 bytes per query row in the workspace) and that does
+ *    not fit, this call forms dQ by the separate pass, whose workspace is 8
+ *    bytes per query row; shapes needing more than FA_NOALLOC_SCRATCH_BYTES
+ *    even so return FA_ERR_WORKSPACE and launch nothing.  8 MiB covers about
+ *    one million query rows (B*H*Nq).
  *  - Every call shares the one array: calls whose GPU work overlaps (other
  *    streams, other host threads) race on it.  Serialise them.
  *  - The array's previous contents never matter: each call writes every
  *    scratch word before reading it.
  *  - The first call on each device looks up the array's address with that
- *    device current; make it before any stream capture starts.
+ *    device current; make it before any stream capture starts.  The address
+ *    is kept for the life of the process: after cudaDeviceReset the array is
+ *    loaded again elsewhere, so do not call this entry point after a reset.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)

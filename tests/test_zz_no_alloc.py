@@ -53,7 +53,28 @@ def test_noalloc_matches_fa_bwd_twice(cuda_lib, bh, n, d, dt, causal):
         if binding.dq_strategy(t_q(t, dev), t_q(t, dev, 1), causal) == binding.FA_DQ_SEPARATE_PASS:
             assert torch.equal(a, b), f"dQ differs from fa_bwd (seed {seed})"
         else:
-            assert bool(((a - b).abs() <= 2.0 ** -7 * torch.maximum(a.abs(), b.abs())).all()), f"dQ (seed {seed})"
+            big = max(a.abs().max().item(), b.abs().max().item())
+            assert bool(((a - b).abs() <= 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 2.0 ** -16 * big).all()), \
+                f"dQ (seed {seed})"
+
+
+def test_noalloc_falls_back_to_the_separate_dq_pass_when_the_accumulator_does_not_fit(cuda_lib):
+    """16 heads of 4096 causal query rows at d = 64: fa_bwd forms dQ by reduction,
+    whose fp32 accumulator (16 MiB) exceeds the 8 MiB array; the no-alloc call
+    forms dQ by the separate pass instead (no accumulator) and gives fa_bwd's
+    results: dK and dV bit for bit, dQ to one bf16 rounding step."""
+    import torch
+    from tiled_attention_04_gb300 import binding
+    t = inputs.make_custom(16, 4096, 4096, 64, "bf16", seed=33)
+    Q, K = t_q(t, torch.device("cuda")), t_q(t, torch.device("cuda"), 1)
+    assert binding.dq_strategy(Q, K, True) == binding.FA_DQ_REDUCTION
+    assert binding.fa_bwd_workspace_size(Q, K, True) > binding.lib().fa_noalloc_scratch_bytes()
+    got, ref = _both(torch, binding, t, True)
+    for name, g, r in zip(("dK", "dV"), got[1:], ref[1:]):
+        assert torch.equal(g, r), name
+    a, b = got[0].double(), ref[0].double()
+    big = max(a.abs().max().item(), b.abs().max().item())
+    assert bool(((a - b).abs() <= 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 2.0 ** -16 * big).all())
 
 
 def test_noalloc_empty_queries_zero_gradients(cuda_lib):

@@ -277,7 +277,7 @@ const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype dtype) {
 
 int fa_set_dq_strategy(int strategy) {
     if (strategy < FA_DQ_AUTO || strategy > FA_DQ_REDUCTION) return -1;
-    const int prev = static_cast<int>(tc_get_dq_strategy());
+    const int prev = static_cast<int>(tc_get_dq_setting());
     tc_set_dq_strategy(static_cast<DqStrategy>(strategy));
     return prev;
 }

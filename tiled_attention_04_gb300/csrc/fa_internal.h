@@ -94,6 +94,9 @@ size_t tc_bwd_ld_rows(const FaProblem &p);
 enum class DqStrategy { kAuto = 0, kSeparatePass = 1, kReduction = 2 };
 void tc_set_dq_strategy(DqStrategy s);
 DqStrategy tc_get_dq_strategy();
+// the strategy for the calling thread's calls until reset with kAuto (overrides the setting)
+void tc_override_dq_strategy(DqStrategy s);
+DqStrategy tc_get_dq_setting();   // the process-wide setting alone
 bool tc_bwd_dq_by_reduction(const FaProblem &p);
 size_t tc_bwd_dqa_floats(const FaProblem &p);   // 0 unless tc_bwd_dq_by_reduction(p)
 // D, L staged (and the dQ accumulator, when dQa is not NULL, cleared)

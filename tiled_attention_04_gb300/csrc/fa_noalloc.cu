@@ -17,8 +17,11 @@
 //    scratch word it later reads, so the previous call's leftovers are harmless;
 //  * the first call on a device looks up the array's device address (with that
 //    device current) and caches it; make that first call before any stream
-//    capture begins;
-//  * shapes whose workspace would exceed FA_NOALLOC_SCRATCH_BYTES are refused
+//    capture begins.  The cache lives as long as the process: cudaDeviceReset
+//    reloads the module (and the array) elsewhere, so no call may follow a reset;
+//  * where the library would form dQ by reduction (an fp32 dQ accumulator in the
+//    workspace) and that does not fit, the call forms dQ by the separate pass;
+//    shapes whose workspace exceeds FA_NOALLOC_SCRATCH_BYTES even so are refused
 //    with FA_ERR_WORKSPACE before anything is launched.
 #include <cuda_runtime.h>
 
@@ -65,17 +68,30 @@ size_t fa_noalloc_scratch_bytes(void) { return FA_NOALLOC_SCRATCH_BYTES; }
 fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *L,
                          void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nk, int d, float scale,
                          int is_causal, fa_dtype dtype, fa_stream_t stream) {
-    const size_t need = fa_bwd_workspace_size(B, H, Nq, Nk, d, is_causal, dtype);
+    size_t need = fa_bwd_workspace_size(B, H, Nq, Nk, d, is_causal, dtype);
     if (need == 0) {
         // unsupported arguments: let fa_bwd name the problem (it launches nothing)
         return fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, nullptr, 0, stream);
     }
-    if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+    // dQ formed by reduction keeps an fp32 dQ accumulator in the workspace; where that
+    // does not fit the array, this call forms dQ by the separate pass, which needs
+    // only the two per-row constants
+    DqStrategy forced = DqStrategy::kAuto;
+    if (need > FA_NOALLOC_SCRATCH_BYTES) {
+        tc_override_dq_strategy(DqStrategy::kSeparatePass);
+        need = fa_bwd_workspace_size(B, H, Nq, Nk, d, is_causal, dtype);
+        tc_override_dq_strategy(DqStrategy::kAuto);
+        if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+        forced = DqStrategy::kSeparatePass;
+    }
     void *scratch = nullptr;
-    const fa_status s = scratch_for_current_device(&scratch);
+    fa_status s = scratch_for_current_device(&scratch);
     if (s != FA_OK) return s;
-    return fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, scratch,
-                  FA_NOALLOC_SCRATCH_BYTES, stream);
+    tc_override_dq_strategy(forced);
+    s = fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, scratch,
+               FA_NOALLOC_SCRATCH_BYTES, stream);
+    tc_override_dq_strategy(DqStrategy::kAuto);
+    return s;
 }
 
 }  // extern "C"

@@ -1865,10 +1865,15 @@ size_t tc_bwd_ld_rows(const FaProblem &p) { return (size_t)p.BH * padded_rows(p.
 
 namespace {
 std::atomic<int> g_dq_strategy{0};
+thread_local int t_dq_override = 0;   // DqStrategy for this thread's calls; 0: the library setting
 }
 
 void tc_set_dq_strategy(DqStrategy s) { g_dq_strategy.store(static_cast<int>(s)); }
-DqStrategy tc_get_dq_strategy() { return static_cast<DqStrategy>(g_dq_strategy.load()); }
+DqStrategy tc_get_dq_strategy() {
+    return static_cast<DqStrategy>(t_dq_override ? t_dq_override : g_dq_strategy.load());
+}
+void tc_override_dq_strategy(DqStrategy s) { t_dq_override = static_cast<int>(s); }
+DqStrategy tc_get_dq_setting() { return static_cast<DqStrategy>(g_dq_strategy.load()); }
 
 // dQ by fp32 reduction inside the dK/dV items exists for head dims up to 64 (the
 // 128-wide items).  Measured on GB300 (gradient launch, reduction / separate pass):

@@ -144,6 +144,8 @@ WORKLOADS = {
                                              projected=True),
     "layer_xl_b4_h25_n1024_full": Workload("layer_xl_b4_h25_n1024_full", 4, 25, 1024, 64, "bf16", False, 4,
                                            projected=True),
+    # a cell of the attention sweep in fp32 (the CUDA-core kernels), for profiling that path
+    "sweep_f32_b1_n4096_d64_causal": Workload("sweep_f32_b1_n4096_d64_causal", 1, 1, 4096, 64, "f32", True, 5),
 }
 
 
