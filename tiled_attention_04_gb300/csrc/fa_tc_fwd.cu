@@ -114,7 +114,13 @@ struct FwdCfg {
     // (double-buffered by work unit in the persistent kernel; the split form's
     // rank 1 stores its half into rank 0's copy)
     static constexpr uint32_t DSUM_OFF = OROW_OFF + 256 * 8;
-    static constexpr uint32_t USED = DSUM_OFF + 2 * 256 * 4;
+    // fused backward preprocessing, d = 64, one unit per CTA: the tile's dO rows
+    // (packed, d * 2 bytes each), fetched by an otherwise idle warp during the main loop
+    // (the destination of a bulk copy: 16-byte aligned; the barrier block above leaves
+    // the offsets after it only 8-byte aligned, hence the rounding)
+    static constexpr uint32_t DOS_OFF = (DSUM_OFF + 2 * 256 * 4 + 127) / 128 * 128;
+    static_assert(DOS_OFF % 16 == 0, "bulk-copy destination on a 16-byte boundary");
+    static constexpr uint32_t USED = DOS_OFF + (D == 64 ? 128 * 64 * 2 : 0);
     // split items: rank 1's partial O (fp32, rows padded by 4 floats) and its m, l, in the K ring
     static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
     static constexpr uint32_t PART_OFF = K_OFF;
@@ -133,18 +139,20 @@ struct FwdCfg {
 
 // ------------------------------------------------------------------ fused backward preprocessing
 // Half of rowsum(dO * O) for one query row: this thread's D/2 output columns of
-// the unrounded fp32 O (vals * inv) against the same columns of dO.
+// the unrounded fp32 O (vals * inv) against the same columns of dO, read from
+// global memory or (drow not NULL) from the row staged in shared memory.
 template <int D, bool VIEW4>
 __device__ __forceinline__ float prep_half_rowsum(const FwdPrep &prep, const float *vals, float inv, int bh, int row,
-                                                  int Nq, int H, int dv, int t) {
-    const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(prep.dO);
-    if constexpr (VIEW4) g += fa_row_offset(prep.sdo, H, bh, row) + t * (D / 2);
-    else g += ((size_t)bh * Nq + row) * D + t * (D / 2);
+                                                  int Nq, int H, int dv, int t, const __nv_bfloat16 *drow = nullptr) {
+    const __nv_bfloat16 *g = drow;
+    if (g) g += t * (D / 2);
+    else if constexpr (VIEW4) g = static_cast<const __nv_bfloat16 *>(prep.dO) + fa_row_offset(prep.sdo, H, bh, row) + t * (D / 2);
+    else g = static_cast<const __nv_bfloat16 *>(prep.dO) + ((size_t)bh * Nq + row) * D + t * (D / 2);
     float acc = 0.f;
 #pragma unroll
     for (int c = 0; c < D / 16; ++c) {
         if (!VIEW4 || t * (D / 2) + 8 * c < dv) {   // columns past a head dim below 64 are padding
-            const uint4 x = __ldg(reinterpret_cast<const uint4 *>(g) + c);
+            const uint4 x = drow ? reinterpret_cast<const uint4 *>(g)[c] : __ldg(reinterpret_cast<const uint4 *>(g) + c);
             const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&x);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -163,7 +171,8 @@ __device__ __forceinline__ float prep_half_rowsum(const FwdPrep &prep, const flo
 // accumulator cleared (d <= 64 kernels, when dQ is formed by reduction).
 template <int D>
 __device__ __forceinline__ void prep_row_finish(const FwdPrep &prep, float half0, float half1, bool write_consts,
-                                                float Mrow, float lrow, int bh, int row, int Nq, int t) {
+                                                float Mrow, float lrow, int bh, int row, int Nq, int t,
+                                                bool clear_acc = true) {
     const size_t gr = (size_t)bh * ((Nq + 127) / 128 * 128) + row;
     if (write_consts) {
         if (row < Nq) {
@@ -176,7 +185,7 @@ __device__ __forceinline__ void prep_row_finish(const FwdPrep &prep, float half0
         }
     }
     if constexpr (D == 64) {
-        if (prep.dQa) {
+        if (prep.dQa && clear_acc) {
             float4 *z = reinterpret_cast<float4 *>(prep.dQa + gr * 64 + t * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -222,6 +231,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t drain = bar(RB + 4);
     const uint32_t never = bar(RB + 5);   // fault injection: nothing ever arrives here
     auto s_free = [&](int t) { return bar(RB + 6 + t); };   // softmax has read S_t (separate-P layout)
+    const uint32_t do_full = bar(RB + 8);   // fused preprocessing (d = 64): the tile's dO rows have landed
     float *m_sm = reinterpret_cast<float *>(sb + C::STAT_OFF);
     float *l_sm = m_sm + 256;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
@@ -239,6 +249,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tc::mbar_init(drain, 1);
         tc::mbar_init(never, 1);
+        tc::mbar_init(do_full, 1);
         if (SPLIT > 1) {
             tc::mbar_init(base + C::PEER_BAR_OFF, 256);       // peer_free: the peer's 256 softmax threads
             tc::mbar_init(base + C::PEER_BAR_OFF + 8, 128);   // peer_ready: the peer's 128 senders
@@ -320,6 +331,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, 0); ++i) {
                     }
             }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ fused preprocessing
+        // While the tile runs: fetch its dO rows into shared memory for the epilogue's
+        // rowsum (d = 64: one bulk copy of the contiguous rows) and clear its rows of
+        // the dQ accumulator (rank 0 of a split item), off the epilogue's path.
+        if (prep.dO && q0 < Nq) {
+            if (D == 64 && lane == 0) {
+                const int rows = min(BM, Nq - q0);
+                const uint32_t bytes = (uint32_t)rows * dv * 2;
+                const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(prep.dO) +
+                                           (VIEW4 ? fa_row_offset(prep.sdo, H, bh, q0) : ((size_t)bh * Nq + q0) * D);
+                tc::mbar_arrive_expect_tx(do_full, bytes);
+                tc::bulk_load(base + C::DOS_OFF, src, bytes, do_full);
+            }
+            if (D == 64 && prep.dQa && rank == 0) {
+                float4 *z = reinterpret_cast<float4 *>(prep.dQa + ((size_t)bh * ((Nq + 127) / 128 * 128) + q0) * 64);
+                for (int i = lane; i < BM * 64 / 4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (D == 64 && lane == 0)   // the copy lands before the CTA may exit
+                for (uint32_t i = 0; i < (1u << 22) && !tc::mbar_try_wait(do_full, 0); ++i) {
+                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -496,6 +529,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool fine = !*abort_flag;
         if (fine && n0 > 0) fine = W.wait(pv_done_bar(2 * n0 - 2), ((2 * n0 - 2) / C::R) & 1);
         if (fine && n1 > 0) fine = W.wait(pv_done_bar(2 * n1 - 1), ((2 * n1 - 1) / C::R) & 1);
+        if (D == 64 && prep.dO && fine) fine = W.wait(do_full, 0);   // the dO rows are in shared memory
         fine = __all_sync(0xffffffffu, fine);
         // this CTA's partial for row r, columns [t*D/2, (t+1)*D/2), relative to max Mc (unnormalised)
         float v[D / 2];
@@ -548,7 +582,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         reinterpret_cast<uint4 *>(orow)[c] = q;
                 }
                 if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
-                if (prep.dO) part = prep_half_rowsum<D, VIEW4>(prep, vals, inv, bh, row, Nq, H, dv, t);
+                if (prep.dO) {
+                    const __nv_bfloat16 *drow = nullptr;
+                    if constexpr (D == 64)
+                        drow = reinterpret_cast<const __nv_bfloat16 *>(sb + C::DOS_OFF) + (size_t)r * dv;
+                    part = prep_half_rowsum<D, VIEW4>(prep, vals, inv, bh, row, Nq, H, dv, t, drow);
+                }
             }
             return part;
         };
@@ -573,7 +612,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float *dsum = reinterpret_cast<float *>(sb + C::DSUM_OFF);
                 dsum[t * 128 + r] = part;
                 tc::named_bar_sync(1, 256);
-                if (fine) prep_row_finish<D>(prep, part, t == 0 ? dsum[128 + r] : 0.f, t == 0, Mc, lc, bh, row, Nq, t);
+                if (fine)
+                    prep_row_finish<D>(prep, part, t == 0 ? dsum[128 + r] : 0.f, t == 0, Mc, lc, bh, row, Nq, t, false);
             }
         } else {
             // rank r finalises the columns of warpgroup r; the other warpgroup sends its
@@ -626,12 +666,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (rank == 1) {
                         tc::st_cluster_f32(tc::map_to_rank(base + C::DSUM_OFF + 4u * r, 0u), part);
                         tc::mbar_arrive_remote(tc::map_to_rank(peer_d, 0u));   // release: the store above
-                        if (both) prep_row_finish<D>(prep, part, 0.f, false, M, lrow, bh, row, Nq, t);
+                        if (both) prep_row_finish<D>(prep, part, 0.f, false, M, lrow, bh, row, Nq, t, false);
                     } else {
                         const bool got_d = wait_peer(peer_d);
                         if (both) {
                             const float other = got_d ? reinterpret_cast<const float *>(sb + C::DSUM_OFF)[r] : 0.f;
-                            prep_row_finish<D>(prep, part, other, got_d, M, lrow, bh, row, Nq, t);
+                            prep_row_finish<D>(prep, part, other, got_d, M, lrow, bh, row, Nq, t, false);
                         }
                     }
                 }
