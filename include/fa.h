@@ -266,8 +266,10 @@ FA_API const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype d
  *                        the last bit of its fp32 sum, about one bf16 rounding
  *                        step at most; dK, dV, O and L stay bit-reproducible);
  *   FA_DQ_AUTO           per shape, the faster form as measured on GB300: the
- *                        reduction for causal attention with head dims up to 64
- *                        on the tensor-core path, the separate pass otherwise.
+ *                        reduction for head dims up to 64 on the tensor-core path
+ *                        when causal, or when there are many short key tiles
+ *                        (their items then run on persistent CTAs); the separate
+ *                        pass otherwise.
  * The CUDA-core (fp32) path always uses the separate pass.
  */
 #define FA_DQ_AUTO 0

@@ -1707,6 +1707,414 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
     }
 }
 
+// ================================================================== persistent dK/dV items (d = 64, dQ by reduction)
+// One CTA per SM walks a snake-ordered list of dK/dV items (longest first), with
+// the work of the 128-wide d = 64 items and dQ formed by reduction.  Unlike the
+// one-item-per-CTA launch, nothing is set up per item: TMEM is allocated once,
+// the barriers are initialised once and their phases run on across items (the
+// query sub-tiles are numbered over all of the CTA's items), and the register
+// split is set once.  Between items the next item's K/V tile loads once the
+// previous item's MMAs are done, and its first S^T / dP^T MMAs start while the
+// element-wise warps still store the previous item's dK and dV.
+struct DkdvPersistCfg : DkdvWideCfg<64, true> {
+    using Base = DkdvWideCfg<64, true>;
+    // the base barriers, then kv_empty (an item's MMAs are done: K/V may be
+    // reloaded) and acc_free (the epilogue has read dV / dK from TMEM)
+    static constexpr int NBAR = Base::NBAR + 2;
+    static constexpr uint32_t MISC_OFF = Base::BAR_OFF + NBAR * 8;
+    static constexpr uint32_t SMEM_BYTES = (MISC_OFF + 16 + 1024 > 120u * 1024u ? MISC_OFF + 16 + 1024 : 120u * 1024u);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <bool CAUSAL, bool VIEW4>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    fa_bwd_red_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                                 const __grid_constant__ CUtensorMap dqa, const float *__restrict__ Lp,
+                                 const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
+                                 __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH, int k_tiles, float scale,
+                                 float scale_log2, uint32_t wait_limit, int H, int dv, FaStrides sdk, FaStrides sdv) {
+    constexpr int D = 64;
+    using C = DkdvPersistCfg;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    tc::pdl_launch_dependents();
+
+    const int nqp = padded_rows(Nq);
+    const int i_end = (Nq + C::BQ - 1) / C::BQ;
+    const int num_items = k_tiles * BH;
+    const int G = (int)gridDim.x, cb = (int)blockIdx.x;
+    // item r of this CTA (snake order over the longest-first list): key tile kt of
+    // batch*head bh, with query sub-tiles [first, first + n)
+    auto item_of = [&](int r, int &kt, int &bh, int &first, int &n) -> bool {
+        const int u = r * G + ((r & 1) ? G - 1 - cb : cb);
+        if (u >= num_items) return false;
+        const int rr = u / BH;
+        kt = CAUSAL ? rr : k_tiles - 1 - rr;   // causal: the first key tiles see the most queries
+        bh = u % BH;
+        first = CAUSAL ? kt : 0;
+        n = i_end > first ? i_end - first : 0;
+        return true;
+    };
+
+    auto bar = [&](int i) { return base + C::BAR_OFF + 8u * i; };
+    const uint32_t kv_full = bar(0);
+    auto q_full = [&](int s) { return bar(1 + s); };
+    auto q_empty = [&](int s) { return bar(1 + C::STAGES + s); };
+    const uint32_t sd_full = bar(1 + 2 * C::STAGES);
+    const uint32_t sd_free = bar(2 + 2 * C::STAGES);
+    const uint32_t p_full = bar(3 + 2 * C::STAGES);
+    const uint32_t drain = bar(4 + 2 * C::STAGES);
+    const uint32_t dq_staged = bar(5 + 2 * C::STAGES);
+    const uint32_t dq_free = bar(6 + 2 * C::STAGES);
+    const uint32_t kv_empty = bar(7 + 2 * C::STAGES);
+    const uint32_t acc_free = bar(8 + 2 * C::STAGES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(kv_full, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            tc::mbar_init(q_full(s), 1);
+            tc::mbar_init(q_empty(s), 1);
+        }
+        tc::mbar_init(sd_full, 1);
+        tc::mbar_init(sd_free, 256);
+        tc::mbar_init(p_full, 256);
+        tc::mbar_init(drain, 1);
+        tc::mbar_init(dq_staged, 256);
+        tc::mbar_init(dq_free, 1);
+        tc::mbar_init(kv_empty, 1);
+        tc::mbar_init(acc_free, 256);
+        *abort_flag = 0u;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    tc::pdl_wait();   // D and L staged by the preprocessing (or the forward) are complete
+    const tc::Waiter W{abort_flag, &g_fa_bwd_status, wait_limit, 2u};
+
+    if (warp < 4) {
+    tc::regs_dec<56>();
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmQ);
+            tc::tma_prefetch_desc(&tmdO);
+            int g = 0, issued = 0, kt, bh, first, n;
+            int kv_r = -1;   // the last item whose K/V load was issued
+            for (int r = 0; item_of(r, kt, bh, first, n); ++r) {
+                // the K/V buffer is refilled once the previous item's MMAs have completed
+                if (r > 0 && !W.wait(kv_empty, (r - 1) & 1)) break;
+                const int k0 = kt * C::BK;
+                if (!tc::in_bounds(k0 < Nk && bh < BH, &g_fa_bwd_status, abort_flag)) break;
+                if (n > 0) {
+                    tc::mbar_arrive_expect_tx(kv_full, 2 * C::KT::BYTES);
+                    tc::tma_load_rows<VIEW4>(base + C::K_OFF, &tmK, kv_full, 0, k0, bh, H);
+                    tc::tma_load_rows<VIEW4>(base + C::V_OFF, &tmV, kv_full, 0, k0, bh, H);
+                    kv_r = r;
+                } else {
+                    tc::mbar_arrive(kv_full);   // an item with no queries still moves the phase on
+                }
+                bool ok = true;
+                for (int it = 0; it < n; ++it, ++g) {
+                    const int s = g % C::STAGES;
+                    if (!(ok = W.wait(q_empty(s), ((g / C::STAGES) & 1) ^ 1u))) break;
+                    const int q0 = (first + it) * C::BQ;
+                    if (!(ok = tc::in_bounds(q0 < Nq && (!CAUSAL || q0 + C::BQ - 1 >= k0), &g_fa_bwd_status,
+                                             abort_flag)))
+                        break;
+                    tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 1024);
+                    tc::tma_load_rows<VIEW4>(base + C::Q_OFF + s * C::QT::BYTES, &tmQ, q_full(s), 0, q0, bh, H);
+                    tc::tma_load_rows<VIEW4>(base + C::DO_OFF + s * C::QT::BYTES, &tmdO, q_full(s), 0, q0, bh, H);
+                    const size_t off = (size_t)bh * nqp + q0;
+                    tc::bulk_load(base + C::LD_OFF + s * 1024, Lp + off, 512, q_full(s));
+                    tc::bulk_load(base + C::LD_OFF + s * 1024 + 512, Dp + off, 512, q_full(s));
+                    issued = g + 1;
+                }
+                if (!ok) break;
+                if constexpr (tc::kDebug) atomicAdd(&g_fa_bwd_rows[0], (unsigned long long)n * C::BQ);
+            }
+            if (*abort_flag) {
+                for (int gg = issued - 1; gg >= 0 && gg >= issued - C::STAGES; --gg)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full(gg % C::STAGES), (gg / C::STAGES) & 1);
+                         ++i) {
+                    }
+                // the last K/V load lands before the CTA may exit
+                if (kv_r >= 0)
+                    for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(kv_full, kv_r & 1); ++i) {
+                    }
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ dQ reduction
+        if (lane == 0) {
+            int g = 0, kt, bh, first, n;
+            bool ok = true;
+            for (int r = 0; ok && item_of(r, kt, bh, first, n); ++r) {
+                for (int it = 0; it < n; ++it, ++g) {
+                    if (!(ok = W.wait(dq_staged, g & 1))) break;
+                    const int q0 = (first + it) * C::BQ;
+                    if (!(ok = tc::in_bounds(q0 + C::BQ <= nqp, &g_fa_bwd_status, abort_flag))) break;
+#pragma unroll
+                    for (int x = 0; x < D / 32; ++x)
+                        tc::tma_reduce_add_3d(&dqa, base + C::DQS_OFF + x * C::DQS_BOX, 32 * x, q0, bh);
+                    tc::bulk_commit_group();
+                    tc::bulk_wait_read_all();
+                    tc::mbar_arrive(dq_free);
+                }
+            }
+            tc::bulk_wait_all();
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const bool leader = tc::elect_one();
+        constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BQ, false, false);
+        constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
+        constexpr uint32_t idesc_q = tc::idesc_bf16(128, D, true, true);
+        const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);
+        const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, 16, 1024);
+        const uint64_t qk = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);
+        const uint64_t gk = tc::sdesc_sw128(base + C::DO_OFF, 16, 1024);
+        const uint64_t qm = tc::sdesc_sw128(base + C::Q_OFF, C::QT::CHUNK, 1024);
+        const uint64_t gm = tc::sdesc_sw128(base + C::DO_OFF, C::QT::CHUNK, 1024);
+        const uint64_t dsk = tc::sdesc_sw128(base + C::DS_OFF, 16, 1024);
+        const uint64_t dsm = tc::sdesc_sw128(base + C::DS_OFF, 128 * 128, 1024);
+        const uint64_t km = tc::sdesc_sw128(base + C::K_OFF, C::KT::CHUNK, 1024);
+        // S^T = K Q^T and dP^T = V dO^T of global sub-tile gg (its S^T / dP^T columns
+        // must have been read for sub-tile gg-1 first)
+        auto sdp = [&](int gg) -> bool {
+            const int s = gg % C::STAGES;
+            const bool ready = gg > 0 ? W.wait2(sd_free, (gg - 1) & 1, q_full(s), (gg / C::STAGES) & 1)
+                                      : W.wait(q_full(s), (gg / C::STAGES) & 1);
+            if (!__all_sync(0xffffffffu, ready)) return false;
+            if (leader) {
+                const uint32_t st = (s * C::QT::BYTES) >> 4;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t oa = ((kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + C::ST_COL, kd + oa, qk + st + oa, idesc_s, kk > 0 ? 1u : 0u);
+                    tc::mma_ss(tmem + C::DP_COL, vd + oa, gk + st + oa, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(sd_full);
+            }
+            __syncwarp();
+            return true;
+        };
+        // dV += P^T dO, dK += dS^T Q (fresh at an item's first sub-tile), dQ partial = dS K
+        auto grads = [&](int gg, bool fresh) -> bool {
+            const int s = gg % C::STAGES;
+            if (!__all_sync(0xffffffffu, W.wait(p_full, gg & 1))) return false;
+            tc::fence_after_sync();
+            if (leader) {
+                const uint32_t st = (s * C::QT::BYTES) >> 4;
+#pragma unroll
+                for (int kk = 0; kk < C::BQ / 16; ++kk) {
+                    const uint32_t acc = (!fresh || kk > 0) ? 1u : 0u;
+                    tc::mma_ts(tmem + C::DV_COL, tmem + C::PT_COL + kk * 8, gm + st + kk * 128, idesc_g, acc);
+                    tc::mma_ss(tmem + C::DK_COL, dsk + (((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4), qm + st + kk * 128,
+                               idesc_g, acc);
+                }
+#pragma unroll
+                for (int kk = 0; kk < C::BK / 16; ++kk)
+                    tc::mma_ss(tmem + C::DQ_COL, dsm + kk * 128, km + kk * 128, idesc_q, kk > 0 ? 1u : 0u);
+                tc::mma_commit(q_empty(s));
+            }
+            __syncwarp();
+            return true;
+        };
+        int g = 0, kt, bh, first, n;
+        bool ok = true;
+        for (int r = 0; ok && item_of(r, kt, bh, first, n); ++r) {
+            if (!(ok = __all_sync(0xffffffffu, W.wait(kv_full, r & 1)))) break;
+            if (n > 0) {
+                if (!(ok = sdp(g))) break;
+                for (int it = 0; ok && it < n; ++it) {
+                    if (it + 1 < n && !(ok = sdp(g + it + 1))) break;
+                    // dV / dK of the previous item must have been read before the first
+                    // gradient MMAs of this one overwrite them
+                    if (it == 0 && r > 0 && !(ok = __all_sync(0xffffffffu, W.wait(acc_free, (r - 1) & 1)))) break;
+                    ok = grads(g + it, it == 0);
+                }
+            }
+            if (ok && leader) tc::mma_commit(kv_empty);   // this item's MMAs are done with K and V
+            __syncwarp();
+            g += n;
+        }
+        if (!ok && leader) {
+            tc::mma_commit(drain);
+            for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(drain, 0); ++i) {
+            }
+        }
+        __syncwarp();
+    }
+    } else {
+        tc::regs_inc<224>();
+        // ------------------------------------------------------------ element-wise warpgroups
+        const int t = (warp - 4) >> 2;                       // query columns [64t, 64t + 64)
+        const int rrow = ((warp & 3) << 5) + lane;           // key row within the tile = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+        const uint32_t tS = tmem + lane_base + C::ST_COL + 64 * t;
+        const uint32_t tD = tmem + lane_base + C::DP_COL + 64 * t;
+        const uint32_t tPT = tmem + lane_base + C::PT_COL + 32 * t;
+        const uint32_t tDQ = tmem + lane_base + C::DQ_COL + 32 * t;
+        auto store_ds = [&](const uint32_t (&v)[32]) {
+            uint8_t *row = sb + C::DS_OFF + t * (128 * 128) + rrow * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<uint4 *>(row + ((u ^ (rrow & 7)) << 4)) =
+                    make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        };
+        auto stage_dq = [&](int gg, const uint32_t (&v)[32]) -> bool {
+            if (gg > 0 && !__all_sync(0xffffffffu, W.wait(dq_free, (gg - 1) & 1))) return false;
+            uint8_t *row = sb + C::DQS_OFF + t * C::DQS_BOX + rrow * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<uint4 *>(row + ((u ^ (rrow & 7)) << 4)) =
+                    make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(dq_staged);
+            return true;
+        };
+        int g = 0, kt, bh, first, n;
+        bool alive = true;
+        for (int r = 0; item_of(r, kt, bh, first, n); ++r) {
+            const int k0 = kt * C::BK, key = k0 + rrow;
+            for (int it = 0; alive && it < n; ++it) {
+                const int gg = g + it, s = gg % C::STAGES;
+                const int qc = (first + it) * C::BQ + 64 * t;
+                bool ok = W.wait2(sd_full, gg & 1, q_full(s), (gg / C::STAGES) & 1);
+                if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+                tc::fence_after_sync();
+                uint32_t sv[2][32], dv_[2][32];
+                tmem_ld_x32(tS, sv[0]);
+                tmem_ld_x32(tS + 32, sv[1]);
+                tmem_ld_x32(tD, dv_[0]);
+                tmem_ld_x32(tD + 32, dv_[1]);
+                tc::tmem_ld_wait();
+                reg_fence_x32(sv[0]);
+                reg_fence_x32(sv[1]);
+                reg_fence_x32(dv_[0]);
+                reg_fence_x32(dv_[1]);
+                tc::fence_before_sync();
+                tc::mbar_arrive(sd_free);
+                const float *lds = reinterpret_cast<const float *>(sb + C::LD_OFF + s * 1024) + 64 * t;
+                const int first_visible = key - qc;
+                if (CAUSAL && __any_sync(0xffffffffu, first_visible > 0)) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (c < first_visible) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                }
+                uint32_t pp[32], dsp[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float4 nl = *reinterpret_cast<const float4 *>(lds + 4 * i);
+                    const float4 nd = *reinterpret_cast<const float4 *>(lds + 128 + 4 * i);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = 4 * i + 2 * h;
+                        const float l0 = h ? nl.z : nl.x, l1 = h ? nl.w : nl.y;
+                        const float d0 = h ? nd.z : nd.x, d1 = h ? nd.w : nd.y;
+                        float x0, x1, g0, g1;
+                        tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
+                                 scale_log2, scale_log2, l0, l1);
+                        const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+                        tc::add2(g0, g1, __uint_as_float(dv_[c >> 5][c & 31]), __uint_as_float(dv_[c >> 5][(c & 31) + 1]),
+                                 d0, d1);
+                        tc::mul2(g0, g1, g0, g1, p0, p1);
+                        pp[2 * i + h] = tc::pack_bf16(p0, p1);
+                        dsp[2 * i + h] = tc::pack_bf16(g0, g1);
+                    }
+                }
+                uint32_t dq[32];
+                if (it > 0) {
+                    // the previous sub-tile's MMAs read P^T and dS and wrote its dQ partial
+                    ok = W.wait(q_empty((gg - 1) % C::STAGES), ((gg - 1) / C::STAGES) & 1);
+                    if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+                    tc::fence_after_sync();
+                    tmem_ld_x32(tDQ, dq);
+                }
+                tmem_st_x32(tPT, pp);
+                store_ds(dsp);
+                tc::tmem_st_wait();
+                if (it > 0) {
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(dq);
+                }
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
+                tc::mbar_arrive(p_full);
+                if (it > 0 && !stage_dq(gg - 1, dq)) { alive = false; break; }
+            }
+            // ---- item epilogue: the last dQ partial, then dV (warpgroup 0) / dK (1)
+            bool fine = alive && !*abort_flag;
+            if (fine && n > 0) fine = W.wait(q_empty((g + n - 1) % C::STAGES), ((g + n - 1) / C::STAGES) & 1);
+            fine = __all_sync(0xffffffffu, fine);
+            if (fine && n > 0) {
+                tc::fence_after_sync();
+                uint32_t dq[32];
+                tmem_ld_x32(tDQ, dq);
+                tc::tmem_ld_wait();
+                reg_fence_x32(dq);
+                fine = stage_dq(g + n - 1, dq);
+            }
+            __nv_bfloat16 *dst;
+            if constexpr (VIEW4)
+                dst = t == 0 ? dV + fa_row_offset(sdv, tc::opaque(H), bh, key) : dK + fa_row_offset(sdk, tc::opaque(H), bh, key);
+            else
+                dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
+            const float mul = t == 0 ? 1.f : scale;
+            const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
+            uint32_t a[2][32];
+            if (fine && n > 0) {
+                tmem_ld_x32(tA, a[0]);
+                tmem_ld_x32(tA + 32, a[1]);
+                tc::tmem_ld_wait();
+                reg_fence_x32(a[0]);
+                reg_fence_x32(a[1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a[0][i] = a[1][i] = 0u;
+            }
+            tc::fence_before_sync();
+            tc::mbar_arrive(acc_free);   // dV / dK may be overwritten by the next item
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = tc::pack_bf16(__uint_as_float(a[c][2 * i]) * mul, __uint_as_float(a[c][2 * i + 1]) * mul);
+                if ((fine || n == 0) && key < Nk) {
+                    uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (!VIEW4 || 32 * c + 8 * i < dv)
+                            o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
+            }
+            g += n;
+            if (!fine && n > 0) alive = false;
+            if (!alive) break;
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
 // Both gradient passes in one launch.  The two lists of work items (dK/dV per
 // key tile, dQ per query tile; each longest first) are interleaved so that the
 // long items of both start first and the short ones of both fill the end --
@@ -1851,6 +2259,43 @@ cudaError_t launch_bwd_any(const FaProblem &p, const Maps2 &m, const float *Lp, 
                  : launch_bwd<D, CAUSAL, 1, false, RED>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
 }
 
+// the persistent dK/dV items of dQ by reduction (d = 64): one CTA per SM
+template <bool CAUSAL, bool VIEW4>
+cudaError_t launch_red_persistent(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dK,
+                                  void *dV, cudaStream_t st) {
+    using C = DkdvPersistCfg;
+    const int kt = (p.Nk + 127) / 128;
+    const long long items = (long long)kt * p.BH;
+    const long long grid = std::min<long long>(items, sm_count());
+    cudaError_t e = set_smem(fa_bwd_red_persistent_kernel<CAUSAL, VIEW4>, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fa_bwd_red_persistent_kernel<CAUSAL, VIEW4>, m.a.q, m.a.k, m.a.v, m.a.dO, m.dqa, Lp,
+                           Dp, static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH,
+                           kt, p.scale, p.scale * kLog2e, p.wait_limit, p.H, p.d, p.sdK, p.sdV);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+// Persistent dK/dV items where there are many short ones: at least two items per
+// SM and no item whose loop alone would set the run time.  Measured (gradient
+// launch, persistent / one item per CTA): 4 x 25 x 1024 causal 68.6 / 80.0 us,
+// non-causal 99.3 / 108.3 us; batch 8 x N 4096 causal and N 65536 causal (long
+// items, not chosen) equal within 0.3 %.
+bool red_persistent(const FaProblem &p) {
+    const long long ktiles = (p.Nk + 127) / 128, i_end = (p.Nq + 127) / 128;
+    return ktiles * p.BH >= 2LL * sm_count() && i_end <= 16 && !dkdv_split(p);
+}
+
 bool make_maps(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO, int q_rows,
                int k_rows, bool view4, Maps *m) {
     return tc_make_map(&m->q, Q, p, p.sQ, p.Nq, q_rows, view4) && tc_make_map(&m->dO, dO, p, p.sdO, p.Nq, q_rows, view4) &&
@@ -1878,16 +2323,18 @@ DqStrategy tc_get_dq_setting() { return static_cast<DqStrategy>(g_dq_strategy.lo
 // dQ by fp32 reduction inside the dK/dV items exists for head dims up to 64 (the
 // 128-wide items).  Measured on GB300 (gradient launch, reduction / separate pass):
 // batch 8 x N 4096 causal 54.9 / 58.6 us, N 65536 causal 1204 / 1279 us, the
-// 4 x 25 x 1024 layer causal 75.6 / 78.2 us but non-causal 103.8 / 101.0 us -- the
-// reductions (32 KB per key tile and query tile) cost more where every key tile
-// meets every query tile.  So: the reduction for causal shapes, the separate pass
-// otherwise.  A forced strategy overrides the choice.
+// 4 x 25 x 1024 layer causal 75.6 / 78.2 us (68.6 with the reduction's persistent
+// items) but non-causal 103.8 / 101.0 us one item per CTA -- the reductions (32 KB
+// per key tile and query tile) cost more where every key tile meets every query
+// tile -- and 99.3 / 107.5 us with persistent items.  So: the reduction for causal
+// shapes and wherever its items run persistent, the separate pass otherwise.  A
+// forced strategy overrides the choice.
 bool tc_bwd_dq_by_reduction(const FaProblem &p) {
     if (!tc_bwd_supported(p) || p.d > 64) return false;
     switch (tc_get_dq_strategy()) {
         case DqStrategy::kSeparatePass: return false;
         case DqStrategy::kReduction: return true;
-        default: return p.causal != 0;
+        default: return p.causal != 0 || red_persistent(p);
     }
 }
 
@@ -1973,8 +2420,15 @@ cudaError_t grads_impl(const FaProblem &p, const void *Q, const void *K, const v
         if (p.d > 64) return cudaErrorInvalidValue;
         if (!tc_make_map_acc(reinterpret_cast<CUtensorMap_st *>(&m.dqa), dQa, p.BH, padded_rows(p.Nq), 64))
             return cudaErrorInvalidValue;
-        cudaError_t e = p.causal ? launch_bwd_any<64, true, true>(p, m, Lp, Dp, dQ, dK, dV, true, true, st)
-                                 : launch_bwd_any<64, false, true>(p, m, Lp, Dp, dQ, dK, dV, true, true, st);
+        cudaError_t e;
+        if (red_persistent(p))
+            e = m.view4 ? (p.causal ? launch_red_persistent<true, true>(p, m, Lp, Dp, dK, dV, st)
+                                    : launch_red_persistent<false, true>(p, m, Lp, Dp, dK, dV, st))
+                        : (p.causal ? launch_red_persistent<true, false>(p, m, Lp, Dp, dK, dV, st)
+                                    : launch_red_persistent<false, false>(p, m, Lp, Dp, dK, dV, st));
+        else
+            e = p.causal ? launch_bwd_any<64, true, true>(p, m, Lp, Dp, dQ, dK, dV, true, true, st)
+                         : launch_bwd_any<64, false, true>(p, m, Lp, Dp, dQ, dK, dV, true, true, st);
         if (e != cudaSuccess) return e;
         return launch_dq_convert<64>(p, dQa, dQ, !tc_plain_layout(p, p.sdQ, p.Nq), st);
     }
