@@ -28,9 +28,13 @@
  * (absolute indices), so every query row sees key 0 and no row is empty.
  *
  * Ownership.  The caller owns every buffer (device memory), including the
- * backward workspace.  The library allocates no device memory per call.
- * Calls are asynchronous and ordered on the caller's stream; nothing
- * synchronises inside a call.
+ * backward workspace.  The library allocates no device memory per call, with
+ * one exception: fa_fwd / fa_fwd_strided with fp32 inputs on the tensor-core
+ * path (fa_set_fp32_mode below) take the split bf16 copies of Q, K and V
+ * (256 bytes per row each) from a stream-ordered memory pool the library owns,
+ * one per device; the pool keeps its memory between calls, so only the first
+ * call, or the first larger one, allocates.  Calls are asynchronous and
+ * ordered on the caller's stream; nothing synchronises inside a call.
  *
  * Errors.  Every entry point returns fa_status and never throws.  Arguments
  * are checked before anything is launched; on a bad argument nothing runs and
@@ -38,7 +42,8 @@
  * bound every wait; a wait that runs out sets a device-side status word that
  * fa_get_device_status() reports as FA_ERR_TIMEOUT.
  *
- * Supported: d in {16, 32, 64, 128}; dtype fp32 or bf16; Nq >= 0, Nk >= 1
+ * Supported: d in {16, 32, 64, 128}; dtype fp32 or bf16 (fp32 on the tensor
+ * cores as split bf16 pairs, see fa_set_fp32_mode); Nq >= 0, Nk >= 1
  * (Nk >= 0 when Nq == 0); B*H*max(Nq,Nk) < 2^31; every pointer 16-byte
  * aligned; scale finite.  B*H*Nq == 0 (and B*H*Nk == 0) is a valid empty call.
  */
@@ -92,7 +97,9 @@ FA_API fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, fl
 /*
  * Bytes of device workspace fa_bwd needs for this shape (fp32 D per query row;
  * on the tensor-core path fp32 D and L per query row, rows padded to a
- * multiple of 128).  Returns 0 for unsupported arguments.
+ * multiple of 128, plus, for fp32 inputs on that path, the split bf16 copies of
+ * Q, dO, K and V at 256 bytes per row each).  Returns 0 for unsupported
+ * arguments.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype);
 
@@ -244,11 +251,40 @@ FA_API fa_status fa_bwd_strided(const void *Q, const fa_strides *sQ, const void 
                                 void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
- * Name of the kernel family fa_fwd / fa_bwd would use for these arguments:
- * "tc" (tcgen05 tensor-core kernels) or "simt" (fp32 CUDA-core kernels), or
- * NULL for unsupported arguments.  Host-only; launches nothing.
+ * Name of the kernel family fa_fwd / fa_bwd would use for these arguments and
+ * the default scale 1/sqrt(d): "tc" (tcgen05 tensor-core kernels) or "simt"
+ * (fp32 CUDA-core kernels), or NULL for unsupported arguments.  Host-only;
+ * launches nothing.
  */
 FA_API const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype dtype);
+
+/*
+ * fp32 inputs.  The CUDA-core kernels compute in fp32 throughout.  For head dims
+ * 16, 32 and 64 (and Nq, Nk >= 128) fp32 inputs can instead run on the tensor
+ * cores: every operand x is split into two bf16 numbers, hi = bf16(x) and
+ * lo = bf16(x - hi), and every product of the method (S = Q K^T, O = P V, and
+ * the backward's five) takes three bf16 products with fp32 accumulation,
+ * hi*hi + hi*lo + lo*hi.  With u = 2^-8 (bf16's unit roundoff) each such sum
+ * of products x_i y_i carries an error of at most about 3 u^2 sum |x_i y_i|
+ * (3 * 2^-16 relative, against about 2^-7 for a product of two bf16-rounded
+ * operands and 2^-24 for fp32);
+ * through the softmax the scores' absolute error becomes P's relative error,
+ * so the outputs' error grows with the size of the scores.
+ *   FA_FP32_AUTO   the split path when |scale| * sqrt(d) <= 1 (unit-variance
+ *                  inputs then give unit-variance scores, and the outputs meet
+ *                  an elementwise 1e-4 tolerance with room to spare), the
+ *                  CUDA-core kernels otherwise;
+ *   FA_FP32_EXACT  always the CUDA-core kernels;
+ *   FA_FP32_SPLIT  the split path wherever the shape allows.
+ * The split path forms dQ by the separate pass.  fa_bwd_workspace_size covers
+ * the split copies whenever some scale may take them.  Returns the previous
+ * mode, or -1 for an unknown value (which changes nothing); do not change it
+ * while calls are queued on a stream.
+ */
+#define FA_FP32_AUTO 0
+#define FA_FP32_EXACT 1
+#define FA_FP32_SPLIT 2
+FA_API int fa_set_fp32_mode(int mode);
 
 /*
  * How the backward forms dQ = scale * dS K (problem flash_backward; the field

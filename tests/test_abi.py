@@ -102,13 +102,16 @@ def test_bwd_rejects_bad_workspace(L):
 
 def test_path_choice(L):
     from tiled_attention_04_gb300 import binding
-    assert binding.path_name(128, 128, 16, 1, binding.FA_DTYPE_F32) == "simt"
     assert binding.path_name(128, 128, 48, 1, binding.FA_DTYPE_F32) is None
     assert binding.path_name(4096, 4096, 64, 1, binding.FA_DTYPE_BF16) == "tc"
     assert binding.path_name(4096, 4096, 16, 1, binding.FA_DTYPE_BF16) == "tc"    # padded to 64 columns
     assert binding.path_name(4096, 4096, 32, 0, binding.FA_DTYPE_BF16) == "tc"
     assert binding.path_name(100, 4096, 64, 1, binding.FA_DTYPE_BF16) == "simt"   # shorter than one tile
-    assert binding.path_name(4096, 4096, 64, 1, binding.FA_DTYPE_F32) == "simt"   # fp32 keeps fp32 accuracy
+    # fp32 up to d = 64: split into bf16 pairs, three products per contraction
+    assert binding.path_name(128, 128, 16, 1, binding.FA_DTYPE_F32) == "tc"
+    assert binding.path_name(4096, 4096, 64, 1, binding.FA_DTYPE_F32) == "tc"
+    assert binding.path_name(4096, 4096, 128, 1, binding.FA_DTYPE_F32) == "simt"  # no d = 256 layout
+    assert binding.path_name(100, 4096, 32, 1, binding.FA_DTYPE_F32) == "simt"
 
 
 def test_valid_call_without_a_device_reports_no_device(L):

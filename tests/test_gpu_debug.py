@@ -24,15 +24,16 @@ def _cdiv(a, b):
     return (a + b - 1) // b
 
 
-def expected_rows(bh, nq, nk, d, causal, reduction):
+def expected_rows(bh, nq, nk, d, causal, reduction, narrow=False):
     """Tile rows the tensor-core kernels must load, by the loops of the method:
     forward   every 128-row query tile loads the 128-key tiles up to its last
               visible key;
     dK/dV     every 128-key tile loads the query sub-tiles (128 rows; 64 at
               d = 128) from the one holding its first key's row to the end;
     dQ        every 128-row query tile loads the key sub-tiles (128 / 64 rows)
-              up to its last visible key (none when dQ is formed by reduction)."""
-    sub = 64 if d == 128 else 128
+              up to its last visible key (none when dQ is formed by reduction).
+    narrow: fp32 split into bf16 pairs, which runs the d = 128 items."""
+    sub = 64 if (d == 128 or narrow) else 128
     fwd = kv = dq = 0
     for qt in range(_cdiv(nq, 128)):
         kend = min(nk, qt * 128 + 128) if causal else nk
@@ -115,3 +116,26 @@ def test_release_build_counts_nothing(cuda_lib):
     _run(t, True, "fused")
     assert binding.lib().fa_debug_build() == 0
     assert binding.debug_tile_rows() == [0, 0, 0]
+
+
+@pytest.mark.parametrize("bh,nq,nk,d,causal", [(2, 512, 512, 64, True), (1, 300, 1000, 32, False),
+                                               (1, 2048, 2048, 64, True)])
+def test_debug_build_split_fp32(cuda_lib, bh, nq, nk, d, causal):
+    """fp32 split into bf16 pairs (the d = 128 kernels on 128-column copies): no failed
+    check, the visible tiles' rows exactly, the release library's results bit for bit
+    (dQ by the separate pass) and the oracle's at 1e-4."""
+    from tiled_attention_04_gb300 import binding
+    t = inputs.make_custom(bh, nq, nk, d, "f32", seed=6300 + nq + d)
+    release = _run(t, causal, "two_calls")
+    with binding.debug_library() as D:
+        assert D.fa_debug_build() == 1
+        binding.fa_reset_device_status()
+        binding.debug_reset_tile_rows()
+        got = _run(t, causal, "fused")
+        status = binding.fa_get_device_status()
+        rows = binding.debug_tile_rows()
+    assert status == binding.FA_OK, binding.STATUS.get(status, status)
+    assert rows == expected_rows(bh, nq, nk, d, causal, False, narrow=True)
+    for k in got:
+        assert np.array_equal(got[k], release[k]), k
+    assert_close(got, oracle_all(t, causal, 1.0 / math.sqrt(d)), 1e-4, f"debug split fp32 {bh}x{nq}x{nk}")

@@ -279,7 +279,7 @@ def test_fwd_bwd_in_one_call(cuda_lib, bh, n, d, dt, causal):
     for name, a, b in (("O", O, O2), ("L", L, L2), ("dV", dV, dV2)):
         assert torch.equal(a, b), name
     if dt == "f32" and binding.dq_strategy(Q, K, causal) == binding.FA_DQ_SEPARATE_PASS:
-        # the CUDA-core path forms D from its fp32 O in both calls
+        # fp32 (split pairs or CUDA cores): both calls form D from the same fp32 O
         assert torch.equal(dQ, dQ2) and torch.equal(dK, dK2)
     got = {k: v.double().cpu().numpy() for k, v in (("O", O), ("L", L), ("dQ", dQ), ("dK", dK), ("dV", dV))}
     assert_close(got, oracle_all(t, causal, 1.0 / math.sqrt(d)), TOL[dt], f"fwd_bwd bh={bh} n={n} d={d} {dt}")

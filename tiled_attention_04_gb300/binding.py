@@ -24,11 +24,12 @@ STATUS = {
 }
 FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
 FA_DQ_AUTO, FA_DQ_SEPARATE_PASS, FA_DQ_REDUCTION = 0, 1, 2
+FA_FP32_AUTO, FA_FP32_EXACT, FA_FP32_SPLIT = 0, 1, 2
 
 # every function include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq",
            "fa_bwd_grads", "fa_fwd_strided", "fa_bwd_strided", "fa_fwd_bwd",
-           "fa_bwd_noalloc", "fa_noalloc_scratch_bytes", "fa_path_name", "fa_set_dq_strategy",
+           "fa_bwd_noalloc", "fa_noalloc_scratch_bytes", "fa_path_name", "fa_set_fp32_mode", "fa_set_dq_strategy",
            "fa_bwd_dq_strategy", "fa_get_device_status",
            "fa_reset_device_status", "fa_set_wait_limit", "fa_debug_force_stall", "fa_debug_build",
            "fa_debug_tile_rows", "fa_debug_reset_tile_rows", "fa_status_string")
@@ -99,6 +100,8 @@ def _load(path) -> ctypes.CDLL:
     L.fa_noalloc_scratch_bytes.restype = sz
     L.fa_path_name.argtypes = [i, i, i, i, i]
     L.fa_path_name.restype = ctypes.c_char_p
+    L.fa_set_fp32_mode.argtypes = [i]
+    L.fa_set_fp32_mode.restype = i
     L.fa_set_dq_strategy.argtypes = [i]
     L.fa_set_dq_strategy.restype = i
     L.fa_bwd_dq_strategy.argtypes = [i, i, i, i, i, i, i]
@@ -242,6 +245,24 @@ def set_dq_strategy(strategy: int) -> int:
     if prev < 0:
         raise ValueError(f"unknown dQ strategy {strategy}")
     return prev
+
+
+def set_fp32_mode(mode: int) -> int:
+    """fa_set_fp32_mode: FA_FP32_AUTO, FA_FP32_EXACT or FA_FP32_SPLIT; returns the previous one."""
+    prev = int(lib().fa_set_fp32_mode(int(mode)))
+    if prev < 0:
+        raise ValueError(f"unknown fp32 mode {mode}")
+    return prev
+
+
+@contextlib.contextmanager
+def fp32_mode(mode: int):
+    """Within the block, fp32 inputs run in `mode` (the library's setting, restored after)."""
+    prev = set_fp32_mode(mode)
+    try:
+        yield
+    finally:
+        set_fp32_mode(prev)
 
 
 def dq_strategy(Q, K, is_causal=False) -> int:

@@ -10,6 +10,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -122,27 +123,103 @@ fa_status take_strides(const fa_strides *in, int B, int H, int N, int d, fa_dtyp
     return FA_OK;
 }
 
-// Backward workspace.  CUDA-core path: D (BH*Nq fp32).  Tensor-core path:
-// D then L*log2(e), each BH * padded_rows(Nq) fp32, then (dQ by reduction) the
-// fp32 dQ accumulator (see fa_tc_bwd.cu).
+// Backward workspace.  CUDA-core path: D (BH*Nq fp32) at sd_off.  Tensor-core
+// path: -D then -L*log2(e), each BH * padded_rows(Nq) fp32, then (dQ by
+// reduction) the fp32 dQ accumulator (see fa_tc_bwd.cu).  fp32 inputs that may
+// take the split pairs (for some scale: the preprocessing phase has no scale
+// argument) get both layouts: the tensor-core rows, the split bf16 copies of Q,
+// dO, K and V (256 bytes per row each), and the CUDA-core D at sd_off.
 struct Workspace {
     bool tc;
     size_t d_off, l_off, dqa_off, total;
-    bool red;   // dQ by fp32 reduction into the accumulator at dqa_off
+    bool red;           // dQ by fp32 reduction into the accumulator at dqa_off
+    bool x3;            // this call runs on split bf16 copies at q2_off, do2_off, k2_off, v2_off
+    bool x3_possible;   // some scale would (the layout then holds both paths' data)
+    size_t q2_off, do2_off, k2_off, v2_off;
+    size_t sd_off;      // D of the CUDA-core kernels
 };
+size_t x3_bytes(const FaProblem &p, int N) { return align_up((size_t)p.BH * N * kX3RowBytes, 256); }
 Workspace workspace_layout(const FaProblem &p) {
     Workspace w{};
     w.tc = tc_bwd_supported(p);
-    const size_t rows = w.tc ? tc_bwd_ld_rows(p) : (size_t)p.BH * p.Nq;
+    w.x3_possible = tc_x3_possible(p);
+    w.x3 = w.x3_possible && tc_x3(p);
+    const bool tc_rows = w.tc || w.x3_possible;
+    const size_t rows = tc_rows ? tc_bwd_ld_rows(p) : (size_t)p.BH * p.Nq;
     const size_t bytes = align_up(rows * sizeof(float), 256);
     const size_t dqa = w.tc ? tc_bwd_dqa_floats(p) * sizeof(float) : 0;
     w.red = dqa > 0;
     w.d_off = 0;
     w.l_off = bytes;
     w.dqa_off = 2 * bytes;
-    w.total = w.tc ? 2 * bytes + align_up(dqa, 256) : bytes;
+    w.sd_off = 0;
+    w.total = tc_rows ? 2 * bytes + align_up(dqa, 256) : bytes;
+    if (w.x3_possible) {
+        w.q2_off = w.total;
+        w.do2_off = w.q2_off + x3_bytes(p, p.Nq);
+        w.k2_off = w.do2_off + x3_bytes(p, p.Nq);
+        w.v2_off = w.k2_off + x3_bytes(p, p.Nk);
+        w.sd_off = w.v2_off + x3_bytes(p, p.Nk);
+        w.total = w.sd_off + align_up((size_t)p.BH * p.Nq * sizeof(float), 256);
+    }
     if (w.total == 0) w.total = 256;
     return w;
+}
+
+// fp32 inputs on the tensor cores: Q, K, V split into the bf16 pair copies at q2, k2, v2
+cudaError_t split_qkv(const FaProblem &p, const void *Q, const void *K, const void *V, void *q2, void *k2, void *v2,
+                      cudaStream_t st) {
+    const void *X[3] = {Q, K, V};
+    const FaStrides s[3] = {p.sQ, p.sK, p.sV};
+    const int N[3] = {p.Nq, p.Nk, p.Nk};
+    void *X2[3] = {q2, k2, v2};
+    return tc_split_x3(p, 3, X, s, N, X2, st);
+}
+
+// The forward alone has no workspace argument, so fp32 inputs take their split
+// copies from a stream-ordered pool of the library's own, one per device, that
+// keeps its memory between calls: the first call (or the first larger one)
+// allocates, later ones reuse the memory without synchronising anything.
+cudaError_t x3_pool(cudaMemPool_t *out) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static cudaMemPool_t pools[kMaxDevices] = {};
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return e;
+        uint64_t keep = UINT64_MAX;   // never hand memory back between calls
+        if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return e;
+        }
+        pools[dev] = pool;
+    }
+    *out = pools[dev];
+    return cudaSuccess;
+}
+
+cudaError_t fwd_x3_pooled(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
+                          cudaStream_t st) {
+    const size_t qb = x3_bytes(p, p.Nq), kb = x3_bytes(p, p.Nk);
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = x3_pool(&pool);
+    if (e != cudaSuccess) return e;
+    void *buf = nullptr;
+    if ((e = cudaMallocFromPoolAsync(&buf, qb + 2 * kb, pool, st)) != cudaSuccess) return e;
+    char *b = static_cast<char *>(buf);
+    e = split_qkv(p, Q, K, V, b, b + qb, b + qb + kb, st);
+    if (e == cudaSuccess) e = tc_fwd_x3(p, b, b + qb, b + qb + kb, O, L, st);
+    const cudaError_t f = cudaFreeAsync(buf, st);   // stream-ordered: after the forward's reads
+    return e != cudaSuccess ? e : f;
 }
 
 fa_status bwd_args(const void *Q, const void *K, const void *V, const void *dO, const float *L, const void *dQ,
@@ -172,11 +249,14 @@ fa_status run_fwd(const FaProblem &p, const void *Q, const void *K, const void *
     fa_status s = device_ok();
     if (s != FA_OK) return s;
     const cudaStream_t st = as_stream(stream);
+    if (tc_x3(p)) return map_cuda(fwd_x3_pooled(p, Q, K, V, O, L, st));
     return map_cuda(tc_fwd_supported(p) ? tc_fwd(p, Q, K, V, O, L, st) : simt_fwd(p, Q, K, V, O, L, st));
 }
 
+// scale_known: false for the exported preprocessing phase, whose fp32 inputs may
+// go either way afterwards; it then prepares both paths' data
 fa_status run_preprocess(const FaProblem &p, const Workspace &w, const void *O, const void *dO, const float *L,
-                         void *workspace, fa_stream_t stream) {
+                         void *workspace, fa_stream_t stream, bool scale_known = true) {
     if ((long long)p.BH * p.Nq == 0) return FA_OK;
     fa_status s = device_ok();
     if (s != FA_OK) return s;
@@ -184,8 +264,30 @@ fa_status run_preprocess(const FaProblem &p, const Workspace &w, const void *O, 
     float *Dv = reinterpret_cast<float *>(ws + w.d_off);
     const cudaStream_t st = as_stream(stream);
     float *dqa = w.red ? reinterpret_cast<float *>(ws + w.dqa_off) : nullptr;
-    return map_cuda(w.tc ? tc_bwd_preprocess(p, O, dO, L, Dv, reinterpret_cast<float *>(ws + w.l_off), dqa, st)
-                         : simt_bwd_preprocess(p, O, dO, Dv, st));
+    if (w.x3 || (w.x3_possible && !scale_known)) {
+        // the row constants and dO's split copy; without the scale, the CUDA-core
+        // kernels' D as well (their own preprocessing: the same bits as fa_bwd's)
+        cudaError_t e =
+            tc_bwd_preprocess_x3(p, O, dO, L, Dv, reinterpret_cast<float *>(ws + w.l_off), ws + w.do2_off, st);
+        if (e == cudaSuccess && !scale_known)
+            e = simt_bwd_preprocess(p, O, dO, reinterpret_cast<float *>(ws + w.sd_off), st);
+        return map_cuda(e);
+    }
+    if (!w.tc) return map_cuda(simt_bwd_preprocess(p, O, dO, reinterpret_cast<float *>(ws + w.sd_off), st));
+    return map_cuda(tc_bwd_preprocess(p, O, dO, L, Dv, reinterpret_cast<float *>(ws + w.l_off), dqa, st));
+}
+
+// fp32 inputs on the tensor cores: Q, K, V split into the workspace, then the gradient
+// items on the copies (dO's copy was made by the preprocessing)
+fa_status run_grads_x3(const FaProblem &p, const Workspace &w, const void *Q, const void *K, const void *V,
+                       void *dQ, void *dK, void *dV, bool do_kv, bool do_q, void *workspace, cudaStream_t st) {
+    char *ws = static_cast<char *>(workspace);
+    cudaError_t e = split_qkv(p, Q, K, V, ws + w.q2_off, ws + w.k2_off, ws + w.v2_off, st);
+    if (e == cudaSuccess)
+        e = tc_bwd_grads_x3(p, ws + w.q2_off, ws + w.k2_off, ws + w.v2_off, ws + w.do2_off,
+                            reinterpret_cast<const float *>(ws + w.l_off), reinterpret_cast<const float *>(ws + w.d_off),
+                            dQ, dK, dV, do_kv, do_q, st);
+    return map_cuda(e);
 }
 
 fa_status run_dkdv(const FaProblem &p, const Workspace &w, const void *Q, const void *K, const void *V,
@@ -199,10 +301,12 @@ fa_status run_dkdv(const FaProblem &p, const Workspace &w, const void *Q, const 
         if (e == cudaSuccess) e = simt_zero_rows(p, dV, p.sdV, p.Nk, st);
         return map_cuda(e);
     }
+    if (w.x3) return run_grads_x3(p, w, Q, K, V, nullptr, dK, dV, true, false, workspace, st);
     char *ws = static_cast<char *>(workspace);
     const float *Dv = reinterpret_cast<const float *>(ws + w.d_off);
     return map_cuda(w.tc ? tc_bwd_dkdv(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off), Dv, dK, dV, st)
-                         : simt_bwd_dkdv(p, Q, K, V, dO, L, Dv, dK, dV, st));
+                         : simt_bwd_dkdv(p, Q, K, V, dO, L, reinterpret_cast<const float *>(ws + w.sd_off), dK, dV,
+                                         st));
 }
 
 fa_status run_dq(const FaProblem &p, const Workspace &w, const void *Q, const void *K, const void *V,
@@ -213,8 +317,9 @@ fa_status run_dq(const FaProblem &p, const Workspace &w, const void *Q, const vo
     char *ws = static_cast<char *>(workspace);
     const float *Dv = reinterpret_cast<const float *>(ws + w.d_off);
     const cudaStream_t st = as_stream(stream);
+    if (w.x3) return run_grads_x3(p, w, Q, K, V, dQ, nullptr, nullptr, false, true, workspace, st);
     return map_cuda(w.tc ? tc_bwd_dq(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off), Dv, dQ, st)
-                         : simt_bwd_dq(p, Q, K, V, dO, L, Dv, dQ, st));
+                         : simt_bwd_dq(p, Q, K, V, dO, L, reinterpret_cast<const float *>(ws + w.sd_off), dQ, st));
 }
 
 fa_status run_grads(const FaProblem &p, const Workspace &w, const void *Q, const void *K, const void *V,
@@ -228,6 +333,7 @@ fa_status run_grads(const FaProblem &p, const Workspace &w, const void *Q, const
     }
     fa_status s = device_ok();
     if (s != FA_OK) return s;
+    if (w.x3) return run_grads_x3(p, w, Q, K, V, dQ, dK, dV, true, true, workspace, as_stream(stream));
     char *ws = static_cast<char *>(workspace);
     float *dqa = w.red ? reinterpret_cast<float *>(ws + w.dqa_off) : nullptr;
     return map_cuda(tc_bwd_grads(p, Q, K, V, dO, reinterpret_cast<const float *>(ws + w.l_off),
@@ -272,7 +378,15 @@ void fa_debug_force_stall(int on) { g_force_stall.store(on ? 1u : 0u, std::memor
 const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype dtype) {
     FaProblem p{};
     if (check_common(1, 1, Nq, Nk, d, is_causal, dtype, 1.f, false, &p) != FA_OK) return nullptr;
+    p.scale = 1.f / sqrtf((float)d);   // the default scale
     return tc_fwd_supported(p) ? "tc" : "simt";
+}
+
+int fa_set_fp32_mode(int mode) {
+    if (mode < FA_FP32_AUTO || mode > FA_FP32_SPLIT) return -1;
+    const int prev = tc_get_fp32_mode();
+    tc_set_fp32_mode(mode);
+    return prev;
 }
 
 int fa_set_dq_strategy(int strategy) {
@@ -313,7 +427,7 @@ fa_status fa_fwd_strided(const void *Q, const fa_strides *sQ, const void *K, con
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype) {
     FaProblem p{};
     if (check_common(B, H, Nq, Nk, d, is_causal, dtype, 1.f, false, &p) != FA_OK) return 0;
-    return workspace_layout(p).total;
+    return workspace_layout(p).total;   // (the layout does not depend on the scale)
 }
 
 fa_status fa_bwd_preprocess(const void *O, const void *dO, const float *L, int B, int H, int Nq, int Nk, int d,
@@ -326,7 +440,7 @@ fa_status fa_bwd_preprocess(const void *O, const void *dO, const float *L, int B
     if (s != FA_OK) return s;
     if ((long long)p.BH * p.Nq == 0) return FA_OK;
     if ((s = check_ptrs({O, dO, L})) != FA_OK) return s;
-    return run_preprocess(p, w, O, dO, L, workspace, stream);
+    return run_preprocess(p, w, O, dO, L, workspace, stream, false);
 }
 
 fa_status fa_bwd_dkdv(const void *Q, const void *K, const void *V, const void *dO, const float *L, void *dQ,
@@ -416,6 +530,20 @@ fa_status fa_fwd_bwd(const void *Q, const void *K, const void *V, const void *dO
     if (s != FA_OK) return s;
     if ((long long)p.BH * p.Nq == 0 && (long long)p.BH * p.Nk == 0) return FA_OK;
     if ((s = bwd_ptrs(p, Q, K, V, O, dO, L, dQ, dK, dV)) != FA_OK) return s;
+    if (w.x3) {
+        // fp32 on the tensor cores: Q, K, V split once into the workspace serve both passes
+        if ((s = device_ok()) != FA_OK) return s;
+        const cudaStream_t st = as_stream(stream);
+        char *ws = static_cast<char *>(workspace);
+        float *Dv = reinterpret_cast<float *>(ws + w.d_off), *Lv = reinterpret_cast<float *>(ws + w.l_off);
+        cudaError_t e = split_qkv(p, Q, K, V, ws + w.q2_off, ws + w.k2_off, ws + w.v2_off, st);
+        if (e == cudaSuccess) e = tc_fwd_x3(p, ws + w.q2_off, ws + w.k2_off, ws + w.v2_off, O, L, st);
+        if (e == cudaSuccess) e = tc_bwd_preprocess_x3(p, O, dO, L, Dv, Lv, ws + w.do2_off, st);
+        if (e == cudaSuccess)
+            e = tc_bwd_grads_x3(p, ws + w.q2_off, ws + w.k2_off, ws + w.v2_off, ws + w.do2_off, Lv, Dv, dQ, dK, dV,
+                                true, true, st);
+        return map_cuda(e);
+    }
     bool prep_done = false;
     if (w.tc && (long long)p.BH * p.Nq > 0) {
         // tensor-core path: the forward's epilogue also forms D = rowsum(dO * O) from

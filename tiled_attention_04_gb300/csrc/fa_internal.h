@@ -68,7 +68,7 @@ cudaError_t tc_set_smem_once(const void *kernel, int bytes);
 int tc_sm_count();
 
 // ---- tcgen05 tensor-core kernels (fa_tc_fwd.cu, fa_tc_bwd.cu): bf16, d in {16, 32, 64, 128}
-// (16 and 32 run the d = 64 kernels with zero-filled columns).
+// (16 and 32 run the d = 64 kernels with zero-filled columns), and fp32 with d <= 64 (X3 below).
 bool tc_fwd_supported(const FaProblem &p);
 bool tc_bwd_supported(const FaProblem &p);
 // The backward's preprocessing done by the forward's epilogue when dO is known
@@ -81,6 +81,30 @@ struct FwdPrep {
     float *Dp, *Lp;   // per batch*head, padded_rows(Nq) rows
     float *dQa;       // NULL unless dQ is formed by reduction
 };
+// ---- fp32 inputs with d in {16, 32, 64} (X3): each operand is first split into a
+// bf16 pair (hi = bf16(x), lo = bf16(x - hi)) held as a contiguous (B*H, N, 128)
+// bf16 copy, hi in columns [0, 64) and lo in [64, 128); the d = 128 kernels then
+// take three products per contraction (hi hi + hi lo + lo hi).
+bool tc_x3(const FaProblem &p);            // this problem runs X3 (mode, shape and scale)
+bool tc_x3_possible(const FaProblem &p);   // X3 for some scale (mode and shape): workspace sizing
+void tc_disable_x3(bool off);   // for the calling thread's calls (off: fp32 on the CUDA cores)
+void tc_set_fp32_mode(int mode);          // FA_FP32_AUTO / _EXACT / _SPLIT
+int tc_get_fp32_mode();
+constexpr size_t kX3RowBytes = 256;   // bytes of one split row
+// count (1..4) tensors X[i] with strides s[i] and N[i] rows per batch*head -> X2[i]
+cudaError_t tc_split_x3(const FaProblem &p, int count, const void *const *X, const FaStrides *s, const int *N,
+                        void *const *X2, cudaStream_t st);
+// forward on split copies; O (fp32) is written through p.sO
+cudaError_t tc_fwd_x3(const FaProblem &p, const void *Q2, const void *K2, const void *V2, void *O, float *L,
+                      cudaStream_t st);
+// backward on split copies: -D, -L*log2(e) rows as tc_bwd_preprocess (from fp32 O and
+// dO through p.sO, p.sdO) plus dO's split copy; then the gradient items (dQ by the
+// separate pass), dQ, dK, dV written in fp32 through their strides
+cudaError_t tc_bwd_preprocess_x3(const FaProblem &p, const void *O, const void *dO, const float *L, float *Dp,
+                                 float *Lp, void *dO2, cudaStream_t st);
+cudaError_t tc_bwd_grads_x3(const FaProblem &p, const void *Q2, const void *K2, const void *V2, const void *dO2,
+                            const float *Lp, const float *Dp, void *dQ, void *dK, void *dV, bool do_kv, bool do_q,
+                            cudaStream_t st);
 // Forward.  With prep (dO not NULL) the forward's epilogue also does the
 // backward's preprocessing (*prep_done tells whether it did).
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,

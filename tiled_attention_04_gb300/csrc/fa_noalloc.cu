@@ -21,6 +21,7 @@
 //    reloads the module (and the array) elsewhere, so no call may follow a reset;
 //  * where the library would form dQ by reduction (an fp32 dQ accumulator in the
 //    workspace) and that does not fit, the call forms dQ by the separate pass;
+//    fp32 inputs whose split bf16 copies do not fit run the CUDA-core kernels;
 //    shapes whose workspace exceeds FA_NOALLOC_SCRATCH_BYTES even so are refused
 //    with FA_ERR_WORKSPACE before anything is launched.
 #include <cuda_runtime.h>
@@ -77,7 +78,16 @@ fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V, const void
     // does not fit the array, this call forms dQ by the separate pass, which needs
     // only the two per-row constants
     DqStrategy forced = DqStrategy::kAuto;
-    if (need > FA_NOALLOC_SCRATCH_BYTES) {
+    bool x3_off = false;
+    if (need > FA_NOALLOC_SCRATCH_BYTES && dtype == FA_DTYPE_F32) {
+        // fp32 inputs: the split bf16 copies of the tensor-core path (1 KB per query
+        // and key row) do not fit; the CUDA-core kernels need only D
+        tc_disable_x3(true);
+        need = fa_bwd_workspace_size(B, H, Nq, Nk, d, is_causal, dtype);
+        tc_disable_x3(false);
+        if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+        x3_off = true;
+    } else if (need > FA_NOALLOC_SCRATCH_BYTES) {
         tc_override_dq_strategy(DqStrategy::kSeparatePass);
         need = fa_bwd_workspace_size(B, H, Nq, Nk, d, is_causal, dtype);
         tc_override_dq_strategy(DqStrategy::kAuto);
@@ -88,8 +98,10 @@ fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V, const void
     fa_status s = scratch_for_current_device(&scratch);
     if (s != FA_OK) return s;
     tc_override_dq_strategy(forced);
+    tc_disable_x3(x3_off);
     s = fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, is_causal, dtype, scratch,
                FA_NOALLOC_SCRATCH_BYTES, stream);
+    tc_disable_x3(false);
     tc_override_dq_strategy(DqStrategy::kAuto);
     return s;
 }

@@ -127,6 +127,40 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__
     }
 }
 
+// fp32 inputs (X3): the same row constants from fp32 O and dO (head dim up to
+// 64), and dO split into its bf16 pair row [hi | lo] (zeros past d) for the
+// gradient launch.  Sixteen threads per row, four columns each.
+__global__ void __launch_bounds__(256) fa_bwd_pre_x3_kernel(const float *__restrict__ O, const float *__restrict__ dO,
+                                                            const float *__restrict__ L, float *__restrict__ Dp,
+                                                            float *__restrict__ Lp, __nv_bfloat16 *__restrict__ dO2,
+                                                            int Nq, int H, int d, FaStrides so, FaStrides sdo) {
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();   // O (from the forward) and dO are complete
+    const int nqp = padded_rows(Nq);
+    const long long gr = (long long)blockIdx.x * 16 + threadIdx.x / 16;   // padded row (rows per block divide 128)
+    const int bh = (int)(gr / nqp), q = (int)(gr - (long long)bh * nqp);
+    const int cg = threadIdx.x % 16;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (q < Nq && 4 * cg < d) {
+        a = __ldg(reinterpret_cast<const float4 *>(O + fa_row_offset(so, H, bh, q) + 4 * cg));
+        b = __ldg(reinterpret_cast<const float4 *>(dO + fa_row_offset(sdo, H, bh, q) + 4 * cg));
+    }
+    const float lrow = (cg == 0 && q < Nq) ? __ldg(L + (long long)bh * Nq + q) : 0.f;
+    float acc = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (q < Nq) {
+        const uint32_t h0 = tc::pack_bf16(b.x, b.y), h1 = tc::pack_bf16(b.z, b.w);
+        uint2 *dst = reinterpret_cast<uint2 *>(dO2 + ((long long)bh * Nq + q) * 128);
+        dst[cg] = make_uint2(h0, h1);
+        dst[16 + cg] = make_uint2(tc::pack_bf16_residual(b.x, b.y, h0), tc::pack_bf16_residual(b.z, b.w, h1));
+    }
+    if (cg == 0) {
+        Dp[gr] = q < Nq ? -acc : 0.f;
+        Lp[gr] = q < Nq ? -lrow * kLog2e : -INFINITY;
+    }
+}
+
 // ------------------------------------------------------------------ dQ from its fp32 accumulator
 // dQ = scale * dQa, rounded to bf16: 8 columns per thread (two 16-byte loads,
 // one 16-byte store), grid-stride over the BH * Nq rows' d / 8 column groups.
@@ -1052,15 +1086,22 @@ struct DkdvNarrowCfg {
     static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
 };
 
-// one dK/dV work item: key tile kt of batch*head bh (a half of it when SPLIT = 2)
-template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
+// one dK/dV work item: key tile kt of batch*head bh (a half of it when SPLIT = 2).
+// X3 (fp32 inputs, head dim up to 64, operands as bf16 pairs [hi | lo] in the
+// d = 128 layout): S^T and dP^T take the chunk pairs (hi, hi), (hi, lo), (lo, hi);
+// P^T and dS^T are split too (lo in the second 32 columns of their TMEM
+// buffers), dV = Phi^T [dOhi | dOlo] + Plo^T dOhi and dK likewise; output column
+// c is accumulator column c plus 64 + c, written in fp32.
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool X3 = false>
 __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                           const CUtensorMap &tmdO, const float *__restrict__ Lp,
-                                          const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
-                                          __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, int H,
+                                          const float *__restrict__ Dp, void *__restrict__ dKv,
+                                          void *__restrict__ dVv, int Nq, int Nk, int kt, int bh, int H,
                                           int dv, const FaStrides &sdk, const FaStrides &sdv, float scale,
                                           float scale_log2, uint32_t wait_limit) {
+    static_assert(!X3 || (D == 128 && !VIEW4), "split fp32 operands use the d = 128 layout of contiguous copies");
     using C = DkdvNarrowCfg<D>;
+    __nv_bfloat16 *dK = static_cast<__nv_bfloat16 *>(dKv), *dV = static_cast<__nv_bfloat16 *>(dVv);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1174,6 +1215,7 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
         if (n > 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BQ, false, false);
             constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
+            constexpr uint32_t idesc_g_hi = tc::idesc_bf16(128, 64, false, true);   // X3: lo times hi
             const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);     // A of S^T, K-major
             const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, 16, 1024);     // A of dP^T
             const uint64_t qk = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);     // B of S^T, K-major, stage 0
@@ -1193,6 +1235,13 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                         tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + kk * 8, om + st + kk * 128, idesc_g, acc);
                         tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + kk * 8, qm + st + kk * 128, idesc_g, acc);
                     }
+                    if constexpr (X3) {   // Plo^T dOhi and dSlo^T Qhi into the first 64 columns
+#pragma unroll
+                        for (int kk = 0; kk < C::BQ / 16; ++kk) {
+                            tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + 32 + kk * 8, om + st + kk * 128, idesc_g_hi, 1u);
+                            tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 96 + kk * 8, qm + st + kk * 128, idesc_g_hi, 1u);
+                        }
+                    }
                     tc::mma_commit(q_empty(s));   // sub-tile `it` done: its stage is free
                 }
                 __syncwarp();
@@ -1203,10 +1252,13 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                 if (!(ok = __all_sync(0xffffffffu, W.wait(q_full(s), (it / C::STAGES) & 1)))) break;
                 if (leader) {
                     const uint32_t st = (s * C::QT::BYTES) >> 4;
+                    // X3: chunk pairs (hi, hi), (hi, lo), (lo, hi), four k-steps each
+                    constexpr int KSTEPS = X3 ? 12 : D / 16;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q^T and dP^T = V dO^T, interleaved
-                        const uint32_t oa = ((kk >> 2) * C::KT::CHUNK + (kk & 3) * 32) >> 4;
-                        const uint32_t ob = ((kk >> 2) * C::QT::CHUNK + (kk & 3) * 32) >> 4;
+                    for (int kk = 0; kk < KSTEPS; ++kk) {   // S^T = K Q^T and dP^T = V dO^T, interleaved
+                        const int ca = X3 ? ((kk >> 2) == 2) : (kk >> 2), cb = X3 ? ((kk >> 2) == 1) : (kk >> 2);
+                        const uint32_t oa = (ca * C::KT::CHUNK + (kk & 3) * 32) >> 4;
+                        const uint32_t ob = (cb * C::QT::CHUNK + (kk & 3) * 32) >> 4;
                         tc::mma_ss(tmem + 128 * t, kd + oa, qk + st + ob, idesc_s, kk > 0 ? 1u : 0u);
                         tc::mma_ss(tmem + 128 * t + 64, vd + oa, ok_ + st + ob, idesc_s, kk > 0 ? 1u : 0u);
                     }
@@ -1263,6 +1315,7 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                     if (c < first_visible) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
             }
             uint32_t pp[32], dsp[32];
+            uint32_t ppl[X3 ? 32 : 1], dspl[X3 ? 32 : 1];   // X3: the bf16 residuals
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float4 nl = *reinterpret_cast<const float4 *>(lds + 4 * i);
@@ -1281,10 +1334,18 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                     tc::mul2(g0, g1, g0, g1, p0, p1);
                     pp[2 * i + h] = tc::pack_bf16(p0, p1);
                     dsp[2 * i + h] = tc::pack_bf16(g0, g1);
+                    if constexpr (X3) {
+                        ppl[2 * i + h] = tc::pack_bf16_residual(p0, p1, pp[2 * i + h]);
+                        dspl[2 * i + h] = tc::pack_bf16_residual(g0, g1, dsp[2 * i + h]);
+                    }
                 }
             }
             tmem_st_x32(tS, pp);
             tmem_st_x32(tP, dsp);
+            if constexpr (X3) {   // over S^T / dP^T columns 32..63, already read
+                tmem_st_x32(tS + 32, ppl);
+                tmem_st_x32(tP + 32, dspl);
+            }
             tc::tmem_st_wait();
             tc::fence_before_sync();
             tc::mbar_arrive(p_full(t));
@@ -1334,6 +1395,40 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                 }
             }
             tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, rank ^ 1u));   // release: the stores above
+        } else if constexpr (X3) {
+            if constexpr (SPLIT > 1) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 2u);
+            const float *pr = reinterpret_cast<const float *>(sb + (part - base));
+            float *drow = static_cast<float *>(t == 0 ? dVv : dKv) +
+                          fa_row_offset(t == 0 ? sdv : sdk, tc::opaque(H), bh, key);
+            // accumulator chunk c (hi products) plus chunk c + 2 (hi x lo products): output columns 32c..32c+31
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t a[32], b[32];
+                if (fine && n > 0) {
+                    tmem_ld_x32(tA + 32 * c, a);
+                    tmem_ld_x32(tA + 32 * (c + 2), b);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(a);
+                    reg_fence_x32(b);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) a[i] = b[i] = 0u;
+                }
+                float o[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x = __uint_as_float(a[i]) + __uint_as_float(b[i]);
+                    if (merge) x += pr[32 * c + i] + pr[32 * (c + 2) + i];
+                    o[i] = x * mul;
+                }
+                if (fine && (SPLIT == 1 || merge) && key < Nk) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (32 * c + 4 * i < dv)   // columns past the head dim are padding
+                            reinterpret_cast<float4 *>(drow + 32 * c)[i] =
+                                make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                }
+            }
         } else {
             if constexpr (SPLIT > 1) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 2u);
             const float *pr = reinterpret_cast<const float *>(sb + (part - base));
@@ -1408,15 +1503,20 @@ struct DqNarrowCfg {
     static constexpr uint32_t DQ_COL = 256;
 };
 
-// one dQ work item: query tile qt of batch*head bh (a half of its keys when SPLIT = 2)
-template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
+// one dQ work item: query tile qt of batch*head bh (a half of its keys when SPLIT = 2).
+// X3 as in dkdv_item_narrow: S and dP from three chunk pairs, dS split in TMEM
+// (lo in the second 32 columns of its buffer), dQ = dShi [Khi | Klo] + dSlo Khi,
+// output column c = accumulator column c plus 64 + c, written in fp32.
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool X3 = false>
 __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                         const CUtensorMap &tmdO, const float *__restrict__ Lp,
-                                        const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ, int Nq, int Nk,
+                                        const float *__restrict__ Dp, void *__restrict__ dQv, int Nq, int Nk,
                                         int qt, int bh, int H, int dv, const FaStrides &sdq, float scale,
                                         float scale_log2,
                                         uint32_t wait_limit) {
+    static_assert(!X3 || (D == 128 && !VIEW4), "split fp32 operands use the d = 128 layout of contiguous copies");
     using C = DqNarrowCfg<D>;
+    __nv_bfloat16 *dQ = static_cast<__nv_bfloat16 *>(dQv);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1521,6 +1621,7 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
         const bool leader = tc::elect_one();
         constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BK, false, false);
         constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
+        constexpr uint32_t idesc_g_hi = tc::idesc_bf16(128, 64, false, true);   // X3: dSlo Khi
         const uint64_t qd = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);      // A of S, K-major
         const uint64_t od = tc::sdesc_sw128(base + C::DO_OFF, 16, 1024);     // A of dP
         const uint64_t kk_ = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);    // B of S, K-major, stage 0
@@ -1537,6 +1638,11 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                 for (int kk = 0; kk < C::BK / 16; ++kk)
                     tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 64 + kk * 8, km + st + kk * 128, idesc_g,
                                (j > 0 || kk > 0) ? 1u : 0u);
+                if constexpr (X3) {
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / 16; ++kk)
+                        tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 96 + kk * 8, km + st + kk * 128, idesc_g_hi, 1u);
+                }
                 tc::mma_commit(kv_empty(s));   // sub-tile j done: its stage is free
             }
             __syncwarp();
@@ -1547,10 +1653,13 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
             if (!(ok = __all_sync(0xffffffffu, W.wait(kv_full(s), (j / C::STAGES) & 1)))) break;
             if (leader) {
                 const uint32_t st = (s * C::KT::BYTES) >> 4;
+                // X3: chunk pairs (hi, hi), (hi, lo), (lo, hi), four k-steps each
+                constexpr int KSTEPS = X3 ? 12 : D / 16;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {   // S = Q K^T and dP = dO V^T, interleaved
-                    const uint32_t oa = ((kk >> 2) * C::QT::CHUNK + (kk & 3) * 32) >> 4;
-                    const uint32_t ob = ((kk >> 2) * C::KT::CHUNK + (kk & 3) * 32) >> 4;
+                for (int kk = 0; kk < KSTEPS; ++kk) {   // S = Q K^T and dP = dO V^T, interleaved
+                    const int ca = X3 ? ((kk >> 2) == 2) : (kk >> 2), cb = X3 ? ((kk >> 2) == 1) : (kk >> 2);
+                    const uint32_t oa = (ca * C::QT::CHUNK + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = (cb * C::KT::CHUNK + (kk & 3) * 32) >> 4;
                     tc::mma_ss(tmem + 128 * t, qd + oa, kk_ + st + ob, idesc_s, kk > 0 ? 1u : 0u);
                     tc::mma_ss(tmem + 128 * t + 64, od + oa, vk + st + ob, idesc_s, kk > 0 ? 1u : 0u);
                 }
@@ -1602,6 +1711,7 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                     if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
             }
             uint32_t dsp[32];
+            uint32_t dspl[X3 ? 32 : 1];   // X3: the bf16 residuals
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int c = 2 * i;
@@ -1613,8 +1723,10 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                          ndrow, ndrow);
                 tc::mul2(g0, g1, g0, g1, p0, p1);
                 dsp[i] = tc::pack_bf16(g0, g1);
+                if constexpr (X3) dspl[i] = tc::pack_bf16_residual(g0, g1, dsp[i]);
             }
             tmem_st_x32(tP, dsp);
+            if constexpr (X3) tmem_st_x32(tP + 32, dspl);   // over dP columns 32..63, already read
             tc::tmem_st_wait();
             tc::fence_before_sync();
             tc::mbar_arrive(p_full(t));
@@ -1641,7 +1753,7 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
             const uint32_t rdst = tc::map_to_rank(part, rank ^ 1u);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
-                const int col = t * (D / 2) + 32 * c;
+                const int col = X3 ? t * 32 + 64 * c : t * (D / 2) + 32 * c;
                 uint32_t a[32];
                 if (fine && n > 0) {
                     tmem_ld_x32(tA + col, a);
@@ -1658,6 +1770,36 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                 }
             }
             tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, rank ^ 1u));   // release: the stores above
+        } else if constexpr (X3) {
+            // this warpgroup's output columns [32t, 32t + 32): accumulator columns 32t + i and 64 + 32t + i
+            bool merge = false;
+            if constexpr (SPLIT > 1) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 4u);
+            const float *pr = reinterpret_cast<const float *>(sb + (part - base));
+            uint32_t a[32], b[32];
+            if (fine && n > 0) {
+                tmem_ld_x32(tA + 32 * t, a);
+                tmem_ld_x32(tA + 64 + 32 * t, b);
+                tc::tmem_ld_wait();
+                reg_fence_x32(a);
+                reg_fence_x32(b);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a[i] = b[i] = 0u;
+            }
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float x = __uint_as_float(a[i]) + __uint_as_float(b[i]);
+                if (merge) x += pr[i] + pr[32 + i];
+                o[i] = x * scale;
+            }
+            if (fine && (SPLIT == 1 || merge) && row < Nq) {
+                float *drow = static_cast<float *>(dQv) + fa_row_offset(sdq, tc::opaque(H), bh, row) + 32 * t;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (32 * t + 4 * i < dv)   // columns past the head dim are padding
+                        reinterpret_cast<float4 *>(drow)[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            }
         } else {
             bool merge = false;
             if constexpr (SPLIT > 1) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 4u);
@@ -2121,14 +2263,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // one kernel tail instead of two, and the passes balance each other's load.
 // RED: dK/dV items only, each adding its dQ partials into the fp32 accumulator
 // behind dqa (no dQ items; a short kernel converts the accumulator afterwards).
-template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool RED>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool RED, bool X3 = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap qA, const __grid_constant__ CUtensorMap kA,
                      const __grid_constant__ CUtensorMap vA, const __grid_constant__ CUtensorMap dOA,
                      const __grid_constant__ CUtensorMap qB, const __grid_constant__ CUtensorMap kB,
                      const __grid_constant__ CUtensorMap vB, const __grid_constant__ CUtensorMap dOB,
-                     const __grid_constant__ CUtensorMap dqa, const float *__restrict__ Lp, const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dQ,
-                     __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH,
+                     const __grid_constant__ CUtensorMap dqa, const float *__restrict__ Lp, const float *__restrict__ Dp,
+                     void *__restrict__ dQ, void *__restrict__ dK, void *__restrict__ dV, int Nq, int Nk, int BH,
                      int k_tiles, int q_tiles, int n_kv_items, int n_q_items, float scale, float scale_log2,
                      uint32_t wait_limit, int H, int dv, FaStrides sdq, FaStrides sdk, FaStrides sdv) {
     tc::pdl_launch_dependents();
@@ -2148,19 +2290,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int r = idx / BH;
         const int kt = CAUSAL ? r : k_tiles - 1 - r;    // causal: the first key tiles see the most queries
         if constexpr (D == 64)
-            dkdv_item_wide<D, CAUSAL, SPLIT, VIEW4, RED>(qA, kA, vA, dOA, &dqa, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, dv,
+            dkdv_item_wide<D, CAUSAL, SPLIT, VIEW4, RED>(qA, kA, vA, dOA, &dqa, Lp, Dp,
+                                                         static_cast<__nv_bfloat16 *>(dK),
+                                                         static_cast<__nv_bfloat16 *>(dV), Nq, Nk, kt, bh, H, dv,
                                                          sdk, sdv, scale, scale_log2, wait_limit);
         else
-            dkdv_item_narrow<D, CAUSAL, SPLIT, VIEW4>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, dv, sdk, sdv, scale,
-                                               scale_log2, wait_limit);
+            dkdv_item_narrow<D, CAUSAL, SPLIT, VIEW4, X3>(qA, kA, vA, dOA, Lp, Dp, dK, dV, Nq, Nk, kt, bh, H, dv, sdk,
+                                                          sdv, scale, scale_log2, wait_limit);
     } else if constexpr (!RED) {
         const int qt = q_tiles - 1 - idx / BH;           // causal: the last query tiles see the most keys
         if constexpr (D == 64)
-            dq_item_wide<D, CAUSAL, SPLIT, VIEW4>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, dv, sdq, scale, scale_log2,
-                                           wait_limit);
+            dq_item_wide<D, CAUSAL, SPLIT, VIEW4>(qB, kB, vB, dOB, Lp, Dp, static_cast<__nv_bfloat16 *>(dQ), Nq, Nk,
+                                                  qt, bh, H, dv, sdq, scale, scale_log2, wait_limit);
         else
-            dq_item_narrow<D, CAUSAL, SPLIT, VIEW4>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, dv, sdq, scale, scale_log2,
-                                             wait_limit);
+            dq_item_narrow<D, CAUSAL, SPLIT, VIEW4, X3>(qB, kB, vB, dOB, Lp, Dp, dQ, Nq, Nk, qt, bh, H, dv, sdq, scale,
+                                                        scale_log2, wait_limit);
     }
 }
 
@@ -2232,19 +2376,19 @@ struct Maps2 {
     bool view4;       // 4-D maps over strided views (else 3-D maps over contiguous tensors)
 };
 
-template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool RED>
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool RED, bool X3 = false>
 cudaError_t launch_bwd(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dQ, void *dK,
                        void *dV, bool do_kv, bool do_q, cudaStream_t st) {
     static_assert(!RED || D == 64, "the dQ reduction form exists for the d = 64 items");
+    static_assert(!X3 || (D == 128 && !RED && !VIEW4), "split fp32 operands: d = 128 items, dQ by the separate pass");
     using KvC = std::conditional_t<D == 64, DkdvWideCfg<D, RED>, DkdvNarrowCfg<D>>;
     using QC = std::conditional_t<D == 64, DqWideCfg<D>, DqNarrowCfg<D>>;
     constexpr uint32_t smem = KvC::SMEM_BYTES > QC::SMEM_BYTES ? KvC::SMEM_BYTES : QC::SMEM_BYTES;
     const int kt = (p.Nk + 127) / 128, qt = (p.Nq + 127) / 128;
     const long long na = do_kv ? (long long)kt * p.BH : 0, nb = (do_q && !RED) ? (long long)qt * p.BH : 0;
-    return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4, RED>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q,
-                          m.a.k, m.a.v, m.a.dO, m.b.q, m.b.k, m.b.v, m.b.dO, m.dqa, Lp, Dp,
-                          static_cast<__nv_bfloat16 *>(dQ), static_cast<__nv_bfloat16 *>(dK),
-                          static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH, kt, qt, (int)na, (int)nb, p.scale,
+    return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4, RED, X3>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q,
+                          m.a.k, m.a.v, m.a.dO, m.b.q, m.b.k, m.b.v, m.b.dO, m.dqa, Lp, Dp, dQ, dK, dV, p.Nq, p.Nk,
+                          p.BH, kt, qt, (int)na, (int)nb, p.scale,
                           p.scale * kLog2e, p.wait_limit, p.H, p.d, p.sdQ, p.sdK, p.sdV);
 }
 
@@ -2330,7 +2474,8 @@ DqStrategy tc_get_dq_setting() { return static_cast<DqStrategy>(g_dq_strategy.lo
 // shapes and wherever its items run persistent, the separate pass otherwise.  A
 // forced strategy overrides the choice.
 bool tc_bwd_dq_by_reduction(const FaProblem &p) {
-    if (!tc_bwd_supported(p) || p.d > 64) return false;
+    // (split fp32 operands run the d = 128 items, which form dQ by the separate pass)
+    if (!tc_bwd_supported(p) || p.d > 64 || p.dtype != FA_DTYPE_BF16) return false;
     switch (tc_get_dq_strategy()) {
         case DqStrategy::kSeparatePass: return false;
         case DqStrategy::kReduction: return true;
@@ -2455,6 +2600,52 @@ cudaError_t tc_bwd_dkdv(const FaProblem &p, const void *Q, const void *K, const 
 cudaError_t tc_bwd_dq(const FaProblem &p, const void *Q, const void *K, const void *V, const void *dO,
                       const float *Lp, const float *Dp, void *dQ, cudaStream_t st) {
     return grads_impl(p, Q, K, V, dO, Lp, Dp, nullptr, dQ, nullptr, nullptr, false, true, st);
+}
+
+// ------------------------------------------------------------------ fp32 inputs (X3)
+cudaError_t tc_bwd_preprocess_x3(const FaProblem &p, const void *O, const void *dO, const float *L, float *Dp,
+                                 float *Lp, void *dO2, cudaStream_t st) {
+    const long long rows = (long long)p.BH * padded_rows(p.Nq);
+    if (rows == 0) return cudaSuccess;
+    if (!tc_x3_possible(p)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows / 16));   // rows is a multiple of 128
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_x3_kernel, static_cast<const float *>(O),
+                                       static_cast<const float *>(dO), L, Dp, Lp, static_cast<__nv_bfloat16 *>(dO2),
+                                       p.Nq, p.H, p.d, p.sO, p.sdO);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t tc_bwd_grads_x3(const FaProblem &p, const void *Q2, const void *K2, const void *V2, const void *dO2,
+                            const float *Lp, const float *Dp, void *dQ, void *dK, void *dV, bool do_kv, bool do_q,
+                            cudaStream_t st) {
+    if (!tc_x3(p)) return cudaErrorInvalidValue;
+    // the d = 128 items over the contiguous (B*H, N, 128) copies: 64-row sub-tiles of
+    // the looped-over operand, 128-row tiles of the item's own
+    auto map = [&](CUtensorMap *m, const void *ptr, int N, int rows) {
+        return tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(m), ptr, p.BH, N, 128, rows);
+    };
+    Maps2 m;
+    m.view4 = false;
+    if (!map(&m.a.q, Q2, p.Nq, 64) || !map(&m.a.dO, dO2, p.Nq, 64) || !map(&m.a.k, K2, p.Nk, 128) ||
+        !map(&m.a.v, V2, p.Nk, 128) || !map(&m.b.q, Q2, p.Nq, 128) || !map(&m.b.dO, dO2, p.Nq, 128) ||
+        !map(&m.b.k, K2, p.Nk, 64) || !map(&m.b.v, V2, p.Nk, 64))
+        return cudaErrorInvalidValue;
+    m.dqa = m.a.q;   // unused
+    const bool split = (do_kv && dkdv_split(p)) || (do_q && dq_split(p));
+    if (p.causal)
+        return split ? launch_bwd<128, true, 2, false, false, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                     : launch_bwd<128, true, 1, false, false, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
+    return split ? launch_bwd<128, false, 2, false, false, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                 : launch_bwd<128, false, 1, false, false, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
 }
 
 cudaError_t tc_bwd_read_status(unsigned *out, cudaStream_t st) {

@@ -193,13 +193,56 @@ __device__ __forceinline__ void prep_row_finish(const FwdPrep &prep, float half0
     }
 }
 
-template <int D, bool CAUSAL, int SPLIT, bool VIEW4>
+// ------------------------------------------------------------------ fp32 operands as bf16 pairs
+// X (B, H, N, d) fp32 with d <= 64, through its strides -> X2, B*H*N contiguous
+// rows of 128 bf16: hi = bf16(x) in columns [0, 64), lo = bf16(x - hi) in
+// [64, 128), zeros past d.  x - hi is exact in fp32, so hi + lo meets x to
+// within 2^-17 relative.  Sixteen threads per row, four columns each.
+struct SplitJob {
+    const float *X;
+    __nv_bfloat16 *X2;
+    FaStrides s;
+    int N;
+};
+struct SplitJobs {
+    SplitJob j[4];   // blockIdx.y selects the tensor
+};
+__global__ void __launch_bounds__(256) fa_split_x3_kernel(const __grid_constant__ SplitJobs jobs, int BH, int H,
+                                                          int d) {
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();   // the tensors may come from the previous kernel
+    const SplitJob &J = jobs.j[blockIdx.y];
+    const long long g = (long long)blockIdx.x * 256 + threadIdx.x;
+    const long long row = g >> 4;
+    const int cg = (int)(g & 15);
+    if (row >= (long long)BH * J.N) return;
+    const int bh = (int)(row / J.N), n = (int)(row - (long long)bh * J.N);
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (4 * cg < d) x = __ldg(reinterpret_cast<const float4 *>(J.X + fa_row_offset(J.s, H, bh, n) + 4 * cg));
+    const uint32_t h0 = tc::pack_bf16(x.x, x.y), h1 = tc::pack_bf16(x.z, x.w);
+    uint2 *dst = reinterpret_cast<uint2 *>(J.X2 + row * 128);
+    dst[cg] = make_uint2(h0, h1);
+    dst[16 + cg] = make_uint2(tc::pack_bf16_residual(x.x, x.y, h0), tc::pack_bf16_residual(x.z, x.w, h1));
+}
+
+// X3 (fp32 inputs, head dim up to 64): Q, K and V arrive as bf16 pairs, each
+// 128-column row holding hi = bf16(x) in columns [0, 64) and lo = bf16(x - hi) in
+// [64, 128), and the kernel runs the d = 128 layout with three products per
+// contraction: Q K^T = Qhi Khi^T + Qhi Klo^T + Qlo Khi^T (12 k-steps instead of
+// 8), and P V = Phi [Vhi | Vlo] + Plo Vhi, with P split the same way in TMEM (hi
+// over the first 64 columns of its S, lo over the other 64).  Output column c
+// is then accumulator column c plus column 64 + c, and O is written in fp32.
+// The product lo * lo and the rounding of lo leave a relative error near 2^-16
+// per product, against 2^-8 for one bf16 product.
+template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool X3 = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
+                     const __grid_constant__ CUtensorMap tmV, void *__restrict__ Ov,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
                      uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so, FwdPrep prep) {
+    static_assert(!X3 || (D == 128 && !VIEW4), "split fp32 operands use the d = 128 layout of contiguous copies");
     using C = FwdCfg<D>;
+    __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(Ov);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -361,6 +404,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool leader = tc::elect_one();
         constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN, false, false);
         constexpr uint32_t idesc_o = tc::idesc_bf16(BM, D, false, true);
+        constexpr uint32_t idesc_o_hi = tc::idesc_bf16(BM, 64, false, true);   // X3: Plo Vhi
         const uint64_t qd = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);
         const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);
         const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, C::CHUNK_BYTES, 1024);
@@ -372,10 +416,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_after_sync();
             if (leader) {
                 const uint64_t vs = vd + ((s * C::TILE_BYTES) >> 4);
+                const uint32_t tP = tmem + C::P_COL0 + t * C::P_STRIDE;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 16 rows of V = 2048 bytes per k-step
-                    tc::mma_ts(tmem + C::O_COL0 + t * D, tmem + C::P_COL0 + t * C::P_STRIDE + kk * 8, vs + kk * 128,
-                               idesc_o, (k > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_ts(tmem + C::O_COL0 + t * D, tP + kk * 8, vs + kk * 128, idesc_o,
+                               (k > 0 || kk > 0) ? 1u : 0u);
+                if constexpr (X3) {
+                    // Plo (TMEM columns 64..127 of P_t) times Vhi (the first 64 columns) into O's first 64
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc::mma_ts(tmem + C::O_COL0 + t * D, tP + 64 + kk * 8, vs + kk * 128, idesc_o_hi, 1u);
+                }
                 tc::mma_commit(pv_done_bar(j));
             }
             __syncwarp();
@@ -391,10 +442,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!__all_sync(0xffffffffu, ok_k)) return false;
             if (leader) {
                 const uint64_t ks = kd + ((s * C::TILE_BYTES) >> 4);
+                if constexpr (X3) {
+                    // chunk pairs (Q, K): (hi, hi), (hi, lo), (lo, hi), four k-steps each
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                    tc::mma_ss(tmem + C::S_COL0 + t * 128, qd + off, ks + off, idesc_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 12; ++kk) {
+                        const uint32_t oq = ((kk >> 2) == 2 ? C::CHUNK_BYTES : 0u) + (kk & 3) * 32;
+                        const uint32_t ok_ = ((kk >> 2) == 1 ? C::CHUNK_BYTES : 0u) + (kk & 3) * 32;
+                        tc::mma_ss(tmem + C::S_COL0 + t * 128, qd + (oq >> 4), ks + (ok_ >> 4), idesc_s,
+                                   kk > 0 ? 1u : 0u);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                        tc::mma_ss(tmem + C::S_COL0 + t * 128, qd + off, ks + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
                 }
                 tc::mma_commit(s_full(t));
             }
@@ -484,13 +546,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float nm = -m;
             uint32_t p[64];
             float rs[4][2] = {};
+            if constexpr (X3) {
+                // P = hi + lo: hi over P_t's first 64 columns, lo over the other 64, stored
+                // half by half (S_t has been read into registers; P aliases it)
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                float x0, x1;
-                tc::fma2(x0, x1, s[2 * i], s[2 * i + 1], scale_log2, scale_log2, nm, nm);
-                const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
-                tc::add2(rs[i & 3][0], rs[i & 3][1], rs[i & 3][0], rs[i & 3][1], e0, e1);
-                p[i] = tc::pack_bf16(e0, e1);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t ph[32], pl[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int ii = 32 * h + i;
+                        float x0, x1;
+                        tc::fma2(x0, x1, s[2 * ii], s[2 * ii + 1], scale_log2, scale_log2, nm, nm);
+                        const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
+                        tc::add2(rs[i & 3][0], rs[i & 3][1], rs[i & 3][0], rs[i & 3][1], e0, e1);
+                        ph[i] = tc::pack_bf16(e0, e1);
+                        pl[i] = tc::pack_bf16_residual(e0, e1, ph[i]);
+                    }
+                    tmem_st_x32(tP + 32 * h, ph);
+                    tmem_st_x32(tP + 64 + 32 * h, pl);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    float x0, x1;
+                    tc::fma2(x0, x1, s[2 * i], s[2 * i + 1], scale_log2, scale_log2, nm, nm);
+                    const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
+                    tc::add2(rs[i & 3][0], rs[i & 3][1], rs[i & 3][0], rs[i & 3][1], e0, e1);
+                    p[i] = tc::pack_bf16(e0, e1);
+                }
             }
             l += ((rs[0][0] + rs[0][1]) + (rs[1][0] + rs[1][1])) + ((rs[2][0] + rs[2][1]) + (rs[3][0] + rs[3][1]));
             if (C::SEP_P && k > 0) {
@@ -499,8 +582,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::fence_after_sync();
             }
-            tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-            tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+            if constexpr (!X3) {
+                tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+                tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+            }
             if (k > 0 && __any_sync(0xffffffffu, rescale)) {
                 // O_t holds the sum up to this warpgroup's previous tile: rescale it in place
                 ok = W.wait(pv_done_bar(2 * k + t - 2), ((2 * k + t - 2) / C::R) & 1);
@@ -531,11 +616,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (fine && n1 > 0) fine = W.wait(pv_done_bar(2 * n1 - 1), ((2 * n1 - 1) / C::R) & 1);
         if (D == 64 && prep.dO && fine) fine = W.wait(do_full, 0);   // the dO rows are in shared memory
         fine = __all_sync(0xffffffffu, fine);
-        // this CTA's partial for row r, columns [t*D/2, (t+1)*D/2), relative to max Mc (unnormalised)
-        float v[D / 2];
+        // this CTA's partial for row r, output columns [t*VW, (t+1)*VW), relative to max Mc
+        // (unnormalised); X3: output column c sums accumulator columns c and 64 + c
+        constexpr int VW = X3 ? 32 : D / 2;
+        float v[VW];
         float Mc = -INFINITY, lc = 0.f;
 #pragma unroll
-        for (int i = 0; i < D / 2; ++i) v[i] = 0.f;
+        for (int i = 0; i < VW; ++i) v[i] = 0.f;
         if (fine && n0 > 0) {
             tc::fence_after_sync();
             const float m0 = m_sm[r], l0 = l_sm[r];
@@ -546,8 +633,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             lc = l0 * a0 + l1 * a1;
             const uint32_t tO0 = tmem + lane_base + C::O_COL0, tO1 = tO0 + D;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                const int col = t * (D / 2) + 32 * c;
+            for (int c = 0; c < (X3 ? 2 : D / 64); ++c) {
+                const int col = X3 ? t * VW + 64 * c : t * (D / 2) + 32 * c;
                 uint32_t o0[32], o1[32] = {};
                 tmem_ld_x32(tO0 + col, o0);
                 if (n1 > 0) tmem_ld_x32(tO1 + col, o1);
@@ -558,7 +645,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int i = 0; i < 32; ++i) {
                     float x = __uint_as_float(o0[i]) * a0;
                     if (n1 > 0) x = fmaf(__uint_as_float(o1[i]), a1, x);
-                    v[32 * c + i] = x;
+                    if (X3) v[i] += x;
+                    else v[32 * c + i] = x;
                 }
             }
         }
@@ -566,6 +654,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // rowsum(dO * O) from the unrounded O when the preprocessing is fused
         auto store_row = [&](const float *vals, float Mrow, float lrow) -> float {
             const float inv = 1.f / lrow;
+            if constexpr (X3) {
+                // fp32 output row through O's strides; columns past the head dim are padding
+                float *orow = static_cast<float *>(Ov) + fa_row_offset(so, tc::opaque(H), bh, row) + t * VW;
+                if (row < Nq) {
+#pragma unroll
+                    for (int c = 0; c < VW / 4; ++c)
+                        if (t * VW + 4 * c < dv)
+                            reinterpret_cast<float4 *>(orow)[c] =
+                                make_float4(vals[4 * c] * inv, vals[4 * c + 1] * inv, vals[4 * c + 2] * inv,
+                                            vals[4 * c + 3] * inv);
+                    if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
+                }
+                return 0.f;
+            }
             __nv_bfloat16 *orow;
             if constexpr (VIEW4) orow = O + fa_row_offset(so, tc::opaque(H), bh, row) + t * (D / 2);
             else orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
@@ -628,7 +730,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t pml = tc::map_to_rank(base + C::PART_ML_OFF, rank ^ 1u);
                     const bool ok_part = fine && n > 0;
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c)
+                    for (int c = 0; c < VW / 4; ++c)
                         tc::st_cluster_v4(prow + 16 * c, __float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
                                           __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
                     tc::st_cluster_f32(pml + r * 4, ok_part ? Mc : -INFINITY);
@@ -647,7 +749,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const float b0 = Mc > -INFINITY ? exp2f(Mc - M) : 0.f;
                     const float b1 = l1 > 0.f ? exp2f(M1 - M) : 0.f;
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
+                    for (int c = 0; c < VW / 4; ++c) {
                         const float4 pv = reinterpret_cast<const float4 *>(prow)[c];
                         v[4 * c + 0] = fmaf(pv.x, b1, v[4 * c + 0] * b0);
                         v[4 * c + 1] = fmaf(pv.y, b1, v[4 * c + 1] * b0);
@@ -696,10 +798,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int D, bool CAUSAL, bool VIEW4>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
+                     const __grid_constant__ CUtensorMap tmV, void *__restrict__ Ov,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
                      uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so, FwdPrep prep) {
     using C = FwdCfg<D>;
+    __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(Ov);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1293,22 +1396,48 @@ bool tc_make_map_4d(CUtensorMap_st *m, const void *ptr, int B, int H, int N, int
 // bf16 with d in {16, 32, 64, 128}.  Head dims 16 and 32 run the d = 64 kernels:
 // their TMA boxes are 64 columns wide and the columns past d read as zero, which
 // adds nothing to Q K^T and leaves zero output columns that are never stored.
+// fp32 with d in {16, 32, 64} may run the same kernels on split bf16 pairs (X3):
+// always (FA_FP32_SPLIT), never (FA_FP32_EXACT), or (FA_FP32_AUTO) when
+// |scale| * sqrt(d) <= 1, where unit-variance inputs give unit-variance scores and
+// the split products' relative error (about 3 * 2^-16 of sum |x y|) stays well
+// inside fp32's tolerance; larger scales take the CUDA-core kernels.  A thread may
+// turn X3 off for its own calls (the no-allocation entry point does, where the
+// split copies do not fit its scratch).
+static std::atomic<int> g_fp32_mode{FA_FP32_AUTO};
+static thread_local bool t_x3_off = false;
+void tc_disable_x3(bool off) { t_x3_off = off; }
+void tc_set_fp32_mode(int mode) { g_fp32_mode.store(mode); }
+int tc_get_fp32_mode() { return g_fp32_mode.load(); }
+
+static bool tiles_fit(const FaProblem &p) { return p.Nq >= 128 && p.Nk >= 128 && p.BH >= 1; }
+
+bool tc_x3_possible(const FaProblem &p) {
+    return p.dtype == FA_DTYPE_F32 && (p.d == 16 || p.d == 32 || p.d == 64) && tiles_fit(p) && !t_x3_off &&
+           g_fp32_mode.load() != FA_FP32_EXACT;
+}
+
+bool tc_x3(const FaProblem &p) {
+    return tc_x3_possible(p) &&
+           (g_fp32_mode.load() == FA_FP32_SPLIT || fabsf(p.scale) * sqrtf((float)p.d) <= 1.0001f);
+}
+
 bool tc_fwd_supported(const FaProblem &p) {
-    return p.dtype == FA_DTYPE_BF16 && (p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128) && p.Nq >= 128 &&
-           p.Nk >= 128 && p.BH >= 1;
+    if (p.dtype == FA_DTYPE_F32) return tc_x3(p);
+    return p.dtype == FA_DTYPE_BF16 && (p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128) && tiles_fit(p);
 }
 
 static int sm_count() { return tc_sm_count(); }
 
-template <int D, bool CAUSAL, int SPLIT, bool PERSIST, bool VIEW4>
+template <int D, bool CAUSAL, int SPLIT, bool PERSIST, bool VIEW4, bool X3 = false>
 static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                               void *O, float *L, const FwdPrep &prep, cudaStream_t st) {
     static_assert(!(PERSIST && SPLIT > 1), "persistent units are not split");
+    static_assert(!(PERSIST && X3), "split fp32 operands run one unit per CTA (or cluster)");
     using C = FwdCfg<D>;
-    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, __nv_bfloat16 *, float *, int, int, int, int,
+    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, void *, float *, int, int, int, int,
                  float, uint32_t, uint32_t, int, int, FaStrides, FwdPrep);
     if constexpr (PERSIST) kern = fa_fwd_tc_persistent_kernel<D, CAUSAL, VIEW4>;
-    else kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4>;
+    else kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4, X3>;
     cudaError_t e = tc_set_smem_once(reinterpret_cast<const void *>(kern), (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int qtiles = (p.Nq + BM - 1) / BM;
@@ -1331,7 +1460,7 @@ static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const C
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = SPLIT > 1 ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, static_cast<__nv_bfloat16 *>(O), L, p.Nq, p.Nk, p.BH, qtiles,
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, O, L, p.Nq, p.Nk, p.BH, qtiles,
                            scale_log2, p.wait_limit, p.force_stall, p.H, p.d, p.sO, prep);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -1400,6 +1529,49 @@ cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void 
                                     : launch_fwd_any<128, false>(p, mq, mk, mv, O, L, view4, pr, st);
     return p.causal ? launch_fwd_any<64, true>(p, mq, mk, mv, O, L, view4, pr, st)
                     : launch_fwd_any<64, false>(p, mq, mk, mv, O, L, view4, pr, st);
+}
+
+// ------------------------------------------------------------------ fp32 inputs (X3)
+cudaError_t tc_split_x3(const FaProblem &p, int count, const void *const *X, const FaStrides *s, const int *N,
+                        void *const *X2, cudaStream_t st) {
+    if (count < 1 || count > 4) return cudaErrorInvalidValue;
+    SplitJobs jobs{};
+    long long rows_max = 0;
+    for (int i = 0; i < count; ++i) {
+        jobs.j[i] = SplitJob{static_cast<const float *>(X[i]), static_cast<__nv_bfloat16 *>(X2[i]), s[i], N[i]};
+        rows_max = std::max(rows_max, (long long)p.BH * N[i]);
+    }
+    if (rows_max == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows_max * 16 + 255) / 256), (unsigned)count);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fa_split_x3_kernel, jobs, p.BH, p.H, p.d);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t tc_fwd_x3(const FaProblem &p, const void *Q2, const void *K2, const void *V2, void *O, float *L,
+                      cudaStream_t st) {
+    if (!tc_x3(p)) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv;
+    if (!tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(&mq), Q2, p.BH, p.Nq, 128, BM) ||
+        !tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(&mk), K2, p.BH, p.Nk, 128, BN) ||
+        !tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(&mv), V2, p.BH, p.Nk, 128, BN))
+        return cudaErrorInvalidValue;
+    const FwdPrep none{};
+    // the split form where it pays; otherwise one unit per CTA (no persistent form)
+    const bool split = fwd_mode(p) == FwdMode::kSplit;
+    if (p.causal)
+        return split ? launch_fwd<128, true, 2, false, false, true>(p, mq, mk, mv, O, L, none, st)
+                     : launch_fwd<128, true, 1, false, false, true>(p, mq, mk, mv, O, L, none, st);
+    return split ? launch_fwd<128, false, 2, false, false, true>(p, mq, mk, mv, O, L, none, st)
+                 : launch_fwd<128, false, 1, false, false, true>(p, mq, mk, mv, O, L, none, st);
 }
 
 cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st) {

@@ -390,6 +390,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// The second bf16 of a split fp32 pair: with hi = pack_bf16(x0, x1), the
+// rounding residuals x - hi (exact in fp32) rounded to bf16, packed the same way.
+__device__ __forceinline__ uint32_t pack_bf16_residual(float x0, float x1, uint32_t hi) {
+    return pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

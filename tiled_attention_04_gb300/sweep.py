@@ -18,7 +18,10 @@ Timing: CUDA events on the current stream around each call, after warm-up;
 the L2 cache (129 MB) is flushed before every timed call by writing a 256 MiB
 buffer; the median of `reps` calls is reported, in milliseconds.
 
-Run: python -m tiled_attention_04_gb300.sweep [--reps R] [--max-n N] [--json PATH]
+fp32 cells run in the library's fp32 mode (--fp32-mode; default auto: split
+bf16 pairs on the tensor cores for d <= 64 at this scale, see include/fa.h).
+
+Run: python -m tiled_attention_04_gb300.sweep [--reps R] [--max-n N] [--json PATH] [--fp32-mode M]
      python -m tiled_attention_04_gb300.sweep --layer [--non-causal]   (the xl attention block)
 """
 from __future__ import annotations
@@ -174,10 +177,15 @@ def main(argv=None):
     ap.add_argument("--non-causal", action="store_true")
     ap.add_argument("--json", default=None, help="also write the cells as JSON lines to this file")
     ap.add_argument("--layer", action="store_true", help="time the xl-shaped attention block instead")
+    ap.add_argument("--fp32-mode", choices=("auto", "exact", "split"), default="auto",
+                    help="the library's fp32 mode for the fp32 cells")
     a = ap.parse_args(argv)
     torch = _torch()
     if not torch.cuda.is_available():
         raise SystemExit("the sweep needs a CUDA device")
+    from . import binding
+    binding.set_fp32_mode({"auto": binding.FA_FP32_AUTO, "exact": binding.FA_FP32_EXACT,
+                           "split": binding.FA_FP32_SPLIT}[a.fp32_mode])
     causal = not a.non_causal
     if a.layer:
         res = layer_block(causal=causal)
@@ -203,6 +211,7 @@ def main(argv=None):
                 print(f"| {dt} | {d} | {N} | {f[0]:.3f} | {f[1]:.3f} | {f[2]:.3f} | {vcols} | {sp} |")
                 sys.stdout.flush()
                 rec = {"dtype": dt, "d": d, "N": N, "causal": causal, "batch": 1, "heads": 1, "unit": "ms",
+                       "fp32_mode": a.fp32_mode if dt == "fp32" else None,
                        "flash": {"fwd": f[0], "bwd": f[1], "e2e": f[2]},
                        "vanilla": v if v == "OOM" else {"fwd": v[0], "bwd": v[1], "e2e": v[2]}}
                 rows.append(rec)
