@@ -278,14 +278,16 @@ def kernel_flops(w, path):
     return {"fwd": f, "bwd_pre": 0.0, "bwd_grads": 2.5 * f}
 
 
-def executed_factor(kernel, strategy):
+def executed_factor(kernel, strategy, split_pairs=False):
     """Matmul FLOP the kernels execute per algorithmic FLOP.  dQ by a separate pass:
     the dK/dV items recompute S and dP and form dV and dK (four matmuls), the dQ
     items recompute S and dP again and form dQ (three): 3.5/2.5.  dQ by reduction:
-    the five matmuls of the method, once each."""
+    the five matmuls of the method, once each.  fp32 inputs as split bf16 pairs:
+    three bf16 products for each (and the forward's FLOPs as d = 64 products)."""
+    k = 3.0 if split_pairs else 1.0
     if kernel == "bwd_grads":
-        return 1.0 if strategy == "reduction" else 3.5 / 2.5
-    return 1.0 if kernel == "fwd" else 0.0
+        return k * (1.0 if strategy == "reduction" else 3.5 / 2.5)
+    return k if kernel == "fwd" else 0.0
 
 # Kernel source of each launch: a DRAM traffic figure below is reported only while
 # that source is unchanged since the capture it came from (else the key is null).
@@ -362,6 +364,8 @@ class Problem:
         (which also does the backward's preprocessing) and the gradient launch, plus
         the dQ conversion when dQ is formed by reduction."""
         if self.path != "tc":
+            return 4
+        if self.Q.element_size() == 4:   # fp32 as split bf16 pairs: split, forward, preprocessing, gradients
             return 4
         return 3 if self.strategy == "reduction" else 2
 
@@ -445,7 +449,7 @@ def summarize(w, pk, step_ms, fwd_ms, bwd_ms, kern_ms, strategy):
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(tf(kf[dom], kern_ms[dom]) / pk["bf16_tflops"], 4), "traffic": traffic,
                      "traffic_source": note,
-                     "executed_tflops": round(tf(kf[dom], kern_ms[dom]) * executed_factor(dom, strategy), 2),
+                     "executed_tflops": round(tf(kf[dom], kern_ms[dom]) * executed_factor(dom, strategy, w.dtype == "f32"), 2),
                      "peak_source": f"{pk['source']} bf16 dense burst"},
     }
     return r
@@ -462,6 +466,8 @@ def run_gpu(args, w, rank, world):
     binding.lib()
     binding.set_dq_strategy({"auto": binding.FA_DQ_AUTO, "separate": binding.FA_DQ_SEPARATE_PASS,
                              "reduction": binding.FA_DQ_REDUCTION}[args.dq_strategy])
+    binding.set_fp32_mode({"auto": binding.FA_FP32_AUTO, "exact": binding.FA_FP32_EXACT,
+                           "split": binding.FA_FP32_SPLIT}[args.fp32_mode])
     pk = peaks()
     prob = Problem(w, dev)
     from tiled_attention_04_gb300 import inputs
@@ -687,6 +693,8 @@ def main():
     ap.add_argument("--sustain-s", type=float, default=1.0, help="seconds of the sustained pass")
     ap.add_argument("--dq-strategy", default="auto", choices=["auto", "separate", "reduction"],
                     help="how the backward forms dQ (fa_set_dq_strategy)")
+    ap.add_argument("--fp32-mode", default="auto", choices=["auto", "exact", "split"],
+                    help="how fp32 inputs are computed (fa_set_fp32_mode)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
