@@ -103,7 +103,7 @@ struct FwdCfg {
     static constexpr uint32_t K_OFF = Q_OFF + TILE_BYTES;
     static constexpr uint32_t V_OFF = K_OFF + KST * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = V_OFF + VST * TILE_BYTES;
-    static constexpr int NBAR = 1 + KST + VST + R + 12;
+    static constexpr int NBAR = 1 + KST + VST + R + 16;
     // per-row (m, l) of both warpgroups, double-buffered by work unit: 2 x (256 + 256) floats
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t MISC_OFF = STAT_OFF + 2 * 512 * 4;
@@ -114,13 +114,15 @@ struct FwdCfg {
     // (double-buffered by work unit in the persistent kernel; the split form's
     // rank 1 stores its half into rank 0's copy)
     static constexpr uint32_t DSUM_OFF = OROW_OFF + 256 * 8;
-    // fused backward preprocessing, d = 64, one unit per CTA: the tile's dO rows
-    // (packed, d * 2 bytes each), fetched by an otherwise idle warp during the main loop
-    // (the destination of a bulk copy: 16-byte aligned; the barrier block above leaves
-    // the offsets after it only 8-byte aligned, hence the rounding)
+    // fused backward preprocessing, d = 64: the tile's dO rows (packed, d * 2 bytes
+    // each), fetched by an otherwise idle warp during the main loop; two buffers,
+    // alternating by unit in the persistent kernel (the destination of a bulk copy:
+    // 16-byte aligned; the barrier block above leaves the offsets after it only
+    // 8-byte aligned, hence the rounding)
     static constexpr uint32_t DOS_OFF = (DSUM_OFF + 2 * 256 * 4 + 127) / 128 * 128;
-    static_assert(DOS_OFF % 16 == 0, "bulk-copy destination on a 16-byte boundary");
-    static constexpr uint32_t USED = DOS_OFF + (D == 64 ? 128 * 64 * 2 : 0);
+    static constexpr uint32_t DOS_BYTES = 128 * 64 * 2;
+    static_assert(DOS_OFF % 16 == 0 && DOS_BYTES % 16 == 0, "bulk-copy destinations on 16-byte boundaries");
+    static constexpr uint32_t USED = DOS_OFF + (D == 64 ? 2 * DOS_BYTES : 0);
     // split items: rank 1's partial O (fp32, rows padded by 4 floats) and its m, l, in the K ring
     static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
     static constexpr uint32_t PART_OFF = K_OFF;
@@ -852,6 +854,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t o_free = bar(RB + 9);      // epilogue has read O_0, O_1: the next unit may overwrite them
     const uint32_t merge_bar = bar(RB + 10);  // both warpgroups have published their (m, l)
     const uint32_t dsum_bar = bar(RB + 11);   // both warpgroups have published their half rowsums (fused preprocessing)
+    // fused preprocessing, d = 64: a unit's dO rows have landed in buffer b (do_full) /
+    // have been read by the epilogue (do_free); buffers alternate by unit
+    auto do_full = [&](int b) { return bar(RB + 12 + b); };
+    auto do_free = [&](int b) { return bar(RB + 14 + b); };
     float *stat_sm = reinterpret_cast<float *>(sb + C::STAT_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
     volatile uint32_t *abort_flag = tmem_slot + 1;
@@ -872,6 +878,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::mbar_init(o_free, 256);
         tc::mbar_init(merge_bar, 256);
         tc::mbar_init(dsum_bar, 256);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(do_full(b), 1);
+            tc::mbar_init(do_free(b), 256);
+        }
         *abort_flag = 0u;
         tc::fence_mbar_init();
     }
@@ -950,6 +960,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (uint32_t i = 0; i < (1u << 20) && !tc::mbar_try_wait(q_full, (q_issued - 1) & 1); ++i) {
                     }
             }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ fused preprocessing
+        // d = 64: each unit's dO rows into the unit's buffer (one bulk copy of the
+        // contiguous rows), and the unit's rows of the dQ accumulator cleared, ahead of
+        // the epilogue that reads them
+        if (D == 64 && prep.dO) {
+            Unit w;
+            int issued = 0;
+            bool ok = true;
+            for (int u = 0; ok && unit_of(u, w); ++u) {
+                const int b = u & 1;
+                if (lane == 0) {
+                    // the buffer last held unit u - 2's rows: wait until its epilogue read them
+                    if (u >= 2) ok = W.wait(do_free(b), ((u - 2) >> 1) & 1);
+                    if (ok) {
+                        const int rows = min(BM, Nq - w.q0);
+                        const uint32_t bytes = (uint32_t)rows * dv * 2;
+                        const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(prep.dO) +
+                                                   (VIEW4 ? fa_row_offset(prep.sdo, H, w.bh, w.q0)
+                                                          : ((size_t)w.bh * Nq + w.q0) * D);
+                        tc::mbar_arrive_expect_tx(do_full(b), bytes);
+                        tc::bulk_load(base + C::DOS_OFF + b * C::DOS_BYTES, src, bytes, do_full(b));
+                        issued = u + 1;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok && prep.dQa) {
+                    float4 *z = reinterpret_cast<float4 *>(prep.dQa + ((size_t)w.bh * ((Nq + 127) / 128 * 128) + w.q0) * 64);
+                    for (int i = lane; i < BM * 64 / 4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            // the copies land before the CTA may exit
+            if (lane == 0)
+                for (int u = issued - 1; u >= 0 && u >= issued - 2; --u)
+                    for (uint32_t i = 0; i < (1u << 22) && !tc::mbar_try_wait(do_full(u & 1), (u >> 1) & 1); ++i) {
+                    }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -1202,11 +1249,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             reinterpret_cast<uint4 *>(orow)[c] = q;
                     }
                     if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
-                    if (prep.dO) part = prep_half_rowsum<D, VIEW4>(prep, vals, inv, bh, row, Nq, H, dv, t);
+                    if (prep.dO) {
+                        const __nv_bfloat16 *drow = nullptr;
+                        if constexpr (D == 64)
+                            drow = reinterpret_cast<const __nv_bfloat16 *>(sb + C::DOS_OFF + (u & 1) * C::DOS_BYTES) +
+                                   (size_t)r * dv;
+                        part = prep_half_rowsum<D, VIEW4>(prep, vals, inv, bh, row, Nq, H, dv, t, drow);
+                    }
                 }
                 return part;
             };
+            if (D == 64 && prep.dO && fine) fine = __all_sync(0xffffffffu, W.wait(do_full(u & 1), (u >> 1) & 1));
             const float part = fine ? store_row(v, Mc, lc) : 0.f;
+            if (D == 64 && prep.dO) {
+                // this unit's dO rows have been read: the buffer may take unit u + 2's
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(do_free(u & 1));
+            }
             if (prep.dO) {
                 // the two halves of the row meet in shared memory (double-buffered by
                 // unit: the merge barrier keeps the warpgroups within one unit)
@@ -1215,7 +1274,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc::mbar_arrive(dsum_bar);
                 const bool got = t == 0 ? W.wait(dsum_bar, u & 1) : true;
                 if (fine) prep_row_finish<D>(prep, part, got && t == 0 ? dsum[128 + r] : 0.f, got && t == 0, Mc, lc, bh,
-                                             row, Nq, t);
+                                             row, Nq, t, D != 64);   // d = 64: warp 2 cleared the accumulator rows
             }
             g0 += n;
             if (!fine) ok = false;
