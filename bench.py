@@ -296,10 +296,15 @@ KERNEL_SOURCE = {"fwd": "fa_tc_fwd.cu", "bwd_pre": "fa_tc_bwd.cu", "bwd_grads": 
 # DRAM bytes (read + write) per launch, from one `ncu --set full` capture per
 # workload of the kernel built from the source whose SHA-256 prefix is given.
 NCU_TRAFFIC = {
-    ("bench_b8_n4096_d64_causal", "bwd_grads"): (25470976, "2a9c2fe0277c320e"),
-    ("bench_b8_n4096_d64_causal", "fwd"): (16823040, "1c58d8e54de19951"),
-    ("long_n16384_d128_causal", "bwd_grads"): (16977408, "2a9c2fe0277c320e"),
-    ("long_n16384_d128_causal", "fwd"): (16833536, "1c58d8e54de19951"),
+    ("bench_b8_n4096_d64_causal", "bwd_grads"): (25466624, "a6224f497e935de3"),
+    ("bench_b8_n4096_d64_causal", "fwd"): (16825856, "585b589ee66be827"),
+    ("long_n16384_d128_causal", "bwd_grads"): (16977408, "a6224f497e935de3"),
+    ("long_n16384_d128_causal", "fwd"): (16834048, "585b589ee66be827"),
+    ("vlong_n65536_d64_causal", "bwd_grads"): (50986752, "a6224f497e935de3"),
+    ("layer_xl_b4_h25_n1024_causal", "bwd_grads"): (85127680, "a6224f497e935de3"),
+    ("layer_xl_b4_h25_n1024_causal", "fwd"): (59701248, "585b589ee66be827"),
+    ("layer_xl_b4_h25_n1024_full", "bwd_grads"): (86116096, "a6224f497e935de3"),
+    ("sweep_f32_b1_n4096_d64_causal", "bwd_grads"): (4309248, "a6224f497e935de3"),
 }
 
 

@@ -196,17 +196,26 @@ def _on_gpu(*ts):
             raise ValueError("tensors must be on a CUDA device")
 
 
+_strides_seen = {}   # (shape, strides) -> FaStrides: the library only reads them
+
+
 def _strides(t):
     """fa_strides of a (B, H, N, d) or (B, N, d) view whose last dimension is contiguous,
     or None for a contiguous tensor (the plain layout)."""
     if t.is_contiguous():
         return None
-    if t.dim() not in (3, 4) or (t.shape[-1] > 1 and t.stride(-1) != 1):
+    shape, st = tuple(t.shape), t.stride()
+    key = (shape, st)
+    fs = _strides_seen.get(key)
+    if fs is not None:
+        return fs
+    if len(shape) not in (3, 4) or (shape[-1] > 1 and st[-1] != 1):
         raise ValueError("a non-contiguous view must be (B, H, N, d) or (B, N, d) with the last dimension "
                          "contiguous")
-    if t.dim() == 3:
-        return FaStrides(t.stride(0), t.stride(0), t.stride(1))
-    return FaStrides(t.stride(0), t.stride(1), t.stride(2))
+    fs = FaStrides(st[0], st[0], st[1]) if len(shape) == 3 else FaStrides(st[0], st[1], st[2])
+    if len(_strides_seen) < 1024:
+        _strides_seen[key] = fs
+    return fs
 
 
 def accepts_view(t) -> bool:
