@@ -31,9 +31,9 @@
  * backward workspace.  The library allocates no device memory per call, with
  * one exception: fa_fwd / fa_fwd_strided with fp32 inputs on the tensor-core
  * path (fa_set_fp32_mode below) take the split bf16 copies of Q, K and V
- * (256 bytes per row each) from a stream-ordered memory pool the library owns,
- * one per device; the pool keeps its memory between calls, so only the first
- * call, or the first larger one, allocates.  Calls are asynchronous and
+ * (256 bytes per row each, 512 at head dim 128) from a stream-ordered memory
+ * pool the library owns, one per device; the pool keeps its memory between
+ * calls, so only the first call, or the first larger one, allocates.  Calls are asynchronous and
  * ordered on the caller's stream; nothing synchronises inside a call.
  *
  * Errors.  Every entry point returns fa_status and never throws.  Arguments
@@ -259,9 +259,11 @@ FA_API fa_status fa_bwd_strided(const void *Q, const fa_strides *sQ, const void 
 FA_API const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype dtype);
 
 /*
- * fp32 inputs.  The CUDA-core kernels compute in fp32 throughout.  For head dims
- * 16, 32 and 64 (and Nq, Nk >= 128) fp32 inputs can instead run on the tensor
- * cores: every operand x is split into two bf16 numbers, hi = bf16(x) and
+ * fp32 inputs.  The CUDA-core kernels compute in fp32 throughout.  With Nq and
+ * Nk >= 128, fp32 inputs can instead run on the tensor cores (the forward and
+ * backward for head dims 16, 32 and 64, the forward alone for 128, whose
+ * backward stays on the CUDA cores): every operand x is split into two bf16
+ * numbers, hi = bf16(x) and
  * lo = bf16(x - hi), and every product of the method (S = Q K^T, O = P V, and
  * the backward's five) takes three bf16 products with fp32 accumulation,
  * hi*hi + hi*lo + lo*hi.  With u = 2^-8 (bf16's unit roundoff) each such sum

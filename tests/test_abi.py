@@ -110,7 +110,7 @@ def test_path_choice(L):
     # fp32 up to d = 64: split into bf16 pairs, three products per contraction
     assert binding.path_name(128, 128, 16, 1, binding.FA_DTYPE_F32) == "tc"
     assert binding.path_name(4096, 4096, 64, 1, binding.FA_DTYPE_F32) == "tc"
-    assert binding.path_name(4096, 4096, 128, 1, binding.FA_DTYPE_F32) == "simt"  # no d = 256 layout
+    assert binding.path_name(4096, 4096, 128, 1, binding.FA_DTYPE_F32) == "tc"    # 256-column split rows
     assert binding.path_name(100, 4096, 32, 1, binding.FA_DTYPE_F32) == "simt"
 
 

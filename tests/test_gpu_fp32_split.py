@@ -1,6 +1,7 @@
 """fp32 inputs on the tensor cores: every operand split into a bf16 pair
 (hi = bf16(x), lo = bf16(x - hi)) and every product of the method taken as
-hi*hi + hi*lo + lo*hi with fp32 accumulation (include/fa.h, fa_set_fp32_mode).
+hi*hi + hi*lo + lo*hi with fp32 accumulation (include/fa.h, fa_set_fp32_mode);
+head dims up to 64 run 128-column split rows, head dim 128 256-column ones.
 
 At the default scale 1/sqrt(d) the outputs meet the fp32 tolerance of 1e-4
 elementwise against the oracle (here on shapes of several tiles with ragged
@@ -26,6 +27,9 @@ CASES = [
     (2, 256, 256, 64, True), (2, 256, 256, 64, False), (3, 384, 384, 32, True), (2, 256, 256, 16, False),
     (1, 1000, 300, 64, True), (1, 300, 1000, 32, False), (3, 130, 130, 16, True), (1, 1088, 1088, 64, True),
     (1, 4096, 4096, 64, True), (8, 1024, 1024, 64, False),
+    # head dim 128: 256-column split rows
+    (2, 256, 256, 128, True), (2, 256, 256, 128, False), (1, 1000, 300, 128, True), (1, 300, 1000, 128, False),
+    (1, 1088, 1088, 128, True), (4, 1024, 1024, 128, False),
 ]
 
 
@@ -47,7 +51,7 @@ def test_split_fp32_modes_pick_the_kernels(cuda_lib):
         assert binding.path_name(512, 512, 64, 1, f32) == "simt"
     with binding.fp32_mode(binding.FA_FP32_SPLIT):
         assert binding.path_name(512, 512, 64, 1, f32) == "tc"
-        assert binding.path_name(512, 512, 128, 1, f32) == "simt"   # no d = 256 layout
+        assert binding.path_name(512, 512, 128, 1, f32) == "tc"     # 256-column split rows
         assert binding.path_name(100, 512, 64, 1, f32) == "simt"    # shorter than one tile
     assert binding.path_name(512, 512, 64, 1, f32) == "tc"          # automatic, default scale
     with pytest.raises(ValueError):
@@ -67,32 +71,40 @@ def test_split_fp32_exact_mode_matches_the_cuda_core_kernels(cuda_lib):
     assert_close(split, exact, 2e-4, "split against exact")
 
 
-def test_split_fp32_scale_one_within_the_product_bound(cuda_lib):
-    """Forced split mode at scale 1: scores of standard deviation 8, where the
+@pytest.mark.parametrize("d", [64, 128])
+def test_split_fp32_scale_one_within_the_product_bound(cuda_lib, d):
+    """Forced split mode at scale 1: scores of standard deviation sqrt(d), where the
     products' 3 * 2^-16 relative error reaches the outputs through the softmax;
-    every output stays inside the first-order bound of those products."""
+    every output stays inside the first-order bound of those products.  At d <= 64
+    forward and backward are split, so the errors also stay within twice those of
+    the numerical model of that arithmetic; at d = 128 the backward is exact fp32
+    on the CUDA cores but recomputes P from the split forward's L (its rows then sum
+    to exp(L - L_split) rather than 1), a different error pattern that only the
+    bound covers."""
     from tiled_attention_04_gb300 import binding
-    t = inputs.make_custom(2, 256, 256, 64, "f32", seed=7200)
+    t = inputs.make_custom(2, 256, 256, d, "f32", seed=7200 + d)
     with binding.fp32_mode(binding.FA_FP32_SPLIT):
         got = run_gpu(t, True, scale=1.0)
     want = oracle_all(t, True, 1.0)
     bound = split_bound(t, True, 1.0)
-    model = split_model(t, True, 1.0)
+    model = split_model(t, True, 1.0) if d <= 64 else None
     for k in ("O", "L", "dQ", "dK", "dV"):
         err = np.abs(got[k] - want[k])
         allowed = bound[k] + 1e-5 * (1.0 + np.abs(want[k]))   # fp32 exp2 and accumulation
         assert (err <= allowed).all(), f"{k}: max err {err.max():.3g}, worst err/bound {(err / allowed).max():.3g}"
         # and no worse than the split arithmetic itself (the bound is a worst case over signs)
-        model_err = np.abs(model[k] - want[k]).max()
-        assert err.max() <= 2 * model_err + 1e-5 * (1.0 + np.abs(want[k]).max()), (k, err.max(), model_err)
+        if d <= 64:
+            model_err = np.abs(model[k] - want[k]).max()
+            assert err.max() <= 2 * model_err + 1e-5 * (1.0 + np.abs(want[k]).max()), (k, err.max(), model_err)
 
 
-def test_split_fp32_phases_and_fused_call(cuda_lib):
+@pytest.mark.parametrize("d", [64, 128])
+def test_split_fp32_phases_and_fused_call(cuda_lib, d):
     """The exported phases one by one, and fa_fwd_bwd, give fa_fwd + fa_bwd's
     results bit for bit (the same split copies and kernels)."""
     import torch
     from tiled_attention_04_gb300 import binding
-    t = inputs.make_custom(2, 640, 640, 64, "f32", seed=7300)
+    t = inputs.make_custom(2, 640, 640, d, "f32", seed=7300 + d)
     dev = torch.device("cuda")
     Q, K, V, dO = (inputs.to_torch(x, dev) for x in t)
     O, L = binding.fa_fwd(Q, K, V, is_causal=True)
@@ -109,7 +121,7 @@ def test_split_fp32_phases_and_fused_call(cuda_lib):
                        ("fused dQ", fdQ, dQ), ("fused dK", fdK, dK), ("fused dV", fdV, dV)):
         assert torch.equal(a, b), name
     got = {k: v.double().cpu().numpy() for k, v in (("O", O), ("L", L), ("dQ", dQ), ("dK", dK), ("dV", dV))}
-    assert_close(got, oracle_all(t, True, 0.125), 1e-4, "split fp32 two calls")
+    assert_close(got, oracle_all(t, True, 1.0 / math.sqrt(d)), 1e-4, f"split fp32 two calls d={d}")
 
 
 def test_split_fp32_deterministic(cuda_lib):

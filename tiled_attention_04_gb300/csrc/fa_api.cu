@@ -138,11 +138,12 @@ struct Workspace {
     size_t q2_off, do2_off, k2_off, v2_off;
     size_t sd_off;      // D of the CUDA-core kernels
 };
-size_t x3_bytes(const FaProblem &p, int N) { return align_up((size_t)p.BH * N * kX3RowBytes, 256); }
+size_t x3_bytes(const FaProblem &p, int N) { return align_up((size_t)p.BH * N * tc_x3_row_bytes(p), 256); }
 Workspace workspace_layout(const FaProblem &p) {
     Workspace w{};
     w.tc = tc_bwd_supported(p);
-    w.x3_possible = tc_x3_possible(p);
+    // (split pairs in the backward up to head dim 64; at 128 only the forward takes them)
+    w.x3_possible = tc_x3_possible(p) && p.d <= 64;
     w.x3 = w.x3_possible && tc_x3(p);
     const bool tc_rows = w.tc || w.x3_possible;
     const size_t rows = tc_rows ? tc_bwd_ld_rows(p) : (size_t)p.BH * p.Nq;

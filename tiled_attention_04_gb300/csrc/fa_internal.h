@@ -81,16 +81,17 @@ struct FwdPrep {
     float *Dp, *Lp;   // per batch*head, padded_rows(Nq) rows
     float *dQa;       // NULL unless dQ is formed by reduction
 };
-// ---- fp32 inputs with d in {16, 32, 64} (X3): each operand is first split into a
-// bf16 pair (hi = bf16(x), lo = bf16(x - hi)) held as a contiguous (B*H, N, 128)
-// bf16 copy, hi in columns [0, 64) and lo in [64, 128); the d = 128 kernels then
-// take three products per contraction (hi hi + hi lo + lo hi).
+// ---- fp32 inputs (X3): each operand is first split into a bf16 pair (hi = bf16(x),
+// lo = bf16(x - hi)) held as a contiguous (B*H, N, 2W) bf16 copy, hi in columns
+// [0, W) and lo in [W, 2W), W = 64 for d <= 64 (the d = 128 kernels) and 128 for
+// d = 128 (the 256-column forward; that head dim's backward stays on the CUDA
+// cores); every contraction takes three products (hi hi + hi lo + lo hi).
 bool tc_x3(const FaProblem &p);            // this problem runs X3 (mode, shape and scale)
 bool tc_x3_possible(const FaProblem &p);   // X3 for some scale (mode and shape): workspace sizing
 void tc_disable_x3(bool off);   // for the calling thread's calls (off: fp32 on the CUDA cores)
 void tc_set_fp32_mode(int mode);          // FA_FP32_AUTO / _EXACT / _SPLIT
 int tc_get_fp32_mode();
-constexpr size_t kX3RowBytes = 256;   // bytes of one split row
+size_t tc_x3_row_bytes(const FaProblem &p);   // bytes of one split row: 256 or 512
 // count (1..4) tensors X[i] with strides s[i] and N[i] rows per batch*head -> X2[i]
 cudaError_t tc_split_x3(const FaProblem &p, int count, const void *const *X, const FaStrides *s, const int *N,
                         void *const *X2, cudaStream_t st);

@@ -2448,7 +2448,11 @@ bool make_maps(const FaProblem &p, const void *Q, const void *K, const void *V, 
 
 }  // namespace
 
-bool tc_bwd_supported(const FaProblem &p) { return tc_fwd_supported(p); }
+// fp32 at head dim 128 takes split pairs in the forward only: the backward's
+// 256-column rows would need two stages of 64-row sub-tiles next to 64 KB K and
+// V tiles (the next sub-tile's scores are computed while the previous one's
+// gradients are), which shared memory does not hold; it runs on the CUDA cores.
+bool tc_bwd_supported(const FaProblem &p) { return tc_fwd_supported(p) && !(p.dtype == FA_DTYPE_F32 && p.d > 64); }
 
 size_t tc_bwd_ld_rows(const FaProblem &p) { return (size_t)p.BH * padded_rows(p.Nq); }
 

@@ -90,13 +90,17 @@ struct FwdCfg {
     // separate K and V rings: a K slot frees when its S MMAs finish, a V slot
     // when its PV MMAs finish; K runs one tile ahead of V.  Deep enough to
     // cover an L2-resident TMA reload (~2000 cycles).
-    static constexpr int KST = D == 128 ? 3 : 6;
-    static constexpr int VST = D == 128 ? 2 : 4;
+    // (D = 256: fp32 head dim 128 as split bf16 pairs; one 64 KB tile per ring)
+    static constexpr int KST = D == 256 ? 1 : D == 128 ? 3 : 6;
+    static constexpr int VST = D == 256 ? 1 : D == 128 ? 2 : 4;
     // one "PV_j complete" barrier per tile in a ring of R > KST, VST: it frees K_j's
     // and V_j's slots (in-order completion covers S_j) and tells the softmax that
     // P_j / O may be touched again -- one commit instead of three
-    static constexpr int R = D == 128 ? 4 : 8;
+    static constexpr int R = D == 64 ? 8 : 4;
     static constexpr int CHUNKS = D / 64;                      // 128-byte swizzle chunks per row
+    // O accumulator columns per warpgroup: d, except for the 256-column split rows of
+    // a head dim of 128, whose three products all add into the 128 output columns
+    static constexpr int OW = D == 256 ? 128 : D;
     static constexpr uint32_t CHUNK_BYTES = 128u * 128u;       // 128 rows x 128 bytes
     static constexpr uint32_t TILE_BYTES = CHUNKS * CHUNK_BYTES;
     static constexpr uint32_t Q_OFF = 0;
@@ -124,14 +128,15 @@ struct FwdCfg {
     static_assert(DOS_OFF % 16 == 0 && DOS_BYTES % 16 == 0, "bulk-copy destinations on 16-byte boundaries");
     static constexpr uint32_t USED = DOS_OFF + (D == 64 ? 2 * DOS_BYTES : 0);
     // split items: rank 1's partial O (fp32, rows padded by 4 floats) and its m, l, in the K ring
-    static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
+    static constexpr uint32_t PART_STRIDE = (OW + 4) * 4;
     static constexpr uint32_t PART_OFF = K_OFF;
     static constexpr uint32_t PART_ML_OFF = PART_OFF + 128 * PART_STRIDE;
-    static_assert(PART_ML_OFF + 2 * 128 * 4 <= K_OFF + KST * TILE_BYTES, "partial fits the K ring");
+    static_assert(PART_ML_OFF + 2 * 128 * 4 <= V_OFF + VST * TILE_BYTES, "partial fits the K and V rings");
     // at least ~116 KB so that one CTA (which owns all 512 TMEM columns) runs per SM
     static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u ? USED + 1024 : 120u * 1024u);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
+    static_assert(O_COL0 + 2 * OW <= TMEM_COLS, "two O accumulators after the two S buffers");
     // d = 64 leaves 128 TMEM columns free: P gets its own columns there, so the
     // next S of a warpgroup can be issued as soon as the current S has been read
     static constexpr bool SEP_P = D == 64;
@@ -196,10 +201,11 @@ __device__ __forceinline__ void prep_row_finish(const FwdPrep &prep, float half0
 }
 
 // ------------------------------------------------------------------ fp32 operands as bf16 pairs
-// X (B, H, N, d) fp32 with d <= 64, through its strides -> X2, B*H*N contiguous
-// rows of 128 bf16: hi = bf16(x) in columns [0, 64), lo = bf16(x - hi) in
-// [64, 128), zeros past d.  x - hi is exact in fp32, so hi + lo meets x to
-// within 2^-17 relative.  Sixteen threads per row, four columns each.
+// X (B, H, N, d) fp32, through its strides -> X2, B*H*N contiguous rows of 2W
+// bf16 (W = 64 for d <= 64, 128 for d = 128): hi = bf16(x) in columns [0, W),
+// lo = bf16(x - hi) in [W, 2W), zeros past d.  x - hi is exact in fp32, so
+// hi + lo meets x to within 2^-16 relative.  W/4 threads per row, four
+// columns each.
 struct SplitJob {
     const float *X;
     __nv_bfloat16 *X2;
@@ -209,22 +215,24 @@ struct SplitJob {
 struct SplitJobs {
     SplitJob j[4];   // blockIdx.y selects the tensor
 };
+template <int W>
 __global__ void __launch_bounds__(256) fa_split_x3_kernel(const __grid_constant__ SplitJobs jobs, int BH, int H,
                                                           int d) {
+    constexpr int TPR = W / 4;   // threads per row
     tc::pdl_launch_dependents();
     tc::pdl_wait();   // the tensors may come from the previous kernel
     const SplitJob &J = jobs.j[blockIdx.y];
     const long long g = (long long)blockIdx.x * 256 + threadIdx.x;
-    const long long row = g >> 4;
-    const int cg = (int)(g & 15);
+    const long long row = g / TPR;
+    const int cg = (int)(g % TPR);
     if (row >= (long long)BH * J.N) return;
     const int bh = (int)(row / J.N), n = (int)(row - (long long)bh * J.N);
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (4 * cg < d) x = __ldg(reinterpret_cast<const float4 *>(J.X + fa_row_offset(J.s, H, bh, n) + 4 * cg));
     const uint32_t h0 = tc::pack_bf16(x.x, x.y), h1 = tc::pack_bf16(x.z, x.w);
-    uint2 *dst = reinterpret_cast<uint2 *>(J.X2 + row * 128);
+    uint2 *dst = reinterpret_cast<uint2 *>(J.X2 + row * (2 * W));
     dst[cg] = make_uint2(h0, h1);
-    dst[16 + cg] = make_uint2(tc::pack_bf16_residual(x.x, x.y, h0), tc::pack_bf16_residual(x.z, x.w, h1));
+    dst[TPR + cg] = make_uint2(tc::pack_bf16_residual(x.x, x.y, h0), tc::pack_bf16_residual(x.z, x.w, h1));
 }
 
 // X3 (fp32 inputs, head dim up to 64): Q, K and V arrive as bf16 pairs, each
@@ -242,8 +250,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      const __grid_constant__ CUtensorMap tmV, void *__restrict__ Ov,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
                      uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so, FwdPrep prep) {
-    static_assert(!X3 || (D == 128 && !VIEW4), "split fp32 operands use the d = 128 layout of contiguous copies");
+    static_assert(!X3 || ((D == 128 || D == 256) && !VIEW4), "split fp32 operands: 128- or 256-column copies");
+    static_assert(X3 || D <= 128, "the 256-column layout holds split pairs only");
+    static_assert(!X3 || D == 128 || SPLIT == 1, "256-column split rows run one unit per CTA");
     using C = FwdCfg<D>;
+    // X3 at D = 128 (head dims up to 64): output column c is accumulator column c plus
+    // 64 + c (hi and lo products of V); at D = 256 all products add into the same columns
+    constexpr bool FOLD = X3 && D == 128;
     __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(Ov);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -343,8 +356,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int key0 = (jb + j) * BN;
                 if (!tc::in_bounds(key0 < Nk && (!CAUSAL || key0 <= q0 + BM - 1), &g_fa_fwd_status, abort_flag))
                     return false;
-                const int g = j - st - lag < 0 ? 0 : j - st - lag;
-                if (j >= st && !W.wait(pv_done_bar(g), (g / C::R) & 1)) return false;
+                if (st == 1 && lag == 1) {
+                    // one K slot (256-column rows): it last held tile j - 1, whose S MMAs are
+                    // issued before PV_{j-2} completes, so wait for S_{j-1} itself
+                    if (j >= 1 && !W.wait(s_full((j - 1) & 1), ((j - 1) >> 1) & 1)) return false;
+                } else {
+                    const int g = j - st - lag < 0 ? 0 : j - st - lag;
+                    if (j >= st && !W.wait(pv_done_bar(g), (g / C::R) & 1)) return false;
+                }
                 tc::mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int c = 0; c < C::CHUNKS; ++c)
                     tc::tma_load_rows<VIEW4>(ring + (j % st) * C::TILE_BYTES + c * C::CHUNK_BYTES, m, full, c * 64,
@@ -405,8 +424,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // cheap to form; one elected lane issues the tcgen05 instructions.
         const bool leader = tc::elect_one();
         constexpr uint32_t idesc_s = tc::idesc_bf16(BM, BN, false, false);
-        constexpr uint32_t idesc_o = tc::idesc_bf16(BM, D, false, true);
-        constexpr uint32_t idesc_o_hi = tc::idesc_bf16(BM, 64, false, true);   // X3: Plo Vhi
+        constexpr uint32_t idesc_o = tc::idesc_bf16(BM, C::OW, false, true);
+        constexpr uint32_t idesc_o_hi = tc::idesc_bf16(BM, 64, false, true);   // X3, D = 128: Plo Vhi
         const uint64_t qd = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);
         const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);
         const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, C::CHUNK_BYTES, 1024);
@@ -421,13 +440,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t tP = tmem + C::P_COL0 + t * C::P_STRIDE;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 16 rows of V = 2048 bytes per k-step
-                    tc::mma_ts(tmem + C::O_COL0 + t * D, tP + kk * 8, vs + kk * 128, idesc_o,
+                    tc::mma_ts(tmem + C::O_COL0 + t * C::OW, tP + kk * 8, vs + kk * 128, idesc_o,
                                (k > 0 || kk > 0) ? 1u : 0u);
-                if constexpr (X3) {
+                if constexpr (X3 && D == 128) {
                     // Plo (TMEM columns 64..127 of P_t) times Vhi (the first 64 columns) into O's first 64
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        tc::mma_ts(tmem + C::O_COL0 + t * D, tP + 64 + kk * 8, vs + kk * 128, idesc_o_hi, 1u);
+                        tc::mma_ts(tmem + C::O_COL0 + t * C::OW, tP + 64 + kk * 8, vs + kk * 128, idesc_o_hi, 1u);
+                } else if constexpr (X3) {
+                    // D = 256: Phi times Vlo (chunks 2, 3), then Plo times Vhi (chunks 0, 1), into the same O
+                    const uint64_t vlo = vs + ((2 * C::CHUNK_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc::mma_ts(tmem + C::O_COL0 + t * C::OW, tP + kk * 8, vlo + kk * 128, idesc_o, 1u);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc::mma_ts(tmem + C::O_COL0 + t * C::OW, tP + 64 + kk * 8, vs + kk * 128, idesc_o, 1u);
                 }
                 tc::mma_commit(pv_done_bar(j));
             }
@@ -445,13 +473,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (leader) {
                 const uint64_t ks = kd + ((s * C::TILE_BYTES) >> 4);
                 if constexpr (X3) {
-                    // chunk pairs (Q, K): (hi, hi), (hi, lo), (lo, hi), four k-steps each
+                    // chunk pairs (Q, K): (hi, hi), (hi, lo), (lo, hi) for each of the HC hi chunks
+                    // (the lo chunks follow them), four k-steps each
+                    constexpr int HC = D / 128;
+                    auto pair = [&](int pr) {
+                        const int grp = pr / HC, c = pr % HC;
+                        const uint32_t bq = (grp == 2 ? HC + c : c) * C::CHUNK_BYTES;
+                        const uint32_t bk = (grp == 1 ? HC + c : c) * C::CHUNK_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < 12; ++kk) {
-                        const uint32_t oq = ((kk >> 2) == 2 ? C::CHUNK_BYTES : 0u) + (kk & 3) * 32;
-                        const uint32_t ok_ = ((kk >> 2) == 1 ? C::CHUNK_BYTES : 0u) + (kk & 3) * 32;
-                        tc::mma_ss(tmem + C::S_COL0 + t * 128, qd + (oq >> 4), ks + (ok_ >> 4), idesc_s,
-                                   kk > 0 ? 1u : 0u);
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            tc::mma_ss(tmem + C::S_COL0 + t * 128, qd + ((bq + k4 * 32) >> 4),
+                                       ks + ((bk + k4 * 32) >> 4), idesc_s, (pr > 0 || k4 > 0) ? 1u : 0u);
+                    };
+                    if constexpr (HC == 1) {
+#pragma unroll
+                        for (int pr = 0; pr < 3; ++pr) pair(pr);
+                    } else {
+                        // (kept rolled: unrolled, the 24 descriptors spill the issuer's 56 registers)
+#pragma unroll 1
+                        for (int pr = 0; pr < 3 * HC; ++pr) pair(pr);
                     }
                 } else {
 #pragma unroll
@@ -497,7 +537,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
         const uint32_t tS = tmem + lane_base + C::S_COL0 + t * 128;
         const uint32_t tP = tmem + lane_base + C::P_COL0 + t * C::P_STRIDE;
-        const uint32_t tO = tmem + lane_base + C::O_COL0 + t * D;
+        const uint32_t tO = tmem + lane_base + C::O_COL0 + t * C::OW;
         const int nt = (n - t + 1) >> 1;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
@@ -594,7 +634,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::fence_after_sync();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < C::OW / 32; ++c) {
                     uint32_t o[32];
                     tmem_ld_x32(tO + 32 * c, o);
                     tc::tmem_ld_wait();
@@ -620,7 +660,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         fine = __all_sync(0xffffffffu, fine);
         // this CTA's partial for row r, output columns [t*VW, (t+1)*VW), relative to max Mc
         // (unnormalised); X3: output column c sums accumulator columns c and 64 + c
-        constexpr int VW = X3 ? 32 : D / 2;
+        constexpr int VW = FOLD ? 32 : C::OW / 2;
         float v[VW];
         float Mc = -INFINITY, lc = 0.f;
 #pragma unroll
@@ -633,10 +673,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float a0 = exp2f(m0 - Mc);
             const float a1 = n1 > 0 ? exp2f(m1 - Mc) : 0.f;
             lc = l0 * a0 + l1 * a1;
-            const uint32_t tO0 = tmem + lane_base + C::O_COL0, tO1 = tO0 + D;
+            const uint32_t tO0 = tmem + lane_base + C::O_COL0, tO1 = tO0 + C::OW;
 #pragma unroll
-            for (int c = 0; c < (X3 ? 2 : D / 64); ++c) {
-                const int col = X3 ? t * VW + 64 * c : t * (D / 2) + 32 * c;
+            for (int c = 0; c < (FOLD ? 2 : C::OW / 64); ++c) {
+                const int col = FOLD ? t * VW + 64 * c : t * (C::OW / 2) + 32 * c;
                 uint32_t o0[32], o1[32] = {};
                 tmem_ld_x32(tO0 + col, o0);
                 if (n1 > 0) tmem_ld_x32(tO1 + col, o1);
@@ -647,7 +687,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int i = 0; i < 32; ++i) {
                     float x = __uint_as_float(o0[i]) * a0;
                     if (n1 > 0) x = fmaf(__uint_as_float(o1[i]), a1, x);
-                    if (X3) v[i] += x;
+                    if (FOLD) v[i] += x;
                     else v[32 * c + i] = x;
                 }
             }
@@ -712,7 +752,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         };
         if constexpr (SPLIT == 1) {
             const float part = fine ? store_row(v, Mc, lc) : 0.f;
-            if (prep.dO) {   // the same for every thread: all 256 reach the barrier
+            if (!X3 && prep.dO) {   // the same for every thread: all 256 reach the barrier
                 float *dsum = reinterpret_cast<float *>(sb + C::DSUM_OFF);
                 dsum[t * 128 + r] = part;
                 tc::named_bar_sync(1, 256);
@@ -1471,9 +1511,11 @@ int tc_get_fp32_mode() { return g_fp32_mode.load(); }
 static bool tiles_fit(const FaProblem &p) { return p.Nq >= 128 && p.Nk >= 128 && p.BH >= 1; }
 
 bool tc_x3_possible(const FaProblem &p) {
-    return p.dtype == FA_DTYPE_F32 && (p.d == 16 || p.d == 32 || p.d == 64) && tiles_fit(p) && !t_x3_off &&
-           g_fp32_mode.load() != FA_FP32_EXACT;
+    return p.dtype == FA_DTYPE_F32 && (p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128) && tiles_fit(p) &&
+           !t_x3_off && g_fp32_mode.load() != FA_FP32_EXACT;
 }
+
+size_t tc_x3_row_bytes(const FaProblem &p) { return p.d <= 64 ? 256 : 512; }
 
 bool tc_x3(const FaProblem &p) {
     return tc_x3_possible(p) &&
@@ -1601,8 +1643,9 @@ cudaError_t tc_split_x3(const FaProblem &p, int count, const void *const *X, con
         rows_max = std::max(rows_max, (long long)p.BH * N[i]);
     }
     if (rows_max == 0) return cudaSuccess;
+    const int tpr = p.d <= 64 ? 16 : 32;   // threads per row: W / 4
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((rows_max * 16 + 255) / 256), (unsigned)count);
+    cfg.gridDim = dim3((unsigned)((rows_max * tpr + 255) / 256), (unsigned)count);
     cfg.blockDim = dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1610,7 +1653,8 @@ cudaError_t tc_split_x3(const FaProblem &p, int count, const void *const *X, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fa_split_x3_kernel, jobs, p.BH, p.H, p.d);
+    cudaError_t e = p.d <= 64 ? cudaLaunchKernelEx(&cfg, fa_split_x3_kernel<64>, jobs, p.BH, p.H, p.d)
+                              : cudaLaunchKernelEx(&cfg, fa_split_x3_kernel<128>, jobs, p.BH, p.H, p.d);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1624,6 +1668,15 @@ cudaError_t tc_fwd_x3(const FaProblem &p, const void *Q2, const void *K2, const 
         !tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(&mv), V2, p.BH, p.Nk, 128, BN))
         return cudaErrorInvalidValue;
     const FwdPrep none{};
+    if (p.d == 128) {   // 256-column rows: one unit per CTA
+        CUtensorMap wq, wk, wv;
+        if (!tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(&wq), Q2, p.BH, p.Nq, 256, BM) ||
+            !tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(&wk), K2, p.BH, p.Nk, 256, BN) ||
+            !tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(&wv), V2, p.BH, p.Nk, 256, BN))
+            return cudaErrorInvalidValue;
+        return p.causal ? launch_fwd<256, true, 1, false, false, true>(p, wq, wk, wv, O, L, none, st)
+                        : launch_fwd<256, false, 1, false, false, true>(p, wq, wk, wv, O, L, none, st);
+    }
     // the split form where it pays; otherwise one unit per CTA (no persistent form)
     const bool split = fwd_mode(p) == FwdMode::kSplit;
     if (p.causal)
