@@ -98,8 +98,8 @@ FA_API fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, fl
  * Bytes of device workspace fa_bwd needs for this shape (fp32 D per query row;
  * on the tensor-core path fp32 D and L per query row, rows padded to a
  * multiple of 128, plus, for fp32 inputs on that path, the split bf16 copies of
- * Q, dO, K and V at 256 bytes per row each).  Returns 0 for unsupported
- * arguments.
+ * Q, dO, K and V at 256 bytes per row each, 512 at head dim 128).  Returns 0
+ * for unsupported arguments.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, int is_causal, fa_dtype dtype);
 
@@ -260,10 +260,8 @@ FA_API const char *fa_path_name(int Nq, int Nk, int d, int is_causal, fa_dtype d
 
 /*
  * fp32 inputs.  The CUDA-core kernels compute in fp32 throughout.  With Nq and
- * Nk >= 128, fp32 inputs can instead run on the tensor cores (the forward and
- * backward for head dims 16, 32 and 64, the forward alone for 128, whose
- * backward stays on the CUDA cores): every operand x is split into two bf16
- * numbers, hi = bf16(x) and
+ * Nk >= 128, fp32 inputs of every head dim can instead run on the tensor
+ * cores: every operand x is split into two bf16 numbers, hi = bf16(x) and
  * lo = bf16(x - hi), and every product of the method (S = Q K^T, O = P V, and
  * the backward's five) takes three bf16 products with fp32 accumulation,
  * hi*hi + hi*lo + lo*hi.  With u = 2^-8 (bf16's unit roundoff) each such sum

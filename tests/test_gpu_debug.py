@@ -32,8 +32,12 @@ def expected_rows(bh, nq, nk, d, causal, reduction, narrow=False):
               d = 128) from the one holding its first key's row to the end;
     dQ        every 128-row query tile loads the key sub-tiles (128 / 64 rows)
               up to its last visible key (none when dQ is formed by reduction).
-    narrow: fp32 split into bf16 pairs, which runs the d = 128 items."""
-    sub = 64 if (d == 128 or narrow) else 128
+    narrow: fp32 split into bf16 pairs, which runs the 64-wide d = 128 items
+    (32-wide for head dim 128, whose split rows are 256 columns)."""
+    if narrow:
+        sub = 32 if d == 128 else 64
+    else:
+        sub = 64 if d == 128 else 128
     fwd = kv = dq = 0
     for qt in range(_cdiv(nq, 128)):
         kend = min(nk, qt * 128 + 128) if causal else nk
@@ -119,7 +123,8 @@ def test_release_build_counts_nothing(cuda_lib):
 
 
 @pytest.mark.parametrize("bh,nq,nk,d,causal", [(2, 512, 512, 64, True), (1, 300, 1000, 32, False),
-                                               (1, 2048, 2048, 64, True)])
+                                               (1, 2048, 2048, 64, True), (2, 640, 640, 128, True),
+                                               (1, 333, 777, 128, False)])
 def test_debug_build_split_fp32(cuda_lib, bh, nq, nk, d, causal):
     """fp32 split into bf16 pairs (the d = 128 kernels on 128-column copies): no failed
     check, the visible tiles' rows exactly, the release library's results bit for bit

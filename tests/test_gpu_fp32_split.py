@@ -75,27 +75,22 @@ def test_split_fp32_exact_mode_matches_the_cuda_core_kernels(cuda_lib):
 def test_split_fp32_scale_one_within_the_product_bound(cuda_lib, d):
     """Forced split mode at scale 1: scores of standard deviation sqrt(d), where the
     products' 3 * 2^-16 relative error reaches the outputs through the softmax;
-    every output stays inside the first-order bound of those products.  At d <= 64
-    forward and backward are split, so the errors also stay within twice those of
-    the numerical model of that arithmetic; at d = 128 the backward is exact fp32
-    on the CUDA cores but recomputes P from the split forward's L (its rows then sum
-    to exp(L - L_split) rather than 1), a different error pattern that only the
-    bound covers."""
+    every output stays inside the first-order bound of those products, and within
+    twice the errors of the numerical model of that arithmetic."""
     from tiled_attention_04_gb300 import binding
     t = inputs.make_custom(2, 256, 256, d, "f32", seed=7200 + d)
     with binding.fp32_mode(binding.FA_FP32_SPLIT):
         got = run_gpu(t, True, scale=1.0)
     want = oracle_all(t, True, 1.0)
     bound = split_bound(t, True, 1.0)
-    model = split_model(t, True, 1.0) if d <= 64 else None
+    model = split_model(t, True, 1.0)
     for k in ("O", "L", "dQ", "dK", "dV"):
         err = np.abs(got[k] - want[k])
         allowed = bound[k] + 1e-5 * (1.0 + np.abs(want[k]))   # fp32 exp2 and accumulation
         assert (err <= allowed).all(), f"{k}: max err {err.max():.3g}, worst err/bound {(err / allowed).max():.3g}"
         # and no worse than the split arithmetic itself (the bound is a worst case over signs)
-        if d <= 64:
-            model_err = np.abs(model[k] - want[k]).max()
-            assert err.max() <= 2 * model_err + 1e-5 * (1.0 + np.abs(want[k]).max()), (k, err.max(), model_err)
+        model_err = np.abs(model[k] - want[k]).max()
+        assert err.max() <= 2 * model_err + 1e-5 * (1.0 + np.abs(want[k]).max()), (k, err.max(), model_err)
 
 
 @pytest.mark.parametrize("d", [64, 128])

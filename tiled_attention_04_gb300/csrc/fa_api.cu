@@ -128,7 +128,7 @@ fa_status take_strides(const fa_strides *in, int B, int H, int N, int d, fa_dtyp
 // reduction) the fp32 dQ accumulator (see fa_tc_bwd.cu).  fp32 inputs that may
 // take the split pairs (for some scale: the preprocessing phase has no scale
 // argument) get both layouts: the tensor-core rows, the split bf16 copies of Q,
-// dO, K and V (256 bytes per row each), and the CUDA-core D at sd_off.
+// dO, K and V (256 or 512 bytes per row each), and the CUDA-core D at sd_off.
 struct Workspace {
     bool tc;
     size_t d_off, l_off, dqa_off, total;
@@ -142,8 +142,7 @@ size_t x3_bytes(const FaProblem &p, int N) { return align_up((size_t)p.BH * N * 
 Workspace workspace_layout(const FaProblem &p) {
     Workspace w{};
     w.tc = tc_bwd_supported(p);
-    // (split pairs in the backward up to head dim 64; at 128 only the forward takes them)
-    w.x3_possible = tc_x3_possible(p) && p.d <= 64;
+    w.x3_possible = tc_x3_possible(p);
     w.x3 = w.x3_possible && tc_x3(p);
     const bool tc_rows = w.tc || w.x3_possible;
     const size_t rows = tc_rows ? tc_bwd_ld_rows(p) : (size_t)p.BH * p.Nq;

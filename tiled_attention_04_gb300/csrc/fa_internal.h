@@ -84,8 +84,8 @@ struct FwdPrep {
 // ---- fp32 inputs (X3): each operand is first split into a bf16 pair (hi = bf16(x),
 // lo = bf16(x - hi)) held as a contiguous (B*H, N, 2W) bf16 copy, hi in columns
 // [0, W) and lo in [W, 2W), W = 64 for d <= 64 (the d = 128 kernels) and 128 for
-// d = 128 (the 256-column forward; that head dim's backward stays on the CUDA
-// cores); every contraction takes three products (hi hi + hi lo + lo hi).
+// d = 128 (256-column kernels: one K / V slot in the forward, 32-row sub-tiles in
+// the backward); every contraction takes three products (hi hi + hi lo + lo hi).
 bool tc_x3(const FaProblem &p);            // this problem runs X3 (mode, shape and scale)
 bool tc_x3_possible(const FaProblem &p);   // X3 for some scale (mode and shape): workspace sizing
 void tc_disable_x3(bool off);   // for the calling thread's calls (off: fp32 on the CUDA cores)

@@ -80,8 +80,8 @@ fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V, const void
     DqStrategy forced = DqStrategy::kAuto;
     bool x3_off = false;
     if (need > FA_NOALLOC_SCRATCH_BYTES && dtype == FA_DTYPE_F32) {
-        // fp32 inputs: the split bf16 copies of the tensor-core path (256 bytes per row
-        // of each of Q, dO, K, V) do not fit; the CUDA-core kernels need only D
+        // fp32 inputs: the split bf16 copies of the tensor-core path (256 or 512 bytes
+        // per row of each of Q, dO, K, V) do not fit; the CUDA-core kernels need only D
         tc_disable_x3(true);
         need = fa_bwd_workspace_size(B, H, Nq, Nk, d, is_causal, dtype);
         tc_disable_x3(false);

@@ -127,19 +127,21 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16 *__
     }
 }
 
-// fp32 inputs (X3): the same row constants from fp32 O and dO (head dim up to
-// 64), and dO split into its bf16 pair row [hi | lo] (zeros past d) for the
-// gradient launch.  Sixteen threads per row, four columns each.
+// fp32 inputs (X3): the same row constants from fp32 O and dO, and dO split into
+// its bf16 pair row [hi | lo] of 2W columns (W = 64 for d <= 64, 128 for d = 128;
+// zeros past d) for the gradient launch.  W/4 threads per row, four columns each.
+template <int W>
 __global__ void __launch_bounds__(256) fa_bwd_pre_x3_kernel(const float *__restrict__ O, const float *__restrict__ dO,
                                                             const float *__restrict__ L, float *__restrict__ Dp,
                                                             float *__restrict__ Lp, __nv_bfloat16 *__restrict__ dO2,
                                                             int Nq, int H, int d, FaStrides so, FaStrides sdo) {
+    constexpr int TPR = W / 4, RPB = 256 / TPR;   // threads per row, rows per block (divides 128)
     tc::pdl_launch_dependents();
     tc::pdl_wait();   // O (from the forward) and dO are complete
     const int nqp = padded_rows(Nq);
-    const long long gr = (long long)blockIdx.x * 16 + threadIdx.x / 16;   // padded row (rows per block divide 128)
+    const long long gr = (long long)blockIdx.x * RPB + threadIdx.x / TPR;   // padded row
     const int bh = (int)(gr / nqp), q = (int)(gr - (long long)bh * nqp);
-    const int cg = threadIdx.x % 16;
+    const int cg = threadIdx.x % TPR;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
     if (q < Nq && 4 * cg < d) {
         a = __ldg(reinterpret_cast<const float4 *>(O + fa_row_offset(so, H, bh, q) + 4 * cg));
@@ -148,12 +150,12 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_x3_kernel(const float *__restr
     const float lrow = (cg == 0 && q < Nq) ? __ldg(L + (long long)bh * Nq + q) : 0.f;
     float acc = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (q < Nq) {
         const uint32_t h0 = tc::pack_bf16(b.x, b.y), h1 = tc::pack_bf16(b.z, b.w);
-        uint2 *dst = reinterpret_cast<uint2 *>(dO2 + ((long long)bh * Nq + q) * 128);
+        uint2 *dst = reinterpret_cast<uint2 *>(dO2 + ((long long)bh * Nq + q) * (2 * W));
         dst[cg] = make_uint2(h0, h1);
-        dst[16 + cg] = make_uint2(tc::pack_bf16_residual(b.x, b.y, h0), tc::pack_bf16_residual(b.z, b.w, h1));
+        dst[TPR + cg] = make_uint2(tc::pack_bf16_residual(b.x, b.y, h0), tc::pack_bf16_residual(b.z, b.w, h1));
     }
     if (cg == 0) {
         Dp[gr] = q < Nq ? -acc : 0.f;
@@ -1060,17 +1062,22 @@ __device__ __forceinline__ void dq_item_wide(const CUtensorMap &tmQ, const CUten
 template <int D>
 struct DkdvNarrowCfg {
     static constexpr int BK = 128;                 // keys per CTA (MMA M)
-    static constexpr int BQ = 64;                  // queries per sub-tile (MMA N of S^T, K of dV/dK)
+    // queries per sub-tile (MMA N of S^T, K of dV/dK); 32 for the 256-column split rows
+    static constexpr int BQ = D == 256 ? 32 : 64;
     // deep ring: a stage is refilled only after its sub-tile's dV/dK MMAs finish, and
     // an L2-resident TMA reload takes ~2000 cycles, several sub-tiles' worth of MMA time
-    static constexpr int STAGES = D == 128 ? 4 : 8;
+    // (D = 256, the split pairs of fp32 head dim 128: 32-row sub-tiles, two stages next to
+    // the 64 KB K and V tiles)
+    static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 4 : 8;
+    // dV / dK accumulator columns: d, but 128 for the 256-column split rows
+    static constexpr int OW = D == 256 ? 128 : D;
     using KT = TileShape<BK, D>;
     using QT = TileShape<BQ, D>;
     static constexpr uint32_t K_OFF = 0;
     static constexpr uint32_t V_OFF = K_OFF + KT::BYTES;
     static constexpr uint32_t Q_OFF = V_OFF + KT::BYTES;                 // stages of Q sub-tiles
     static constexpr uint32_t DO_OFF = Q_OFF + STAGES * QT::BYTES;       // stages of dO sub-tiles
-    static constexpr uint32_t LD_OFF = DO_OFF + STAGES * QT::BYTES;      // stages of 64 Lp + 64 D floats
+    static constexpr uint32_t LD_OFF = DO_OFF + STAGES * QT::BYTES;      // stages of BQ Lp + BQ D floats (512 B)
     static constexpr uint32_t BAR_OFF = LD_OFF + STAGES * 512;
     // kv_full, q_full[S], q_empty[S], sd_full[2], p_full[2], mma_done[2], drain
     static constexpr int NBAR = 1 + 2 * STAGES + 6 + 1;
@@ -1079,11 +1086,12 @@ struct DkdvNarrowCfg {
     static constexpr uint32_t SMEM_BYTES = (PEER_BAR_OFF + 16 + 1024 > 120u * 1024u ? PEER_BAR_OFF + 16 + 1024 : 120u * 1024u);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     // split items: rank 1's partial dV (rows 0..127) and dK (rows 128..255), fp32, over the tile rings
-    static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
+    static constexpr uint32_t PART_STRIDE = (OW + 4) * 4;
     static constexpr uint32_t PART_OFF = 0;
     static_assert(PART_OFF + 256 * PART_STRIDE <= BAR_OFF, "partial fits the rings");
-    // TMEM: S^T_t [128t, 128t+64), dP^T_t [128t+64, 128t+128), dV [256, 256+D), dK [256+D, 256+2D)
-    static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
+    // TMEM: S^T_t [128t, 128t+64), dP^T_t [128t+64, 128t+128), dV [256, 256+OW), dK [256+OW, 256+2OW)
+    static constexpr uint32_t DV_COL = 256, DK_COL = 256 + OW;
+    static_assert(DK_COL + OW <= TMEM_COLS, "dV and dK after the score buffers");
 };
 
 // one dK/dV work item: key tile kt of batch*head bh (a half of it when SPLIT = 2).
@@ -1099,8 +1107,10 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                                           void *__restrict__ dVv, int Nq, int Nk, int kt, int bh, int H,
                                           int dv, const FaStrides &sdk, const FaStrides &sdv, float scale,
                                           float scale_log2, uint32_t wait_limit) {
-    static_assert(!X3 || (D == 128 && !VIEW4), "split fp32 operands use the d = 128 layout of contiguous copies");
+    static_assert(!X3 || ((D == 128 || D == 256) && !VIEW4), "split fp32 operands: 128- or 256-column copies");
+    static_assert(X3 || D <= 128, "the 256-column layout holds split pairs only");
     using C = DkdvNarrowCfg<D>;
+    constexpr bool FOLD = X3 && D == 128;   // outputs folded from [hi | lo] accumulator columns
     __nv_bfloat16 *dK = static_cast<__nv_bfloat16 *>(dKv), *dV = static_cast<__nv_bfloat16 *>(dVv);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -1184,7 +1194,7 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                 // debug build: a query sub-tile past the queries, or wholly on the
                 // masked side of the diagonal, is never loaded
                 if (!tc::in_bounds(q0 < Nq && (!CAUSAL || q0 + C::BQ - 1 >= k0), &g_fa_bwd_status, abort_flag)) break;
-                tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 512);
+                tc::mbar_arrive_expect_tx(q_full(s), 2 * C::QT::BYTES + 2 * C::BQ * 4);
                 for (int c = 0; c < D / 64; ++c) {
                     tc::tma_load_rows<VIEW4>(base + C::Q_OFF + s * C::QT::BYTES + c * C::QT::CHUNK, &tmQ, q_full(s), c * 64,
                                     q0, bh, H);
@@ -1192,8 +1202,8 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                                     c * 64, q0, bh, H);
                 }
                 const size_t off = (size_t)bh * nqp + q0;
-                tc::bulk_load(base + C::LD_OFF + s * 512, Lp + off, 256, q_full(s));
-                tc::bulk_load(base + C::LD_OFF + s * 512 + 256, Dp + off, 256, q_full(s));
+                tc::bulk_load(base + C::LD_OFF + s * 512, Lp + off, C::BQ * 4, q_full(s));
+                tc::bulk_load(base + C::LD_OFF + s * 512 + 256, Dp + off, C::BQ * 4, q_full(s));
                 issued = it + 1;
             }
             if constexpr (tc::kDebug) atomicAdd(&g_fa_bwd_rows[0], (unsigned long long)issued * C::BQ);
@@ -1214,8 +1224,8 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
         const bool leader = tc::elect_one();
         if (n > 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BQ, false, false);
-            constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
-            constexpr uint32_t idesc_g_hi = tc::idesc_bf16(128, 64, false, true);   // X3: lo times hi
+            constexpr uint32_t idesc_g = tc::idesc_bf16(128, C::OW, false, true);
+            constexpr uint32_t idesc_g_hi = tc::idesc_bf16(128, 64, false, true);   // X3, D = 128: lo times hi
             const uint64_t kd = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);     // A of S^T, K-major
             const uint64_t vd = tc::sdesc_sw128(base + C::V_OFF, 16, 1024);     // A of dP^T
             const uint64_t qk = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);     // B of S^T, K-major, stage 0
@@ -1235,11 +1245,29 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                         tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + kk * 8, om + st + kk * 128, idesc_g, acc);
                         tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + kk * 8, qm + st + kk * 128, idesc_g, acc);
                     }
-                    if constexpr (X3) {   // Plo^T dOhi and dSlo^T Qhi into the first 64 columns
+                    if constexpr (FOLD) {   // Plo^T dOhi and dSlo^T Qhi into the first 64 columns
 #pragma unroll
                         for (int kk = 0; kk < C::BQ / 16; ++kk) {
-                            tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + 32 + kk * 8, om + st + kk * 128, idesc_g_hi, 1u);
-                            tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 96 + kk * 8, qm + st + kk * 128, idesc_g_hi, 1u);
+                            tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + C::BQ / 2 + kk * 8, om + st + kk * 128,
+                                       idesc_g_hi, 1u);
+                            tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + C::BQ / 2 + kk * 8, qm + st + kk * 128,
+                                       idesc_g_hi, 1u);
+                        }
+                    } else if constexpr (X3) {
+                        // D = 256: Phi^T dOlo, dShi^T Qlo (chunks 2, 3), then Plo^T dOhi, dSlo^T Qhi, all
+                        // into the same dV / dK columns
+                        const uint32_t lo = (2 * C::QT::CHUNK) >> 4;
+#pragma unroll
+                        for (int kk = 0; kk < C::BQ / 16; ++kk) {
+                            tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + kk * 8, om + st + lo + kk * 128, idesc_g, 1u);
+                            tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + kk * 8, qm + st + lo + kk * 128, idesc_g, 1u);
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < C::BQ / 16; ++kk) {
+                            tc::mma_ts(tmem + C::DV_COL, tmem + 128 * t + C::BQ / 2 + kk * 8, om + st + kk * 128,
+                                       idesc_g, 1u);
+                            tc::mma_ts(tmem + C::DK_COL, tmem + 128 * t + 64 + C::BQ / 2 + kk * 8, qm + st + kk * 128,
+                                       idesc_g, 1u);
                         }
                     }
                     tc::mma_commit(q_empty(s));   // sub-tile `it` done: its stage is free
@@ -1252,15 +1280,33 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                 if (!(ok = __all_sync(0xffffffffu, W.wait(q_full(s), (it / C::STAGES) & 1)))) break;
                 if (leader) {
                     const uint32_t st = (s * C::QT::BYTES) >> 4;
-                    // X3: chunk pairs (hi, hi), (hi, lo), (lo, hi), four k-steps each
-                    constexpr int KSTEPS = X3 ? 12 : D / 16;
+                    // S^T = K Q^T and dP^T = V dO^T, interleaved, four k-steps per chunk pair:
+                    // (c, c) for each chunk, or X3: (hi, hi), (hi, lo), (lo, hi) for each of the
+                    // HC hi chunks (the lo chunks follow them)
+                    constexpr int HC = X3 ? D / 128 : 1;
+                    constexpr int PAIRS = X3 ? 3 * HC : D / 64;
+                    auto pair = [&](int pr) {
+                        int ca = pr, cb = pr;
+                        if constexpr (X3) {
+                            const int grp = pr / HC, c = pr % HC;
+                            ca = grp == 2 ? HC + c : c;
+                            cb = grp == 1 ? HC + c : c;
+                        }
 #pragma unroll
-                    for (int kk = 0; kk < KSTEPS; ++kk) {   // S^T = K Q^T and dP^T = V dO^T, interleaved
-                        const int ca = X3 ? ((kk >> 2) == 2) : (kk >> 2), cb = X3 ? ((kk >> 2) == 1) : (kk >> 2);
-                        const uint32_t oa = (ca * C::KT::CHUNK + (kk & 3) * 32) >> 4;
-                        const uint32_t ob = (cb * C::QT::CHUNK + (kk & 3) * 32) >> 4;
-                        tc::mma_ss(tmem + 128 * t, kd + oa, qk + st + ob, idesc_s, kk > 0 ? 1u : 0u);
-                        tc::mma_ss(tmem + 128 * t + 64, vd + oa, ok_ + st + ob, idesc_s, kk > 0 ? 1u : 0u);
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const uint32_t oa = (ca * C::KT::CHUNK + k4 * 32) >> 4;
+                            const uint32_t ob = (cb * C::QT::CHUNK + k4 * 32) >> 4;
+                            const uint32_t acc = (pr > 0 || k4 > 0) ? 1u : 0u;
+                            tc::mma_ss(tmem + 128 * t, kd + oa, qk + st + ob, idesc_s, acc);
+                            tc::mma_ss(tmem + 128 * t + 64, vd + oa, ok_ + st + ob, idesc_s, acc);
+                        }
+                    };
+                    if constexpr (PAIRS <= 3) {
+#pragma unroll
+                        for (int pr = 0; pr < PAIRS; ++pr) pair(pr);
+                    } else {
+#pragma unroll 1
+                        for (int pr = 0; pr < PAIRS; ++pr) pair(pr);
                     }
                     tc::mma_commit(sd_full(t));
                 }
@@ -1295,29 +1341,32 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
             ok = W.wait(q_full(s), (it / C::STAGES) & 1);      // L and D of this sub-tile are in smem
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
-            uint32_t sv[2][32], dv[2][32];
-            tmem_ld_x32(tS, sv[0]);
-            tmem_ld_x32(tS + 32, sv[1]);
-            tmem_ld_x32(tP, dv[0]);
-            tmem_ld_x32(tP + 32, dv[1]);
+            constexpr int NC = C::BQ / 32;   // 32-column TMEM loads per buffer
+            uint32_t sv[NC][32], dv[NC][32];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                tmem_ld_x32(tS + 32 * c, sv[c]);
+                tmem_ld_x32(tP + 32 * c, dv[c]);
+            }
             tc::tmem_ld_wait();
-            reg_fence_x32(sv[0]);
-            reg_fence_x32(sv[1]);
-            reg_fence_x32(dv[0]);
-            reg_fence_x32(dv[1]);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                reg_fence_x32(sv[c]);
+                reg_fence_x32(dv[c]);
+            }
             const float *lds = reinterpret_cast<const float *>(sb + C::LD_OFF + s * 512);   // -L*log2e, -D
             // causal: query columns c < key - q0 cannot see this key; where a sub-tile
             // has such columns, S^T is set to -inf first (P = 0, dS = 0)
             const int first_visible = key - q0;
             if (CAUSAL && __any_sync(0xffffffffu, first_visible > 0)) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
+                for (int c = 0; c < C::BQ; ++c)
                     if (c < first_visible) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
             }
-            uint32_t pp[32], dsp[32];
-            uint32_t ppl[X3 ? 32 : 1], dspl[X3 ? 32 : 1];   // X3: the bf16 residuals
+            uint32_t pp[C::BQ / 2], dsp[C::BQ / 2];
+            uint32_t ppl[X3 ? C::BQ / 2 : 1], dspl[X3 ? C::BQ / 2 : 1];   // X3: the bf16 residuals
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < C::BQ / 4; ++i) {
                 const float4 nl = *reinterpret_cast<const float4 *>(lds + 4 * i);
                 const float4 nd = *reinterpret_cast<const float4 *>(lds + 64 + 4 * i);
 #pragma unroll
@@ -1340,11 +1389,20 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                     }
                 }
             }
-            tmem_st_x32(tS, pp);
-            tmem_st_x32(tP, dsp);
-            if constexpr (X3) {   // over S^T / dP^T columns 32..63, already read
-                tmem_st_x32(tS + 32, ppl);
-                tmem_st_x32(tP + 32, dspl);
+            if constexpr (C::BQ == 64) {
+                tmem_st_x32(tS, pp);
+                tmem_st_x32(tP, dsp);
+                if constexpr (X3) {   // over S^T / dP^T columns 32..63, already read
+                    tmem_st_x32(tS + 32, ppl);
+                    tmem_st_x32(tP + 32, dspl);
+                }
+            } else {   // 32-query sub-tiles: 16 packed columns each, lo over columns 16..31
+                tmem_st_x16(tS, pp);
+                tmem_st_x16(tP, dsp);
+                if constexpr (X3) {
+                    tmem_st_x16(tS + 16, ppl);
+                    tmem_st_x16(tP + 16, dspl);
+                }
             }
             tc::tmem_st_wait();
             tc::fence_before_sync();
@@ -1378,7 +1436,7 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
             const bool dst_ok = tc::wait_peer(peer_free, &g_fa_bwd_status, 2u);
             const uint32_t rdst = tc::map_to_rank(part, rank ^ 1u);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < C::OW / 32; ++c) {
                 uint32_t a[32];
                 if (fine && n > 0) {
                     tmem_ld_x32(tA + 32 * c, a);
@@ -1395,6 +1453,38 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
                 }
             }
             tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, rank ^ 1u));   // release: the stores above
+        } else if constexpr (X3 && !FOLD) {
+            // D = 256: the accumulator columns are the output columns, written in fp32
+            if constexpr (SPLIT > 1) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 2u);
+            const float *pr = reinterpret_cast<const float *>(sb + (part - base));
+            float *drow = static_cast<float *>(t == 0 ? dVv : dKv) +
+                          fa_row_offset(t == 0 ? sdv : sdk, tc::opaque(H), bh, key);
+#pragma unroll
+            for (int c = 0; c < C::OW / 32; ++c) {
+                uint32_t a[32];
+                if (fine && n > 0) {
+                    tmem_ld_x32(tA + 32 * c, a);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(a);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) a[i] = 0u;
+                }
+                float o[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x = __uint_as_float(a[i]);
+                    if (merge) x += pr[32 * c + i];
+                    o[i] = x * mul;
+                }
+                if (fine && (SPLIT == 1 || merge) && key < Nk) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (32 * c + 4 * i < dv)
+                            reinterpret_cast<float4 *>(drow + 32 * c)[i] =
+                                make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                }
+            }
         } else if constexpr (X3) {
             if constexpr (SPLIT > 1) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 2u);
             const float *pr = reinterpret_cast<const float *>(sb + (part - base));
@@ -1480,8 +1570,9 @@ __device__ __forceinline__ void dkdv_item_narrow(const CUtensorMap &tmQ, const C
 template <int D>
 struct DqNarrowCfg {
     static constexpr int BQ = 128;                 // queries per CTA (MMA M)
-    static constexpr int BK = 64;                  // keys per sub-tile
-    static constexpr int STAGES = D == 128 ? 4 : 8;    // see DkdvNarrowCfg
+    static constexpr int BK = D == 256 ? 32 : 64;  // keys per sub-tile (32 for the 256-column split rows)
+    static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 4 : 8;    // see DkdvNarrowCfg
+    static constexpr int OW = D == 256 ? 128 : D;                     // dQ accumulator columns
     using QT = TileShape<BQ, D>;
     using KT = TileShape<BK, D>;
     static constexpr uint32_t Q_OFF = 0;
@@ -1496,10 +1587,11 @@ struct DqNarrowCfg {
     static constexpr uint32_t SMEM_BYTES = (PEER_BAR_OFF + 16 + 1024 > 120u * 1024u ? PEER_BAR_OFF + 16 + 1024 : 120u * 1024u);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     // split items: rank 1's partial dQ (fp32) over the K/V rings
-    static constexpr uint32_t PART_STRIDE = (D + 4) * 4;
-    static constexpr uint32_t PART_OFF = K_OFF;
+    // (the 256-column layout, never split, would need the Q and dO tiles' room as well)
+    static constexpr uint32_t PART_STRIDE = (OW + 4) * 4;
+    static constexpr uint32_t PART_OFF = D == 256 ? 0 : K_OFF;
     static_assert(PART_OFF + 128 * PART_STRIDE <= BAR_OFF, "partial fits the rings");
-    // TMEM: S_t [128t, 128t+64), dP_t [128t+64, 128t+128), dQ [256, 256+D)
+    // TMEM: S_t [128t, 128t+BK), dP_t [128t+64, 128t+64+BK), dQ [256, 256+OW)
     static constexpr uint32_t DQ_COL = 256;
 };
 
@@ -1514,8 +1606,10 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                                         int qt, int bh, int H, int dv, const FaStrides &sdq, float scale,
                                         float scale_log2,
                                         uint32_t wait_limit) {
-    static_assert(!X3 || (D == 128 && !VIEW4), "split fp32 operands use the d = 128 layout of contiguous copies");
+    static_assert(!X3 || ((D == 128 || D == 256) && !VIEW4), "split fp32 operands: 128- or 256-column copies");
+    static_assert(X3 || D <= 128, "the 256-column layout holds split pairs only");
     using C = DqNarrowCfg<D>;
+    constexpr bool FOLD = X3 && D == 128;   // outputs folded from [hi | lo] accumulator columns
     __nv_bfloat16 *dQ = static_cast<__nv_bfloat16 *>(dQv);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -1620,8 +1714,8 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
         // whole warp in the loop (uniform descriptors), one elected lane issues
         const bool leader = tc::elect_one();
         constexpr uint32_t idesc_s = tc::idesc_bf16(128, C::BK, false, false);
-        constexpr uint32_t idesc_g = tc::idesc_bf16(128, D, false, true);
-        constexpr uint32_t idesc_g_hi = tc::idesc_bf16(128, 64, false, true);   // X3: dSlo Khi
+        constexpr uint32_t idesc_g = tc::idesc_bf16(128, C::OW, false, true);
+        constexpr uint32_t idesc_g_hi = tc::idesc_bf16(128, 64, false, true);   // X3, D = 128: dSlo Khi
         const uint64_t qd = tc::sdesc_sw128(base + C::Q_OFF, 16, 1024);      // A of S, K-major
         const uint64_t od = tc::sdesc_sw128(base + C::DO_OFF, 16, 1024);     // A of dP
         const uint64_t kk_ = tc::sdesc_sw128(base + C::K_OFF, 16, 1024);    // B of S, K-major, stage 0
@@ -1638,10 +1732,21 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                 for (int kk = 0; kk < C::BK / 16; ++kk)
                     tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 64 + kk * 8, km + st + kk * 128, idesc_g,
                                (j > 0 || kk > 0) ? 1u : 0u);
-                if constexpr (X3) {
+                if constexpr (FOLD) {
 #pragma unroll
                     for (int kk = 0; kk < C::BK / 16; ++kk)
-                        tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 96 + kk * 8, km + st + kk * 128, idesc_g_hi, 1u);
+                        tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 64 + C::BK / 2 + kk * 8, km + st + kk * 128,
+                                   idesc_g_hi, 1u);
+                } else if constexpr (X3) {
+                    // D = 256: dShi Klo (chunks 2, 3), then dSlo Khi, into the same dQ columns
+                    const uint32_t lo = (2 * C::KT::CHUNK) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / 16; ++kk)
+                        tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 64 + kk * 8, km + st + lo + kk * 128, idesc_g, 1u);
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / 16; ++kk)
+                        tc::mma_ts(tmem + C::DQ_COL, tmem + 128 * t + 64 + C::BK / 2 + kk * 8, km + st + kk * 128,
+                                   idesc_g, 1u);
                 }
                 tc::mma_commit(kv_empty(s));   // sub-tile j done: its stage is free
             }
@@ -1653,15 +1758,33 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
             if (!(ok = __all_sync(0xffffffffu, W.wait(kv_full(s), (j / C::STAGES) & 1)))) break;
             if (leader) {
                 const uint32_t st = (s * C::KT::BYTES) >> 4;
-                // X3: chunk pairs (hi, hi), (hi, lo), (lo, hi), four k-steps each
-                constexpr int KSTEPS = X3 ? 12 : D / 16;
+                // S = Q K^T and dP = dO V^T, interleaved, four k-steps per chunk pair: (c, c)
+                // for each chunk, or X3: (hi, hi), (hi, lo), (lo, hi) for each of the HC hi
+                // chunks (the lo chunks follow them)
+                constexpr int HC = X3 ? D / 128 : 1;
+                constexpr int PAIRS = X3 ? 3 * HC : D / 64;
+                auto pair = [&](int pr) {
+                    int ca = pr, cb = pr;
+                    if constexpr (X3) {
+                        const int grp = pr / HC, c = pr % HC;
+                        ca = grp == 2 ? HC + c : c;
+                        cb = grp == 1 ? HC + c : c;
+                    }
 #pragma unroll
-                for (int kk = 0; kk < KSTEPS; ++kk) {   // S = Q K^T and dP = dO V^T, interleaved
-                    const int ca = X3 ? ((kk >> 2) == 2) : (kk >> 2), cb = X3 ? ((kk >> 2) == 1) : (kk >> 2);
-                    const uint32_t oa = (ca * C::QT::CHUNK + (kk & 3) * 32) >> 4;
-                    const uint32_t ob = (cb * C::KT::CHUNK + (kk & 3) * 32) >> 4;
-                    tc::mma_ss(tmem + 128 * t, qd + oa, kk_ + st + ob, idesc_s, kk > 0 ? 1u : 0u);
-                    tc::mma_ss(tmem + 128 * t + 64, od + oa, vk + st + ob, idesc_s, kk > 0 ? 1u : 0u);
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const uint32_t oa = (ca * C::QT::CHUNK + k4 * 32) >> 4;
+                        const uint32_t ob = (cb * C::KT::CHUNK + k4 * 32) >> 4;
+                        const uint32_t acc = (pr > 0 || k4 > 0) ? 1u : 0u;
+                        tc::mma_ss(tmem + 128 * t, qd + oa, kk_ + st + ob, idesc_s, acc);
+                        tc::mma_ss(tmem + 128 * t + 64, od + oa, vk + st + ob, idesc_s, acc);
+                    }
+                };
+                if constexpr (PAIRS <= 3) {
+#pragma unroll
+                    for (int pr = 0; pr < PAIRS; ++pr) pair(pr);
+                } else {
+#pragma unroll 1
+                    for (int pr = 0; pr < PAIRS; ++pr) pair(pr);
                 }
                 tc::mma_commit(sd_full(t));
             }
@@ -1693,27 +1816,30 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
             bool ok = W.wait(sd_full(t), k & 1);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after_sync();
-            uint32_t sv[2][32], dv[2][32];
-            tmem_ld_x32(tS, sv[0]);
-            tmem_ld_x32(tS + 32, sv[1]);
-            tmem_ld_x32(tP, dv[0]);
-            tmem_ld_x32(tP + 32, dv[1]);
+            constexpr int NC = C::BK / 32;   // 32-column TMEM loads per buffer
+            uint32_t sv[NC][32], dv[NC][32];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                tmem_ld_x32(tS + 32 * c, sv[c]);
+                tmem_ld_x32(tP + 32 * c, dv[c]);
+            }
             tc::tmem_ld_wait();
-            reg_fence_x32(sv[0]);
-            reg_fence_x32(sv[1]);
-            reg_fence_x32(dv[0]);
-            reg_fence_x32(dv[1]);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                reg_fence_x32(sv[c]);
+                reg_fence_x32(dv[c]);
+            }
             // key columns past the diagonal (causal) or past Nk: S set to -inf first (P = 0, dS = 0)
             const int lim = min(Nk - 1, CAUSAL ? row : Nk - 1) - kb0;   // last visible key column
             if (__any_sync(0xffffffffu, lim < C::BK - 1)) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
+                for (int c = 0; c < C::BK; ++c)
                     if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
             }
-            uint32_t dsp[32];
-            uint32_t dspl[X3 ? 32 : 1];   // X3: the bf16 residuals
+            uint32_t dsp[C::BK / 2];
+            uint32_t dspl[X3 ? C::BK / 2 : 1];   // X3: the bf16 residuals
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < C::BK / 2; ++i) {
                 const int c = 2 * i;
                 float x0, x1, g0, g1;
                 tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
@@ -1725,8 +1851,13 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                 dsp[i] = tc::pack_bf16(g0, g1);
                 if constexpr (X3) dspl[i] = tc::pack_bf16_residual(g0, g1, dsp[i]);
             }
-            tmem_st_x32(tP, dsp);
-            if constexpr (X3) tmem_st_x32(tP + 32, dspl);   // over dP columns 32..63, already read
+            if constexpr (C::BK == 64) {
+                tmem_st_x32(tP, dsp);
+                if constexpr (X3) tmem_st_x32(tP + 32, dspl);   // over dP columns 32..63, already read
+            } else {   // 32-key sub-tiles: 16 packed columns, lo over columns 16..31
+                tmem_st_x16(tP, dsp);
+                if constexpr (X3) tmem_st_x16(tP + 16, dspl);
+            }
             tc::tmem_st_wait();
             tc::fence_before_sync();
             tc::mbar_arrive(p_full(t));
@@ -1752,8 +1883,8 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
             const bool dst_ok = tc::wait_peer(peer_free, &g_fa_bwd_status, 4u);
             const uint32_t rdst = tc::map_to_rank(part, rank ^ 1u);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                const int col = X3 ? t * 32 + 64 * c : t * (D / 2) + 32 * c;
+            for (int c = 0; c < C::OW / 64; ++c) {
+                const int col = FOLD ? t * 32 + 64 * c : t * (C::OW / 2) + 32 * c;
                 uint32_t a[32];
                 if (fine && n > 0) {
                     tmem_ld_x32(tA + col, a);
@@ -1770,6 +1901,39 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
                 }
             }
             tc::mbar_arrive_remote(tc::map_to_rank(peer_ready, rank ^ 1u));   // release: the stores above
+        } else if constexpr (X3 && !FOLD) {
+            // D = 256: this warpgroup's output columns [64t, 64t + 64) are its accumulator columns
+            bool merge = false;
+            if constexpr (SPLIT > 1) merge = tc::wait_peer(peer_ready, &g_fa_bwd_status, 4u);
+            const float *pr = reinterpret_cast<const float *>(sb + (part - base));
+            float *drow = static_cast<float *>(dQv) + fa_row_offset(sdq, tc::opaque(H), bh, row);
+#pragma unroll
+            for (int c = 0; c < C::OW / 64; ++c) {
+                const int col = t * (C::OW / 2) + 32 * c;
+                uint32_t a[32];
+                if (fine && n > 0) {
+                    tmem_ld_x32(tA + col, a);
+                    tc::tmem_ld_wait();
+                    reg_fence_x32(a);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) a[i] = 0u;
+                }
+                float o[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x = __uint_as_float(a[i]);
+                    if (merge) x += pr[32 * c + i];
+                    o[i] = x * scale;
+                }
+                if (fine && (SPLIT == 1 || merge) && row < Nq) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (col + 4 * i < dv)
+                            reinterpret_cast<float4 *>(drow + col)[i] =
+                                make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                }
+            }
         } else if constexpr (X3) {
             // this warpgroup's output columns [32t, 32t + 32): accumulator columns 32t + i and 64 + 32t + i
             bool merge = false;
@@ -2380,7 +2544,9 @@ template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool RED, bool X3 = false>
 cudaError_t launch_bwd(const FaProblem &p, const Maps2 &m, const float *Lp, const float *Dp, void *dQ, void *dK,
                        void *dV, bool do_kv, bool do_q, cudaStream_t st) {
     static_assert(!RED || D == 64, "the dQ reduction form exists for the d = 64 items");
-    static_assert(!X3 || (D == 128 && !RED && !VIEW4), "split fp32 operands: d = 128 items, dQ by the separate pass");
+    static_assert(!X3 || ((D == 128 || D == 256) && !RED && !VIEW4),
+                  "split fp32 operands: 128- or 256-column items, dQ by the separate pass");
+    static_assert(!X3 || D == 128 || SPLIT == 1, "256-column split rows run one item per CTA");
     using KvC = std::conditional_t<D == 64, DkdvWideCfg<D, RED>, DkdvNarrowCfg<D>>;
     using QC = std::conditional_t<D == 64, DqWideCfg<D>, DqNarrowCfg<D>>;
     constexpr uint32_t smem = KvC::SMEM_BYTES > QC::SMEM_BYTES ? KvC::SMEM_BYTES : QC::SMEM_BYTES;
@@ -2448,11 +2614,7 @@ bool make_maps(const FaProblem &p, const void *Q, const void *K, const void *V, 
 
 }  // namespace
 
-// fp32 at head dim 128 takes split pairs in the forward only: the backward's
-// 256-column rows would need two stages of 64-row sub-tiles next to 64 KB K and
-// V tiles (the next sub-tile's scores are computed while the previous one's
-// gradients are), which shared memory does not hold; it runs on the CUDA cores.
-bool tc_bwd_supported(const FaProblem &p) { return tc_fwd_supported(p) && !(p.dtype == FA_DTYPE_F32 && p.d > 64); }
+bool tc_bwd_supported(const FaProblem &p) { return tc_fwd_supported(p); }
 
 size_t tc_bwd_ld_rows(const FaProblem &p) { return (size_t)p.BH * padded_rows(p.Nq); }
 
@@ -2612,8 +2774,9 @@ cudaError_t tc_bwd_preprocess_x3(const FaProblem &p, const void *O, const void *
     const long long rows = (long long)p.BH * padded_rows(p.Nq);
     if (rows == 0) return cudaSuccess;
     if (!tc_x3_possible(p)) return cudaErrorInvalidValue;
+    const int rpb = p.d <= 64 ? 16 : 8;   // rows per block: 256 / (W / 4)
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(rows / 16));   // rows is a multiple of 128
+    cfg.gridDim = dim3((unsigned)(rows / rpb));   // rows is a multiple of 128
     cfg.blockDim = dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -2621,9 +2784,12 @@ cudaError_t tc_bwd_preprocess_x3(const FaProblem &p, const void *O, const void *
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fa_bwd_pre_x3_kernel, static_cast<const float *>(O),
-                                       static_cast<const float *>(dO), L, Dp, Lp, static_cast<__nv_bfloat16 *>(dO2),
-                                       p.Nq, p.H, p.d, p.sO, p.sdO);
+    const auto *o = static_cast<const float *>(O), *g = static_cast<const float *>(dO);
+    auto *g2 = static_cast<__nv_bfloat16 *>(dO2);
+    cudaError_t e = p.d <= 64
+                        ? cudaLaunchKernelEx(&cfg, fa_bwd_pre_x3_kernel<64>, o, g, L, Dp, Lp, g2, p.Nq, p.H, p.d, p.sO, p.sdO)
+                        : cudaLaunchKernelEx(&cfg, fa_bwd_pre_x3_kernel<128>, o, g, L, Dp, Lp, g2, p.Nq, p.H, p.d, p.sO,
+                                             p.sdO);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -2634,16 +2800,22 @@ cudaError_t tc_bwd_grads_x3(const FaProblem &p, const void *Q2, const void *K2, 
     if (!tc_x3(p)) return cudaErrorInvalidValue;
     // the d = 128 items over the contiguous (B*H, N, 128) copies: 64-row sub-tiles of
     // the looped-over operand, 128-row tiles of the item's own
+    // columns of a split row, and rows of a looped-over sub-tile (the 256-column items
+    // take 32-row sub-tiles, so that two stages fit next to the 64 KB K / V or Q / dO tiles)
+    const int width = p.d <= 64 ? 128 : 256, sub = p.d <= 64 ? 64 : 32;
     auto map = [&](CUtensorMap *m, const void *ptr, int N, int rows) {
-        return tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(m), ptr, p.BH, N, 128, rows);
+        return tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(m), ptr, p.BH, N, width, rows);
     };
     Maps2 m;
     m.view4 = false;
-    if (!map(&m.a.q, Q2, p.Nq, 64) || !map(&m.a.dO, dO2, p.Nq, 64) || !map(&m.a.k, K2, p.Nk, 128) ||
+    if (!map(&m.a.q, Q2, p.Nq, sub) || !map(&m.a.dO, dO2, p.Nq, sub) || !map(&m.a.k, K2, p.Nk, 128) ||
         !map(&m.a.v, V2, p.Nk, 128) || !map(&m.b.q, Q2, p.Nq, 128) || !map(&m.b.dO, dO2, p.Nq, 128) ||
-        !map(&m.b.k, K2, p.Nk, 64) || !map(&m.b.v, V2, p.Nk, 64))
+        !map(&m.b.k, K2, p.Nk, sub) || !map(&m.b.v, V2, p.Nk, sub))
         return cudaErrorInvalidValue;
     m.dqa = m.a.q;   // unused
+    if (p.d == 128)   // 256-column rows: one item per CTA
+        return p.causal ? launch_bwd<256, true, 1, false, false, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
+                        : launch_bwd<256, false, 1, false, false, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
     const bool split = (do_kv && dkdv_split(p)) || (do_q && dq_split(p));
     if (p.causal)
         return split ? launch_bwd<128, true, 2, false, false, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
