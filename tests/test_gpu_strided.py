@@ -92,8 +92,11 @@ CASES = [
     (4, 40, 256, 64, "bf16", True, "bnhd"),      # many short units: persistent CTAs
     (2, 3, 256, 32, "bf16", True, "bnhd"),       # head dims below 64 on the tensor cores
     (1, 2, 300, 16, "bf16", False, "qkv"),
-    # fp32 CUDA-core path, and a bf16 shape shorter than one 128-row tile
+    # fp32: split bf16 pairs on the tensor cores (N >= 128, every head dim), the
+    # CUDA-core kernels below one tile, and a bf16 shape shorter than one 128-row tile
     (2, 3, 130, 32, "f32", True, "bnhd"),
+    (2, 2, 256, 128, "f32", True, "qkv"),
+    (1, 3, 300, 128, "f32", False, "padded"),
     (1, 3, 100, 64, "f32", False, "qkv"),
     (2, 2, 96, 16, "bf16", True, "padded"),
 ]

@@ -34,7 +34,7 @@ def _both(torch, binding, t, causal):
 
 
 @pytest.mark.parametrize("bh,n,d,dt,causal", [(2, 1024, 128, "bf16", True), (3, 200, 64, "bf16", False),
-                                              (1, 128, 16, "f32", True)])
+                                              (1, 128, 16, "f32", True), (2, 512, 128, "f32", False)])
 def test_noalloc_matches_fa_bwd_twice(cuda_lib, bh, n, d, dt, causal):
     import torch
     from tiled_attention_04_gb300 import binding
