@@ -107,7 +107,7 @@ struct FwdCfg {
     static constexpr uint32_t K_OFF = Q_OFF + TILE_BYTES;
     static constexpr uint32_t V_OFF = K_OFF + KST * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = V_OFF + VST * TILE_BYTES;
-    static constexpr int NBAR = 1 + KST + VST + R + 16;
+    static constexpr int NBAR = 1 + KST + VST + R + 17;
     // per-row (m, l) of both warpgroups, double-buffered by work unit: 2 x (256 + 256) floats
     static constexpr uint32_t STAT_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t MISC_OFF = STAT_OFF + 2 * 512 * 4;
@@ -892,8 +892,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto s_free = [&](int t) { return bar(RB + 6 + t); };   // softmax has read S_t (separate-P layout)
     const uint32_t q_empty = bar(RB + 8);     // S MMAs of the unit done: the Q buffer may be refilled
     const uint32_t o_free = bar(RB + 9);      // epilogue has read O_0, O_1: the next unit may overwrite them
-    const uint32_t merge_bar = bar(RB + 10);  // both warpgroups have published their (m, l)
-    const uint32_t dsum_bar = bar(RB + 11);   // both warpgroups have published their half rowsums (fused preprocessing)
+    // the warpgroup not holding unit u's last tile has published its (m, l); one barrier
+    // per unit parity, so that it can publish unit u + 1's before the merge of u waits
+    auto merge_bar = [&](int u) { return bar(u & 1 ? RB + 16 : RB + 10); };
     // fused preprocessing, d = 64: a unit's dO rows have landed in buffer b (do_full) /
     // have been read by the epilogue (do_free); buffers alternate by unit
     auto do_full = [&](int b) { return bar(RB + 12 + b); };
@@ -915,12 +916,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::mbar_init(drain, 1);
         tc::mbar_init(never, 1);
         tc::mbar_init(q_empty, 1);
-        tc::mbar_init(o_free, 256);
-        tc::mbar_init(merge_bar, 256);
-        tc::mbar_init(dsum_bar, 256);
+        tc::mbar_init(o_free, 128);
+        tc::mbar_init(merge_bar(0), 128);
+        tc::mbar_init(merge_bar(1), 128);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(do_full(b), 1);
-            tc::mbar_init(do_free(b), 256);
+            tc::mbar_init(do_free(b), 128);
         }
         *abort_flag = 0u;
         tc::fence_mbar_init();
@@ -1227,94 +1228,109 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc::fence_before_sync();
                 tc::mbar_arrive(p_full(t));
             }
-            // ---- merge the two warpgroups' partial results
+            // ---- merge.  The warpgroup holding the unit's last tile merges both partial
+            // results and writes the rows; the other publishes its (m, l) and goes on to
+            // the next unit at once, so the epilogue overlaps its tiles.
+            const int t_last = n > 0 ? (g0 + n - 1) & 1 : 0;
             float *m_sm = stat_sm + (u & 1) * 512;
             float *l_sm = m_sm + 256;
-            m_sm[t * 128 + r] = m;
-            l_sm[t * 128 + r] = l;
-            tc::mbar_arrive(merge_bar);
-            bool fine = W.wait(merge_bar, u & 1) && ok;
-            if (fine && n > 0) fine = W.wait(pv_done_bar(g0 + n - 1), pv_done_par(g0 + n - 1));
-            fine = __all_sync(0xffffffffu, fine);
-            const bool has0 = n > j_0, has1 = n > j_1;
-            // this CTA's partial for row r, columns [t*D/2, (t+1)*D/2), relative to max Mc (unnormalised)
-            float v[D / 2];
-            float Mc = -INFINITY, lc = 0.f;
-#pragma unroll
-            for (int i = 0; i < D / 2; ++i) v[i] = 0.f;
-            if (fine && n > 0) {
-                tc::fence_after_sync();
-                const float m0 = m_sm[r], l0 = l_sm[r];
-                const float m1 = m_sm[128 + r], l1 = l_sm[128 + r];
-                Mc = fmaxf(m0, m1);
-                const float a0 = has0 ? exp2f(m0 - Mc) : 0.f;
-                const float a1 = has1 ? exp2f(m1 - Mc) : 0.f;
-                lc = l0 * a0 + l1 * a1;
-                const uint32_t tO0 = tmem + lane_base + C::O_COL0, tO1 = tO0 + D;
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    const int col = t * (D / 2) + 32 * c;
-                    uint32_t o0[32] = {}, o1[32] = {};
-                    if (has0) tmem_ld_x32(tO0 + col, o0);
-                    if (has1) tmem_ld_x32(tO1 + col, o1);
-                    tc::tmem_ld_wait();
-                    reg_fence_x32(o0);
-                    reg_fence_x32(o1);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x = has0 ? __uint_as_float(o0[i]) * a0 : 0.f;
-                        if (has1) x = fmaf(__uint_as_float(o1[i]), a1, x);
-                        v[32 * c + i] = x;
-                    }
+            bool fine = ok;
+            if (t != t_last) {
+                m_sm[t * 128 + r] = m;
+                l_sm[t * 128 + r] = l;
+                tc::mbar_arrive(merge_bar(u));   // release: the stores above
+            } else {
+                const int to = t ^ 1;
+                const bool has_o = n > (to == 0 ? j_0 : j_1);   // the other warpgroup had tiles
+                fine = W.wait(merge_bar(u), (u >> 1) & 1) && fine;
+                if (fine && n > 0) fine = W.wait(pv_done_bar(g0 + n - 1), pv_done_par(g0 + n - 1));
+                fine = __all_sync(0xffffffffu, fine);
+                float mo = -INFINITY, lo = 0.f;
+                if (fine && has_o) {
+                    mo = m_sm[to * 128 + r];
+                    lo = l_sm[to * 128 + r];
                 }
-            }
-            // O_0 and O_1 have been read: the next unit's first PV may overwrite them
-            tc::fence_before_sync();
-            tc::mbar_arrive(o_free);
-            auto store_row = [&](const float *vals, float Mrow, float lrow) -> float {
-                const float inv = 1.f / lrow;
+                const float Mc = fmaxf(m, mo);
+                const float am = exp2f(m - Mc), ao = has_o ? exp2f(mo - Mc) : 0.f;
+                const float lc = l * am + lo * ao;
+                const float inv = 1.f / lc;
+                const uint32_t tOm = tmem + lane_base + C::O_COL0 + t * D;
+                const uint32_t tOo = tmem + lane_base + C::O_COL0 + to * D;
                 __nv_bfloat16 *orow;
-                if constexpr (VIEW4) orow = O + *orow_sm + t * (D / 2);
-                else orow = O + ((size_t)bh * Nq + row) * D + t * (D / 2);
+                if constexpr (VIEW4) orow = O + *orow_sm;
+                else orow = O + ((size_t)bh * Nq + row) * D;
+                if (D == 64 && prep.dO && fine)
+                    fine = __all_sync(0xffffffffu, W.wait(do_full(u & 1), (u >> 1) & 1));
+                const __nv_bfloat16 *drow = nullptr;   // d = 64: the row of dO in shared memory
+                if constexpr (D == 64)
+                    drow = reinterpret_cast<const __nv_bfloat16 *>(sb + C::DOS_OFF + (u & 1) * C::DOS_BYTES) +
+                           (size_t)r * dv;
+                if (fine) tc::fence_after_sync();
+                // 32 columns at a time: both accumulators, the merged and normalised row, its
+                // store, and (fused preprocessing) its part of rowsum(dO * O)
                 float part = 0.f;
-                if (row < Nq) {
-#pragma unroll
-                    for (int c = 0; c < D / 16; ++c) {
-                        uint4 q;
-                        q.x = tc::pack_bf16(vals[8 * c + 0] * inv, vals[8 * c + 1] * inv);
-                        q.y = tc::pack_bf16(vals[8 * c + 2] * inv, vals[8 * c + 3] * inv);
-                        q.z = tc::pack_bf16(vals[8 * c + 4] * inv, vals[8 * c + 5] * inv);
-                        q.w = tc::pack_bf16(vals[8 * c + 6] * inv, vals[8 * c + 7] * inv);
-                        if (!VIEW4 || t * (D / 2) + 8 * c < dv)   // columns past a head dim below 64 are padding
-                            reinterpret_cast<uint4 *>(orow)[c] = q;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t om[32] = {}, oo[32] = {};
+                    if (fine) {
+                        tmem_ld_x32(tOm + 32 * c, om);
+                        if (has_o) tmem_ld_x32(tOo + 32 * c, oo);
+                        tc::tmem_ld_wait();
                     }
-                    if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
-                    if (prep.dO) {
-                        const __nv_bfloat16 *drow = nullptr;
-                        if constexpr (D == 64)
-                            drow = reinterpret_cast<const __nv_bfloat16 *>(sb + C::DOS_OFF + (u & 1) * C::DOS_BYTES) +
-                                   (size_t)r * dv;
-                        part = prep_half_rowsum<D, VIEW4>(prep, vals, inv, bh, row, Nq, H, dv, t, drow);
+                    reg_fence_x32(om);
+                    reg_fence_x32(oo);
+                    float x[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        x[i] = fmaf(__uint_as_float(oo[i]), ao, __uint_as_float(om[i]) * am) * inv;
+                    if (fine && row < Nq) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 q;
+                            q.x = tc::pack_bf16(x[8 * q4 + 0], x[8 * q4 + 1]);
+                            q.y = tc::pack_bf16(x[8 * q4 + 2], x[8 * q4 + 3]);
+                            q.z = tc::pack_bf16(x[8 * q4 + 4], x[8 * q4 + 5]);
+                            q.w = tc::pack_bf16(x[8 * q4 + 6], x[8 * q4 + 7]);
+                            if (!VIEW4 || 32 * c + 8 * q4 < dv)   // columns past a head dim below 64 are padding
+                                reinterpret_cast<uint4 *>(orow + 32 * c)[q4] = q;
+                        }
+                        if (prep.dO) {
+                            const __nv_bfloat16 *g = drow ? drow + 32 * c : nullptr;
+                            if (!g) {
+                                if constexpr (VIEW4)
+                                    g = static_cast<const __nv_bfloat16 *>(prep.dO) +
+                                        fa_row_offset(prep.sdo, H, bh, row) + 32 * c;
+                                else
+                                    g = static_cast<const __nv_bfloat16 *>(prep.dO) + ((size_t)bh * Nq + row) * D + 32 * c;
+                            }
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                if (!VIEW4 || 32 * c + 8 * q4 < dv) {
+                                    const uint4 y = drow ? reinterpret_cast<const uint4 *>(g)[q4]
+                                                         : __ldg(reinterpret_cast<const uint4 *>(g) + q4);
+                                    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&y);
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float2 f = __bfloat1622float2(h[e]);
+                                        part = fmaf(x[8 * q4 + 2 * e], f.x, part);
+                                        part = fmaf(x[8 * q4 + 2 * e + 1], f.y, part);
+                                    }
+                                }
+                            }
+                        }
                     }
                 }
-                return part;
-            };
-            if (D == 64 && prep.dO && fine) fine = __all_sync(0xffffffffu, W.wait(do_full(u & 1), (u >> 1) & 1));
-            const float part = fine ? store_row(v, Mc, lc) : 0.f;
-            if (D == 64 && prep.dO) {
-                // this unit's dO rows have been read: the buffer may take unit u + 2's
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(do_free(u & 1));
-            }
-            if (prep.dO) {
-                // the two halves of the row meet in shared memory (double-buffered by
-                // unit: the merge barrier keeps the warpgroups within one unit)
-                float *dsum = reinterpret_cast<float *>(sb + C::DSUM_OFF) + (u & 1) * 256;
-                dsum[t * 128 + r] = part;
-                tc::mbar_arrive(dsum_bar);
-                const bool got = t == 0 ? W.wait(dsum_bar, u & 1) : true;
-                if (fine) prep_row_finish<D>(prep, part, got && t == 0 ? dsum[128 + r] : 0.f, got && t == 0, Mc, lc, bh,
-                                             row, Nq, t, D != 64);   // d = 64: warp 2 cleared the accumulator rows
+                // O_0 and O_1 have been read: the next unit's first PV may overwrite them
+                tc::fence_before_sync();
+                tc::mbar_arrive(o_free);
+                if (D == 64 && prep.dO) {
+                    // this unit's dO rows have been read: the buffer may take unit u + 2's
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(do_free(u & 1));
+                }
+                if (fine && row < Nq) Lout[(size_t)bh * Nq + row] = Mc * kLn2 + logf(lc);
+                if (fine && prep.dO)   // d = 64: warp 2 cleared the accumulator rows
+                    prep_row_finish<D>(prep, part, 0.f, true, Mc, lc, bh, row, Nq, 0, D != 64);
             }
             g0 += n;
             if (!fine) ok = false;
