@@ -118,14 +118,15 @@ struct FwdCfg {
     // (double-buffered by work unit in the persistent kernel; the split form's
     // rank 1 stores its half into rank 0's copy)
     static constexpr uint32_t DSUM_OFF = OROW_OFF + 256 * 8;
-    // fused backward preprocessing, d = 64: the tile's dO rows (packed, d * 2 bytes
-    // each), fetched by an otherwise idle warp during the main loop; two buffers,
-    // alternating by unit in the persistent kernel (the destination of a bulk copy:
-    // 16-byte aligned; the barrier block above leaves the offsets after it only
-    // 8-byte aligned, hence the rounding)
-    static constexpr uint32_t DOS_OFF = (DSUM_OFF + 2 * 256 * 4 + 127) / 128 * 128;
+    // fused backward preprocessing, d = 64: the tile's dO rows (128 bytes each, the
+    // 16-byte chunks of row r swizzled by r mod 8 so that the epilogue's row-per-thread
+    // reads hit eight different bank groups), fetched by TMA from an otherwise idle
+    // warp during the main loop; two buffers, alternating by unit in the persistent
+    // kernel (the 128-byte swizzle wants 1024-byte aligned destinations; the barrier
+    // block above leaves the offsets after it only 8-byte aligned, hence the rounding)
+    static constexpr uint32_t DOS_OFF = (DSUM_OFF + 2 * 256 * 4 + 1023) / 1024 * 1024;
     static constexpr uint32_t DOS_BYTES = 128 * 64 * 2;
-    static_assert(DOS_OFF % 16 == 0 && DOS_BYTES % 16 == 0, "bulk-copy destinations on 16-byte boundaries");
+    static_assert(DOS_OFF % 1024 == 0 && DOS_BYTES % 1024 == 0, "swizzled TMA destinations on 1024-byte boundaries");
     static constexpr uint32_t USED = DOS_OFF + (D == 64 ? 2 * DOS_BYTES : 0);
     // split items: rank 1's partial O (fp32, rows padded by 4 floats) and its m, l, in the K ring
     static constexpr uint32_t PART_STRIDE = (OW + 4) * 4;
@@ -145,21 +146,27 @@ struct FwdCfg {
 };
 
 // ------------------------------------------------------------------ fused backward preprocessing
+// One 16-byte chunk (8 columns) of a dO row staged by a 128-byte-swizzled TMA
+// load: chunk j of tile row r sits at chunk position j ^ (r mod 8) of the row.
+__device__ __forceinline__ uint4 swizzled_chunk(const uint8_t *srow, int r, int j) {
+    return *reinterpret_cast<const uint4 *>(srow + ((j ^ (r & 7)) << 4));
+}
+
 // Half of rowsum(dO * O) for one query row: this thread's D/2 output columns of
 // the unrounded fp32 O (vals * inv) against the same columns of dO, read from
-// global memory or (drow not NULL) from the row staged in shared memory.
+// global memory or (srow not NULL) from tile row r staged in shared memory.
 template <int D, bool VIEW4>
 __device__ __forceinline__ float prep_half_rowsum(const FwdPrep &prep, const float *vals, float inv, int bh, int row,
-                                                  int Nq, int H, int dv, int t, const __nv_bfloat16 *drow = nullptr) {
-    const __nv_bfloat16 *g = drow;
-    if (g) g += t * (D / 2);
-    else if constexpr (VIEW4) g = static_cast<const __nv_bfloat16 *>(prep.dO) + fa_row_offset(prep.sdo, H, bh, row) + t * (D / 2);
+                                                  int Nq, int H, int dv, int t, const uint8_t *srow = nullptr,
+                                                  int r = 0) {
+    const __nv_bfloat16 *g;
+    if constexpr (VIEW4) g = static_cast<const __nv_bfloat16 *>(prep.dO) + fa_row_offset(prep.sdo, H, bh, row) + t * (D / 2);
     else g = static_cast<const __nv_bfloat16 *>(prep.dO) + ((size_t)bh * Nq + row) * D + t * (D / 2);
     float acc = 0.f;
 #pragma unroll
     for (int c = 0; c < D / 16; ++c) {
         if (!VIEW4 || t * (D / 2) + 8 * c < dv) {   // columns past a head dim below 64 are padding
-            const uint4 x = drow ? reinterpret_cast<const uint4 *>(g)[c] : __ldg(reinterpret_cast<const uint4 *>(g) + c);
+            const uint4 x = srow ? swizzled_chunk(srow, r, t * (D / 16) + c) : __ldg(reinterpret_cast<const uint4 *>(g) + c);
             const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&x);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -247,7 +254,8 @@ __global__ void __launch_bounds__(256) fa_split_x3_kernel(const __grid_constant_
 template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool X3 = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, void *__restrict__ Ov,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     void *__restrict__ Ov,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
                      uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so, FwdPrep prep) {
     static_assert(!X3 || ((D == 128 || D == 256) && !VIEW4), "split fp32 operands: 128- or 256-column copies");
@@ -399,16 +407,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp == 2) {
         // ------------------------------------------------------------ fused preprocessing
         // While the tile runs: fetch its dO rows into shared memory for the epilogue's
-        // rowsum (d = 64: one bulk copy of the contiguous rows) and clear its rows of
-        // the dQ accumulator (rank 0 of a split item), off the epilogue's path.
+        // rowsum (d = 64: one swizzled TMA tile; rows past Nq and columns past a head
+        // dim below 64 read as zeros) and clear its rows of the dQ accumulator (rank 0
+        // of a split item), off the epilogue's path.
         if (prep.dO && q0 < Nq) {
             if (D == 64 && lane == 0) {
-                const int rows = min(BM, Nq - q0);
-                const uint32_t bytes = (uint32_t)rows * dv * 2;
-                const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(prep.dO) +
-                                           (VIEW4 ? fa_row_offset(prep.sdo, H, bh, q0) : ((size_t)bh * Nq + q0) * D);
-                tc::mbar_arrive_expect_tx(do_full, bytes);
-                tc::bulk_load(base + C::DOS_OFF, src, bytes, do_full);
+                tc::mbar_arrive_expect_tx(do_full, C::DOS_BYTES);
+                tc::tma_load_rows<VIEW4>(base + C::DOS_OFF, &tmdO, do_full, 0, q0, bh, H);
             }
             if (D == 64 && prep.dQa && rank == 0) {
                 float4 *z = reinterpret_cast<float4 *>(prep.dQa + ((size_t)bh * ((Nq + 127) / 128 * 128) + q0) * 64);
@@ -727,10 +732,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 if (t == 0) Lout[(size_t)bh * Nq + row] = Mrow * kLn2 + logf(lrow);
                 if (prep.dO) {
-                    const __nv_bfloat16 *drow = nullptr;
-                    if constexpr (D == 64)
-                        drow = reinterpret_cast<const __nv_bfloat16 *>(sb + C::DOS_OFF) + (size_t)r * dv;
-                    part = prep_half_rowsum<D, VIEW4>(prep, vals, inv, bh, row, Nq, H, dv, t, drow);
+                    const uint8_t *srow = nullptr;
+                    if constexpr (D == 64) srow = sb + C::DOS_OFF + r * 128;
+                    part = prep_half_rowsum<D, VIEW4>(prep, vals, inv, bh, row, Nq, H, dv, t, srow, r);
                 }
             }
             return part;
@@ -840,7 +844,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int D, bool CAUSAL, bool VIEW4>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_fwd_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, void *__restrict__ Ov,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     void *__restrict__ Ov,
                      float *__restrict__ Lout, int Nq, int Nk, int BH, int num_q_tiles, float scale_log2,
                      uint32_t wait_limit, uint32_t force_stall, int H, int dv, FaStrides so, FwdPrep prep) {
     using C = FwdCfg<D>;
@@ -1017,13 +1022,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // the buffer last held unit u - 2's rows: wait until its epilogue read them
                     if (u >= 2) ok = W.wait(do_free(b), ((u - 2) >> 1) & 1);
                     if (ok) {
-                        const int rows = min(BM, Nq - w.q0);
-                        const uint32_t bytes = (uint32_t)rows * dv * 2;
-                        const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(prep.dO) +
-                                                   (VIEW4 ? fa_row_offset(prep.sdo, H, w.bh, w.q0)
-                                                          : ((size_t)w.bh * Nq + w.q0) * D);
-                        tc::mbar_arrive_expect_tx(do_full(b), bytes);
-                        tc::bulk_load(base + C::DOS_OFF + b * C::DOS_BYTES, src, bytes, do_full(b));
+                        tc::mbar_arrive_expect_tx(do_full(b), C::DOS_BYTES);
+                        tc::tma_load_rows<VIEW4>(base + C::DOS_OFF + b * C::DOS_BYTES, &tmdO, do_full(b), 0, w.q0, w.bh,
+                                                 H);
                         issued = u + 1;
                     }
                 }
@@ -1261,10 +1262,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 else orow = O + ((size_t)bh * Nq + row) * D;
                 if (D == 64 && prep.dO && fine)
                     fine = __all_sync(0xffffffffu, W.wait(do_full(u & 1), (u >> 1) & 1));
-                const __nv_bfloat16 *drow = nullptr;   // d = 64: the row of dO in shared memory
-                if constexpr (D == 64)
-                    drow = reinterpret_cast<const __nv_bfloat16 *>(sb + C::DOS_OFF + (u & 1) * C::DOS_BYTES) +
-                           (size_t)r * dv;
+                const uint8_t *srow = nullptr;   // d = 64: the row of dO in shared memory (swizzled)
+                if constexpr (D == 64) srow = sb + C::DOS_OFF + (u & 1) * C::DOS_BYTES + r * 128;
                 if (fine) tc::fence_after_sync();
                 // 32 columns at a time: both accumulators, the merged and normalised row, its
                 // store, and (fused preprocessing) its part of rowsum(dO * O)
@@ -1295,8 +1294,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                 reinterpret_cast<uint4 *>(orow + 32 * c)[q4] = q;
                         }
                         if (prep.dO) {
-                            const __nv_bfloat16 *g = drow ? drow + 32 * c : nullptr;
-                            if (!g) {
+                            const __nv_bfloat16 *g = nullptr;
+                            if (!srow) {
                                 if constexpr (VIEW4)
                                     g = static_cast<const __nv_bfloat16 *>(prep.dO) +
                                         fa_row_offset(prep.sdo, H, bh, row) + 32 * c;
@@ -1306,7 +1305,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
                                 if (!VIEW4 || 32 * c + 8 * q4 < dv) {
-                                    const uint4 y = drow ? reinterpret_cast<const uint4 *>(g)[q4]
+                                    const uint4 y = srow ? swizzled_chunk(srow, r, 4 * c + q4)
                                                          : __ldg(reinterpret_cast<const uint4 *>(g) + q4);
                                     const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&y);
 #pragma unroll
@@ -1547,12 +1546,12 @@ static int sm_count() { return tc_sm_count(); }
 
 template <int D, bool CAUSAL, int SPLIT, bool PERSIST, bool VIEW4, bool X3 = false>
 static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                              void *O, float *L, const FwdPrep &prep, cudaStream_t st) {
+                              const CUtensorMap &mdo, void *O, float *L, const FwdPrep &prep, cudaStream_t st) {
     static_assert(!(PERSIST && SPLIT > 1), "persistent units are not split");
     static_assert(!(PERSIST && X3), "split fp32 operands run one unit per CTA (or cluster)");
     using C = FwdCfg<D>;
-    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, void *, float *, int, int, int, int,
-                 float, uint32_t, uint32_t, int, int, FaStrides, FwdPrep);
+    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, void *, float *, int, int,
+                 int, int, float, uint32_t, uint32_t, int, int, FaStrides, FwdPrep);
     if constexpr (PERSIST) kern = fa_fwd_tc_persistent_kernel<D, CAUSAL, VIEW4>;
     else kern = fa_fwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4, X3>;
     cudaError_t e = tc_set_smem_once(reinterpret_cast<const void *>(kern), (int)C::SMEM_BYTES);
@@ -1577,7 +1576,7 @@ static cudaError_t launch_fwd(const FaProblem &p, const CUtensorMap &mq, const C
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = SPLIT > 1 ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, O, L, p.Nq, p.Nk, p.BH, qtiles,
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, O, L, p.Nq, p.Nk, p.BH, qtiles,
                            scale_log2, p.wait_limit, p.force_stall, p.H, p.d, p.sO, prep);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -1611,20 +1610,21 @@ static FwdMode fwd_mode(const FaProblem &p) {
 
 template <int D, bool CAUSAL, bool VIEW4>
 static cudaError_t launch_fwd_mode(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                                   const CUtensorMap &mv, void *O, float *L, const FwdPrep &prep, cudaStream_t st) {
+                                   const CUtensorMap &mv, const CUtensorMap &mdo, void *O, float *L, const FwdPrep &prep,
+                                   cudaStream_t st) {
     switch (fwd_mode(p)) {
-        case FwdMode::kSplit: return launch_fwd<D, CAUSAL, 2, false, VIEW4>(p, mq, mk, mv, O, L, prep, st);
-        case FwdMode::kPersist: return launch_fwd<D, CAUSAL, 1, true, VIEW4>(p, mq, mk, mv, O, L, prep, st);
-        default: return launch_fwd<D, CAUSAL, 1, false, VIEW4>(p, mq, mk, mv, O, L, prep, st);
+        case FwdMode::kSplit: return launch_fwd<D, CAUSAL, 2, false, VIEW4>(p, mq, mk, mv, mdo, O, L, prep, st);
+        case FwdMode::kPersist: return launch_fwd<D, CAUSAL, 1, true, VIEW4>(p, mq, mk, mv, mdo, O, L, prep, st);
+        default: return launch_fwd<D, CAUSAL, 1, false, VIEW4>(p, mq, mk, mv, mdo, O, L, prep, st);
     }
 }
 
 template <int D, bool CAUSAL>
 static cudaError_t launch_fwd_any(const FaProblem &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                                  const CUtensorMap &mv, void *O, float *L, bool view4, const FwdPrep &prep,
-                                  cudaStream_t st) {
-    return view4 ? launch_fwd_mode<D, CAUSAL, true>(p, mq, mk, mv, O, L, prep, st)
-                 : launch_fwd_mode<D, CAUSAL, false>(p, mq, mk, mv, O, L, prep, st);
+                                  const CUtensorMap &mv, const CUtensorMap &mdo, void *O, float *L, bool view4,
+                                  const FwdPrep &prep, cudaStream_t st) {
+    return view4 ? launch_fwd_mode<D, CAUSAL, true>(p, mq, mk, mv, mdo, O, L, prep, st)
+                 : launch_fwd_mode<D, CAUSAL, false>(p, mq, mk, mv, mdo, O, L, prep, st);
 }
 
 cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void *V, void *O, float *L,
@@ -1641,11 +1641,14 @@ cudaError_t tc_fwd(const FaProblem &p, const void *Q, const void *K, const void 
         return cudaErrorInvalidValue;
     FwdPrep none{};
     const FwdPrep &pr = (prep && prep->dO) ? *prep : none;
+    // d <= 64 kernels stage the tile's dO rows in shared memory through their own map
+    CUtensorMap mdo = mq;
+    if (pr.dO && p.d <= 64 && !tc_make_map(&mdo, pr.dO, p, pr.sdo, p.Nq, BM, view4)) return cudaErrorInvalidValue;
     if (prep_done) *prep_done = pr.dO != nullptr;   // every kernel form does it
-    if (p.d == 128) return p.causal ? launch_fwd_any<128, true>(p, mq, mk, mv, O, L, view4, pr, st)
-                                    : launch_fwd_any<128, false>(p, mq, mk, mv, O, L, view4, pr, st);
-    return p.causal ? launch_fwd_any<64, true>(p, mq, mk, mv, O, L, view4, pr, st)
-                    : launch_fwd_any<64, false>(p, mq, mk, mv, O, L, view4, pr, st);
+    if (p.d == 128) return p.causal ? launch_fwd_any<128, true>(p, mq, mk, mv, mdo, O, L, view4, pr, st)
+                                    : launch_fwd_any<128, false>(p, mq, mk, mv, mdo, O, L, view4, pr, st);
+    return p.causal ? launch_fwd_any<64, true>(p, mq, mk, mv, mdo, O, L, view4, pr, st)
+                    : launch_fwd_any<64, false>(p, mq, mk, mv, mdo, O, L, view4, pr, st);
 }
 
 // ------------------------------------------------------------------ fp32 inputs (X3)
@@ -1690,16 +1693,16 @@ cudaError_t tc_fwd_x3(const FaProblem &p, const void *Q2, const void *K2, const 
             !tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(&wk), K2, p.BH, p.Nk, 256, BN) ||
             !tc_make_map_3d(reinterpret_cast<CUtensorMap_st *>(&wv), V2, p.BH, p.Nk, 256, BN))
             return cudaErrorInvalidValue;
-        return p.causal ? launch_fwd<256, true, 1, false, false, true>(p, wq, wk, wv, O, L, none, st)
-                        : launch_fwd<256, false, 1, false, false, true>(p, wq, wk, wv, O, L, none, st);
+        return p.causal ? launch_fwd<256, true, 1, false, false, true>(p, wq, wk, wv, wq, O, L, none, st)
+                        : launch_fwd<256, false, 1, false, false, true>(p, wq, wk, wv, wq, O, L, none, st);
     }
     // the split form where it pays; otherwise one unit per CTA (no persistent form)
     const bool split = fwd_mode(p) == FwdMode::kSplit;
     if (p.causal)
-        return split ? launch_fwd<128, true, 2, false, false, true>(p, mq, mk, mv, O, L, none, st)
-                     : launch_fwd<128, true, 1, false, false, true>(p, mq, mk, mv, O, L, none, st);
-    return split ? launch_fwd<128, false, 2, false, false, true>(p, mq, mk, mv, O, L, none, st)
-                 : launch_fwd<128, false, 1, false, false, true>(p, mq, mk, mv, O, L, none, st);
+        return split ? launch_fwd<128, true, 2, false, false, true>(p, mq, mk, mv, mq, O, L, none, st)
+                     : launch_fwd<128, true, 1, false, false, true>(p, mq, mk, mv, mq, O, L, none, st);
+    return split ? launch_fwd<128, false, 2, false, false, true>(p, mq, mk, mv, mq, O, L, none, st)
+                 : launch_fwd<128, false, 1, false, false, true>(p, mq, mk, mv, mq, O, L, none, st);
 }
 
 cudaError_t tc_fwd_read_status(unsigned *out, cudaStream_t st) {
