@@ -293,18 +293,19 @@ def executed_factor(kernel, strategy, split_pairs=False):
 # that source is unchanged since the capture it came from (else the key is null).
 KERNEL_SOURCE = {"fwd": "fa_tc_fwd.cu", "bwd_pre": "fa_tc_bwd.cu", "bwd_grads": "fa_tc_bwd.cu"}
 
-# DRAM bytes (read + write) per launch, from one `ncu --set full` capture per
-# workload of the kernel built from the source whose SHA-256 prefix is given.
+# DRAM bytes (read + write) per launch, from one ncu capture per workload (`--set
+# full`, or just the two DRAM byte counters and the duration) of the kernel built
+# from the source whose SHA-256 prefix is given.
 NCU_TRAFFIC = {
-    ("bench_b8_n4096_d64_causal", "bwd_grads"): (25466624, "a6224f497e935de3"),
-    ("bench_b8_n4096_d64_causal", "fwd"): (16825856, "585b589ee66be827"),
-    ("long_n16384_d128_causal", "bwd_grads"): (16977408, "a6224f497e935de3"),
-    ("long_n16384_d128_causal", "fwd"): (16834048, "585b589ee66be827"),
-    ("vlong_n65536_d64_causal", "bwd_grads"): (50986752, "a6224f497e935de3"),
-    ("layer_xl_b4_h25_n1024_causal", "bwd_grads"): (85127680, "a6224f497e935de3"),
-    ("layer_xl_b4_h25_n1024_causal", "fwd"): (59701248, "585b589ee66be827"),
-    ("layer_xl_b4_h25_n1024_full", "bwd_grads"): (86116096, "a6224f497e935de3"),
-    ("sweep_f32_b1_n4096_d64_causal", "bwd_grads"): (4309248, "a6224f497e935de3"),
+    ("bench_b8_n4096_d64_causal", "bwd_grads"): (25466624, "560343985e0486e1"),
+    ("bench_b8_n4096_d64_causal", "fwd"): (16825600, "ae9e6c60e21b3abf"),
+    ("long_n16384_d128_causal", "bwd_grads"): (16980992, "560343985e0486e1"),
+    ("long_n16384_d128_causal", "fwd"): (16833792, "ae9e6c60e21b3abf"),
+    ("vlong_n65536_d64_causal", "bwd_grads"): (50957568, "560343985e0486e1"),
+    ("layer_xl_b4_h25_n1024_causal", "bwd_grads"): (84609792, "560343985e0486e1"),
+    ("layer_xl_b4_h25_n1024_causal", "fwd"): (60608768, "ae9e6c60e21b3abf"),
+    ("layer_xl_b4_h25_n1024_full", "bwd_grads"): (87192832, "560343985e0486e1"),
+    ("sweep_f32_b1_n4096_d64_causal", "bwd_grads"): (4314880, "560343985e0486e1"),
 }
 
 
