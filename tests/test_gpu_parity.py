@@ -260,13 +260,15 @@ def test_backward_phases_launched_separately(cuda_lib, bh, n, d, causal):
 
 @pytest.mark.parametrize("bh,n,d,dt,causal", [(8, 512, 64, "bf16", True), (2, 1152, 128, "bf16", True),
                                                (3, 300, 32, "bf16", False), (2, 200, 64, "f32", True),
-                                               (320, 256, 64, "bf16", True), (1, 4096, 64, "bf16", True)])
+                                               (320, 256, 64, "bf16", True), (1, 4096, 64, "bf16", True),
+                                               (320, 200, 64, "bf16", True), (320, 136, 16, "bf16", False)])
 def test_fwd_bwd_in_one_call(cuda_lib, bh, n, d, dt, causal):
     """fa_fwd_bwd against fa_fwd followed by fa_bwd: O, L and dV bit for bit; dQ and
     dK (which depend on D) from D formed in the forward's epilogue from the
     unrounded O on the tensor-core path, so they differ from the two-call results
     by that rounding only; all five match the oracle.  The cases cover the plain,
-    persistent (320 heads) and two-CTA split (one head of 4096) forward forms."""
+    persistent (320 heads; with ragged rows, and a head dim of 16 whose staged dO
+    rows are zero past d) and two-CTA split (one head of 4096) forward forms."""
     torch = _torch()
     from tiled_attention_04_gb300 import binding
     t = inputs.make_custom(bh, n, n, d, dt, seed=500 + n + d)

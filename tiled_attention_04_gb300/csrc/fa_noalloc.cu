@@ -26,7 +26,6 @@
 //    with FA_ERR_WORKSPACE before anything is launched.
 #include <cuda_runtime.h>
 
-#include <mutex>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -35,28 +34,16 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// device address of the scratch array on the current device (looked up once per device)
+// device address of the scratch array on the current device, looked up on every
+// call (a cached address would not survive a cudaDeviceReset, which reloads the module)
 fa_status scratch_for_current_device(void **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
         cudaGetLastError();
-        return FA_ERR_NO_DEVICE;
+        return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? FA_ERR_NO_DEVICE : FA_ERR_LAUNCH;
     }
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return FA_ERR_LAUNCH;
-        }
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return FA_OK;
 }
 

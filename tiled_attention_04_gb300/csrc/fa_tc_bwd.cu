@@ -508,15 +508,6 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         const uint32_t tPT = tmem + lane_base + C::PT_COL + 32 * t;
         const uint32_t tDS = tmem + lane_base + C::DS_COL + 32 * t;
         const uint32_t tDQ = tmem + lane_base + C::DQ_COL + 32 * t;   // RED: query row r, columns [32t, 32t+32)
-        // RED: this thread's 64 dS^T values (key r, queries [64t, 64t+64)) into the
-        // swizzled shared tile the dK and dQ MMAs read
-        auto store_ds = [&](const uint32_t (&v)[32]) {
-            uint8_t *row = sb + C::DS_OFF + t * (128 * 128) + r * 128;
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<uint4 *>(row + ((u ^ (r & 7)) << 4)) =
-                    make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        };
         // RED: stage sub-tile j's dQ partial (row r, columns [32t, 32t+32)) once the
         // reduction has read sub-tile j-1's, then hand it to the reducing warp
         auto stage_dq = [&](int j, const uint32_t (&v)[32]) -> bool {
@@ -564,27 +555,46 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                 for (int c = 0; c < 64; ++c)
                     if (c < first_visible) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
             }
+            // P^T and dS^T in two halves of 16 columns each: the first half is stored
+            // while the second is computed
             uint32_t pp[32], dsp[32];
+            auto half = [&](int hh) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 nl = *reinterpret_cast<const float4 *>(lds + 4 * i);
-                const float4 nd = *reinterpret_cast<const float4 *>(lds + 128 + 4 * i);   // -D
+                for (int i = 8 * hh; i < 8 * hh + 8; ++i) {
+                    const float4 nl = *reinterpret_cast<const float4 *>(lds + 4 * i);
+                    const float4 nd = *reinterpret_cast<const float4 *>(lds + 128 + 4 * i);   // -D
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = 4 * i + 2 * h;
-                    const float l0 = h ? nl.z : nl.x, l1 = h ? nl.w : nl.y;
-                    const float d0 = h ? nd.z : nd.x, d1 = h ? nd.w : nd.y;
-                    float x0, x1, g0, g1;
-                    tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
-                             scale_log2, scale_log2, l0, l1);
-                    const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-                    tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
-                             d0, d1);
-                    tc::mul2(g0, g1, g0, g1, p0, p1);
-                    pp[2 * i + h] = tc::pack_bf16(p0, p1);
-                    dsp[2 * i + h] = tc::pack_bf16(g0, g1);
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = 4 * i + 2 * h;
+                        const float l0 = h ? nl.z : nl.x, l1 = h ? nl.w : nl.y;
+                        const float d0 = h ? nd.z : nd.x, d1 = h ? nd.w : nd.y;
+                        float x0, x1, g0, g1;
+                        tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
+                                 scale_log2, scale_log2, l0, l1);
+                        const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+                        tc::add2(g0, g1, __uint_as_float(dv[c >> 5][c & 31]), __uint_as_float(dv[c >> 5][(c & 31) + 1]),
+                                 d0, d1);
+                        tc::mul2(g0, g1, g0, g1, p0, p1);
+                        pp[2 * i + h] = tc::pack_bf16(p0, p1);
+                        dsp[2 * i + h] = tc::pack_bf16(g0, g1);
+                    }
                 }
-            }
+            };
+            auto store_half = [&](int hh) {
+                const uint32_t(&ph)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pp[16 * hh]);
+                const uint32_t(&dh)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&dsp[16 * hh]);
+                tmem_st_x16(tPT + 16 * hh, ph);
+                if constexpr (RED) {
+                    uint8_t *row = sb + C::DS_OFF + t * (128 * 128) + r * 128;
+#pragma unroll
+                    for (int uu = 0; uu < 4; ++uu)
+                        *reinterpret_cast<uint4 *>(row + (((4 * hh + uu) ^ (r & 7)) << 4)) =
+                            make_uint4(dh[4 * uu], dh[4 * uu + 1], dh[4 * uu + 2], dh[4 * uu + 3]);
+                } else {
+                    tmem_st_x16(tDS + 16 * hh, dh);
+                }
+            };
+            half(0);
             if (C::SEP && it > 0) {
                 // P^T and dS^T are still read by the previous sub-tile's gradient MMAs until they complete
                 ok = W.wait(q_empty((it - 1) % C::STAGES), ((it - 1) / C::STAGES) & 1);
@@ -593,9 +603,9 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
             }
             uint32_t dq[32];
             if (RED && it > 0) tmem_ld_x32(tDQ, dq);   // sub-tile it-1's dQ, before this sub-tile's MMA rewrites it
-            tmem_st_x32(tPT, pp);
-            if constexpr (RED) store_ds(dsp);
-            else tmem_st_x32(tDS, dsp);
+            store_half(0);
+            half(1);
+            store_half(1);
             tc::tmem_st_wait();
             if constexpr (RED) {
                 if (it > 0) {
@@ -2273,13 +2283,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t tD = tmem + lane_base + C::DP_COL + 64 * t;
         const uint32_t tPT = tmem + lane_base + C::PT_COL + 32 * t;
         const uint32_t tDQ = tmem + lane_base + C::DQ_COL + 32 * t;
-        auto store_ds = [&](const uint32_t (&v)[32]) {
-            uint8_t *row = sb + C::DS_OFF + t * (128 * 128) + rrow * 128;
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<uint4 *>(row + ((u ^ (rrow & 7)) << 4)) =
-                    make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        };
         auto stage_dq = [&](int gg, const uint32_t (&v)[32]) -> bool {
             if (gg > 0 && !__all_sync(0xffffffffu, W.wait(dq_free, (gg - 1) & 1))) return false;
             uint8_t *row = sb + C::DQS_OFF + t * C::DQS_BOX + rrow * 128;
@@ -2320,27 +2323,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (int c = 0; c < 64; ++c)
                         if (c < first_visible) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
                 }
+                // P^T and dS^T in two halves of 16 columns each: the first half is stored
+                // while the second is computed
                 uint32_t pp[32], dsp[32];
+                auto half = [&](int hh) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float4 nl = *reinterpret_cast<const float4 *>(lds + 4 * i);
-                    const float4 nd = *reinterpret_cast<const float4 *>(lds + 128 + 4 * i);
+                    for (int i = 8 * hh; i < 8 * hh + 8; ++i) {
+                        const float4 nl = *reinterpret_cast<const float4 *>(lds + 4 * i);
+                        const float4 nd = *reinterpret_cast<const float4 *>(lds + 128 + 4 * i);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = 4 * i + 2 * h;
-                        const float l0 = h ? nl.z : nl.x, l1 = h ? nl.w : nl.y;
-                        const float d0 = h ? nd.z : nd.x, d1 = h ? nd.w : nd.y;
-                        float x0, x1, g0, g1;
-                        tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]),
-                                 scale_log2, scale_log2, l0, l1);
-                        const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-                        tc::add2(g0, g1, __uint_as_float(dv_[c >> 5][c & 31]), __uint_as_float(dv_[c >> 5][(c & 31) + 1]),
-                                 d0, d1);
-                        tc::mul2(g0, g1, g0, g1, p0, p1);
-                        pp[2 * i + h] = tc::pack_bf16(p0, p1);
-                        dsp[2 * i + h] = tc::pack_bf16(g0, g1);
+                        for (int h = 0; h < 2; ++h) {
+                            const int c = 4 * i + 2 * h;
+                            const float l0 = h ? nl.z : nl.x, l1 = h ? nl.w : nl.y;
+                            const float d0 = h ? nd.z : nd.x, d1 = h ? nd.w : nd.y;
+                            float x0, x1, g0, g1;
+                            tc::fma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]),
+                                     __uint_as_float(sv[c >> 5][(c & 31) + 1]), scale_log2, scale_log2, l0, l1);
+                            const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+                            tc::add2(g0, g1, __uint_as_float(dv_[c >> 5][c & 31]),
+                                     __uint_as_float(dv_[c >> 5][(c & 31) + 1]), d0, d1);
+                            tc::mul2(g0, g1, g0, g1, p0, p1);
+                            pp[2 * i + h] = tc::pack_bf16(p0, p1);
+                            dsp[2 * i + h] = tc::pack_bf16(g0, g1);
+                        }
                     }
-                }
+                };
+                auto store_half = [&](int hh) {
+                    const uint32_t(&ph)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&pp[16 * hh]);
+                    tmem_st_x16(tPT + 16 * hh, ph);
+                    uint8_t *row = sb + C::DS_OFF + t * (128 * 128) + rrow * 128;
+#pragma unroll
+                    for (int uu = 0; uu < 4; ++uu)
+                        *reinterpret_cast<uint4 *>(row + (((4 * hh + uu) ^ (rrow & 7)) << 4)) =
+                            make_uint4(dsp[16 * hh + 4 * uu], dsp[16 * hh + 4 * uu + 1], dsp[16 * hh + 4 * uu + 2],
+                                       dsp[16 * hh + 4 * uu + 3]);
+                };
+                half(0);
                 uint32_t dq[32];
                 if (it > 0) {
                     // the previous sub-tile's MMAs read P^T and dS and wrote its dQ partial
@@ -2349,8 +2367,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tc::fence_after_sync();
                     tmem_ld_x32(tDQ, dq);
                 }
-                tmem_st_x32(tPT, pp);
-                store_ds(dsp);
+                store_half(0);
+                half(1);
+                store_half(1);
                 tc::tmem_st_wait();
                 if (it > 0) {
                     tc::tmem_ld_wait();
