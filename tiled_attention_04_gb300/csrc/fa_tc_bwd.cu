@@ -248,8 +248,9 @@ struct DkdvWideCfg {
     static constexpr uint32_t DQS_OFF = DS_OFF + (RED ? 2 * 128 * 128 : 0);
     static constexpr uint32_t DQS_BOX = 128 * 128;                       // bytes of one staged box
     static constexpr uint32_t BAR_OFF = DQS_OFF + (RED ? (D / 32) * DQS_BOX : 0);
-    // kv_full, q_full[S], q_empty[S], sd_full, sd_free, p_full, drain (+ dq_staged, dq_free)
-    static constexpr int NBAR = 1 + 2 * STAGES + 4 + (RED ? 2 : 0);
+    // kv_full, q_full[S], q_empty[S], sd_full, sd_free, p_full, drain (+ dq_staged,
+    // dq_free, and ep_staged[2]: a warpgroup's dV or dK rows are staged for their TMA store)
+    static constexpr int NBAR = 1 + 2 * STAGES + 4 + (RED ? 4 : 0);
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t PEER_BAR_OFF = MISC_OFF + 16;
     static constexpr uint32_t SMEM_BYTES = (PEER_BAR_OFF + 16 + 1024 > 120u * 1024u ? PEER_BAR_OFF + 16 + 1024 : 120u * 1024u);
@@ -275,6 +276,7 @@ struct DkdvWideCfg {
 template <int D, bool CAUSAL, int SPLIT, bool VIEW4, bool RED>
 __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                           const CUtensorMap &tmdO, const CUtensorMap *tmdQa,
+                                          const CUtensorMap *tmdK, const CUtensorMap *tmdV,
                                           const float *__restrict__ Lp,
                                           const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
                                           __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int kt, int bh, int H,
@@ -308,6 +310,8 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
     const uint32_t drain = bar(4 + 2 * C::STAGES);
     const uint32_t dq_staged = bar(5 + 2 * C::STAGES);   // RED: the element-wise threads staged a dQ partial
     const uint32_t dq_free = bar(6 + 2 * C::STAGES);     // RED: the reduction has read the staged partial
+    // RED, unsplit: a warpgroup's dV (t = 0) or dK (t = 1) rows are staged for their TMA store
+    auto ep_staged = [&](int t) { return bar(7 + 2 * C::STAGES + t); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -324,6 +328,8 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
         if constexpr (RED) {
             tc::mbar_init(dq_staged, 256);
             tc::mbar_init(dq_free, 1);
+            tc::mbar_init(ep_staged(0), 128);
+            tc::mbar_init(ep_staged(1), 128);
         }
         if (SPLIT > 1) {
             tc::mbar_init(base + C::PEER_BAR_OFF, 256);       // peer_free: the peer's 256 element-wise threads
@@ -408,6 +414,20 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
                 tc::mbar_arrive(dq_free);
             }
             tc::bulk_wait_all();            // the additions have landed before the CTA exits
+        }
+    } else if (RED && SPLIT == 1 && warp == 3) {
+        // ------------------------------------------------------------ dV / dK stores (RED, unsplit)
+        // the rows, staged by the element-wise warpgroups in their halves of the dS^T
+        // tile (128-byte swizzled), go out as two TMA stores (rows past Nk are not written)
+        if constexpr (RED && SPLIT == 1) {
+            if (lane == 0) {
+                for (int t = 0; t < 2; ++t) {
+                    if (!W.wait(ep_staged(t), 0)) break;
+                    tc::tma_store_rows<VIEW4>(t == 0 ? tmdV : tmdK, base + C::DS_OFF + t * (128 * 128), 0, k0, bh, H);
+                }
+                tc::bulk_commit_group();
+                tc::bulk_wait_all();   // the stores have read the tiles (and landed) before the CTA exits
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -700,12 +720,28 @@ __device__ __forceinline__ void dkdv_item_wide(const CUtensorMap &tmQ, const CUt
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     packed[i] = tc::pack_bf16(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
-                if (fine && (SPLIT == 1 || merge) && key < Nk) {
+                if constexpr (RED && SPLIT == 1) {
+                    // into this warpgroup's half of the dS^T tile (free: every MMA is done),
+                    // for warp 3's TMA store
+                    if (fine) {
+                        uint8_t *srow = sb + C::DS_OFF + t * (128 * 128) + r * 128;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            *reinterpret_cast<uint4 *>(srow + (((4 * c + i) ^ (r & 7)) << 4)) =
+                                make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                    }
+                } else if (fine && (SPLIT == 1 || merge) && key < Nk) {
                     uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         if (!VIEW4 || 32 * c + 8 * i < dv)   // columns past a head dim below 64 are padding
                             o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
+            }
+            if constexpr (RED && SPLIT == 1) {
+                if (fine) {
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(ep_staged(t));
                 }
             }
         }
@@ -2035,8 +2071,9 @@ __device__ __forceinline__ void dq_item_narrow(const CUtensorMap &tmQ, const CUt
 struct DkdvPersistCfg : DkdvWideCfg<64, true> {
     using Base = DkdvWideCfg<64, true>;
     // the base barriers, then kv_empty (an item's MMAs are done: K/V may be
-    // reloaded) and acc_free (the epilogue has read dV / dK from TMEM)
-    static constexpr int NBAR = Base::NBAR + 2;
+    // reloaded), acc_free (the epilogue has read dV / dK from TMEM) and ds_free[2]
+    // (the TMA store of a warpgroup's dV or dK rows has read them out of the dS^T tile)
+    static constexpr int NBAR = Base::NBAR + 4;
     static constexpr uint32_t MISC_OFF = Base::BAR_OFF + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = (MISC_OFF + 16 + 1024 > 120u * 1024u ? MISC_OFF + 16 + 1024 : 120u * 1024u);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -2046,7 +2083,8 @@ template <bool CAUSAL, bool VIEW4>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fa_bwd_red_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                                 const __grid_constant__ CUtensorMap dqa, const float *__restrict__ Lp,
+                                 const __grid_constant__ CUtensorMap dqa, const __grid_constant__ CUtensorMap tmdK,
+                                 const __grid_constant__ CUtensorMap tmdV, const float *__restrict__ Lp,
                                  const float *__restrict__ Dp, __nv_bfloat16 *__restrict__ dK,
                                  __nv_bfloat16 *__restrict__ dV, int Nq, int Nk, int BH, int k_tiles, float scale,
                                  float scale_log2, uint32_t wait_limit, int H, int dv, FaStrides sdk, FaStrides sdv) {
@@ -2086,8 +2124,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t drain = bar(4 + 2 * C::STAGES);
     const uint32_t dq_staged = bar(5 + 2 * C::STAGES);
     const uint32_t dq_free = bar(6 + 2 * C::STAGES);
-    const uint32_t kv_empty = bar(7 + 2 * C::STAGES);
-    const uint32_t acc_free = bar(8 + 2 * C::STAGES);
+    auto ep_staged = [&](int t) { return bar(7 + 2 * C::STAGES + t); };   // a warpgroup's dV / dK rows staged
+    const uint32_t kv_empty = bar(9 + 2 * C::STAGES);
+    const uint32_t acc_free = bar(10 + 2 * C::STAGES);
+    auto ds_free = [&](int t) { return bar(11 + 2 * C::STAGES + t); };    // ... and read out by their TMA store
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + C::MISC_OFF);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -2105,6 +2145,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::mbar_init(dq_free, 1);
         tc::mbar_init(kv_empty, 1);
         tc::mbar_init(acc_free, 256);
+        for (int t = 0; t < 2; ++t) {
+            tc::mbar_init(ep_staged(t), 128);
+            tc::mbar_init(ds_free(t), 1);
+        }
         *abort_flag = 0u;
         tc::fence_mbar_init();
     }
@@ -2190,6 +2234,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             tc::bulk_wait_all();
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ dV / dK stores
+        // each item's rows, staged by the element-wise warpgroups in their halves of
+        // the dS^T tile (128-byte swizzled), go out as two TMA stores (rows past Nk
+        // are not written); the halves are handed back once the stores have read them
+        if (lane == 0) {
+            int kt, bh, first, n;
+            for (int r = 0; item_of(r, kt, bh, first, n); ++r) {
+                bool ok = true;
+                for (int t = 0; ok && t < 2; ++t) {
+                    if (!(ok = W.wait(ep_staged(t), r & 1))) break;
+                    tc::tma_store_rows<VIEW4>(t == 0 ? &tmdV : &tmdK, base + C::DS_OFF + t * (128 * 128), 0,
+                                              kt * C::BK, bh, H);
+                }
+                tc::bulk_commit_group();
+                tc::bulk_wait_read_all();
+                if (!ok) break;
+                tc::mbar_arrive(ds_free(0));
+                tc::mbar_arrive(ds_free(1));
+            }
+            tc::bulk_wait_all();   // the stores have landed before the CTA exits
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -2366,6 +2432,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
                     tc::fence_after_sync();
                     tmem_ld_x32(tDQ, dq);
+                } else if (r > 0) {
+                    // the previous item's dV / dK rows left this warpgroup's dS^T half
+                    if (!__all_sync(0xffffffffu, W.wait(ds_free(t), (r - 1) & 1))) { alive = false; break; }
                 }
                 store_half(0);
                 half(1);
@@ -2392,11 +2461,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 reg_fence_x32(dq);
                 fine = stage_dq(g + n - 1, dq);
             }
-            __nv_bfloat16 *dst;
-            if constexpr (VIEW4)
-                dst = t == 0 ? dV + fa_row_offset(sdv, tc::opaque(H), bh, key) : dK + fa_row_offset(sdk, tc::opaque(H), bh, key);
-            else
-                dst = (t == 0 ? dV : dK) + ((size_t)bh * Nk + key) * D;
             const float mul = t == 0 ? 1.f : scale;
             const uint32_t tA = tmem + lane_base + (t == 0 ? C::DV_COL : C::DK_COL);
             uint32_t a[2][32];
@@ -2412,19 +2476,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             tc::fence_before_sync();
             tc::mbar_arrive(acc_free);   // dV / dK may be overwritten by the next item
+            // the row, in bf16, into this warpgroup's half of the dS^T tile (free: the
+            // item's MMAs are done, and an item without sub-tiles waits for the previous
+            // item's store here), then warp 3 stores the tile
+            bool stage = fine || n == 0;
+            if (n == 0 && r > 0 && !__all_sync(0xffffffffu, W.wait(ds_free(t), (r - 1) & 1))) stage = false;
+            if (!stage) alive = false;
+            if (stage) {
+                uint8_t *srow = sb + C::DS_OFF + t * (128 * 128) + rrow * 128;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t packed[16];
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t packed[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    packed[i] = tc::pack_bf16(__uint_as_float(a[c][2 * i]) * mul, __uint_as_float(a[c][2 * i + 1]) * mul);
-                if ((fine || n == 0) && key < Nk) {
-                    uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * c);
+                    for (int i = 0; i < 16; ++i)
+                        packed[i] = tc::pack_bf16(__uint_as_float(a[c][2 * i]) * mul,
+                                                  __uint_as_float(a[c][2 * i + 1]) * mul);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        if (!VIEW4 || 32 * c + 8 * i < dv)
-                            o[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                        *reinterpret_cast<uint4 *>(srow + (((4 * c + i) ^ (rrow & 7)) << 4)) =
+                            make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
                 }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(ep_staged(t));
             }
             g += n;
             if (!fine && n > 0) alive = false;
@@ -2452,7 +2525,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      const __grid_constant__ CUtensorMap vA, const __grid_constant__ CUtensorMap dOA,
                      const __grid_constant__ CUtensorMap qB, const __grid_constant__ CUtensorMap kB,
                      const __grid_constant__ CUtensorMap vB, const __grid_constant__ CUtensorMap dOB,
-                     const __grid_constant__ CUtensorMap dqa, const float *__restrict__ Lp, const float *__restrict__ Dp,
+                     const __grid_constant__ CUtensorMap dqa, const __grid_constant__ CUtensorMap tmdK,
+                     const __grid_constant__ CUtensorMap tmdV, const float *__restrict__ Lp, const float *__restrict__ Dp,
                      void *__restrict__ dQ, void *__restrict__ dK, void *__restrict__ dV, int Nq, int Nk, int BH,
                      int k_tiles, int q_tiles, int n_kv_items, int n_q_items, float scale, float scale_log2,
                      uint32_t wait_limit, int H, int dv, FaStrides sdq, FaStrides sdk, FaStrides sdv) {
@@ -2473,7 +2547,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int r = idx / BH;
         const int kt = CAUSAL ? r : k_tiles - 1 - r;    // causal: the first key tiles see the most queries
         if constexpr (D == 64)
-            dkdv_item_wide<D, CAUSAL, SPLIT, VIEW4, RED>(qA, kA, vA, dOA, &dqa, Lp, Dp,
+            dkdv_item_wide<D, CAUSAL, SPLIT, VIEW4, RED>(qA, kA, vA, dOA, &dqa, &tmdK, &tmdV, Lp, Dp,
                                                          static_cast<__nv_bfloat16 *>(dK),
                                                          static_cast<__nv_bfloat16 *>(dV), Nq, Nk, kt, bh, H, dv,
                                                          sdk, sdv, scale, scale_log2, wait_limit);
@@ -2556,6 +2630,7 @@ bool dq_split(const FaProblem &p) {
 struct Maps2 {
     Maps a, b;        // tensor maps of the dK/dV pass (a) and of the dQ pass (b)
     CUtensorMap dqa;  // the fp32 dQ accumulator (dQ by reduction), else unused
+    CUtensorMap dk, dv;   // dK and dV (dQ by reduction: their rows leave through TMA stores), else unused
     bool view4;       // 4-D maps over strided views (else 3-D maps over contiguous tensors)
 };
 
@@ -2572,7 +2647,7 @@ cudaError_t launch_bwd(const FaProblem &p, const Maps2 &m, const float *Lp, cons
     const int kt = (p.Nk + 127) / 128, qt = (p.Nq + 127) / 128;
     const long long na = do_kv ? (long long)kt * p.BH : 0, nb = (do_q && !RED) ? (long long)qt * p.BH : 0;
     return launch_cluster(fa_bwd_tc_kernel<D, CAUSAL, SPLIT, VIEW4, RED, X3>, smem, (na + nb) * SPLIT, SPLIT, st, m.a.q,
-                          m.a.k, m.a.v, m.a.dO, m.b.q, m.b.k, m.b.v, m.b.dO, m.dqa, Lp, Dp, dQ, dK, dV, p.Nq, p.Nk,
+                          m.a.k, m.a.v, m.a.dO, m.b.q, m.b.k, m.b.v, m.b.dO, m.dqa, m.dk, m.dv, Lp, Dp, dQ, dK, dV, p.Nq, p.Nk,
                           p.BH, kt, qt, (int)na, (int)nb, p.scale,
                           p.scale * kLog2e, p.wait_limit, p.H, p.d, p.sdQ, p.sdK, p.sdV);
 }
@@ -2608,7 +2683,8 @@ cudaError_t launch_red_persistent(const FaProblem &p, const Maps2 &m, const floa
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fa_bwd_red_persistent_kernel<CAUSAL, VIEW4>, m.a.q, m.a.k, m.a.v, m.a.dO, m.dqa, Lp,
+    e = cudaLaunchKernelEx(&cfg, fa_bwd_red_persistent_kernel<CAUSAL, VIEW4>, m.a.q, m.a.k, m.a.v, m.a.dO, m.dqa, m.dk,
+                           m.dv, Lp,
                            Dp, static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), p.Nq, p.Nk, p.BH,
                            kt, p.scale, p.scale * kLog2e, p.wait_limit, p.H, p.d, p.sdK, p.sdV);
     if (e != cudaSuccess) return e;
@@ -2750,6 +2826,8 @@ cudaError_t grads_impl(const FaProblem &p, const void *Q, const void *K, const v
         if (p.d > 64) return cudaErrorInvalidValue;
         if (!tc_make_map_acc(reinterpret_cast<CUtensorMap_st *>(&m.dqa), dQa, p.BH, padded_rows(p.Nq), 64))
             return cudaErrorInvalidValue;
+        if (!tc_make_map(&m.dk, dK, p, p.sdK, p.Nk, 128, m.view4) || !tc_make_map(&m.dv, dV, p, p.sdV, p.Nk, 128, m.view4))
+            return cudaErrorInvalidValue;
         cudaError_t e;
         if (red_persistent(p))
             e = m.view4 ? (p.causal ? launch_red_persistent<true, true>(p, m, Lp, Dp, dK, dV, st)
@@ -2763,6 +2841,7 @@ cudaError_t grads_impl(const FaProblem &p, const void *Q, const void *K, const v
         return launch_dq_convert<64>(p, dQa, dQ, !tc_plain_layout(p, p.sdQ, p.Nq), st);
     }
     m.dqa = m.a.q;   // unused by the two-pass launch
+    m.dk = m.dv = m.a.q;
     if (p.d == 128) return p.causal ? launch_bwd_any<128, true, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
                                     : launch_bwd_any<128, false, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);
     return p.causal ? launch_bwd_any<64, true, false>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
@@ -2832,6 +2911,7 @@ cudaError_t tc_bwd_grads_x3(const FaProblem &p, const void *Q2, const void *K2, 
         !map(&m.b.k, K2, p.Nk, sub) || !map(&m.b.v, V2, p.Nk, sub))
         return cudaErrorInvalidValue;
     m.dqa = m.a.q;   // unused
+    m.dk = m.dv = m.a.q;
     if (p.d == 128)   // 256-column rows: one item per CTA
         return p.causal ? launch_bwd<256, true, 1, false, false, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st)
                         : launch_bwd<256, false, 1, false, false, true>(p, m, Lp, Dp, dQ, dK, dV, do_kv, do_q, st);

@@ -236,6 +236,33 @@ __device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap *m
     else tma_load_3d(dst, m, bar, x, y, bh);
 }
 
+// a shared-memory box (laid out as the map's swizzle wants) stored to rows y.. of
+// batch*head bh, columns x.. (3-D or 4-D map as for the loads); parts of the box
+// past the tensor's extents are not written.  Tracked by the issuing thread's bulk
+// group: the box may be rewritten once a bulk_wait_read covers it.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *m, uint32_t src, int x, int y, int z, int w) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+template <bool VIEW4>
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap *m, uint32_t src, int x, int y, int bh, int H) {
+    if constexpr (VIEW4) {
+        const int h = opaque(H);
+        const int b = bh / h;
+        tma_store_4d(m, src, x, y, bh - b * h, b);
+    } else {
+        tma_store_3d(m, src, x, y, bh);
+    }
+}
+
 // element-wise add of a shared-memory box into global memory through a 3-D
 // tensor map (the reduction runs in L2); tracked by the issuing thread's bulk group
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *m, uint32_t src, int x, int y, int z) {
