@@ -12,7 +12,7 @@ Besides the K timed steps of the headline workload the JSON line carries:
   workloads   the other four full-size workloads, each timed forward alone,
               backward alone and forward + backward, with its own clocks;
   e2e         through the public call with pinned host buffers: throughput
-              with three buffer sets in flight, and the latency of one call
+              with four buffer sets in flight, and the latency of one call
               (copies in, fa_fwd_bwd, copies out, synchronised) on one stream;
   cpu_baseline the fp64 oracle on the host cores (forward and forward +
               backward timed separately; one-thread numbers for the tiny and
@@ -557,8 +557,8 @@ def run_gpu(args, w, rank, world):
 
     # ---- end to end through the public API with host buffers: every step copies its
     # inputs from pinned host memory, runs fa_fwd_bwd and copies O, L, dQ, dK, dV
-    # back.  Throughput: three buffer sets, each step captured once as a CUDA graph
-    # and the graphs replayed in turn on three streams, so the copies of two steps
+    # back.  Throughput: four buffer sets, each step captured once as a CUDA graph
+    # and the graphs replayed in turn on four streams, so the copies of two steps
     # overlap the kernels of a third (as a data loader would); per-step work is
     # unchanged.  The copy engines move about 190 GB/s each way from pinned memory
     # here, so with the short steps the copies, not the kernels, set this number.
@@ -571,7 +571,7 @@ def run_gpu(args, w, rank, world):
         return {"in": dev_in, "out": outs, "ws": binding.alloc_workspace(prob.Q, prob.K, w.causal),
                 "host_out": [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]}
 
-    n_sets = 3
+    n_sets = 4
     sets = [make_set() for _ in range(n_sets)]
     h2d = sum(x.numel() * x.element_size() for x in host)
     d2h = sum(x.numel() * x.element_size() for x in sets[0]["host_out"])
